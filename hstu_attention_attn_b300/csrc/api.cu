@@ -1,0 +1,583 @@
+// api.cu -- the extern "C" entry points of libmtgr.so (declared in mtgr.h):
+// argument checks, workspace carving, tensor-map encoding and kernel dispatch.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "plan.cuh"
+
+namespace mtgr {
+
+// ---- launchers defined in the other translation units ----
+cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, UserInfo*, int32_t*, cudaStream_t);
+cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
+                                  int64_t*, cudaStream_t);
+template <typename T>
+cudaError_t launch_gln_fwd(const T*, T*, float*, float*, const uint8_t*, const float*, const float*, int64_t, int,
+                           float, cudaStream_t);
+template <typename T>
+cudaError_t launch_gln_bwd(const T*, const T*, const float*, const float*, const uint8_t*, const float*, const T*,
+                           T*, float*, float*, float*, int64_t, int, cudaStream_t);
+int gln_bwd_blocks(int64_t rows);
+template <typename T>
+cudaError_t launch_ln_gate_fwd(const T*, const T*, int64_t, T*, float*, float*, int64_t, int, float, cudaStream_t);
+template <typename T>
+cudaError_t launch_ln_gate_bwd(const T*, const T*, const T*, int64_t, const float*, const float*, T*, T*, int64_t,
+                               const T*, int64_t, int, cudaStream_t);
+cudaError_t launch_attn_f32_fwd(const float*, const float*, const float*, int64_t, const UserInfo*, int,
+                                const int64_t*, int64_t, int, int, float*, cudaStream_t);
+cudaError_t launch_attn_f32_bwd(const float*, const float*, const float*, int64_t, const float*, const UserInfo*,
+                                int, const int64_t*, int64_t, int, int, float*, float*, float*, int64_t,
+                                const float*, const float*, const float*, cudaStream_t);
+cudaError_t launch_attn_fwd_bf16(const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*, int64_t,
+                                 int64_t, int, int, const int32_t*, int32_t, const int64_t*, __nv_bfloat16*,
+                                 int32_t*, cudaStream_t);
+cudaError_t launch_attn_bwd_bf16(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                 int64_t ld, const __nv_bfloat16* dO, int64_t T, int H, int d, const int32_t* plan,
+                                 int32_t B, const int64_t* ts, float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                                 __nv_bfloat16* dv, int64_t ldg, const __nv_bfloat16* zq, const __nv_bfloat16* zk,
+                                 const __nv_bfloat16* zv, int32_t* status, cudaStream_t s);
+
+// ---- error state ----
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+mtgr_status cuda_status(cudaError_t e, const char* where) {
+  set_error("%s: %s", where, cudaGetErrorString(e));
+  return MTGR_ERR_CUDA;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                       uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace carving
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+static size_t esize(mtgr_dtype dt) { return dt == MTGR_BF16 ? 2 : 4; }
+
+struct AttnWs {
+  size_t status, plan, dO, dq_acc, total;
+};
+static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt) {
+  AttnWs w;
+  size_t o = 0;
+  w.status = o;
+  o += 256;
+  w.plan = o;
+  o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T).total);
+  w.dO = o;
+  o += align256((size_t)T * H * d * esize(dt));
+  w.dq_acc = o;
+  if (dt == MTGR_BF16) o += align256((size_t)T * H * d * sizeof(float));
+  w.total = o;
+  return w;
+}
+
+struct LayerWs {
+  AttnWs attn;
+  size_t attn_base, dY, dZ, dxn, gln_part, wpart, total;
+  int splits_uqkv, splits_o;
+};
+static int choose_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  const int64_t nk = (K + 63) / 64;
+  int64_t s = (2 * (int64_t)num_sms() + tiles - 1) / tiles;
+  if (s > 16) s = 16;
+  if (s > nk) s = nk;
+  return (int)(s < 1 ? 1 : s);
+}
+static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, mtgr_dtype dt) {
+  LayerWs w;
+  const int64_t HD = (int64_t)H * d;
+  w.attn = attn_ws(B, T, H, d, dt);
+  size_t o = 0;
+  w.attn_base = o;
+  o += w.attn.total;
+  w.dY = o;
+  o += align256((size_t)T * HD * esize(dt));
+  w.dZ = o;
+  o += align256((size_t)T * 4 * HD * esize(dt));
+  w.dxn = o;
+  o += align256((size_t)T * D * esize(dt));
+  w.gln_part = o;
+  o += align256((size_t)gln_bwd_blocks(T) * 8 * D * sizeof(float));
+  w.splits_uqkv = dt == MTGR_BF16 ? choose_splits(D, 4 * HD, T) : 1;
+  w.splits_o = dt == MTGR_BF16 ? choose_splits(HD, D, T) : 1;
+  const size_t p1 = (size_t)w.splits_uqkv * D * 4 * HD, p2 = (size_t)w.splits_o * HD * D;
+  w.wpart = o;
+  o += align256((p1 > p2 ? p1 : p2) * sizeof(float));
+  w.total = o;
+  return w;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, code, ...)   \
+  do {                             \
+    if (!(cond)) {                 \
+      set_error(__VA_ARGS__);      \
+      return code;                 \
+    }                              \
+  } while (0)
+
+static mtgr_status check_meta(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T) {
+  REQUIRE(B >= 0 && T >= 0, MTGR_ERR_INVALID_ARG, "B and T must be non-negative");
+  REQUIRE(T < (int64_t(1) << 31) - 256, MTGR_ERR_UNSUPPORTED, "T must be below 2^31");
+  REQUIRE(offsets != nullptr, MTGR_ERR_INVALID_ARG, "offsets is NULL");
+  REQUIRE(T == 0 || gid != nullptr, MTGR_ERR_INVALID_ARG, "gid is NULL");
+  return MTGR_OK;
+}
+
+}  // namespace mtgr
+
+using namespace mtgr;
+
+// ===========================================================================
+extern "C" {
+
+const char* mtgr_last_error(void) { return g_err; }
+int mtgr_version(void) { return 100; }
+
+mtgr_status mtgr_validate_batch(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T,
+                                int32_t* status_word, mtgr_stream_t stream) {
+  mtgr_status st = check_meta(offsets, B, gid, T);
+  if (st != MTGR_OK) return st;
+  REQUIRE(status_word != nullptr, MTGR_ERR_INVALID_ARG, "status_word is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MTGR_CUDA_TRY(cudaMemsetAsync(status_word, 0, sizeof(int32_t), s), "validate_batch memset");
+  MTGR_CUDA_TRY(launch_user_info(offsets, B, gid, T, nullptr, status_word, s), "validate_batch");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                                      int64_t T, int32_t* cnt, int64_t* total_pairs, mtgr_stream_t stream) {
+  mtgr_status st = check_meta(offsets, B, gid, T);
+  if (st != MTGR_OK) return st;
+  REQUIRE(total_pairs != nullptr && (T == 0 || (cnt && ts)), MTGR_ERR_INVALID_ARG, "NULL output / ts");
+  MTGR_CUDA_TRY(launch_visible_counts(offsets, B, gid, ts, T, cnt, total_pairs,
+                                      reinterpret_cast<cudaStream_t>(stream)),
+                "visible_counts");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_group_layernorm_fwd(const void* x, void* y, float* mean, float* rstd, const uint8_t* gid,
+                                     const float* gamma, const float* beta, int64_t T, int32_t D, float eps,
+                                     mtgr_dtype dtype, mtgr_stream_t stream) {
+  REQUIRE(T >= 0 && D > 0 && D % 8 == 0 && D <= 4096, MTGR_ERR_UNSUPPORTED, "D must be a multiple of 8 in [8, 4096]");
+  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
+  if (T == 0) return MTGR_OK;
+  REQUIRE(x && y && gid && gamma && beta, MTGR_ERR_INVALID_ARG, "NULL pointer");
+  REQUIRE(aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta), MTGR_ERR_INVALID_ARG,
+          "tensors must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == MTGR_BF16
+                      ? launch_gln_fwd(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), mean,
+                                       rstd, gid, gamma, beta, T, D, eps, s)
+                      : launch_gln_fwd(static_cast<const float*>(x), static_cast<float*>(y), mean, rstd, gid, gamma,
+                                       beta, T, D, eps, s);
+  if (e != cudaSuccess) return cuda_status(e, "group_layernorm_fwd");
+  return MTGR_OK;
+}
+
+size_t mtgr_group_layernorm_bwd_workspace_size(int64_t T, int32_t D) {
+  return align256((size_t)gln_bwd_blocks(T) * 8 * (size_t)D * sizeof(float));
+}
+
+mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+                                     const uint8_t* gid, const float* gamma, const void* dx_residual, void* dx,
+                                     float* dgamma, float* dbeta, int64_t T, int32_t D, mtgr_dtype dtype,
+                                     void* workspace, size_t workspace_bytes, mtgr_stream_t stream) {
+  REQUIRE(T >= 0 && D > 0 && D % 8 == 0 && D <= 4096, MTGR_ERR_UNSUPPORTED, "D must be a multiple of 8 in [8, 4096]");
+  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
+  REQUIRE(dgamma && dbeta, MTGR_ERR_INVALID_ARG, "NULL dgamma/dbeta");
+  REQUIRE(workspace && workspace_bytes >= mtgr_group_layernorm_bwd_workspace_size(T, D), MTGR_ERR_WORKSPACE,
+          "workspace too small");
+  REQUIRE(T == 0 || (dy && x && mean && rstd && gid && gamma && dx), MTGR_ERR_INVALID_ARG, "NULL pointer");
+  REQUIRE(aligned16(dy) && aligned16(x) && aligned16(dx) && aligned16(gamma) && aligned16(dx_residual),
+          MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == MTGR_BF16
+          ? launch_gln_bwd(static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd,
+                           gid, gamma, static_cast<const __nv_bfloat16*>(dx_residual), static_cast<__nv_bfloat16*>(dx),
+                           dgamma, dbeta, static_cast<float*>(workspace), T, D, s)
+          : launch_gln_bwd(static_cast<const float*>(dy), static_cast<const float*>(x), mean, rstd, gid, gamma,
+                           static_cast<const float*>(dx_residual), static_cast<float*>(dx), dgamma, dbeta,
+                           static_cast<float*>(workspace), T, D, s);
+  if (e != cudaSuccess) return cuda_status(e, "group_layernorm_bwd");
+  return MTGR_OK;
+}
+
+size_t mtgr_attn_workspace_size(int32_t B, int64_t T, int32_t n_heads, int32_t d_h, mtgr_dtype dtype) {
+  if (B < 0 || T < 0 || n_heads <= 0 || d_h <= 0) return 0;
+  return attn_ws(B, T, n_heads, d_h, dtype).total;
+}
+
+static mtgr_status check_attn(const void* q, const void* k, const void* v, const void* u, int64_t ld_in,
+                              const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T,
+                              int32_t H, int32_t d, mtgr_dtype dtype, void* ws, size_t ws_bytes) {
+  mtgr_status st = check_meta(offsets, B, gid, T);
+  if (st != MTGR_OK) return st;
+  REQUIRE(H >= 1 && d >= 1, MTGR_ERR_INVALID_ARG, "n_heads and d_h must be positive");
+  if (dtype == MTGR_BF16) {
+    REQUIRE(d == 64 || d == 128, MTGR_ERR_UNSUPPORTED, "bf16 path supports d_h in {64, 128}");
+    REQUIRE(ld_in % 8 == 0, MTGR_ERR_INVALID_ARG, "ld_in must be a multiple of 8");
+  } else if (dtype == MTGR_F32) {
+    REQUIRE(d <= 128 && d % 4 == 0, MTGR_ERR_UNSUPPORTED, "fp32 path supports d_h <= 128, d_h % 4 == 0");
+    REQUIRE(ld_in % 4 == 0, MTGR_ERR_INVALID_ARG, "ld_in must be a multiple of 4");
+  } else {
+    REQUIRE(false, MTGR_ERR_INVALID_ARG, "bad dtype");
+  }
+  REQUIRE((int64_t)H * d % 8 == 0 && H * d <= 4096, MTGR_ERR_UNSUPPORTED, "H*d_h must be a multiple of 8, <= 4096");
+  REQUIRE(ld_in >= (int64_t)H * d, MTGR_ERR_INVALID_ARG, "ld_in < H*d_h");
+  REQUIRE(T == 0 || (q && k && v && u && ts), MTGR_ERR_INVALID_ARG, "NULL q/k/v/u/ts");
+  REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(u), MTGR_ERR_INVALID_ARG,
+          "q/k/v/u must be 16-byte aligned");
+  REQUIRE(ws && ws_bytes >= attn_ws(B, T, H, d, dtype).total && aligned16(ws), MTGR_ERR_WORKSPACE,
+          "workspace missing or smaller than mtgr_attn_workspace_size()");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, const void* u, int64_t ld_in,
+                               const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                               int64_t T, int32_t n_heads, int32_t d_h, float eps, void* y, void* o_saved,
+                               float* ln_mean, float* ln_rstd, mtgr_dtype dtype, void* workspace,
+                               size_t workspace_bytes, mtgr_stream_t stream) {
+  mtgr_status st = check_attn(q, k, v, u, ld_in, offsets, B, gid, ts, T, n_heads, d_h, dtype, workspace,
+                              workspace_bytes);
+  if (st != MTGR_OK) return st;
+  REQUIRE(T == 0 || (y && o_saved && ln_mean && ln_rstd), MTGR_ERR_INVALID_ARG, "NULL output");
+  REQUIRE(aligned16(y) && aligned16(o_saved), MTGR_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const AttnWs w = attn_ws(B, T, n_heads, d_h, dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
+  int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
+  MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
+  if (T == 0 || B == 0) return MTGR_OK;
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_fwd plan");
+  const int HD = n_heads * d_h;
+  const PlanLayout L = plan_layout(B, T);
+  if (dtype == MTGR_BF16) {
+    using bf = __nv_bfloat16;
+    MTGR_CUDA_TRY(launch_attn_fwd_bf16(static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
+                                       ld_in, T, n_heads, d_h, plan, B, ts, static_cast<bf*>(o_saved), status, s),
+                  "attn_fwd tcgen05");
+    MTGR_CUDA_TRY(launch_ln_gate_fwd(static_cast<const bf*>(o_saved), static_cast<const bf*>(u), ld_in,
+                                     static_cast<bf*>(y), ln_mean, ln_rstd, T, HD, eps, s),
+                  "attn_fwd gate");
+  } else {
+    MTGR_CUDA_TRY(launch_attn_f32_fwd(static_cast<const float*>(q), static_cast<const float*>(k),
+                                      static_cast<const float*>(v), ld_in,
+                                      reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
+                                      static_cast<float*>(o_saved), s),
+                  "attn_fwd fp32");
+    MTGR_CUDA_TRY(launch_ln_gate_fwd(static_cast<const float*>(o_saved), static_cast<const float*>(u), ld_in,
+                                     static_cast<float*>(y), ln_mean, ln_rstd, T, HD, eps, s),
+                  "attn_fwd gate");
+  }
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, const void* v, const void* u,
+                               int64_t ld_in, const void* o_saved, const float* ln_mean, const float* ln_rstd,
+                               const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                               int64_t T, int32_t n_heads, int32_t d_h, void* dq, void* dk, void* dv, void* du,
+                               int64_t ld_grad, const void* z_uqkv, mtgr_dtype dtype, void* workspace,
+                               size_t workspace_bytes, mtgr_stream_t stream) {
+  mtgr_status st = check_attn(q, k, v, u, ld_in, offsets, B, gid, ts, T, n_heads, d_h, dtype, workspace,
+                              workspace_bytes);
+  if (st != MTGR_OK) return st;
+  const int64_t HD = (int64_t)n_heads * d_h;
+  REQUIRE(T == 0 || (dy && o_saved && ln_mean && ln_rstd && dq && dk && dv && du), MTGR_ERR_INVALID_ARG,
+          "NULL pointer");
+  REQUIRE(ld_grad >= HD && ld_grad % 8 == 0, MTGR_ERR_INVALID_ARG, "ld_grad must be >= H*d_h and a multiple of 8");
+  REQUIRE(aligned16(dy) && aligned16(o_saved) && aligned16(dq) && aligned16(dk) && aligned16(dv) &&
+              aligned16(du) && aligned16(z_uqkv),
+          MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const AttnWs w = attn_ws(B, T, n_heads, d_h, dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
+  int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
+  MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
+  if (T == 0 || B == 0) return MTGR_OK;
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_bwd plan");
+  const PlanLayout L = plan_layout(B, T);
+  const int64_t ldz = 4 * HD;
+  if (dtype == MTGR_BF16) {
+    using bf = __nv_bfloat16;
+    const bf* z = static_cast<const bf*>(z_uqkv);
+    bf* dO = reinterpret_cast<bf*>(ws + w.dO);
+    REQUIRE(z == nullptr || ld_grad == ldz, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
+    MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const bf*>(dy), static_cast<const bf*>(o_saved),
+                                     static_cast<const bf*>(u), ld_in, ln_mean, ln_rstd, dO, static_cast<bf*>(du),
+                                     ld_grad, z, T, (int)HD, s),
+                  "attn_bwd gate");
+    MTGR_CUDA_TRY(launch_attn_bwd_bf16(static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
+                                       ld_in, dO, T, n_heads, d_h, plan, B, ts, reinterpret_cast<float*>(ws + w.dq_acc),
+                                       static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv), ld_grad,
+                                       z ? z + HD : nullptr, z ? z + 2 * HD : nullptr, z ? z + 3 * HD : nullptr,
+                                       status, s),
+                  "attn_bwd tcgen05");
+  } else {
+    const float* z = static_cast<const float*>(z_uqkv);
+    float* dO = reinterpret_cast<float*>(ws + w.dO);
+    REQUIRE(z == nullptr || ld_grad == ldz, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
+    MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const float*>(dy), static_cast<const float*>(o_saved),
+                                     static_cast<const float*>(u), ld_in, ln_mean, ln_rstd, dO,
+                                     static_cast<float*>(du), ld_grad, z, T, (int)HD, s),
+                  "attn_bwd gate");
+    MTGR_CUDA_TRY(launch_attn_f32_bwd(static_cast<const float*>(q), static_cast<const float*>(k),
+                                      static_cast<const float*>(v), ld_in, dO,
+                                      reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
+                                      static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
+                                      ld_grad, z ? z + HD : nullptr, z ? z + 2 * HD : nullptr,
+                                      z ? z + 3 * HD : nullptr, s),
+                  "attn_bwd fp32");
+  }
+  return MTGR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Layer
+// ---------------------------------------------------------------------------
+size_t mtgr_layer_workspace_size(int32_t B, int64_t T, int32_t d_model, int32_t n_heads, int32_t d_h,
+                                 mtgr_dtype dtype) {
+  if (B < 0 || T < 0 || d_model <= 0 || n_heads <= 0 || d_h <= 0) return 0;
+  return layer_ws(B, T, d_model, n_heads, d_h, dtype).total;
+}
+
+static mtgr_status check_layer(const mtgr_layer_weights* w, const int32_t* offsets, int32_t B, const uint8_t* gid,
+                               int64_t T, mtgr_dtype dtype, void* ws, size_t ws_bytes) {
+  REQUIRE(w != nullptr, MTGR_ERR_INVALID_ARG, "weights is NULL");
+  mtgr_status st = check_meta(offsets, B, gid, T);
+  if (st != MTGR_OK) return st;
+  const int D = w->d_model, H = w->n_heads, d = w->d_h;
+  REQUIRE(D > 0 && H > 0 && d > 0, MTGR_ERR_INVALID_ARG, "bad layer dims");
+  REQUIRE(D % 64 == 0 && D <= 4096 && (H * d) % 64 == 0, MTGR_ERR_UNSUPPORTED,
+          "d_model and H*d_h must be multiples of 64 (d_model <= 4096)");
+  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
+  if (dtype == MTGR_BF16) REQUIRE(d == 64 || d == 128, MTGR_ERR_UNSUPPORTED, "bf16 path supports d_h in {64, 128}");
+  REQUIRE(w->w_uqkv && w->w_o && w->gamma && w->beta, MTGR_ERR_INVALID_ARG, "NULL weight");
+  REQUIRE(aligned16(w->w_uqkv) && aligned16(w->w_o) && aligned16(w->gamma) && aligned16(w->beta),
+          MTGR_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+  REQUIRE(ws && aligned16(ws) && ws_bytes >= layer_ws(B, T, D, H, d, dtype).total, MTGR_ERR_WORKSPACE,
+          "workspace missing or smaller than mtgr_layer_workspace_size()");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void* x_out,
+                                const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
+                                const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
+                                size_t workspace_bytes, mtgr_stream_t stream) {
+  mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
+  if (st != MTGR_OK) return st;
+  REQUIRE(sv != nullptr, MTGR_ERR_INVALID_ARG, "saved is NULL");
+  REQUIRE(T == 0 || (x && x_out && sv->xn && sv->z && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
+                     sv->gln_rstd && sv->ln_mean && sv->ln_rstd && ts),
+          MTGR_ERR_INVALID_ARG, "NULL tensor");
+  REQUIRE(aligned16(x) && aligned16(x_out) && aligned16(sv->xn) && aligned16(sv->z) && aligned16(sv->uqkv) &&
+              aligned16(sv->o) && aligned16(sv->y),
+          MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const int D = w->d_model, H = w->n_heads, d = w->d_h;
+  const int64_t HD = (int64_t)H * d, N4 = 4 * HD;
+  const LayerWs L = layer_ws(B, T, D, H, d, dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.attn_base + L.attn.status);
+  if (T == 0) return MTGR_OK;
+  mtgr_status r;
+  r = mtgr_group_layernorm_fwd(x, sv->xn, sv->gln_mean, sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln,
+                               dtype, stream);
+  if (r != MTGR_OK) return r;
+  if (dtype == MTGR_BF16) {
+    using bf = __nv_bfloat16;
+    GemmArgs g{};
+    g.M = T; g.N = N4; g.K = D;
+    g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = false;
+    g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
+    g.epi = EPI_SILU; g.C = sv->uqkv; g.ldc = N4; g.Z = static_cast<bf*>(sv->z); g.ldz = N4;
+    g.splits = 1; g.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
+  } else {
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_SILU, T, N4, D, static_cast<const float*>(sv->xn), D, 1,
+                                  static_cast<const float*>(w->w_uqkv), N4, 1, static_cast<float*>(sv->uqkv), N4,
+                                  nullptr, 0, static_cast<float*>(sv->z), N4, s),
+                  "layer_fwd uqkv gemm");
+  }
+  const uint8_t* a = static_cast<const uint8_t*>(sv->uqkv);
+  const size_t es = esize(dtype);
+  r = mtgr_hstu_attn_fwd(a + HD * es, a + 2 * HD * es, a + 3 * HD * es, a, N4, offsets, B, gid, ts, T, H, d,
+                         w->eps_ln, sv->y, sv->o, sv->ln_mean, sv->ln_rstd, dtype, ws + L.attn_base, L.attn.total,
+                         stream);
+  if (r != MTGR_OK) return r;
+  if (dtype == MTGR_BF16) {
+    using bf = __nv_bfloat16;
+    GemmArgs g{};
+    g.M = T; g.N = D; g.K = HD;
+    g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = false;
+    g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = true;
+    g.epi = EPI_RESIDUAL; g.C = x_out; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
+    g.splits = 1; g.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
+  } else {
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_RESIDUAL, T, D, HD, static_cast<const float*>(sv->y), HD, 1,
+                                  static_cast<const float*>(w->w_o), D, 1, static_cast<float*>(x_out), D,
+                                  static_cast<const float*>(x), D, nullptr, 0, s),
+                  "layer_fwd out gemm");
+  }
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* sv,
+                                const void* dx_out, void* dx, const mtgr_layer_grads* gr, const int32_t* offsets,
+                                int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
+                                void* workspace, size_t workspace_bytes, mtgr_stream_t stream) {
+  mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
+  if (st != MTGR_OK) return st;
+  REQUIRE(sv && gr && gr->dw_uqkv && gr->dw_o && gr->dgamma && gr->dbeta, MTGR_ERR_INVALID_ARG,
+          "NULL saved / grads");
+  REQUIRE(T == 0 || (x && dx_out && dx && sv->xn && sv->z && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
+                     sv->gln_rstd && sv->ln_mean && sv->ln_rstd && ts),
+          MTGR_ERR_INVALID_ARG, "NULL tensor");
+  REQUIRE(aligned16(x) && aligned16(dx_out) && aligned16(dx), MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const int D = w->d_model, H = w->n_heads, d = w->d_h;
+  const int64_t HD = (int64_t)H * d, N4 = 4 * HD;
+  const LayerWs L = layer_ws(B, T, D, H, d, dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.attn_base + L.attn.status);
+  const size_t es = esize(dtype);
+  void* dY = ws + L.dY;
+  void* dZ = ws + L.dZ;
+  void* dxn = ws + L.dxn;
+  float* wpart = reinterpret_cast<float*>(ws + L.wpart);
+  if (T == 0) {
+    MTGR_CUDA_TRY(cudaMemsetAsync(gr->dw_uqkv, 0, sizeof(float) * D * N4, s), "layer_bwd zero");
+    MTGR_CUDA_TRY(cudaMemsetAsync(gr->dw_o, 0, sizeof(float) * HD * D, s), "layer_bwd zero");
+    MTGR_CUDA_TRY(cudaMemsetAsync(gr->dgamma, 0, sizeof(float) * 4 * D, s), "layer_bwd zero");
+    MTGR_CUDA_TRY(cudaMemsetAsync(gr->dbeta, 0, sizeof(float) * 4 * D, s), "layer_bwd zero");
+    return MTGR_OK;
+  }
+  using bf = __nv_bfloat16;
+  // 1. dY = dx' · W_oᵀ
+  if (dtype == MTGR_BF16) {
+    GemmArgs g{};
+    g.M = T; g.N = HD; g.K = D;
+    g.A = static_cast<const bf*>(dx_out); g.lda = D; g.a_mn_major = false;
+    g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = false;
+    g.epi = EPI_PLAIN; g.C = dY; g.ldc = HD; g.splits = 1; g.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dY gemm");
+  } else {
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, HD, D, static_cast<const float*>(dx_out), D, 1,
+                                  static_cast<const float*>(w->w_o), 1, D, static_cast<float*>(dY), HD, nullptr, 0,
+                                  nullptr, 0, s),
+                  "layer_bwd dY gemm");
+  }
+  // 2. dW_o = Yᵀ · dx'
+  if (dtype == MTGR_BF16) {
+    GemmArgs g{};
+    g.M = HD; g.N = D; g.K = T;
+    g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = true;
+    g.B = static_cast<const bf*>(dx_out); g.ldb = D; g.b_mn_major = true;
+    g.epi = EPI_F32; g.C = L.splits_o > 1 ? (void*)wpart : (void*)gr->dw_o; g.ldc = D;
+    g.splits = L.splits_o; g.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_o gemm");
+    if (L.splits_o > 1)
+      MTGR_CUDA_TRY(launch_split_reduce(wpart, L.splits_o, HD * D, HD * D, gr->dw_o, s), "layer_bwd dW_o reduce");
+  } else {
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, HD, D, T, static_cast<const float*>(sv->y), 1, HD,
+                                  static_cast<const float*>(dx_out), D, 1, gr->dw_o, D, nullptr, 0, nullptr, 0, s),
+                  "layer_bwd dW_o gemm");
+  }
+  // 3. attention backward with the SiLU backward of the projection fused: dZ = [dU|dQ|dK|dV] ⊙ silu'(z)
+  const uint8_t* a = static_cast<const uint8_t*>(sv->uqkv);
+  uint8_t* dz = static_cast<uint8_t*>(dZ);
+  mtgr_status r = mtgr_hstu_attn_bwd(dY, a + HD * es, a + 2 * HD * es, a + 3 * HD * es, a, N4, sv->o, sv->ln_mean,
+                                     sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD * es, dz + 2 * HD * es,
+                                     dz + 3 * HD * es, dz, N4, sv->z, dtype, ws + L.attn_base, L.attn.total, stream);
+  if (r != MTGR_OK) return r;
+  // 4. dW_uqkv = xnᵀ · dZ ;  5. dxn = dZ · W_uqkvᵀ
+  if (dtype == MTGR_BF16) {
+    GemmArgs g{};
+    g.M = D; g.N = N4; g.K = T;
+    g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = true;
+    g.B = static_cast<const bf*>(dZ); g.ldb = N4; g.b_mn_major = true;
+    g.epi = EPI_F32; g.C = L.splits_uqkv > 1 ? (void*)wpart : (void*)gr->dw_uqkv; g.ldc = N4;
+    g.splits = L.splits_uqkv; g.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_uqkv gemm");
+    if (L.splits_uqkv > 1)
+      MTGR_CUDA_TRY(launch_split_reduce(wpart, L.splits_uqkv, (int64_t)D * N4, (int64_t)D * N4, gr->dw_uqkv, s),
+                    "layer_bwd dW_uqkv reduce");
+    GemmArgs h{};
+    h.M = T; h.N = D; h.K = N4;
+    h.A = static_cast<const bf*>(dZ); h.lda = N4; h.a_mn_major = false;
+    h.B = static_cast<const bf*>(w->w_uqkv); h.ldb = N4; h.b_mn_major = false;
+    h.epi = EPI_PLAIN; h.C = dxn; h.ldc = D; h.splits = 1; h.status = status;
+    MTGR_CUDA_TRY(launch_gemm_bf16(h, s), "layer_bwd dxn gemm");
+  } else {
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, D, N4, T, static_cast<const float*>(sv->xn), 1, D,
+                                  static_cast<const float*>(dZ), N4, 1, gr->dw_uqkv, N4, nullptr, 0, nullptr, 0, s),
+                  "layer_bwd dW_uqkv gemm");
+    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, D, N4, static_cast<const float*>(dZ), N4, 1,
+                                  static_cast<const float*>(w->w_uqkv), 1, N4, static_cast<float*>(dxn), D, nullptr,
+                                  0, nullptr, 0, s),
+                  "layer_bwd dxn gemm");
+  }
+  // 6. GLN backward + residual path
+  return mtgr_group_layernorm_bwd(dxn, x, sv->gln_mean, sv->gln_rstd, gid, w->gamma, dx_out, dx, gr->dgamma,
+                                  gr->dbeta, T, D, dtype, ws + L.gln_part,
+                                  mtgr_group_layernorm_bwd_workspace_size(T, D), stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,346 @@
+// norm.cu -- the two row-normalisation steps of the HSTU layer, forward and
+// backward.  Both are HBM-bound: one warp streams one row with 16-byte
+// vector accesses, statistics are warp-reduced in fp32.
+//
+//  * Group LayerNorm (fun-rec chapter 7.3, §7.3.3; paper-daily "模型怎么搭"):
+//      y = (x - μ)·rstd·γ_g + β_g, statistics per token over D features,
+//      γ_g/β_g selected by the token's group id.
+//  * Gate (paper-daily "模型怎么搭": normalise the aggregate, multiply by U):
+//      Y = LayerNorm(O) ⊙ U over the H·d_h features of a token, no affine.
+#include "common.cuh"
+
+namespace mtgr {
+
+// 8 consecutive elements <-> 8 floats (one 16-byte vector for bf16, two for fp32)
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 r;
+  r.x = pack_bf16x2(v[0], v[1]);
+  r.y = pack_bf16x2(v[2], v[3]);
+  r.z = pack_bf16x2(v[4], v[5]);
+  r.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = r;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Lane `lane` owns 8-element chunks c = lane + 32*m (m < NCH) of a row of n features.
+#define ROW_CHUNKS_FOR(m, c, lane, n) \
+  _Pragma("unroll") for (int m = 0; m < NCH; ++m) if (const int c = (lane) + 32 * m; 8 * c < (n))
+
+// ---------------------------------------------------------------------------
+// Group LayerNorm
+// ---------------------------------------------------------------------------
+template <typename T, int NCH>
+__global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T* __restrict__ y,
+                                                      float* __restrict__ mean, float* __restrict__ rstd,
+                                                      const uint8_t* __restrict__ gid,
+                                                      const float* __restrict__ gamma,
+                                                      const float* __restrict__ beta, int64_t rows, int D,
+                                                      float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    float v[NCH][8];
+    float s = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      load8(x + r * D + 8 * c, v[m]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[m][i];
+    }
+    const float mu = warp_sum(s) / (float)D;
+    float q = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d = v[m][i] - mu;
+        q += d * d;
+      }
+    }
+    const float rs = rsqrtf(warp_sum(q) / (float)D + eps);
+    const int g = min((int)gid[r], 3);
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float ga[8], be[8], o[8];
+      load8(gamma + (int64_t)g * D + 8 * c, ga);
+      load8(beta + (int64_t)g * D + 8 * c, be);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (v[m][i] - mu) * rs * ga[i] + be[i];
+      store8(y + r * D + 8 * c, o);
+    }
+    if (lane == 0) {
+      if (mean) mean[r] = mu;
+      if (rstd) rstd[r] = rs;
+    }
+  }
+}
+
+// dx = rstd (dŷ - mean(dŷ) - x̂ mean(dŷ x̂)) (+ dres), dŷ = dy ⊙ γ_g;
+// per-block partial sums of dy ⊙ x̂ and dy per group go to `partial`
+// ([gridDim.x][2][4][D] fp32), reduced by gln_param_reduce_kernel.
+template <typename T, int NCH>
+__global__ void __launch_bounds__(256) gln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                      const float* __restrict__ mean,
+                                                      const float* __restrict__ rstd,
+                                                      const uint8_t* __restrict__ gid,
+                                                      const float* __restrict__ gamma,
+                                                      const T* __restrict__ dres, T* __restrict__ dx,
+                                                      float* __restrict__ partial, int64_t rows, int D) {
+  extern __shared__ float acc[];  // [2][4][D]
+  for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) acc[i] = 0.f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const float mu = mean[r], rs = rstd[r];
+    const int g = min((int)gid[r], 3);
+    float xh[NCH][8], gy[NCH][8];
+    float s1 = 0.f, s2 = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float xv[8], dv[8], ga[8];
+      load8(x + r * D + 8 * c, xv);
+      load8(dy + r * D + 8 * c, dv);
+      load8(gamma + (int64_t)g * D + 8 * c, ga);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xh[m][i] = (xv[i] - mu) * rs;
+        gy[m][i] = dv[i] * ga[i];
+        s1 += gy[m][i];
+        s2 += gy[m][i] * xh[m][i];
+        atomicAdd(&acc[(0 * 4 + g) * D + 8 * c + i], dv[i] * xh[m][i]);
+        atomicAdd(&acc[(1 * 4 + g) * D + 8 * c + i], dv[i]);
+      }
+    }
+    const float m1 = warp_sum(s1) / (float)D, m2 = warp_sum(s2) / (float)D;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = rs * (gy[m][i] - m1 - xh[m][i] * m2);
+      if (dres) {
+        float rv[8];
+        load8(dres + r * D + 8 * c, rv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] += rv[i];
+      }
+      store8(dx + r * D + 8 * c, o);
+    }
+  }
+  __syncthreads();
+  float* out = partial + (int64_t)blockIdx.x * 8 * D;
+  for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) out[i] = acc[i];
+}
+
+// dgamma[g][f] / dbeta[g][f] = sum over blocks of the partials (fixed order).
+__global__ void gln_param_reduce_kernel(const float* __restrict__ partial, int nblocks, int D,
+                                        float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over [2][4][D]
+  if (i >= 8 * D) return;
+  float s = 0.f;
+  for (int b = 0; b < nblocks; ++b) s += partial[(int64_t)b * 8 * D + i];
+  if (i < 4 * D)
+    dgamma[i] = s;
+  else
+    dbeta[i - 4 * D] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Gate: Y = LayerNorm(O) ⊙ U
+// ---------------------------------------------------------------------------
+template <typename T, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const T* __restrict__ O, const T* __restrict__ U,
+                                                          int64_t ldu, T* __restrict__ Y,
+                                                          float* __restrict__ mean, float* __restrict__ rstd,
+                                                          int64_t rows, int n, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    float v[NCH][8];
+    float s = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, n) {
+      load8(O + r * n + 8 * c, v[m]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[m][i];
+    }
+    const float mu = warp_sum(s) / (float)n;
+    float q = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, n) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d = v[m][i] - mu;
+        q += d * d;
+      }
+    }
+    const float rs = rsqrtf(warp_sum(q) / (float)n + eps);
+    ROW_CHUNKS_FOR(m, c, lane, n) {
+      float u[8], o[8];
+      load8(U + r * ldu + 8 * c, u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (v[m][i] - mu) * rs * u[i];
+      store8(Y + r * n + 8 * c, o);
+    }
+    if (lane == 0) {
+      mean[r] = mu;
+      rstd[r] = rs;
+    }
+  }
+}
+
+// dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ silu'(z_u) when z given).
+template <typename T, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const T* __restrict__ dY, const T* __restrict__ O,
+                                                          const T* __restrict__ U, int64_t ldu,
+                                                          const float* __restrict__ mean,
+                                                          const float* __restrict__ rstd, T* __restrict__ dO,
+                                                          T* __restrict__ dU, int64_t ldg,
+                                                          const T* __restrict__ z, int64_t rows, int n) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const float mu = mean[r], rs = rstd[r];
+    float oh[NCH][8], g[NCH][8];
+    float s1 = 0.f, s2 = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, n) {
+      float ov[8], dv[8], uv[8], du[8];
+      load8(O + r * n + 8 * c, ov);
+      load8(dY + r * n + 8 * c, dv);
+      load8(U + r * ldu + 8 * c, uv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        oh[m][i] = (ov[i] - mu) * rs;
+        g[m][i] = dv[i] * uv[i];
+        s1 += g[m][i];
+        s2 += g[m][i] * oh[m][i];
+        du[i] = dv[i] * oh[m][i];
+      }
+      if (z) {
+        float zv[8];
+        load8(z + r * ldg + 8 * c, zv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float sg = sigmoid_f(zv[i]);
+          du[i] *= sg * (1.f + zv[i] * (1.f - sg));
+        }
+      }
+      store8(dU + r * ldg + 8 * c, du);
+    }
+    const float m1 = warp_sum(s1) / (float)n, m2 = warp_sum(s2) / (float)n;
+    ROW_CHUNKS_FOR(m, c, lane, n) {
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = rs * (g[m][i] - m1 - oh[m][i] * m2);
+      store8(dO + r * n + 8 * c, o);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static int row_blocks(int64_t rows) {
+  const int64_t want = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+#define NCH_DISPATCH(n, KERNEL_CALL)                   \
+  do {                                                 \
+    const int nch__ = ((n) + 255) / 256;               \
+    if (nch__ <= 1) {                                  \
+      constexpr int NCHV = 1;                          \
+      KERNEL_CALL;                                     \
+    } else if (nch__ <= 2) {                           \
+      constexpr int NCHV = 2;                          \
+      KERNEL_CALL;                                     \
+    } else if (nch__ <= 4) {                           \
+      constexpr int NCHV = 4;                          \
+      KERNEL_CALL;                                     \
+    } else if (nch__ <= 8) {                           \
+      constexpr int NCHV = 8;                          \
+      KERNEL_CALL;                                     \
+    } else {                                           \
+      constexpr int NCHV = 16;                         \
+      KERNEL_CALL;                                     \
+    }                                                  \
+  } while (0)
+
+template <typename T>
+cudaError_t launch_gln_fwd(const T* x, T* y, float* mean, float* rstd, const uint8_t* gid, const float* gamma,
+                           const float* beta, int64_t rows, int D, float eps, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  NCH_DISPATCH(D, (gln_fwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(x, y, mean, rstd, gid, gamma, beta,
+                                                                            rows, D, eps)));
+  return cudaGetLastError();
+}
+
+int gln_bwd_blocks(int64_t rows) {
+  const int64_t want = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms() * 2;
+  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+template <typename T>
+cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const float* rstd, const uint8_t* gid,
+                           const float* gamma, const T* dres, T* dx, float* dgamma, float* dbeta, float* partial,
+                           int64_t rows, int D, cudaStream_t s) {
+  const int nb = gln_bwd_blocks(rows);
+  const size_t smem = (size_t)8 * D * sizeof(float);
+  NCH_DISPATCH(D, ({
+                 auto k = gln_bwd_kernel<T, NCHV>;
+                 cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                 k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D);
+               }));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gln_param_reduce_kernel<<<(8 * D + 255) / 256, 256, 0, s>>>(partial, nb, D, dgamma, dbeta);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_ln_gate_fwd(const T* O, const T* U, int64_t ldu, T* Y, float* mean, float* rstd, int64_t rows,
+                               int n, float eps, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  NCH_DISPATCH(n, (ln_gate_fwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd, rows,
+                                                                                n, eps)));
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_ln_gate_bwd(const T* dY, const T* O, const T* U, int64_t ldu, const float* mean,
+                               const float* rstd, T* dO, T* dU, int64_t ldg, const T* z, int64_t rows, int n,
+                               cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  NCH_DISPATCH(n, (ln_gate_bwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(dY, O, U, ldu, mean, rstd, dO,
+                                                                                dU, ldg, z, rows, n)));
+  return cudaGetLastError();
+}
+
+#define INSTANTIATE(T)                                                                                        \
+  template cudaError_t launch_gln_fwd<T>(const T*, T*, float*, float*, const uint8_t*, const float*,           \
+                                         const float*, int64_t, int, float, cudaStream_t);                    \
+  template cudaError_t launch_gln_bwd<T>(const T*, const T*, const float*, const float*, const uint8_t*,       \
+                                         const float*, const T*, T*, float*, float*, float*, int64_t, int,     \
+                                         cudaStream_t);                                                       \
+  template cudaError_t launch_ln_gate_fwd<T>(const T*, const T*, int64_t, T*, float*, float*, int64_t, int,    \
+                                             float, cudaStream_t);                                            \
+  template cudaError_t launch_ln_gate_bwd<T>(const T*, const T*, const T*, int64_t, const float*,              \
+                                             const float*, T*, T*, int64_t, const T*, int64_t, int,           \
+                                             cudaStream_t);
+INSTANTIATE(float)
+INSTANTIATE(__nv_bfloat16)
+
+}  // namespace mtgr

@@ -1,0 +1,193 @@
+// plan.cu -- batch metadata on the device: validation, per-user group
+// boundaries, integer visible-pair counts, and the longest-first ordered list
+// of jagged attention tiles (see plan.cuh for the tile rule).
+#include "common.cuh"
+#include "plan.cuh"
+
+namespace mtgr {
+
+// One warp per user: clamp the segment to [0, T], find the first RealTime and
+// first candidate token, and (optionally) check the metadata.
+__global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B, const uint8_t* __restrict__ gid,
+                                 int64_t T, UserInfo* __restrict__ users, int32_t* __restrict__ status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= B) return;
+  const int b = warp;
+  int64_t s0 = offsets[b], s1 = offsets[b + 1];
+  int32_t bits = 0;
+  if (b == 0 && s0 != 0) bits |= DEV_ERR_OFFSETS;
+  if (b == B - 1 && s1 != T) bits |= DEV_ERR_OFFSETS;
+  if (s1 < s0) bits |= DEV_ERR_OFFSETS;
+  s0 = s0 < 0 ? 0 : (s0 > T ? T : s0);
+  s1 = s1 < s0 ? s0 : (s1 > T ? T : s1);
+  const int n = (int)(s1 - s0);
+  int eS = n, eR = n;
+  int prev_last = 0;  // group of the last token of the previous chunk
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const int g = (i < n) ? (int)gid[s0 + i] : 3;
+    if (g > 3) bits |= DEV_ERR_GROUP_ID;
+    const int gp = __shfl_up_sync(0xffffffffu, g, 1);
+    const int prev = lane == 0 ? prev_last : gp;
+    if (i < n && g < prev) bits |= DEV_ERR_GROUP_ORDER;
+    const unsigned rt = __ballot_sync(0xffffffffu, i < n && g >= 2);
+    const unsigned cd = __ballot_sync(0xffffffffu, i < n && g >= 3);
+    if (rt && eS == n) eS = base + __ffs(rt) - 1;
+    if (cd && eR == n) eR = base + __ffs(cd) - 1;
+    prev_last = __shfl_sync(0xffffffffu, g, 31);
+  }
+  if (eR < eS) eR = eS;  // only with a bad group order; keeps eS <= eR <= n
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  if (lane == 0) {
+    if (users) users[b] = UserInfo{(int32_t)s0, n, eS, eR};
+    if (status && bits) atomicOr(status, bits);
+  }
+}
+
+// One block: bucket every query tile (forward) and key tile (backward) by the
+// number of tiles it pairs with, then scatter into lists ordered longest first.
+__global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B,
+                                                          int32_t* __restrict__ counts,
+                                                          WorkItem* __restrict__ fwd_items,
+                                                          WorkItem* __restrict__ bwd_items, int64_t max_items,
+                                                          int32_t* __restrict__ status) {
+  __shared__ int32_t hist[2][kBuckets];
+  __shared__ int32_t tot[2];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 2 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += blockDim.x) {
+    const UserInfo u = users[b];
+    const int nt = ceil_div(u.n, kTile);
+    for (int t = 0; t < nt; ++t) {
+      const int cf = min(qtile_keys(u, t).count(), kBuckets - 1);
+      const int cb = min(ktile_queries(u, t).count(), kBuckets - 1);
+      atomicAdd(&hist[0][cf], 1);
+      atomicAdd(&hist[1][cb], 1);
+    }
+  }
+  __syncthreads();
+  // exclusive scan from the most expensive bucket down (two warps, one per list)
+  if (tid < 64) {
+    const int list = tid >> 5, lane = tid & 31;
+    int running = 0;
+    for (int base = kBuckets - 1; base >= 0; base -= 32) {
+      const int c = base - lane;
+      const int v = c >= 0 ? hist[list][c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (c >= 0) hist[list][c] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tot[list] = running;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += blockDim.x) {
+    const UserInfo u = users[b];
+    const int nt = ceil_div(u.n, kTile);
+    for (int t = 0; t < nt; ++t) {
+      const int cf = min(qtile_keys(u, t).count(), kBuckets - 1);
+      const int cb = min(ktile_queries(u, t).count(), kBuckets - 1);
+      const int pf = atomicAdd(&hist[0][cf], 1);
+      const int pb = atomicAdd(&hist[1][cb], 1);
+      if (pf < max_items) fwd_items[pf] = WorkItem{b, t};
+      if (pb < max_items) bwd_items[pb] = WorkItem{b, t};
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    counts[0] = tot[0];
+    counts[1] = tot[1];
+    if ((tot[0] > max_items || tot[1] > max_items) && status) atomicOr(status, DEV_ERR_PLAN);
+  }
+}
+
+// Visible keys per row: User/Seq keys (eS of them) for everyone, plus the
+// RealTime keys allowed by the timestamp rule, plus itself for a candidate.
+// One block per user; the block finds its own group boundaries.
+__global__ void visible_counts_kernel(const int32_t* __restrict__ offsets, const uint8_t* __restrict__ gid,
+                                      const int64_t* __restrict__ ts, int64_t T, int32_t* __restrict__ cnt,
+                                      unsigned long long* __restrict__ total) {
+  __shared__ int eS_s, eR_s;
+  __shared__ unsigned long long part[32];
+  int64_t s0 = offsets[blockIdx.x], s1 = offsets[blockIdx.x + 1];
+  s0 = s0 < 0 ? 0 : (s0 > T ? T : s0);
+  s1 = s1 < s0 ? s0 : (s1 > T ? T : s1);
+  const int n = (int)(s1 - s0);
+  if (threadIdx.x == 0) {
+    eS_s = n;
+    eR_s = n;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+    const int g = gid[s0 + r];
+    if (g >= 2) atomicMin(&eS_s, r);
+    if (g >= 3) atomicMin(&eR_s, r);
+  }
+  __syncthreads();
+  const int eS = eS_s, eR = max(eR_s, eS_s);
+  unsigned long long local = 0;
+  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+    int c;
+    if (r < eS) {
+      c = eS;
+    } else {
+      const int64_t ti = ts[s0 + r];
+      const bool cand = r >= eR;
+      c = eS + (cand ? 1 : 0);
+      for (int j = eS; j < eR; ++j) {
+        const int64_t tj = ts[s0 + j];
+        c += cand ? (tj < ti) : (tj <= ti);
+      }
+    }
+    cnt[s0 + r] = c;
+    local += (unsigned long long)c;
+  }
+  for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long sum = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) sum += part[w];
+    atomicAdd(total, sum);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host wrappers (internal)
+// ---------------------------------------------------------------------------
+cudaError_t launch_user_info(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, UserInfo* users,
+                             int32_t* status, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (int)(((int64_t)B * 32 + threads - 1) / threads);
+  user_info_kernel<<<blocks, threads, 0, s>>>(offsets, B, gid, T, users, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, int32_t* ws,
+                        int32_t* status, cudaStream_t s) {
+  const PlanLayout L = plan_layout(B, T);
+  UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
+  cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s);
+  if (e != cudaSuccess) return e;
+  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
+                                       reinterpret_cast<WorkItem*>(ws + L.bwd_items), L.max_items, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_visible_counts(const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                                  int64_t T, int32_t* cnt, int64_t* total, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(total, 0, sizeof(int64_t), s);
+  if (e != cudaSuccess) return e;
+  if (B <= 0) return cudaSuccess;
+  visible_counts_kernel<<<B, 256, 0, s>>>(offsets, gid, ts, T, cnt, reinterpret_cast<unsigned long long*>(total));
+  return cudaGetLastError();
+}
+
+}  // namespace mtgr

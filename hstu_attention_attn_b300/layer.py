@@ -1,0 +1,126 @@
+"""User-facing helpers around the C ABI: device batches, the attention op and
+one HSTU layer, with buffers allocated through torch (device memory only).
+
+Every computation runs in libmtgr.so; this module allocates outputs and
+workspace and forwards pointers (see ``mtgr.py``).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import mtgr
+
+
+@dataclass
+class DeviceBatch:
+    offsets: torch.Tensor   # int32 [B+1]
+    gid: torch.Tensor       # uint8 [T]
+    ts: torch.Tensor        # int64 [T]
+    B: int
+    T: int
+
+
+def device_batch(batch, device="cuda", pin=False) -> DeviceBatch:
+    """Copy a host batch (offsets / gid / ts numpy arrays) to the device."""
+    def mk(a, dt):
+        t = torch.from_numpy(np.ascontiguousarray(a)).to(dt)
+        if pin:
+            t = t.pin_memory()
+        return t.to(device, non_blocking=pin)
+    return DeviceBatch(mk(batch.offsets, torch.int32), mk(batch.gid, torch.uint8), mk(batch.ts, torch.int64),
+                       len(batch.offsets) - 1, int(batch.offsets[-1]))
+
+
+def _dt(dtype):
+    return mtgr.MTGR_BF16 if dtype == torch.bfloat16 else mtgr.MTGR_F32
+
+
+def workspace(nbytes, device="cuda"):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class HstuAttention:
+    """Y = LayerNorm(A·V) ⊙ U with A = M ⊙ silu(QKᵀ/sqrt(d_h)) / n_u (jagged, per head)."""
+
+    def __init__(self, n_heads, d_h, dtype=torch.bfloat16, eps=1e-5, device="cuda"):
+        self.H, self.dh, self.dtype, self.eps, self.device = n_heads, d_h, dtype, eps, device
+        self._ws = None
+
+    def _workspace(self, db):
+        n = mtgr.mtgr_attn_workspace_size(db.B, db.T, self.H, self.dh, _dt(self.dtype))
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = workspace(n, self.device)
+        return self._ws
+
+    def forward(self, q, k, v, u, db: DeviceBatch, ld=None):
+        T, HD = db.T, self.H * self.dh
+        ld = ld if ld is not None else q.stride(0)
+        y = torch.empty(T, HD, dtype=self.dtype, device=self.device)
+        o = torch.empty(T, HD, dtype=self.dtype, device=self.device)
+        mean = torch.empty(T, dtype=torch.float32, device=self.device)
+        rstd = torch.empty(T, dtype=torch.float32, device=self.device)
+        mtgr.mtgr_hstu_attn_fwd(q, k, v, u, ld, db.offsets, db.gid, db.ts, T, self.H, self.dh, self.eps, y, o,
+                                mean, rstd, self._workspace(db))
+        return y, (o, mean, rstd)
+
+    def backward(self, dy, q, k, v, u, saved, db: DeviceBatch, ld=None, z_uqkv=None, grads=None):
+        T, HD = db.T, self.H * self.dh
+        ld = ld if ld is not None else q.stride(0)
+        o, mean, rstd = saved
+        if grads is None:
+            g = torch.empty(T, 4 * HD, dtype=self.dtype, device=self.device)
+            du, dq, dk, dv = g[:, :HD], g[:, HD:2 * HD], g[:, 2 * HD:3 * HD], g[:, 3 * HD:]
+        else:
+            dq, dk, dv, du = grads
+        mtgr.mtgr_hstu_attn_bwd(dy, q, k, v, u, ld, o, mean, rstd, db.offsets, db.gid, db.ts, T, self.H, self.dh,
+                                dq, dk, dv, du, dq.stride(0), z_uqkv, self._workspace(db))
+        return dq, dk, dv, du
+
+
+class HstuLayer:
+    """One HSTU layer: x' = x + (LN(attn(silu(GLN(x) W_uqkv))) ⊙ U) W_o, forward and backward."""
+
+    def __init__(self, d_model, n_heads, d_h, w_uqkv, w_o, gamma, beta, dtype=torch.bfloat16, eps_gln=1e-5,
+                 eps_ln=1e-5, device="cuda"):
+        self.D, self.H, self.dh, self.dtype, self.device = d_model, n_heads, d_h, dtype, device
+        to = dict(device=device)
+        self.w_uqkv = torch.as_tensor(w_uqkv).to(dtype=dtype, **to).contiguous()
+        self.w_o = torch.as_tensor(w_o).to(dtype=dtype, **to).contiguous()
+        self.gamma = torch.as_tensor(gamma).to(dtype=torch.float32, **to).contiguous()
+        self.beta = torch.as_tensor(beta).to(dtype=torch.float32, **to).contiguous()
+        self.weights = mtgr.make_weights(d_model, n_heads, d_h, self.w_uqkv, self.w_o, self.gamma, self.beta,
+                                         eps_gln, eps_ln)
+        self._ws = None
+
+    def _workspace(self, db):
+        n = mtgr.mtgr_layer_workspace_size(db.B, db.T, self.D, self.H, self.dh, _dt(self.dtype))
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = workspace(n, self.device)
+        return self._ws
+
+    def alloc_saved(self, T):
+        HD = self.H * self.dh
+        e = lambda *s: torch.empty(*s, dtype=self.dtype, device=self.device)
+        f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
+        return dict(xn=e(T, self.D), z=e(T, 4 * HD), uqkv=e(T, 4 * HD), o=e(T, HD), y=e(T, HD),
+                    gln_mean=f(T), gln_rstd=f(T), ln_mean=f(T), ln_rstd=f(T))
+
+    def forward(self, x, db: DeviceBatch, saved=None, x_out=None):
+        saved = saved if saved is not None else self.alloc_saved(db.T)
+        x_out = x_out if x_out is not None else torch.empty_like(x)
+        mtgr.mtgr_hstu_layer_fwd(self.weights, x, x_out, mtgr.make_saved(saved), db.offsets, db.gid, db.ts, db.T,
+                                 self._workspace(db))
+        return x_out, saved
+
+    def backward(self, x, saved, dx_out, db: DeviceBatch, dx=None, grads=None):
+        HD = self.H * self.dh
+        dx = dx if dx is not None else torch.empty_like(x)
+        if grads is None:
+            f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
+            grads = dict(dw_uqkv=f(self.D, 4 * HD), dw_o=f(HD, self.D), dgamma=f(4, self.D), dbeta=f(4, self.D))
+        mtgr.mtgr_hstu_layer_bwd(self.weights, x, mtgr.make_saved(saved), dx_out, dx, mtgr.make_grads(grads),
+                                 db.offsets, db.gid, db.ts, db.T, self._workspace(db))
+        return dx, grads

@@ -1,0 +1,210 @@
+"""Thin Python binding of libmtgr.so (the C ABI declared in include/mtgr.h).
+
+Argument marshalling only: every function has the same name as its C entry
+point, takes torch tensors (device memory owned by the caller) and passes their
+data pointers and the current CUDA stream through.  All compute runs in the
+library's CUDA kernels.  There is no fallback: if libmtgr.so cannot be loaded,
+``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmtgr.so")
+
+MTGR_F32, MTGR_BF16 = 0, 1
+STATUS_BAD_OFFSETS, STATUS_BAD_GROUP_ORDER, STATUS_BAD_GROUP_ID, STATUS_TIMEOUT = 1, 2, 4, 8
+
+_lib = None
+
+
+class MtgrError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [("d_model", C.c_int32), ("n_heads", C.c_int32), ("d_h", C.c_int32),
+                ("w_uqkv", C.c_void_p), ("w_o", C.c_void_p), ("gamma", C.c_void_p), ("beta", C.c_void_p),
+                ("eps_gln", C.c_float), ("eps_ln", C.c_float)]
+
+
+class LayerSaved(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("xn", "z", "uqkv", "o", "y", "gln_mean", "gln_rstd",
+                                          "ln_mean", "ln_rstd")]
+
+
+class LayerGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("dw_uqkv", "dw_o", "dgamma", "dbeta")]
+
+
+EXPORTS = {
+    # name: (restype, argtypes)
+    "mtgr_last_error": (C.c_char_p, []),
+    "mtgr_version": (C.c_int, []),
+    "mtgr_validate_batch": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
+    "mtgr_debug_visible_counts": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64,
+                                            C.c_void_p, C.c_void_p, C.c_void_p]),
+    "mtgr_group_layernorm_fwd": (C.c_int, [C.c_void_p] * 7 + [C.c_int64, C.c_int32, C.c_float, C.c_int,
+                                                               C.c_void_p]),
+    "mtgr_group_layernorm_bwd_workspace_size": (C.c_size_t, [C.c_int64, C.c_int32]),
+    "mtgr_group_layernorm_bwd": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p,
+                                                                C.c_size_t, C.c_void_p]),
+    "mtgr_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int]),
+    "mtgr_hstu_attn_fwd": (C.c_int, [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+                                                         C.c_int64, C.c_int32, C.c_int32, C.c_float]
+                           + [C.c_void_p] * 4 + [C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "mtgr_hstu_attn_bwd": (C.c_int, [C.c_void_p] * 5 + [C.c_int64] + [C.c_void_p] * 3
+                           + [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_int32]
+                           + [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t,
+                                                 C.c_void_p]),
+    "mtgr_layer_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
+    "mtgr_hstu_layer_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.c_void_p, C.POINTER(LayerSaved),
+                                      C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int,
+                                      C.c_void_p, C.c_size_t, C.c_void_p]),
+    "mtgr_hstu_layer_bwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.POINTER(LayerSaved), C.c_void_p,
+                                      C.c_void_p, C.POINTER(LayerGrads), C.c_void_p, C.c_int32, C.c_void_p,
+                                      C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+}
+
+
+def lib():
+    """Load libmtgr.so (built in-tree by hstu_attention_attn_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m hstu_attention_attn_b300.build`")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return MTGR_BF16
+    if t.dtype == torch.float32:
+        return MTGR_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(fn, code):
+    if code != 0:
+        raise MtgrError(fn, code, lib().mtgr_last_error().decode())
+
+
+def mtgr_last_error() -> str:
+    return lib().mtgr_last_error().decode()
+
+
+def mtgr_version() -> int:
+    return lib().mtgr_version()
+
+
+def mtgr_validate_batch(offsets, gid, T, status_word, stream=None):
+    _check("mtgr_validate_batch", lib().mtgr_validate_batch(_p(offsets), offsets.numel() - 1, _p(gid), T,
+                                                            _p(status_word), _stream(stream)))
+
+
+def mtgr_debug_visible_counts(offsets, gid, ts, T, cnt, total_pairs, stream=None):
+    _check("mtgr_debug_visible_counts",
+           lib().mtgr_debug_visible_counts(_p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, _p(cnt),
+                                           _p(total_pairs), _stream(stream)))
+
+
+def mtgr_group_layernorm_fwd(x, y, mean, rstd, gid, gamma, beta, eps=1e-5, stream=None):
+    T, D = x.shape
+    _check("mtgr_group_layernorm_fwd",
+           lib().mtgr_group_layernorm_fwd(_p(x), _p(y), _p(mean), _p(rstd), _p(gid), _p(gamma), _p(beta), T, D,
+                                          eps, _dtype(x), _stream(stream)))
+
+
+def mtgr_group_layernorm_bwd_workspace_size(T, D) -> int:
+    return lib().mtgr_group_layernorm_bwd_workspace_size(T, D)
+
+
+def mtgr_group_layernorm_bwd(dy, x, mean, rstd, gid, gamma, dx_residual, dx, dgamma, dbeta, workspace, stream=None):
+    T, D = x.shape
+    _check("mtgr_group_layernorm_bwd",
+           lib().mtgr_group_layernorm_bwd(_p(dy), _p(x), _p(mean), _p(rstd), _p(gid), _p(gamma), _p(dx_residual),
+                                          _p(dx), _p(dgamma), _p(dbeta), T, D, _dtype(x), _p(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_attn_workspace_size(B, T, n_heads, d_h, dtype) -> int:
+    return lib().mtgr_attn_workspace_size(B, T, n_heads, d_h, dtype)
+
+
+def mtgr_hstu_attn_fwd(q, k, v, u, ld_in, offsets, gid, ts, T, n_heads, d_h, eps, y, o_saved, ln_mean, ln_rstd,
+                       workspace, stream=None):
+    _check("mtgr_hstu_attn_fwd",
+           lib().mtgr_hstu_attn_fwd(_p(q), _p(k), _p(v), _p(u), ld_in, _p(offsets), offsets.numel() - 1, _p(gid),
+                                    _p(ts), T, n_heads, d_h, eps, _p(y), _p(o_saved), _p(ln_mean), _p(ln_rstd),
+                                    _dtype(y), _p(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
+
+
+def mtgr_hstu_attn_bwd(dy, q, k, v, u, ld_in, o_saved, ln_mean, ln_rstd, offsets, gid, ts, T, n_heads, d_h,
+                       dq, dk, dv, du, ld_grad, z_uqkv, workspace, stream=None):
+    _check("mtgr_hstu_attn_bwd",
+           lib().mtgr_hstu_attn_bwd(_p(dy), _p(q), _p(k), _p(v), _p(u), ld_in, _p(o_saved), _p(ln_mean),
+                                    _p(ln_rstd), _p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, n_heads,
+                                    d_h, _p(dq), _p(dk), _p(dv), _p(du), ld_grad, _p(z_uqkv), _dtype(dy),
+                                    _p(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
+
+
+def mtgr_layer_workspace_size(B, T, d_model, n_heads, d_h, dtype) -> int:
+    return lib().mtgr_layer_workspace_size(B, T, d_model, n_heads, d_h, dtype)
+
+
+def make_weights(d_model, n_heads, d_h, w_uqkv, w_o, gamma, beta, eps_gln=1e-5, eps_ln=1e-5) -> LayerWeights:
+    return LayerWeights(d_model, n_heads, d_h, _p(w_uqkv), _p(w_o), _p(gamma), _p(beta), eps_gln, eps_ln)
+
+
+def make_saved(d) -> LayerSaved:
+    return LayerSaved(*[_p(d[n]) for n, _ in LayerSaved._fields_])
+
+
+def make_grads(d) -> LayerGrads:
+    return LayerGrads(*[_p(d[n]) for n, _ in LayerGrads._fields_])
+
+
+def mtgr_hstu_layer_fwd(weights: LayerWeights, x, x_out, saved: LayerSaved, offsets, gid, ts, T, workspace,
+                        stream=None):
+    _check("mtgr_hstu_layer_fwd",
+           lib().mtgr_hstu_layer_fwd(C.byref(weights), _p(x), _p(x_out), C.byref(saved), _p(offsets),
+                                     offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_hstu_layer_bwd(weights: LayerWeights, x, saved: LayerSaved, dx_out, dx, grads: LayerGrads, offsets, gid,
+                        ts, T, workspace, stream=None):
+    _check("mtgr_hstu_layer_bwd",
+           lib().mtgr_hstu_layer_bwd(C.byref(weights), _p(x), C.byref(saved), _p(dx_out), _p(dx), C.byref(grads),
+                                     _p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x),
+                                     _p(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))

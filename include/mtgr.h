@@ -1,0 +1,222 @@
+/*
+ * mtgr.h -- C ABI of libmtgr.so: one MTGR HSTU layer (Group LayerNorm, UQKV
+ * projection + SiLU, jagged HSTU attention under the dynamic mixed mask,
+ * LayerNorm(O) ⊙ U, output projection + residual), forward and backward,
+ * as hand-written CUDA kernels for B300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership.  Every pointer argument is caller-owned.  Tensor arguments are
+ *   DEVICE pointers (current device) unless the comment says "host".  The
+ *   library allocates no device memory of its own: scratch comes from the
+ *   caller's `workspace`, sized by the matching *_workspace_size() query.
+ * Streams.  Every call enqueues work on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream) and returns without synchronising.
+ * Layout.  Row-major.  T tokens of B users, user b owning rows
+ *   offsets[b] .. offsets[b+1]-1 (int32 offsets[B+1], offsets[0] = 0,
+ *   offsets[B] = T), ordered User*, Seq*, RealTime*, Cand* inside a user;
+ *   gid[t] in {0 User, 1 Seq, 2 RealTime, 3 Cand} (uint8); ts[t] int64 seconds.
+ *   Head h of a [T, H*d_h] activation occupies columns h*d_h .. h*d_h+d_h-1.
+ * Types.  MTGR_BF16: activations and weights bf16, statistics fp32, weight /
+ *   GLN-parameter gradients fp32, fp32 accumulation throughout.  MTGR_F32:
+ *   everything fp32.  gamma/beta are fp32 in both modes.
+ * Errors.  A non-zero mtgr_status means nothing was enqueued, except
+ *   MTGR_ERR_CUDA, which reports a launch failure; mtgr_last_error() returns a
+ *   thread-local message.  Malformed device metadata is not checked by the
+ *   compute calls (that would need a host round trip): call
+ *   mtgr_validate_batch() once per batch.  Kernels never trap; they clamp
+ *   offsets to [0, T], so malformed metadata gives wrong numbers, not faults.
+ *
+ * The operations follow these pages on MTGR (Meituan's generative-style ranking
+ * model):
+ *  - marovi.ai, "MTGR: Industrial-Scale Generative Recommendation Framework in
+ *    Meituan/es", section "Métodos": sample D = [U, S, R, (C,I)_1..K], block
+ *    update Ṽ = silu(KᵀQ)/(N_U+N_S+N_R+N_I) · M · V.
+ *  - paper-daily.com, "MTGR：美团外卖生成式推荐Scaling Law落地实践", sections
+ *    "模型怎么搭" (linear + SiLU -> U,Q,K,V; SiLU(QKᵀ) without softmax; normalise
+ *    the aggregate, gate with U, final linear; Group LayerNorm) and
+ *    "训练数据怎么组织，掩码怎么设" (jagged user rows, raw timestamps, mask).
+ *  - fun-rec chapter 7.3 "MTGR：混合范式建模", §7.3.3 (GLN formula) and
+ *    §7.3.4 (the three dynamic-masking rules).
+ */
+#ifndef MTGR_H_
+#define MTGR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MTGR_API __attribute__((visibility("default")))
+#else
+#define MTGR_API
+#endif
+
+typedef struct CUstream_st* mtgr_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  MTGR_OK = 0,
+  MTGR_ERR_INVALID_ARG = -1,     /* a scalar argument or pointer is invalid */
+  MTGR_ERR_BAD_OFFSETS = -2,     /* reported through the status word only */
+  MTGR_ERR_BAD_GROUP_ORDER = -3, /* reported through the status word only */
+  MTGR_ERR_UNSUPPORTED = -4,     /* shape / dtype / device not supported */
+  MTGR_ERR_CUDA = -5,            /* a CUDA runtime call failed */
+  MTGR_ERR_TIMEOUT = -6,         /* reported through the status word only */
+  MTGR_ERR_WORKSPACE = -7        /* workspace missing or smaller than queried */
+} mtgr_status;
+
+typedef enum { MTGR_F32 = 0, MTGR_BF16 = 1 } mtgr_dtype;
+
+/* Bits of the int32 device status word written by mtgr_validate_batch and
+ * OR-ed by kernels that give up a bounded wait. */
+#define MTGR_STATUS_BAD_OFFSETS 1
+#define MTGR_STATUS_BAD_GROUP_ORDER 2
+#define MTGR_STATUS_BAD_GROUP_ID 4
+#define MTGR_STATUS_TIMEOUT 8
+
+/* Thread-local description of the last non-OK status. */
+MTGR_API const char* mtgr_last_error(void);
+/* Library version (major*10000 + minor*100 + patch). */
+MTGR_API int mtgr_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Batch metadata                                                             */
+/* ------------------------------------------------------------------------- */
+
+/* Check the jagged metadata on the device (sample layout of the marovi.ai
+ * "Métodos" section; token order of fun-rec §7.3.1): offsets[0] = 0,
+ * non-decreasing, offsets[B] = T; gid <= 3; inside a segment the group ids do
+ * not decrease (User*, Seq*, RealTime*, Cand*).  Writes the MTGR_STATUS_* bits
+ * into *status_word (device int32, overwritten, 0 = valid). */
+MTGR_API mtgr_status mtgr_validate_batch(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T,
+                                int32_t* status_word, mtgr_stream_t stream);
+
+/* Dynamic mixed mask, integer export (fun-rec §7.3.4 rules 1-3): cnt[t]
+ * (device int32 [T]) = number of keys row t may attend to inside its user;
+ * *total_pairs (device int64, overwritten) = sum over t.  Rule reading:
+ * User/Seq keys are seen by every row; a RealTime key j is seen by RealTime
+ * rows i with ts_j <= ts_i and by candidate rows i with ts_j < ts_i; a
+ * candidate key is seen only by itself. */
+MTGR_API mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                                      int64_t T, int32_t* cnt, int64_t* total_pairs, mtgr_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Group LayerNorm (fun-rec §7.3.3: GLN(x_i) = (x_i - μ)/σ · γ_g(i) + β_g(i);  */
+/* paper-daily "模型怎么搭": one set of normalisation parameters per token      */
+/* class).  μ, σ² are per token over its D features (biased variance,          */
+/* σ = sqrt(σ² + eps)); gamma/beta are fp32 [4, D], row g for group g.         */
+/* ------------------------------------------------------------------------- */
+
+/* x, y: [T, D] (dtype).  mean, rstd: fp32 [T] (may be NULL).  D % 8 == 0,
+ * D <= 8192. */
+MTGR_API mtgr_status mtgr_group_layernorm_fwd(const void* x, void* y, float* mean, float* rstd, const uint8_t* gid,
+                                     const float* gamma, const float* beta, int64_t T, int32_t D, float eps,
+                                     mtgr_dtype dtype, mtgr_stream_t stream);
+
+MTGR_API size_t mtgr_group_layernorm_bwd_workspace_size(int64_t T, int32_t D);
+
+/* dx = GLN'(x)ᵀ dy (+ dx_residual when non-NULL, same dtype as dx);
+ * dgamma, dbeta: fp32 [4, D], overwritten.  mean/rstd from the forward. */
+MTGR_API mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+                                     const uint8_t* gid, const float* gamma, const void* dx_residual, void* dx,
+                                     float* dgamma, float* dbeta, int64_t T, int32_t D, mtgr_dtype dtype,
+                                     void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* HSTU attention (marovi.ai "Métodos" block formula; paper-daily "模型怎么搭")  */
+/*   s_ij = q_i·k_j / sqrt(d_h);  A_ij = M_ij · silu(s_ij) / n_u;              */
+/*   O_i = Σ_j A_ij v_j;  Y_i = LayerNorm(O_i) ⊙ u_i,                          */
+/* per head, over the keys j of row i's own user; n_u = that user's token     */
+/* count; LayerNorm over all H*d_h features of the row, no affine, eps inside  */
+/* the square root; M is the dynamic mixed mask (see visible counts above).    */
+/* ------------------------------------------------------------------------- */
+
+/* Workspace for mtgr_hstu_attn_fwd / _bwd (jagged tile schedule, dO and the
+ * dQ accumulator).  Its first 4 bytes are the call's device status word
+ * (MTGR_STATUS_* bits; cleared by each call, set if a bounded wait gave up). */
+MTGR_API size_t mtgr_attn_workspace_size(int32_t B, int64_t T, int32_t n_heads, int32_t d_h, mtgr_dtype dtype);
+
+/* q, k, v, u: [T, *] with row stride ld_in elements (e.g. views into one
+ * [T, 4*H*d_h] buffer).  y, o_saved: [T, H*d_h] dense (o_saved = O before the
+ * gate, needed by the backward).  ln_mean, ln_rstd: fp32 [T].
+ * Supported: MTGR_BF16 with d_h in {64, 128} (tcgen05 tensor-core path) and
+ * MTGR_F32 with d_h <= 128, d_h % 4 == 0 (fp32 CUDA-core path). */
+MTGR_API mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, const void* u, int64_t ld_in,
+                               const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                               int64_t T, int32_t n_heads, int32_t d_h, float eps, void* y, void* o_saved,
+                               float* ln_mean, float* ln_rstd, mtgr_dtype dtype, void* workspace,
+                               size_t workspace_bytes, mtgr_stream_t stream);
+
+/* Backward of mtgr_hstu_attn_fwd for upstream dy [T, H*d_h].  Writes dq, dk,
+ * dv, du (row stride ld_grad elements; every row of every segment is
+ * overwritten).  silu'(s) = σ(s)(1 + s(1 - σ(s))).  When z_uqkv is not NULL it
+ * is the [T, 4*H*d_h] pre-activation of the layer's UQKV projection (column
+ * blocks U, Q, K, V, each head-major) and every gradient is also multiplied by
+ * silu'(z) of its block (this fuses the SiLU backward of the projection). */
+MTGR_API mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, const void* v, const void* u,
+                               int64_t ld_in, const void* o_saved, const float* ln_mean, const float* ln_rstd,
+                               const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                               int64_t T, int32_t n_heads, int32_t d_h, void* dq, void* dk, void* dv, void* du,
+                               int64_t ld_grad, const void* z_uqkv, mtgr_dtype dtype, void* workspace,
+                               size_t workspace_bytes, mtgr_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* One HSTU layer (paper-daily "模型怎么搭"; paper-daily deep reading §2       */
+/* "统一 HSTU 编码 + Group LayerNorm"):                                       */
+/*   xn = GLN(x);  z = xn · W_uqkv;  [U|Q|K|V] = silu(z);                      */
+/*   Y = LayerNorm(attention(Q,K,V)) ⊙ U;  x' = x + Y · W_o.                   */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t d_model;      /* D; multiple of 64 */
+  int32_t n_heads;      /* H */
+  int32_t d_h;          /* head dim; H*d_h multiple of 64 */
+  const void* w_uqkv;   /* [D, 4*H*d_h] (dtype): column blocks U, Q, K, V */
+  const void* w_o;      /* [H*d_h, D] (dtype) */
+  const float* gamma;   /* [4, D] fp32 */
+  const float* beta;    /* [4, D] fp32 */
+  float eps_gln;        /* 1e-5 */
+  float eps_ln;         /* 1e-5 */
+} mtgr_layer_weights;
+
+typedef struct {        /* written by the forward, read by the backward (dtype unless noted) */
+  void* xn;             /* [T, D] GLN output */
+  void* z;              /* [T, 4*H*d_h] pre-activation */
+  void* uqkv;           /* [T, 4*H*d_h] silu(z) */
+  void* o;              /* [T, H*d_h] attention output before the gate */
+  void* y;              /* [T, H*d_h] gate output */
+  float* gln_mean;      /* [T] */
+  float* gln_rstd;      /* [T] */
+  float* ln_mean;       /* [T] */
+  float* ln_rstd;       /* [T] */
+} mtgr_layer_saved;
+
+typedef struct {        /* fp32, overwritten */
+  float* dw_uqkv;       /* [D, 4*H*d_h] */
+  float* dw_o;          /* [H*d_h, D] */
+  float* dgamma;        /* [4, D] */
+  float* dbeta;         /* [4, D] */
+} mtgr_layer_grads;
+
+MTGR_API size_t mtgr_layer_workspace_size(int32_t B, int64_t T, int32_t d_model, int32_t n_heads, int32_t d_h,
+                                 mtgr_dtype dtype);
+
+/* x, x_out: [T, D] (dtype; may not alias). */
+MTGR_API mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void* x_out,
+                                const mtgr_layer_saved* saved, const int32_t* offsets, int32_t B,
+                                const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
+                                void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
+
+/* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path. */
+MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* saved,
+                                const void* dx_out, void* dx, const mtgr_layer_grads* grads,
+                                const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
+                                int64_t T, mtgr_dtype dtype, void* workspace, size_t workspace_bytes,
+                                mtgr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MTGR_H_ */

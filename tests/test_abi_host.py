@@ -1,0 +1,69 @@
+"""CPU-only checks of the C ABI: the library loads, exports every entry point
+declared in include/mtgr.h, and rejects bad scalar arguments on the host
+(before any CUDA call, so no GPU is needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mtgr.h")).read()
+    return sorted(set(re.findall(r"MTGR_API\s+[\w\s\*]*?\b(mtgr_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hstu_attention_attn_b300 import build, mtgr
+    build.build()
+    return mtgr.lib()
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ("mtgr_group_layernorm_fwd", "mtgr_group_layernorm_bwd", "mtgr_hstu_attn_fwd", "mtgr_hstu_attn_bwd",
+              "mtgr_hstu_layer_fwd", "mtgr_hstu_layer_bwd", "mtgr_validate_batch", "mtgr_debug_visible_counts"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), f"libmtgr.so does not export {n}"
+
+
+def test_binding_covers_every_symbol():
+    from hstu_attention_attn_b300 import mtgr
+    for n in _declared():
+        assert n in mtgr.EXPORTS and hasattr(mtgr, n), n
+
+
+def test_version_and_workspace_queries(lib):
+    from hstu_attention_attn_b300 import mtgr
+    assert mtgr.mtgr_version() >= 100
+    a = mtgr.mtgr_attn_workspace_size(64, 47000, 4, 128, mtgr.MTGR_BF16)
+    b = mtgr.mtgr_attn_workspace_size(64, 94000, 4, 128, mtgr.MTGR_BF16)
+    assert 0 < a < b
+    assert mtgr.mtgr_attn_workspace_size(-1, 10, 4, 128, mtgr.MTGR_BF16) == 0
+    assert mtgr.mtgr_layer_workspace_size(128, 63000, 1024, 8, 128, mtgr.MTGR_BF16) > 0
+
+
+def test_bad_scalars_rejected_on_host(lib):
+    from hstu_attention_attn_b300 import mtgr
+    L = mtgr.lib()
+    # D not a multiple of 8 -> unsupported, no CUDA call made
+    r = L.mtgr_group_layernorm_fwd(None, None, None, None, None, None, None, 10, 7, 1e-5, mtgr.MTGR_BF16, None)
+    assert r == -4 and "multiple of 8" in mtgr.mtgr_last_error()
+    # bf16 attention with d_h = 96 -> unsupported
+    r = L.mtgr_hstu_attn_fwd(None, None, None, None, 384, None, 1, None, None, 10, 4, 96, 1e-5, None, None, None,
+                             None, mtgr.MTGR_BF16, None, 0, None)
+    assert r in (-1, -4)
+    # missing workspace
+    r = L.mtgr_hstu_attn_fwd(16, 16, 16, 16, 512, 16, 1, 16, 16, 10, 4, 128, 1e-5, 16, 16, 16, 16,
+                             mtgr.MTGR_BF16, None, 0, None)
+    assert r == -7
+    # negative sizes
+    r = L.mtgr_validate_batch(16, -1, 16, 10, 16, None)
+    assert r == -1

@@ -1,0 +1,80 @@
+"""bf16 tcgen05 attention vs the fp64 oracle (fed the same bf16-rounded inputs):
+max|err|/RMS(ref) <= 2e-2 on O, Y and every gradient."""
+import numpy as np
+import pytest
+import torch
+
+from hstu_attention_attn_b300 import synth
+from hstu_attention_attn_b300.layer import HstuAttention, device_batch
+from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users, sub_batch
+from tests.util import TOL_BF16, assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+BF = torch.bfloat16
+
+
+def _inputs(rng, batch, H, dh, scale=1.0, packed=False):
+    T, HD = batch.T, H * dh
+    if packed:   # q/k/v/u as column blocks of one [T, 4*HD] buffer, like the layer
+        big = (rng.standard_normal((T, 4 * HD)) * scale).astype(np.float32)
+        t = dev(big, BF)
+        views = [t[:, i * HD:(i + 1) * HD] for i in (1, 2, 3, 0)]   # q, k, v, u
+        host = [bf16_round(big[:, i * HD:(i + 1) * HD]) for i in (1, 2, 3, 0)]
+        return views, host, 4 * HD
+    mats = [(rng.standard_normal((T, HD)) * scale).astype(np.float32) for _ in range(4)]
+    return [dev(m, BF) for m in mats], [bf16_round(m) for m in mats], HD
+
+
+def _run_fwd(batch, H, dh, rng, scale=1.0, packed=False):
+    db = device_batch(batch)
+    (q, k, v, u), host, ld = _inputs(rng, batch, H, dh, scale, packed)
+    op = HstuAttention(H, dh, BF)
+    y, saved = op.forward(q, k, v, u, db, ld=ld)
+    torch.cuda.synchronize()
+    return op, db, (q, k, v, u), host, ld, y, saved
+
+
+@pytest.mark.parametrize("dh", [128, 64])
+@pytest.mark.parametrize("ts_hi", [86400, 40])
+def test_attention_fwd_bf16_ragged(orc, dh, ts_hi):
+    need_gpu()
+    rng = np.random.default_rng(11 + dh + ts_hi)
+    batch = synth.make_batch(rng, ragged_users(), ts_hi=ts_hi)
+    H = 2
+    _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng)
+    Y, O, mean, rstd = orc.attn_fwd(batch, H, dh, *host)
+    assert_close(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close(to_np(y), Y, TOL_BF16, "Y")
+
+
+def test_attention_fwd_bf16_packed_layout(orc):
+    need_gpu()
+    rng = np.random.default_rng(21)
+    batch = synth.make_batch(rng, ragged_users()[:4], ts_hi=500)
+    H, dh = 4, 128
+    _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng, packed=True)
+    Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
+    assert_close(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close(to_np(y), Y, TOL_BF16, "Y")
+
+
+def test_attention_fwd_bf16_small_workload_sampled(orc):
+    """The MTGR-small-like workload at full size (64 users, d_model 512, 4 heads x 128);
+    the oracle recomputes a sample of whole users (users are independent)."""
+    need_gpu()
+    a = synth.small_attn(1)
+    batch, H, dh = a.batch, a.H, a.dh
+    db = device_batch(batch)
+    q, k, v, u = (dev(m, BF) for m in (a.q, a.k, a.v, a.u))
+    op = HstuAttention(H, dh, BF)
+    y, saved = op.forward(q, k, v, u, db)
+    torch.cuda.synchronize()
+    lens = np.diff(batch.offsets)
+    order = np.argsort(lens)
+    pick = sorted(set([int(order[0]), int(order[len(order) // 2]), int(order[-1])] +
+                      [int(i) for i in np.where(lens <= 1200)[0][:5]]))
+    sb, rows = sub_batch(batch, pick)
+    host = [bf16_round(m[rows]) for m in (a.q, a.k, a.v, a.u)]
+    Y, O, _, _ = orc.attn_fwd(sb, H, dh, *host)
+    assert_close(to_np(saved[0])[rows], O, TOL_BF16, "O")
+    assert_close(to_np(y)[rows], Y, TOL_BF16, "Y")
