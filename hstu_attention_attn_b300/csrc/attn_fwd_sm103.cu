@@ -38,7 +38,7 @@ struct FwdCfg {
 };
 
 struct FwdSmem {
-  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_full;
+  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_full, pv_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, 4);
     mbar_init(&S.o_full, 1);
+    mbar_init(&S.pv_done, 1);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -146,6 +147,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       for (int i = 0; i < nk && ok; ++i) {
         const uint32_t par = i & 1;
         if (!mbar_wait(&S.k_full, par, abort_flag)) { ok = false; break; }
+        // S_i overwrites the columns that hold P_{i-1}: wait until P_{i-1} V_{i-1} has read them
+        if (i > 0 && !mbar_wait(&S.pv_done, par ^ 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
         for (int kk = 0; kk < BKV / 16; ++kk)
           tc_mma_ts(t_o, t_s + kk * 8, mnmajor_desc(v_addr, kk), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&S.v_empty);
+        tc_commit(&S.pv_done);
       }
       tc_commit(&S.o_full);
     }

@@ -78,3 +78,42 @@ def test_attention_fwd_bf16_small_workload_sampled(orc):
     Y, O, _, _ = orc.attn_fwd(sb, H, dh, *host)
     assert_close(to_np(saved[0])[rows], O, TOL_BF16, "O")
     assert_close(to_np(y)[rows], Y, TOL_BF16, "Y")
+
+
+@pytest.mark.parametrize("dh", [128, 64])
+@pytest.mark.parametrize("ts_hi", [86400, 40])
+def test_attention_bwd_bf16_ragged(orc, dh, ts_hi):
+    need_gpu()
+    rng = np.random.default_rng(51 + dh + ts_hi)
+    batch = synth.make_batch(rng, ragged_users(), ts_hi=ts_hi)
+    H = 2
+    op, db, (q, k, v, u), host, ld, y, saved = _run_fwd(batch, H, dh, rng)
+    dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
+    dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
+    torch.cuda.synchronize()
+    ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
+    for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
+        assert_close(to_np(got), r, TOL_BF16, name)
+
+
+def test_attention_bwd_bf16_small_workload_sampled(orc):
+    """Backward at the MTGR-small-like size; sampled whole users recomputed by the oracle."""
+    need_gpu()
+    a = synth.small_attn(1)
+    batch, H, dh = a.batch, a.H, a.dh
+    db = device_batch(batch)
+    q, k, v, u = (dev(m, BF) for m in (a.q, a.k, a.v, a.u))
+    op = HstuAttention(H, dh, BF)
+    y, saved = op.forward(q, k, v, u, db)
+    rng = np.random.default_rng(5)
+    dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
+    dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db)
+    torch.cuda.synchronize()
+    lens = np.diff(batch.offsets)
+    pick = sorted(set([int(np.argmin(lens)), int(np.argsort(lens)[len(lens) // 2])] +
+                      [int(i) for i in np.where(lens <= 1000)[0][:4]]))
+    sb, rows = sub_batch(batch, pick)
+    host = [bf16_round(m[rows]) for m in (a.q, a.k, a.v, a.u)]
+    ref = orc.attn_bwd(sb, H, dh, *host, bf16_round(dY[rows]))
+    for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
+        assert_close(to_np(got)[rows], r, TOL_BF16, name)
