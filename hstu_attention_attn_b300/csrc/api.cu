@@ -22,24 +22,25 @@ template <typename T>
 cudaError_t launch_gln_bwd(const T*, const T*, const float*, const float*, const uint8_t*, const float*, const T*,
                            T*, float*, float*, float*, int64_t, int, cudaStream_t);
 int gln_bwd_blocks(int64_t rows);
-template <typename T>
-cudaError_t launch_ln_gate_fwd(const T*, const T*, int64_t, T*, float*, float*, int64_t, int, float, cudaStream_t);
-template <typename T>
-cudaError_t launch_ln_gate_bwd(const T*, const T*, const T*, int64_t, const float*, const float*, T*, T*, int64_t,
-                               const T*, int64_t, int, cudaStream_t);
+template <typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd(const float*, const TU*, int64_t, TY*, float*, float*, int64_t, int, float,
+                               cudaStream_t);
+template <typename TG, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TG*, const float*, const TU*, int64_t, const float*, const float*, TO*, TG*,
+                               int64_t, const TG*, int64_t, int, cudaStream_t);
+cudaError_t launch_bf16_to_f16(const __nv_bfloat16*, int64_t, __half*, int64_t, int64_t, int, cudaStream_t);
 cudaError_t launch_attn_f32_fwd(const float*, const float*, const float*, int64_t, const UserInfo*, int,
                                 const int64_t*, int64_t, int, int, float*, cudaStream_t);
 cudaError_t launch_attn_f32_bwd(const float*, const float*, const float*, int64_t, const float*, const UserInfo*,
                                 int, const int64_t*, int64_t, int, int, float*, float*, float*, int64_t,
                                 const float*, const float*, const float*, cudaStream_t);
-cudaError_t launch_attn_fwd_bf16(const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*, int64_t,
-                                 int64_t, int, int, const int32_t*, int32_t, const int64_t*, __nv_bfloat16*,
-                                 int32_t*, cudaStream_t);
-cudaError_t launch_attn_bwd_bf16(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
-                                 int64_t ld, const __nv_bfloat16* dO, int64_t T, int H, int d, const int32_t* plan,
-                                 int32_t B, const int64_t* ts, float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                                 __nv_bfloat16* dv, int64_t ldg, const __nv_bfloat16* zq, const __nv_bfloat16* zk,
-                                 const __nv_bfloat16* zv, int32_t* status, cudaStream_t s);
+cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int64_t, int64_t, int, int,
+                                const int32_t*, int32_t, const int64_t*, float*, int32_t*, cudaStream_t);
+cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
+                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
+                                float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
+                                const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
+                                int32_t* status, cudaStream_t s);
 
 // ---- error state ----
 static thread_local char g_err[512] = "";
@@ -85,17 +86,25 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
-                       uint32_t box_cols, uint32_t box_rows) {
+static bool make_tmap_16bit_2d(CUtensorMapDataType dt, CUtensorMap* m, const void* base, uint64_t rows,
+                               uint64_t cols, uint64_t ld, uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows == 0 || cols == 0) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                       uint32_t box_cols, uint32_t box_rows) {
+  return make_tmap_16bit_2d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m, base, rows, cols, ld, box_cols, box_rows);
+}
+bool make_tmap_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                      uint32_t box_cols, uint32_t box_rows) {
+  return make_tmap_16bit_2d(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, base, rows, cols, ld, box_cols, box_rows);
 }
 
 // ---------------------------------------------------------------------------
@@ -104,20 +113,26 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static size_t esize(mtgr_dtype dt) { return dt == MTGR_BF16 ? 2 : 4; }
 
+// Attention workspace.  In the bf16 path the tensor-core operands are f16:
+// q, k, v are converted once (exactly) into f16 copies, and dO, P, dS are
+// produced in f16 (11 significand bits instead of 8).
 struct AttnWs {
-  size_t status, plan, dO, dq_acc, total;
+  size_t status, plan, dO, dq_acc, qkv16, total;
 };
-static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt) {
+static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt, bool convert_qkv = true) {
   AttnWs w;
+  const size_t THD = (size_t)T * H * d;
   size_t o = 0;
   w.status = o;
   o += 256;
   w.plan = o;
   o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T).total);
   w.dO = o;
-  o += align256((size_t)T * H * d * esize(dt));
+  o += align256(THD * (dt == MTGR_BF16 ? 2 : 4));
   w.dq_acc = o;
-  if (dt == MTGR_BF16) o += align256((size_t)T * H * d * sizeof(float));
+  if (dt == MTGR_BF16) o += align256(THD * sizeof(float));
+  w.qkv16 = o;
+  if (dt == MTGR_BF16 && convert_qkv) o += 3 * align256(THD * 2);
   w.total = o;
   return w;
 }
@@ -138,7 +153,7 @@ static int choose_splits(int64_t M, int64_t N, int64_t K) {
 static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, mtgr_dtype dt) {
   LayerWs w;
   const int64_t HD = (int64_t)H * d;
-  w.attn = attn_ws(B, T, H, d, dt);
+  w.attn = attn_ws(B, T, H, d, dt, /*convert_qkv=*/false);
   size_t o = 0;
   w.attn_base = o;
   o += w.attn.total;
@@ -174,6 +189,56 @@ static mtgr_status check_meta(const int32_t* offsets, int32_t B, const uint8_t* 
   REQUIRE(T < (int64_t(1) << 31) - 256, MTGR_ERR_UNSUPPORTED, "T must be below 2^31");
   REQUIRE(offsets != nullptr, MTGR_ERR_INVALID_ARG, "offsets is NULL");
   REQUIRE(T == 0 || gid != nullptr, MTGR_ERR_INVALID_ARG, "gid is NULL");
+  return MTGR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// bf16-path attention on f16 tensor-core operands (shared by the attention
+// entry points and the layer).  u is bf16 or f16 (u_f16); y, dq/dk/dv/du bf16.
+// ---------------------------------------------------------------------------
+static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, const __half* v16, int64_t ld16,
+                                      const void* u, bool u_f16, int64_t ldu, const int32_t* offsets, int32_t B,
+                                      const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d, float eps,
+                                      __nv_bfloat16* y, float* o, float* mean, float* rstd, uint8_t* ws,
+                                      const AttnWs& w, cudaStream_t s) {
+  int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
+  int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
+  MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
+  if (T == 0 || B == 0) return MTGR_OK;
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_fwd plan");
+  MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
+  const int HD = H * d;
+  cudaError_t e = u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, y, mean, rstd, T, HD, eps, s)
+                        : launch_ln_gate_fwd(o, static_cast<const __nv_bfloat16*>(u), ldu, y, mean, rstd, T, HD,
+                                             eps, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_fwd gate");
+  return MTGR_OK;
+}
+
+static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16, const __half* k16,
+                                      const __half* v16, int64_t ld16, const void* u, bool u_f16, int64_t ldu,
+                                      const float* o, const float* mean, const float* rstd, const int32_t* offsets,
+                                      int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
+                                      __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, __nv_bfloat16* du,
+                                      int64_t ldg, const __nv_bfloat16* z, uint8_t* ws, const AttnWs& w,
+                                      cudaStream_t s) {
+  int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
+  int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
+  MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
+  if (T == 0 || B == 0) return MTGR_OK;
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_bwd plan");
+  const int64_t HD = (int64_t)H * d;
+  __half* dO = reinterpret_cast<__half*>(ws + w.dO);
+  cudaError_t e = u_f16 ? launch_ln_gate_bwd(dy, o, static_cast<const __half*>(u), ldu, mean, rstd, dO, du, ldg, z,
+                                             T, (int)HD, s)
+                        : launch_ln_gate_bwd(dy, o, static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du,
+                                             ldg, z, T, (int)HD, s);
+  if (e != cudaSuccess) return cuda_status(e, "attn_bwd gate");
+  MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts,
+                                    reinterpret_cast<float*>(ws + w.dq_acc), dq, dk, dv, ldg,
+                                    z ? z + HD : nullptr, z ? z + 2 * HD : nullptr, z ? z + 3 * HD : nullptr, status,
+                                    s),
+                "attn_bwd tcgen05");
   return MTGR_OK;
 }
 
@@ -300,31 +365,32 @@ mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const AttnWs w = attn_ws(B, T, n_heads, d_h, dtype);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t HD = (int64_t)n_heads * d_h;
+  if (dtype == MTGR_BF16) {
+    __half* q16 = reinterpret_cast<__half*>(ws + w.qkv16);
+    __half* k16 = q16 + align256(T * HD * 2) / 2;
+    __half* v16 = k16 + align256(T * HD * 2) / 2;
+    using bf = __nv_bfloat16;
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(q), ld_in, q16, HD, T, (int)HD, s), "attn_fwd f16 q");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(k), ld_in, k16, HD, T, (int)HD, s), "attn_fwd f16 k");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(v), ld_in, v16, HD, T, (int)HD, s), "attn_fwd f16 v");
+    return attn_fwd_bf16_core(q16, k16, v16, HD, u, false, ld_in, offsets, B, gid, ts, T, n_heads, d_h, eps,
+                              static_cast<bf*>(y), static_cast<float*>(o_saved), ln_mean, ln_rstd, ws, w, s);
+  }
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
   if (T == 0 || B == 0) return MTGR_OK;
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_fwd plan");
-  const int HD = n_heads * d_h;
   const PlanLayout L = plan_layout(B, T);
-  if (dtype == MTGR_BF16) {
-    using bf = __nv_bfloat16;
-    MTGR_CUDA_TRY(launch_attn_fwd_bf16(static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-                                       ld_in, T, n_heads, d_h, plan, B, ts, static_cast<bf*>(o_saved), status, s),
-                  "attn_fwd tcgen05");
-    MTGR_CUDA_TRY(launch_ln_gate_fwd(static_cast<const bf*>(o_saved), static_cast<const bf*>(u), ld_in,
-                                     static_cast<bf*>(y), ln_mean, ln_rstd, T, HD, eps, s),
-                  "attn_fwd gate");
-  } else {
-    MTGR_CUDA_TRY(launch_attn_f32_fwd(static_cast<const float*>(q), static_cast<const float*>(k),
-                                      static_cast<const float*>(v), ld_in,
-                                      reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
-                                      static_cast<float*>(o_saved), s),
-                  "attn_fwd fp32");
-    MTGR_CUDA_TRY(launch_ln_gate_fwd(static_cast<const float*>(o_saved), static_cast<const float*>(u), ld_in,
-                                     static_cast<float*>(y), ln_mean, ln_rstd, T, HD, eps, s),
-                  "attn_fwd gate");
-  }
+  MTGR_CUDA_TRY(launch_attn_f32_fwd(static_cast<const float*>(q), static_cast<const float*>(k),
+                                    static_cast<const float*>(v), ld_in,
+                                    reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
+                                    static_cast<float*>(o_saved), s),
+                "attn_fwd fp32");
+  MTGR_CUDA_TRY(launch_ln_gate_fwd(static_cast<const float*>(o_saved), static_cast<const float*>(u), ld_in,
+                                   static_cast<float*>(y), ln_mean, ln_rstd, T, (int)HD, eps, s),
+                "attn_fwd gate");
   return MTGR_OK;
 }
 
@@ -344,47 +410,42 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
   REQUIRE(aligned16(dy) && aligned16(o_saved) && aligned16(dq) && aligned16(dk) && aligned16(dv) &&
               aligned16(du) && aligned16(z_uqkv),
           MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  REQUIRE(z_uqkv == nullptr || ld_grad == 4 * HD, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const AttnWs w = attn_ws(B, T, n_heads, d_h, dtype);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (dtype == MTGR_BF16) {
+    using bf = __nv_bfloat16;
+    __half* q16 = reinterpret_cast<__half*>(ws + w.qkv16);
+    __half* k16 = q16 + align256(T * HD * 2) / 2;
+    __half* v16 = k16 + align256(T * HD * 2) / 2;
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(q), ld_in, q16, HD, T, (int)HD, s), "attn_bwd f16 q");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(k), ld_in, k16, HD, T, (int)HD, s), "attn_bwd f16 k");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(v), ld_in, v16, HD, T, (int)HD, s), "attn_bwd f16 v");
+    return attn_bwd_bf16_core(static_cast<const bf*>(dy), q16, k16, v16, HD, u, false, ld_in,
+                              static_cast<const float*>(o_saved), ln_mean, ln_rstd, offsets, B, gid, ts, T, n_heads,
+                              d_h, static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv),
+                              static_cast<bf*>(du), ld_grad, static_cast<const bf*>(z_uqkv), ws, w, s);
+  }
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
   if (T == 0 || B == 0) return MTGR_OK;
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_bwd plan");
   const PlanLayout L = plan_layout(B, T);
-  const int64_t ldz = 4 * HD;
-  if (dtype == MTGR_BF16) {
-    using bf = __nv_bfloat16;
-    const bf* z = static_cast<const bf*>(z_uqkv);
-    bf* dO = reinterpret_cast<bf*>(ws + w.dO);
-    REQUIRE(z == nullptr || ld_grad == ldz, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
-    MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const bf*>(dy), static_cast<const bf*>(o_saved),
-                                     static_cast<const bf*>(u), ld_in, ln_mean, ln_rstd, dO, static_cast<bf*>(du),
-                                     ld_grad, z, T, (int)HD, s),
-                  "attn_bwd gate");
-    MTGR_CUDA_TRY(launch_attn_bwd_bf16(static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-                                       ld_in, dO, T, n_heads, d_h, plan, B, ts, reinterpret_cast<float*>(ws + w.dq_acc),
-                                       static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv), ld_grad,
-                                       z ? z + HD : nullptr, z ? z + 2 * HD : nullptr, z ? z + 3 * HD : nullptr,
-                                       status, s),
-                  "attn_bwd tcgen05");
-  } else {
-    const float* z = static_cast<const float*>(z_uqkv);
-    float* dO = reinterpret_cast<float*>(ws + w.dO);
-    REQUIRE(z == nullptr || ld_grad == ldz, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
-    MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const float*>(dy), static_cast<const float*>(o_saved),
-                                     static_cast<const float*>(u), ld_in, ln_mean, ln_rstd, dO,
-                                     static_cast<float*>(du), ld_grad, z, T, (int)HD, s),
-                  "attn_bwd gate");
-    MTGR_CUDA_TRY(launch_attn_f32_bwd(static_cast<const float*>(q), static_cast<const float*>(k),
-                                      static_cast<const float*>(v), ld_in, dO,
-                                      reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
-                                      static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
-                                      ld_grad, z ? z + HD : nullptr, z ? z + 2 * HD : nullptr,
-                                      z ? z + 3 * HD : nullptr, s),
-                  "attn_bwd fp32");
-  }
+  const float* z = static_cast<const float*>(z_uqkv);
+  float* dO = reinterpret_cast<float*>(ws + w.dO);
+  MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const float*>(dy), static_cast<const float*>(o_saved),
+                                   static_cast<const float*>(u), ld_in, ln_mean, ln_rstd, dO,
+                                   static_cast<float*>(du), ld_grad, z, T, (int)HD, s),
+                "attn_bwd gate");
+  MTGR_CUDA_TRY(launch_attn_f32_bwd(static_cast<const float*>(q), static_cast<const float*>(k),
+                                    static_cast<const float*>(v), ld_in, dO,
+                                    reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
+                                    static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
+                                    ld_grad, z ? z + HD : nullptr, z ? z + 2 * HD : nullptr,
+                                    z ? z + 3 * HD : nullptr, s),
+                "attn_bwd fp32");
   return MTGR_OK;
 }
 
@@ -446,7 +507,8 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
     g.M = T; g.N = N4; g.K = D;
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
-    g.epi = EPI_SILU; g.C = sv->uqkv; g.ldc = N4; g.Z = static_cast<bf*>(sv->z); g.ldz = N4;
+    // [U|Q|K|V] = silu(z) is written in f16: the attention's tensor-core operands
+    g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->z); g.ldz = N4;
     g.splits = 1; g.status = status;
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
   } else {
@@ -455,11 +517,16 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
                                   nullptr, 0, static_cast<float*>(sv->z), N4, s),
                   "layer_fwd uqkv gemm");
   }
-  const uint8_t* a = static_cast<const uint8_t*>(sv->uqkv);
-  const size_t es = esize(dtype);
-  r = mtgr_hstu_attn_fwd(a + HD * es, a + 2 * HD * es, a + 3 * HD * es, a, N4, offsets, B, gid, ts, T, H, d,
-                         w->eps_ln, sv->y, sv->o, sv->ln_mean, sv->ln_rstd, dtype, ws + L.attn_base, L.attn.total,
-                         stream);
+  if (dtype == MTGR_BF16) {
+    const __half* a = static_cast<const __half*>(sv->uqkv);
+    r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
+                           static_cast<__nv_bfloat16*>(sv->y), sv->o, sv->ln_mean, sv->ln_rstd, ws + L.attn_base,
+                           L.attn, s);
+  } else {
+    const float* a = static_cast<const float*>(sv->uqkv);
+    r = mtgr_hstu_attn_fwd(a + HD, a + 2 * HD, a + 3 * HD, a, N4, offsets, B, gid, ts, T, H, d, w->eps_ln, sv->y,
+                           sv->o, sv->ln_mean, sv->ln_rstd, dtype, ws + L.attn_base, L.attn.total, stream);
+  }
   if (r != MTGR_OK) return r;
   if (dtype == MTGR_BF16) {
     using bf = __nv_bfloat16;
@@ -497,7 +564,6 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.attn_base + L.attn.status);
-  const size_t es = esize(dtype);
   void* dY = ws + L.dY;
   void* dZ = ws + L.dZ;
   void* dxn = ws + L.dxn;
@@ -541,11 +607,20 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
                   "layer_bwd dW_o gemm");
   }
   // 3. attention backward with the SiLU backward of the projection fused: dZ = [dU|dQ|dK|dV] ⊙ silu'(z)
-  const uint8_t* a = static_cast<const uint8_t*>(sv->uqkv);
-  uint8_t* dz = static_cast<uint8_t*>(dZ);
-  mtgr_status r = mtgr_hstu_attn_bwd(dY, a + HD * es, a + 2 * HD * es, a + 3 * HD * es, a, N4, sv->o, sv->ln_mean,
-                                     sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD * es, dz + 2 * HD * es,
-                                     dz + 3 * HD * es, dz, N4, sv->z, dtype, ws + L.attn_base, L.attn.total, stream);
+  mtgr_status r;
+  if (dtype == MTGR_BF16) {
+    const __half* a = static_cast<const __half*>(sv->uqkv);
+    bf* dz = static_cast<bf*>(dZ);
+    r = attn_bwd_bf16_core(static_cast<const bf*>(dY), a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, sv->o,
+                           sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
+                           dz, N4, static_cast<const bf*>(sv->z), ws + L.attn_base, L.attn, s);
+  } else {
+    const float* a = static_cast<const float*>(sv->uqkv);
+    float* dz = static_cast<float*>(dZ);
+    r = mtgr_hstu_attn_bwd(dY, a + HD, a + 2 * HD, a + 3 * HD, a, N4, sv->o, sv->ln_mean, sv->ln_rstd, offsets, B,
+                           gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD, dz, N4, sv->z, dtype,
+                           ws + L.attn_base, L.attn.total, stream);
+  }
   if (r != MTGR_OK) return r;
   // 4. dW_uqkv = xnᵀ · dZ ;  5. dxn = dZ · W_uqkvᵀ
   if (dtype == MTGR_BF16) {

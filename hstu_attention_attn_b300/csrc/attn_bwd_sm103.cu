@@ -1,5 +1,6 @@
 // attn_bwd_sm103.cu -- jagged HSTU attention backward on the 5th-generation
-// tensor cores (tcgen05 + TMEM + TMA), bf16 operands, fp32 accumulation.
+// tensor cores (tcgen05 + TMEM + TMA): f16 operands (q, k, v, dO, P, dS),
+// fp32 accumulation, bf16 gradients.
 //
 // With s = q·k / sqrt(d_h), A = M ⊙ silu(s) / n_u and O = A V (marovi.ai
 // "Métodos" block formula; paper-daily "模型怎么搭"), the gradients are
@@ -12,14 +13,14 @@
 // fun-rec chapter 7.3, §7.3.4).  Per query tile:
 //   Sᵀ  = K Qᵀ            -> TMEM [0,128)
 //   dPᵀ = V dOᵀ           -> TMEM [128,256)
-//   epilogue (thread = key row): Pᵀ (bf16) into TMEM [0,64), dSᵀ (bf16) into
+//   epilogue (thread = key row): Pᵀ (f16) into TMEM [0,64), dSᵀ (f16) into
 //   shared memory (128-byte swizzled, written by threads)
 //   dV += Pᵀ dO           (A from TMEM)            -> TMEM [256, 256+D)
 //   dK += dSᵀ Q           (A K-major from smem)    -> TMEM [256+D, 256+2D)
 //   dQ  = dS K            (A MN-major: same smem)  -> TMEM [128,128+D)
 //   epilogue (thread = query row): dQ added into an fp32 accumulator in global
-//   memory with vector atomics; a final pass scales, applies silu'(z) and
-//   rounds to bf16.
+//   memory with vector atomics; a final pass applies silu'(z) and rounds to
+//   bf16.  P is kept without the 1/n_u factor (dV is scaled once at the end).
 // Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..5 epilogue.
 #include "common.cuh"
 #include "plan.cuh"
@@ -159,9 +160,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t id_sq = idesc_bf16_f32(BT, BT, false, false);  // Sᵀ, dPᵀ
-      constexpr uint32_t id_dv = idesc_bf16_f32(BT, D, false, true);    // dV (A tmem), dK (A K-major)
-      constexpr uint32_t id_dq = idesc_bf16_f32(BT, D, true, true);     // dQ: A = dS MN-major
+      constexpr uint32_t id_sq = idesc_f16_f32(BT, BT, false, false);  // Sᵀ, dPᵀ
+      constexpr uint32_t id_dv = idesc_f16_f32(BT, D, false, true);    // dV (A tmem), dK (A K-major)
+      constexpr uint32_t id_dq = idesc_f16_f32(BT, D, true, true);     // dQ: A = dS MN-major
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
                      adS = smem_u32(sdS);
       if (!mbar_wait(&S.kv_full, 0, abort_flag)) ok = false;
@@ -246,11 +247,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float sg = fmaf(0.5f, tanh_approx(0.5f * s), 0.5f);
             const float silu = s * sg;
             const float dsil = sg * fmaf(s, 1.f - sg, 1.f);
-            pv[t] = vis ? silu * inv_n : 0.f;
+            pv[t] = vis ? silu : 0.f;
             dsv[t] = vis ? __uint_as_float(dr[2 * e + t]) * dsil * cds : 0.f;
           }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[e] = pack_f16x2(pv[0], pv[1]);
+          dk[e] = pack_f16x2(dsv[0], dsv[1]);
         }
         tmem_st16(tmem + Cfg::ST + ch * 16 + lane_sel, pk);
         // dSᵀ row r_in, query columns ch*32 .. ch*32+31 -> 4 swizzled 16-byte chunks
@@ -305,8 +306,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_wait_ld();
           if (!row_ok) continue;
           float x[32];
+          const float sc = nq > 0 ? (which == 0 ? 1.f : inv_n) : 0.f;  // P carries no 1/n_u
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = nq > 0 ? __uint_as_float(r[e]) : 0.f;
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * sc;
           if (z) {
             const uint4* zp = reinterpret_cast<const uint4*>(z + grow * p.ldz + col_h + ch * 32);
 #pragma unroll
@@ -377,8 +379,8 @@ __global__ void dq_finish_kernel(const float* __restrict__ acc, int64_t T, int H
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_bf16(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
-                                 int64_t ld, const __nv_bfloat16* dO, int64_t T, int H, int d, const int32_t* plan,
+cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v,
+                                 int64_t ld, const __half* dO, int64_t T, int H, int d, const int32_t* plan,
                                  int32_t B, const int64_t* ts, float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk,
                                  __nv_bfloat16* dv, int64_t ldg, const __nv_bfloat16* zq, const __nv_bfloat16* zk,
                                  const __nv_bfloat16* zv, int32_t* status, cudaStream_t s) {
@@ -388,8 +390,8 @@ cudaError_t launch_attn_bwd_bf16(const __nv_bfloat16* q, const __nv_bfloat16* k,
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * HD, s);
   if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bf16_2d(&tq, q, T, HD, ld, 64, BT) || !make_tmap_bf16_2d(&tk, k, T, HD, ld, 64, BT) ||
-      !make_tmap_bf16_2d(&tv, v, T, HD, ld, 64, BT) || !make_tmap_bf16_2d(&tdo, dO, T, HD, HD, 64, BT))
+  if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BT) ||
+      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tdo, dO, T, HD, HD, 64, BT))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.users = reinterpret_cast<const UserInfo*>(plan + L.users);

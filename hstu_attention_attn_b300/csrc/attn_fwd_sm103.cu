@@ -1,9 +1,10 @@
 // attn_fwd_sm103.cu -- jagged HSTU attention forward on the 5th-generation
-// tensor cores (tcgen05 + TMEM + TMA), bf16 in, fp32 accumulate.
+// tensor cores (tcgen05 + TMEM + TMA): f16 operands (q, k, v and P), fp32
+// accumulation, fp32 O.
 //
 // Computes, per head and per 128-row query tile of one user segment,
 //   S = Q Kᵀ                       (tcgen05.mma, fp32 in TMEM)
-//   P = M ⊙ silu(S / sqrt(d_h))    (epilogue warps, in registers; bf16 into TMEM)
+//   P = M ⊙ silu(S / sqrt(d_h))    (epilogue warps, in registers; f16 into TMEM)
 //   O += P V                       (tcgen05.mma with P read from TMEM)
 // over the key tiles the dynamic mixed mask leaves visible, then O / n_u.
 // Block formula: marovi.ai "Métodos" (Ṽ = silu(KᵀQ)/(N_U+N_S+N_R+N_I) · M · V);
@@ -16,7 +17,7 @@
 //   warp 0      TMA: Q once, then K_j / V_j (one buffer each)
 //   warp 1      MMA issuer (one thread) + TMEM owner
 //   warps 2..5  P epilogue (thread = query row = TMEM lane) and the O store
-// TMEM: S at columns [0,128) (P aliases its first 64 columns as packed bf16),
+// TMEM: S at columns [0,128) (P aliases its first 64 columns as packed f16),
 // O at [128, 128+d_h).  96 KB of shared memory and 256 TMEM columns per CTA,
 // so two CTAs share an SM and interleave their MMA and epilogue phases.
 #include "common.cuh"
@@ -48,14 +49,14 @@ struct FwdParams {
   const WorkItem* items;
   const int32_t* counts;
   const int64_t* ts;
-  __nv_bfloat16* O;  // [T, H*D]
+  float* O;  // [T, H*D] fp32
   int64_t ldo;
   int H;
   float scale;  // 1/sqrt(d_h)
   int32_t* status;
 };
 
-// Shared-memory descriptors of a [128 rows][D] bf16 tile staged as D/64 boxes
+// Shared-memory descriptors of a [128 rows][D] 16-bit tile staged as D/64 boxes
 // of [128][64] with 128-byte swizzle (16 KB per box).
 template <int D>
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {  // K = d, step 16
@@ -139,8 +140,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, D, false, true);
+      constexpr uint32_t idesc_s = idesc_f16_f32(BQ, BKV, false, false);
+      constexpr uint32_t idesc_o = idesc_f16_f32(BQ, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       const uint32_t t_s = tmem + Cfg::S_COL, t_o = tmem + Cfg::O_COL;
       if (!mbar_wait(&S.q_full, 0, abort_flag)) ok = false;
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float h0 = __uint_as_float(r[2 * e]) * hs, h1 = __uint_as_float(r[2 * e + 1]) * hs;
-            pk[e] = pack_bf16x2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
+            pk[e] = pack_f16x2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
           }
         } else {
 #pragma unroll
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
               const float hh = __uint_as_float(r[2 * e + t]) * hs;
               pv[t] = vis ? fmaf(hh, tanh_approx(hh), hh) : 0.f;
             }
-            pk[e] = pack_bf16x2(pv[0], pv[1]);
+            pk[e] = pack_f16x2(pv[0], pv[1]);
           }
         }
         tmem_st16(tmem + Cfg::S_COL + c * 16 + lane_sel, pk);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
     if (ok && mbar_wait(&S.o_full, 0, abort_flag)) {
       tc_fence_after();
       const float inv_n = 1.0f / (float)u.n;
-      __nv_bfloat16* orow = p.O + (int64_t)(u.start + ri) * p.ldo + col_h;
+      float* orow = p.O + (int64_t)(u.start + ri) * p.ldo + col_h;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -234,14 +235,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_n, __uint_as_float(r[8 * v + 1]) * inv_n);
-            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_n, __uint_as_float(r[8 * v + 3]) * inv_n);
-            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_n, __uint_as_float(r[8 * v + 5]) * inv_n);
-            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_n, __uint_as_float(r[8 * v + 7]) * inv_n);
-            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * v) = o;
-          }
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(orow + c * 32 + 4 * v) =
+                make_float4(__uint_as_float(r[4 * v + 0]) * inv_n, __uint_as_float(r[4 * v + 1]) * inv_n,
+                            __uint_as_float(r[4 * v + 2]) * inv_n, __uint_as_float(r[4 * v + 3]) * inv_n);
         }
       }
     } else {
@@ -263,16 +260,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
 
 }  // namespace
 
-// q, k, v: [T, *] bf16 with row stride ld; O: [T, H*d] bf16.
-cudaError_t launch_attn_fwd_bf16(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+// q, k, v: [T, *] f16 with row stride ld; O: [T, H*d] fp32.
+cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* v,
                                  int64_t ld, int64_t T, int H, int d, const int32_t* plan, int32_t B,
-                                 const int64_t* ts, __nv_bfloat16* O, int32_t* status, cudaStream_t s) {
+                                 const int64_t* ts, float* O, int32_t* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T);
   const int HD = H * d;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_bf16_2d(&tk, k, T, HD, ld, 64, BKV) ||
-      !make_tmap_bf16_2d(&tv, v, T, HD, ld, 64, BKV))
+  if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BKV) ||
+      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.users = reinterpret_cast<const UserInfo*>(plan + L.users);

@@ -31,7 +31,8 @@ struct GemmArgs {
   int64_t ldb;
   bool b_mn_major;
   int epi;
-  void* C;  // bf16, or fp32 for EPI_F32
+  void* C;  // bf16 (f16 when c_f16), or fp32 for EPI_F32
+  bool c_f16;
   int64_t ldc;
   const __nv_bfloat16* R;  // residual (EPI_RESIDUAL)
   int64_t ldr;

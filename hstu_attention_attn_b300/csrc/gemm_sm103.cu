@@ -38,6 +38,7 @@ struct Params {
   int64_t M, N, K;
   int m_tiles, n_tiles, splits, kb_per_split, nk;
   bool a_mn, b_mn;
+  bool c_f16;
   int epi;
   void* C;
   int64_t ldc;
@@ -224,10 +225,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           uint4 o;
-          o.x = pack_bf16x2(x[0], x[1]);
-          o.y = pack_bf16x2(x[2], x[3]);
-          o.z = pack_bf16x2(x[4], x[5]);
-          o.w = pack_bf16x2(x[6], x[7]);
+          if (p.c_f16) {
+            o.x = pack_f16x2(x[0], x[1]);
+            o.y = pack_f16x2(x[2], x[3]);
+            o.z = pack_f16x2(x[4], x[5]);
+            o.w = pack_f16x2(x[6], x[7]);
+          } else {
+            o.x = pack_bf16x2(x[0], x[1]);
+            o.y = pack_bf16x2(x[2], x[3]);
+            o.z = pack_bf16x2(x[4], x[5]);
+            o.w = pack_bf16x2(x[6], x[7]);
+          }
           *reinterpret_cast<uint4*>(C + col0 + 8 * v) = o;
         }
       }
@@ -292,6 +300,7 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   p.a_mn = a.a_mn_major;
   p.b_mn = a.b_mn_major;
   p.epi = a.epi;
+  p.c_f16 = a.c_f16;
   p.C = a.C;
   p.ldc = a.ldc;
   p.R = a.R;

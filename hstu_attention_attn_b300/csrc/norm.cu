@@ -6,7 +6,8 @@
 //      y = (x - μ)·rstd·γ_g + β_g, statistics per token over D features,
 //      γ_g/β_g selected by the token's group id.
 //  * Gate (paper-daily "模型怎么搭": normalise the aggregate, multiply by U):
-//      Y = LayerNorm(O) ⊙ U over the H·d_h features of a token, no affine.
+//      Y = LayerNorm(O) ⊙ U over the H·d_h features of a token, no affine
+//      (O is kept in fp32 in both precision paths).
 #include "common.cuh"
 
 namespace mtgr {
@@ -26,6 +27,23 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   const float4 b = *reinterpret_cast<const float4*>(p + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __half* p, float (&v)[8]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = f16_lo(w[i]);
+    v[2 * i + 1] = f16_hi(w[i]);
+  }
+}
+__device__ __forceinline__ void store8(__half* p, const float (&v)[8]) {
+  uint4 r;
+  r.x = pack_f16x2(v[0], v[1]);
+  r.y = pack_f16x2(v[2], v[3]);
+  r.z = pack_f16x2(v[4], v[5]);
+  r.w = pack_f16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = r;
 }
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
   uint4 r;
@@ -161,9 +179,9 @@ __global__ void gln_param_reduce_kernel(const float* __restrict__ partial, int n
 // ---------------------------------------------------------------------------
 // Gate: Y = LayerNorm(O) ⊙ U
 // ---------------------------------------------------------------------------
-template <typename T, int NCH>
-__global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const T* __restrict__ O, const T* __restrict__ U,
-                                                          int64_t ldu, T* __restrict__ Y,
+template <typename TU, typename TY, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const float* __restrict__ O, const TU* __restrict__ U,
+                                                          int64_t ldu, TY* __restrict__ Y,
                                                           float* __restrict__ mean, float* __restrict__ rstd,
                                                           int64_t rows, int n, float eps) {
   const int lane = threadIdx.x & 31;
@@ -201,13 +219,13 @@ __global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const T* __restrict__ 
 }
 
 // dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ silu'(z_u) when z given).
-template <typename T, int NCH>
-__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const T* __restrict__ dY, const T* __restrict__ O,
-                                                          const T* __restrict__ U, int64_t ldu,
+template <typename TG, typename TU, typename TO, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__ dY, const float* __restrict__ O,
+                                                          const TU* __restrict__ U, int64_t ldu,
                                                           const float* __restrict__ mean,
-                                                          const float* __restrict__ rstd, T* __restrict__ dO,
-                                                          T* __restrict__ dU, int64_t ldg,
-                                                          const T* __restrict__ z, int64_t rows, int n) {
+                                                          const float* __restrict__ rstd, TO* __restrict__ dO,
+                                                          TG* __restrict__ dU, int64_t ldg,
+                                                          const TG* __restrict__ z, int64_t rows, int n) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
@@ -310,22 +328,44 @@ cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const flo
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_ln_gate_fwd(const T* O, const T* U, int64_t ldu, T* Y, float* mean, float* rstd, int64_t rows,
-                               int n, float eps, cudaStream_t s) {
+template <typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd(const float* O, const TU* U, int64_t ldu, TY* Y, float* mean, float* rstd,
+                               int64_t rows, int n, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  NCH_DISPATCH(n, (ln_gate_fwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd, rows,
-                                                                                n, eps)));
+  NCH_DISPATCH(n, (ln_gate_fwd_kernel<TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd,
+                                                                                     rows, n, eps)));
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_ln_gate_bwd(const T* dY, const T* O, const T* U, int64_t ldu, const float* mean,
-                               const float* rstd, T* dO, T* dU, int64_t ldg, const T* z, int64_t rows, int n,
+template <typename TG, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TG* dY, const float* O, const TU* U, int64_t ldu, const float* mean,
+                               const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* z, int64_t rows, int n,
                                cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  NCH_DISPATCH(n, (ln_gate_bwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(dY, O, U, ldu, mean, rstd, dO,
-                                                                                dU, ldg, z, rows, n)));
+  NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
+                      dY, O, U, ldu, mean, rstd, dO, dU, ldg, z, rows, n)));
+  return cudaGetLastError();
+}
+
+// 16-bit copy with a new row stride: dst[r, c] = src[r * lds + c] for c < n (exact
+// for bf16 -> f16 when the value lies in the f16 normal range).
+template <typename TS, typename TD>
+__global__ void convert_rows_kernel(const TS* __restrict__ src, int64_t lds, TD* __restrict__ dst, int64_t ldd,
+                                    int64_t rows, int n) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i >= rows * n) return;
+  const int64_t r = i / n;
+  const int c = (int)(i - r * n);
+  float v[8];
+  load8(src + r * lds + c, v);
+  store8(dst + r * ldd + c, v);
+}
+
+cudaError_t launch_bf16_to_f16(const __nv_bfloat16* src, int64_t lds, __half* dst, int64_t ldd, int64_t rows,
+                               int n, cudaStream_t s) {
+  const int64_t n8 = rows * n / 8;
+  if (n8 == 0) return cudaSuccess;
+  convert_rows_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(src, lds, dst, ldd, rows, n);
   return cudaGetLastError();
 }
 
@@ -334,13 +374,25 @@ cudaError_t launch_ln_gate_bwd(const T* dY, const T* O, const T* U, int64_t ldu,
                                          const float*, int64_t, int, float, cudaStream_t);                    \
   template cudaError_t launch_gln_bwd<T>(const T*, const T*, const float*, const float*, const uint8_t*,       \
                                          const float*, const T*, T*, float*, float*, float*, int64_t, int,     \
-                                         cudaStream_t);                                                       \
-  template cudaError_t launch_ln_gate_fwd<T>(const T*, const T*, int64_t, T*, float*, float*, int64_t, int,    \
-                                             float, cudaStream_t);                                            \
-  template cudaError_t launch_ln_gate_bwd<T>(const T*, const T*, const T*, int64_t, const float*,              \
-                                             const float*, T*, T*, int64_t, const T*, int64_t, int,           \
-                                             cudaStream_t);
+                                         cudaStream_t);
 INSTANTIATE(float)
 INSTANTIATE(__nv_bfloat16)
+
+using bf16_t = __nv_bfloat16;
+template cudaError_t launch_ln_gate_fwd<float, float>(const float*, const float*, int64_t, float*, float*, float*,
+                                                      int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd<bf16_t, bf16_t>(const float*, const bf16_t*, int64_t, bf16_t*, float*,
+                                                        float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd<__half, bf16_t>(const float*, const __half*, int64_t, bf16_t*, float*,
+                                                        float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<float, float, float>(const float*, const float*, const float*, int64_t,
+                                                             const float*, const float*, float*, float*, int64_t,
+                                                             const float*, int64_t, int, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<bf16_t, bf16_t, __half>(const bf16_t*, const float*, const bf16_t*, int64_t,
+                                                                const float*, const float*, __half*, bf16_t*,
+                                                                int64_t, const bf16_t*, int64_t, int, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half>(const bf16_t*, const float*, const __half*, int64_t,
+                                                                const float*, const float*, __half*, bf16_t*,
+                                                                int64_t, const bf16_t*, int64_t, int, cudaStream_t);
 
 }  // namespace mtgr

@@ -59,7 +59,7 @@ class HstuAttention:
         T, HD = db.T, self.H * self.dh
         ld = ld if ld is not None else q.stride(0)
         y = torch.empty(T, HD, dtype=self.dtype, device=self.device)
-        o = torch.empty(T, HD, dtype=self.dtype, device=self.device)
+        o = torch.empty(T, HD, dtype=torch.float32, device=self.device)
         mean = torch.empty(T, dtype=torch.float32, device=self.device)
         rstd = torch.empty(T, dtype=torch.float32, device=self.device)
         mtgr.mtgr_hstu_attn_fwd(q, k, v, u, ld, db.offsets, db.gid, db.ts, T, self.H, self.dh, self.eps, y, o,
@@ -105,7 +105,9 @@ class HstuLayer:
         HD = self.H * self.dh
         e = lambda *s: torch.empty(*s, dtype=self.dtype, device=self.device)
         f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
-        return dict(xn=e(T, self.D), z=e(T, 4 * HD), uqkv=e(T, 4 * HD), o=e(T, HD), y=e(T, HD),
+        u16 = torch.float16 if self.dtype == torch.bfloat16 else self.dtype   # attention operands
+        return dict(xn=e(T, self.D), z=e(T, 4 * HD), uqkv=torch.empty(T, 4 * HD, dtype=u16, device=self.device),
+                    o=f(T, HD), y=e(T, HD),
                     gln_mean=f(T), gln_rstd=f(T), ln_mean=f(T), ln_rstd=f(T))
 
     def forward(self, x, db: DeviceBatch, saved=None, x_out=None):

@@ -7,7 +7,7 @@ import torch
 from hstu_attention_attn_b300 import synth
 from hstu_attention_attn_b300.layer import HstuAttention, device_batch
 from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users, sub_batch
-from tests.util import TOL_BF16, assert_close, to_np
+from tests.util import TOL_BF16, assert_close, assert_close_bf16, to_np
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -43,8 +43,8 @@ def test_attention_fwd_bf16_ragged(orc, dh, ts_hi):
     H = 2
     _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng)
     Y, O, mean, rstd = orc.attn_fwd(batch, H, dh, *host)
-    assert_close(to_np(saved[0]), O, TOL_BF16, "O")
-    assert_close(to_np(y), Y, TOL_BF16, "Y")
+    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
 def test_attention_fwd_bf16_packed_layout(orc):
@@ -54,8 +54,8 @@ def test_attention_fwd_bf16_packed_layout(orc):
     H, dh = 4, 128
     _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng, packed=True)
     Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
-    assert_close(to_np(saved[0]), O, TOL_BF16, "O")
-    assert_close(to_np(y), Y, TOL_BF16, "Y")
+    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
 def test_attention_fwd_bf16_small_workload_sampled(orc):
@@ -76,8 +76,8 @@ def test_attention_fwd_bf16_small_workload_sampled(orc):
     sb, rows = sub_batch(batch, pick)
     host = [bf16_round(m[rows]) for m in (a.q, a.k, a.v, a.u)]
     Y, O, _, _ = orc.attn_fwd(sb, H, dh, *host)
-    assert_close(to_np(saved[0])[rows], O, TOL_BF16, "O")
-    assert_close(to_np(y)[rows], Y, TOL_BF16, "Y")
+    assert_close_bf16(to_np(saved[0])[rows], O, TOL_BF16, "O")
+    assert_close_bf16(to_np(y)[rows], Y, TOL_BF16, "Y")
 
 
 @pytest.mark.parametrize("dh", [128, 64])
@@ -93,7 +93,7 @@ def test_attention_bwd_bf16_ragged(orc, dh, ts_hi):
     torch.cuda.synchronize()
     ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
-        assert_close(to_np(got), r, TOL_BF16, name)
+        assert_close_bf16(to_np(got), r, TOL_BF16, name)
 
 
 def test_attention_bwd_bf16_small_workload_sampled(orc):
@@ -116,4 +116,4 @@ def test_attention_bwd_bf16_small_workload_sampled(orc):
     host = [bf16_round(m[rows]) for m in (a.q, a.k, a.v, a.u)]
     ref = orc.attn_bwd(sb, H, dh, *host, bf16_round(dY[rows]))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
-        assert_close(to_np(got)[rows], r, TOL_BF16, name)
+        assert_close_bf16(to_np(got)[rows], r, TOL_BF16, name)

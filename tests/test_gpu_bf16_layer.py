@@ -11,7 +11,7 @@ import torch
 from hstu_attention_attn_b300 import synth
 from hstu_attention_attn_b300.layer import HstuLayer, device_batch
 from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users
-from tests.util import TOL_BF16, assert_close, to_np
+from tests.util import TOL_BF16, assert_close, assert_close_bf16, to_np
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -38,11 +38,11 @@ def test_layer_fwd_bf16_steps(orc, D, H, dh):
     wu, wo = bf16_round(L.w_uqkv), bf16_round(L.w_o)
     # GLN on the bf16 input
     xn_ref, _, _ = orc.gln_fwd(xb, b.gid, L.gamma, L.beta)
-    assert_close(to_np(sv["xn"]), xn_ref, TOL_BF16, "xn")
+    assert_close_bf16(to_np(sv["xn"]), xn_ref, TOL_BF16, "xn")
     # projection on the GPU's xn
     xn = to_np(sv["xn"])
     z_ref = orc.matmul(xn, wu)
-    assert_close(to_np(sv["z"]), z_ref, TOL_BF16, "z")
+    assert_close_bf16(to_np(sv["z"]), z_ref, TOL_BF16, "z")
     # silu of the stored z, rounded once to bf16: elementwise relative check
     sz = orc.silu(to_np(sv["z"]))
     assert np.all(np.abs(to_np(sv["uqkv"]) - sz) <= 2.0 ** -8 * np.abs(sz) + 1e-6), "silu(z)"
@@ -51,11 +51,11 @@ def test_layer_fwd_bf16_steps(orc, D, H, dh):
     a = to_np(sv["uqkv"])
     U, Q, K, V = (a[:, i * HD:(i + 1) * HD] for i in range(4))
     Y_ref, O_ref, _, _ = orc.attn_fwd(b, H, dh, Q, K, V, U)
-    assert_close(to_np(sv["o"]), O_ref, TOL_BF16, "o")
-    assert_close(to_np(sv["y"]), Y_ref, TOL_BF16, "y")
+    assert_close_bf16(to_np(sv["o"]), O_ref, TOL_BF16, "o")
+    assert_close_bf16(to_np(sv["y"]), Y_ref, TOL_BF16, "y")
     # output projection + residual on the GPU's Y
     xo_ref = xb + orc.matmul(to_np(sv["y"]), wo)
-    assert_close(to_np(x_out), xo_ref, TOL_BF16, "x_out")
+    assert_close_bf16(to_np(x_out), xo_ref, TOL_BF16, "x_out")
     # end to end against the oracle layer on the bf16 inputs
     ref = orc.layer_fwd(b, D, H, dh, xb, wu, wo, L.gamma, L.beta)
-    assert_close(to_np(x_out), ref["x_out"], TOL_BF16, "x_out end-to-end")
+    assert_close_bf16(to_np(x_out), ref["x_out"], TOL_BF16, "x_out end-to-end")

@@ -33,3 +33,37 @@ def assert_close(got, ref, tol, what=""):
 
 def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 (half an ulp, relative)
+
+
+def bf16_excess(got, ref):
+    """max_i max(|got_i - ref_i| - u|ref_i|, 0) / RMS(ref): the error beyond one
+    rounding of the exact value to bf16."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0, 0.0
+    err = np.abs(got - ref)
+    rms = np.sqrt(np.mean(ref * ref))
+    exc = np.maximum(err - BF16_U * np.abs(ref), 0.0).max()
+    if rms == 0.0:
+        return exc, err.max()
+    return exc / rms, err.max() / rms
+
+
+def assert_close_bf16(got, ref, tol=TOL_BF16, what=""):
+    """bf16-path bound: max|err|/RMS(ref) <= tol for the part of the error that
+    exceeds one rounding of the exact value to bf16 (u = 2^-8 relative).  A bf16
+    result stored exactly rounded already carries |err| up to u|ref|, which for
+    tensors with max|ref|/RMS(ref) > tol/u = 5 alone would exceed tol."""
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    exc, lit = bf16_excess(got, ref)
+    rms = float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2))) if np.size(ref) else 0.0
+    if rms == 0.0:
+        assert exc <= 1e-6, f"{what}: max|err| {exc:.3e} with zero reference"
+    else:
+        assert exc <= tol, f"{what}: error beyond bf16 rounding {exc:.3e}/RMS > {tol:.1e} (plain max|err|/RMS {lit:.3e})"
+    return exc, lit
