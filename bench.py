@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the MTGR HSTU hot path on B300.
+
+Default workload (the MTGR-large-like training step): users drawn from the
+MTGR-large length distribution (8 User tokens, Seq ~ lognormal median 300
+clamped to [16, 1000], RealTime ~ U[0, 64], 20 candidates) until the batch
+holds >= 262,144 tokens; one HSTU layer at d_model 1024, 8 heads x d_h 128;
+a step is the layer forward + backward (Group LayerNorm, UQKV projection +
+SiLU, masked jagged attention, LayerNorm(O)*U, output projection + residual,
+and all their gradients), with the upstream gradient non-zero only on
+candidate rows.  Inputs are synthetic and seeded; weights are Xavier.
+
+Printed metric (one JSON line): useful masked HSTU attention fwd+bwd TFLOP/s
+(visible (i, j, head) pairs x 12*d_h FLOP: 4*d_h forward, 8*d_h backward),
+timed as the device time of the attention op's kernels inside the timed layer
+steps (CUDA events on the launching stream), plus tokens/s/layer of the whole
+step.  --impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/layer"
+ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", "dq_zero", "attn_bwd", "dq_finish")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", choices=["large_train", "small_attn"], default="large_train")
+    ap.add_argument("--seed", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"], src="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def attention_useful_flops(npairs, H, dh):
+    return dict(fwd=4.0 * dh * npairs * H, bwd=8.0 * dh * npairs * H)
+
+
+def cpu_baseline(batch, H, dh, budget_s=12.0):
+    """fp64 oracle (as it stands) timed on whole users of the same batch: the
+    attention op forward + backward; returns useful TFLOP/s and the sample."""
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    import oracle
+    from hstu_attention_attn_b300 import synth
+    rng = np.random.default_rng(0)
+    lens = np.diff(batch.offsets)
+    order = rng.permutation(len(lens))
+    chosen, t_used, flops, pairs_tot = [], 0.0, 0.0, 0
+    t_start = time.perf_counter()
+    # grow the sample one group of users at a time until the budget is used
+    i = 0
+    group = max(1, cores)
+    while i < len(order) and t_used < budget_s:
+        users = [int(b) for b in order[i:i + group]]
+        i += group
+        rows, offs = [], [0]
+        for b in users:
+            s0, s1 = int(batch.offsets[b]), int(batch.offsets[b + 1])
+            rows.append(np.arange(s0, s1))
+            offs.append(offs[-1] + s1 - s0)
+        rows = np.concatenate(rows)
+        sb = synth.Batch(np.asarray(offs, np.int32), batch.gid[rows], batch.ts[rows])
+        T = sb.T
+        q, k, v, u, dY = (rng.standard_normal((T, H * dh)) for _ in range(5))
+        _, pairs = oracle.visible_counts(sb)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(sb, H, dh, q, k, v, u)
+        oracle.attn_bwd(sb, H, dh, q, k, v, u, dY)
+        dt = time.perf_counter() - t0
+        t_used += dt
+        f = attention_useful_flops(pairs, H, dh)
+        flops += f["fwd"] + f["bwd"]
+        pairs_tot += pairs
+        chosen += users
+    return {"value": flops / t_used / 1e12, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle",
+            "sample": f"{len(chosen)} whole users ({pairs_tot} visible pairs x {H} heads) of the same batch, "
+                      f"attention op forward+backward in fp64, {t_used:.1f} s of CPU time",
+            "wall_s": time.perf_counter() - t_start}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    """The fp64 CPU oracle timed on the host cores (bounded sample per step)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from hstu_attention_attn_b300 import synth
+    L = synth.large_train_layer(args.seed) if args.workload == "large_train" else None
+    if L is None:
+        a = synth.small_attn(1)
+        batch, H, dh = a.batch, a.H, a.dh
+    else:
+        batch, H, dh = L.batch, L.H, L.dh
+    per_step = 3.0
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(batch, H, dh, budget_s=1.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(batch, H, dh, budget_s=per_step))
+    wall = time.perf_counter() - t0
+    value = float(np.mean([v["value"] for v in vals]))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args, batch, H, dh),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle", "cores": vals[0]["cores"],
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(args, batch, H, dh, D=None):
+    if args.workload == "large_train":
+        return {"workload": f"MTGR-large-like HSTU layer training step (fwd+bwd): {batch.B} users, "
+                            f"{batch.T} tokens, d_model 1024, {H} heads x d_h {dh}, Seq lognormal median 300 "
+                            f"in [16,1000], RealTime U[0,64], 20 candidates, grad on candidates only",
+                "tokens": int(batch.T), "users": int(batch.B), "d_model": 1024, "n_heads": H, "d_h": dh,
+                "l2": "inputs larger than L2 (x and dx_out are 512 MiB each)", "parallelism": "replicas only"}
+    return {"workload": f"MTGR-small-like attention fwd+bwd: {batch.B} users, {batch.T} tokens, {H} heads x d_h {dh}",
+            "tokens": int(batch.T), "users": int(batch.B), "n_heads": H, "d_h": dh,
+            "l2": "inputs larger than L2", "parallelism": "replicas only"}
+
+
+# ---------------------------------------------------------------------------
+def run_mine(args):
+    import torch
+    import torch.distributed as dist
+
+    from hstu_attention_attn_b300 import mtgr, synth
+    from hstu_attention_attn_b300.layer import HstuAttention, HstuLayer, device_batch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    mtgr.lib()
+    pk = peaks()
+
+    # ---- inputs (seeded, synthetic; each replica draws its own batch) ----
+    if args.workload == "large_train":
+        L = synth.large_train_layer(args.seed + rank)
+        batch, H, dh, D = L.batch, L.H, L.dh, L.D
+    else:
+        A = synth.small_attn(1 + rank)
+        batch, H, dh, D = A.batch, A.H, A.dh, None
+    T = batch.T
+    db = device_batch(batch, dev)
+    cnt = torch.empty(T, dtype=torch.int32, device=dev)
+    tot = torch.zeros(1, dtype=torch.int64, device=dev)
+    mtgr.mtgr_debug_visible_counts(db.offsets, db.gid, db.ts, T, cnt, tot)
+    npairs = int(tot.item())
+    uf = attention_useful_flops(npairs, H, dh)
+
+    bf = torch.bfloat16
+    if args.workload == "large_train":
+        layer = HstuLayer(D, H, dh, torch.from_numpy(L.w_uqkv), torch.from_numpy(L.w_o), torch.from_numpy(L.gamma),
+                          torch.from_numpy(L.beta), dtype=bf, device=dev)
+        x_h = torch.from_numpy(L.x).to(bf).pin_memory()
+        dxo_h = torch.from_numpy(L.dx_out).to(bf).pin_memory()
+        x = x_h.to(dev)
+        dxo = dxo_h.to(dev)
+        saved = layer.alloc_saved(T)
+        x_out = torch.empty_like(x)
+        dx = torch.empty_like(x)
+        f = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)
+        grads = dict(dw_uqkv=f(D, 4 * H * dh), dw_o=f(H * dh, D), dgamma=f(4, D), dbeta=f(4, D))
+
+        def step():
+            layer.forward(x, db, saved, x_out)
+            layer.backward(x, saved, dxo, db, dx, grads)
+    else:
+        op = HstuAttention(H, dh, bf, device=dev)
+        q, k, v, u = (torch.from_numpy(m).to(dev).to(bf) for m in (A.q, A.k, A.v, A.u))
+        dy = torch.randn(T, H * dh, device=dev, dtype=bf, generator=torch.Generator(dev).manual_seed(5))
+
+        def step():
+            y, sv = op.forward(q, k, v, u, db)
+            op.backward(dy, q, k, v, u, sv, db)
+
+    # ---- warm-up, then the timed region ----
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    mtgr.mtgr_trace_reset()
+    mtgr.mtgr_trace_enable(True)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mtgr.mtgr_trace_enable(False)
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    cl = clocks.stop()
+    trace = mtgr.mtgr_trace_report()
+    K = args.steps
+    ms_step = ms_total / K
+    attn_ms = sum(trace.get(k, (0.0, 0))[0] for k in ATTN_KERNELS) / K
+    if world > 1:
+        t = torch.tensor([attn_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        attn_ms = float(t.item())
+    launches = sum(c for name, (_, c) in trace.items() if name != "dq_zero")
+    total_flops = (uf["fwd"] + uf["bwd"]) * world
+    value = total_flops / (attn_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel ----
+    dom = max(trace.items(), key=lambda kv: kv[1][0])
+    dname, (dms, dcnt) = dom
+    per_launch_ms = dms / dcnt
+    algo = None
+    if dname == "attn_bwd":
+        algo = dict(bound="tensor", flops=uf["bwd"])
+    elif dname == "attn_fwd":
+        algo = dict(bound="tensor", flops=uf["fwd"])
+    elif dname.startswith("gemm") and args.workload == "large_train":
+        HD, N4 = H * dh, 4 * H * dh
+        shapes = {"gemm_uqkv": (T, N4, D), "gemm_out": (T, D, HD), "gemm_dY": (T, HD, D), "gemm_dWo": (HD, D, T),
+                  "gemm_dWuqkv": (D, N4, T), "gemm_dxn": (T, D, N4)}
+        M, N, Kd = shapes[dname]
+        algo = dict(bound="tensor", flops=2.0 * M * N * Kd)
+    roof = None
+    if algo:
+        ach = algo["flops"] / (per_launch_ms * 1e-3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_sus"], "traffic": None,
+                "peak_note": f"{pk['src']} sustained dense bf16 (f16 operands run at the same tensor rate)"}
+    attn_core_ms = (trace.get("attn_fwd", (0, 0))[0] + trace.get("attn_bwd", (0, 0))[0]) / K
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e and args.workload == "large_train":
+        meta_h = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                  for a in (batch.offsets, batch.gid, batch.ts)]
+        g_h = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in grads.items()}
+        h2d = x_h.numel() * 2 + dxo_h.numel() * 2 + sum(m.numel() * m.element_size() for m in meta_h)
+        d2h = sum(t.numel() * t.element_size() for t in g_h.values())
+
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            dxo.copy_(dxo_h, non_blocking=True)
+            db.offsets.copy_(meta_h[0], non_blocking=True)
+            db.gid.copy_(meta_h[1], non_blocking=True)
+            db.ts.copy_(meta_h[2], non_blocking=True)
+            layer.forward(x, db, saved, x_out)
+            layer.backward(x, saved, dxo, db, dx, grads)
+            for n, t in grads.items():
+                g_h[n].copy_(t, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / K
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+               "note": "whole layer step incl. pinned-host copies of x, dx_out, metadata in and weight grads out"}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (f16 attention operands, fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(args, batch, H, dh, D),
+            "pct_bf16_peak": value / pk["bf16_sus"] * 100.0,
+            "tokens_per_s_per_layer": T * world / (ms_step * 1e-3),
+            "attention": {"visible_pairs": npairs, "useful_gflop_per_step": (uf["fwd"] + uf["bwd"]) / 1e9,
+                          "op_ms_per_step": attn_ms, "core_kernels_ms_per_step": attn_core_ms,
+                          "core_tflops": (uf["fwd"] + uf["bwd"]) / (attn_core_ms * 1e-3) / 1e12},
+            "kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in sorted(trace.items(), key=lambda kv: -kv[1][0])},
+            "gpu_launches": int(launches), "roofline": roof, "clocks": cl, "e2e": e2e}
+    if rank == 0 and not args.no_cpu:
+        try:
+            line["cpu_baseline"] = {k: v for k, v in cpu_baseline(batch, H, dh).items() if k != "wall_s"}
+        except Exception as ex:  # the CPU leg must not hide the GPU result
+            line["cpu_baseline"] = {"error": str(ex)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mine(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -3,6 +3,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "gemm.cuh"
@@ -41,6 +44,46 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
                                 float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
                                 const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
                                 int32_t* status, cudaStream_t s);
+
+// ---- kernel tracing ----
+namespace {
+struct TraceRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_pool;
+size_t g_pool_used = 0;
+int g_open = -1;
+
+cudaEvent_t pool_event() {
+  if (g_pool_used == g_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_pool.push_back(e);
+  }
+  return g_pool[g_pool_used++];
+}
+}  // namespace
+
+void trace_begin(const char* name, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on || g_open >= 0) return;
+  cudaEvent_t a = pool_event(), b = pool_event();
+  if (!a || !b) return;
+  cudaEventRecord(a, s);
+  g_trace.push_back({name, a, b});
+  g_open = (int)g_trace.size() - 1;
+}
+
+void trace_end(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_open < 0) return;
+  cudaEventRecord(g_trace[g_open].b, s);
+  g_open = -1;
+}
 
 // ---- error state ----
 static thread_local char g_err[512] = "";
@@ -250,6 +293,49 @@ using namespace mtgr;
 extern "C" {
 
 const char* mtgr_last_error(void) { return g_err; }
+
+void mtgr_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = on != 0;
+}
+
+void mtgr_trace_reset(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.clear();
+  g_pool_used = 0;
+  g_open = -1;
+}
+
+int mtgr_trace_report(int max_entries, char* names, int name_len, double* total_ms, int32_t* launches) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  std::vector<std::string> keys;
+  std::vector<double> ms;
+  std::vector<int32_t> cnt;
+  for (const TraceRec& r : g_trace) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+    size_t k = 0;
+    while (k < keys.size() && keys[k] != r.name) ++k;
+    if (k == keys.size()) {
+      keys.push_back(r.name);
+      ms.push_back(0.0);
+      cnt.push_back(0);
+    }
+    ms[k] += t;
+    cnt[k] += 1;
+  }
+  const int n = (int)keys.size();
+  for (int k = 0; k < n && k < max_entries; ++k) {
+    if (names && name_len > 0) {
+      strncpy(names + (size_t)k * name_len, keys[k].c_str(), name_len - 1);
+      names[(size_t)k * name_len + name_len - 1] = 0;
+    }
+    if (total_ms) total_ms[k] = ms[k];
+    if (launches) launches[k] = cnt[k];
+  }
+  return n;
+}
 int mtgr_version(void) { return 100; }
 
 mtgr_status mtgr_validate_batch(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T,
@@ -509,7 +595,7 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
     g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
     // [U|Q|K|V] = silu(z) is written in f16: the attention's tensor-core operands
     g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->z); g.ldz = N4;
-    g.splits = 1; g.status = status;
+    g.splits = 1; g.status = status; g.name = "gemm_uqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_SILU, T, N4, D, static_cast<const float*>(sv->xn), D, 1,
@@ -535,7 +621,7 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = true;
     g.epi = EPI_RESIDUAL; g.C = x_out; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
-    g.splits = 1; g.status = status;
+    g.splits = 1; g.status = status; g.name = "gemm_out";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_RESIDUAL, T, D, HD, static_cast<const float*>(sv->y), HD, 1,
@@ -582,7 +668,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     g.M = T; g.N = HD; g.K = D;
     g.A = static_cast<const bf*>(dx_out); g.lda = D; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = false;
-    g.epi = EPI_PLAIN; g.C = dY; g.ldc = HD; g.splits = 1; g.status = status;
+    g.epi = EPI_PLAIN; g.C = dY; g.ldc = HD; g.splits = 1; g.status = status; g.name = "gemm_dY";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dY gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, HD, D, static_cast<const float*>(dx_out), D, 1,
@@ -597,7 +683,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = true;
     g.B = static_cast<const bf*>(dx_out); g.ldb = D; g.b_mn_major = true;
     g.epi = EPI_F32; g.C = L.splits_o > 1 ? (void*)wpart : (void*)gr->dw_o; g.ldc = D;
-    g.splits = L.splits_o; g.status = status;
+    g.splits = L.splits_o; g.status = status; g.name = "gemm_dWo";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_o gemm");
     if (L.splits_o > 1)
       MTGR_CUDA_TRY(launch_split_reduce(wpart, L.splits_o, HD * D, HD * D, gr->dw_o, s), "layer_bwd dW_o reduce");
@@ -629,7 +715,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = true;
     g.B = static_cast<const bf*>(dZ); g.ldb = N4; g.b_mn_major = true;
     g.epi = EPI_F32; g.C = L.splits_uqkv > 1 ? (void*)wpart : (void*)gr->dw_uqkv; g.ldc = N4;
-    g.splits = L.splits_uqkv; g.status = status;
+    g.splits = L.splits_uqkv; g.status = status; g.name = "gemm_dWuqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_uqkv gemm");
     if (L.splits_uqkv > 1)
       MTGR_CUDA_TRY(launch_split_reduce(wpart, L.splits_uqkv, (int64_t)D * N4, (int64_t)D * N4, gr->dw_uqkv, s),
@@ -638,7 +724,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     h.M = T; h.N = D; h.K = N4;
     h.A = static_cast<const bf*>(dZ); h.lda = N4; h.a_mn_major = false;
     h.B = static_cast<const bf*>(w->w_uqkv); h.ldb = N4; h.b_mn_major = false;
-    h.epi = EPI_PLAIN; h.C = dxn; h.ldc = D; h.splits = 1; h.status = status;
+    h.epi = EPI_PLAIN; h.C = dxn; h.ldc = D; h.splits = 1; h.status = status; h.name = "gemm_dxn";
     MTGR_CUDA_TRY(launch_gemm_bf16(h, s), "layer_bwd dxn gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, D, N4, T, static_cast<const float*>(sv->xn), 1, D,

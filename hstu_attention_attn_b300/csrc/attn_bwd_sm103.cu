@@ -387,7 +387,11 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T);
   const int HD = H * d;
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * HD, s);
+  cudaError_t e;
+  {
+    TraceScope tr("dq_zero", s);
+    e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * HD, s);
+  }
   if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BT) ||
@@ -411,6 +415,8 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   p.ldacc = HD;
   const int64_t grid = L.max_items * H;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  {
+  TraceScope tr("attn_bwd", s);
   if (d == 128) {
     auto kern = attn_bwd_kernel<128>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<128>::SMEM);
@@ -425,8 +431,10 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
     return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   const int64_t n8 = (int64_t)T * HD / 8;
+  TraceScope tr2("dq_finish", s);
   dq_finish_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(dq_acc, T, HD, dq, ldg, zq, 4 * (int64_t)HD);
   return cudaGetLastError();
 }

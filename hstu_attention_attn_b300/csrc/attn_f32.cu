@@ -219,6 +219,7 @@ cudaError_t launch_attn_f32_fwd(const float* q, const float* k, const float* v, 
   if (T == 0 || B == 0) return cudaSuccess;
   const int64_t warps = T * H;
   const int blocks = (int)((warps * 32 + 127) / 128);
+  TraceScope tr("attn_f32_fwd", s);
   if (dh <= 64)
     attn_f32_fwd_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, users, B, ts, T, H, dh, O);
   else
@@ -233,6 +234,7 @@ cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, 
   if (T == 0 || B == 0) return cudaSuccess;
   const int64_t warps = T * H;
   const int blocks = (int)((warps * 32 + 127) / 128);
+  TraceScope tr("attn_f32_bwd", s);
   if (dh <= 64) {
     attn_f32_bwd_dq_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dq, ldg, zq);
     attn_f32_bwd_dkdv_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dk, dv, ldg, zk, zv);

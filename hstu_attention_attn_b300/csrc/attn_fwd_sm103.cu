@@ -283,6 +283,7 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
   p.status = status;
   const int64_t grid = L.max_items * H;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  TraceScope tr("attn_fwd", s);
   if (d == 128) {
     auto kern = attn_fwd_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<128>::SMEM);

@@ -334,6 +334,16 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 bool make_tmap_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                       uint32_t box_cols, uint32_t box_rows);
 int num_sms();
+
+// Kernel tracing: when enabled (mtgr_trace_enable), every launch inside a
+// TraceScope is bracketed by two CUDA events recorded on its stream.
+void trace_begin(const char* name, cudaStream_t s);
+void trace_end(cudaStream_t s);
+struct TraceScope {
+  cudaStream_t s;
+  TraceScope(const char* name, cudaStream_t st) : s(st) { trace_begin(name, st); }
+  ~TraceScope() { trace_end(s); }
+};
 }  // namespace mtgr
 
 #define MTGR_CUDA_TRY(expr, where)                      \

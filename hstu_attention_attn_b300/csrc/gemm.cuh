@@ -40,6 +40,7 @@ struct GemmArgs {
   int64_t ldz;
   int splits;  // split-K slices (EPI_F32 only); slice s covers its own K range
   int32_t* status;
+  const char* name;  // trace label
 };
 cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s);
 // fp32 out[i] = sum_s parts[s*stride + i] for i < n

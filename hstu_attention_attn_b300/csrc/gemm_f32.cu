@@ -71,6 +71,7 @@ cudaError_t launch_gemm_f32(int epi, int64_t M, int64_t N, int64_t K, const floa
                             int64_t ldr, float* Z, int64_t ldz, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
   dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + F_BM - 1) / F_BM));
+  TraceScope tr("gemm_f32", s);
   switch (epi) {
     case EPI_SILU:
       gemm_f32_kernel<EPI_SILU><<<grid, 256, 0, s>>>(M, N, K, A, sam, sak, B, sbk, sbn, C, ldc, R, ldr, Z, ldz);

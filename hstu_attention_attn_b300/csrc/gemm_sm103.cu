@@ -271,6 +271,7 @@ __global__ void split_reduce_kernel(const float* __restrict__ parts, int splits,
 cudaError_t launch_split_reduce(const float* parts, int splits, int64_t stride, int64_t n, float* out,
                                 cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  TraceScope tr("split_reduce", s);
   split_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(parts, splits, stride, n, out);
   return cudaGetLastError();
 }
@@ -313,6 +314,7 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   const int tiles = p.splits * p.m_tiles * p.n_tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   if (p.nk == 0) return cudaErrorInvalidValue;
+  TraceScope tr(a.name ? a.name : "gemm", s);
   gemm_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
   return cudaGetLastError();
 }

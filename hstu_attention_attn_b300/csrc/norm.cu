@@ -300,6 +300,7 @@ template <typename T>
 cudaError_t launch_gln_fwd(const T* x, T* y, float* mean, float* rstd, const uint8_t* gid, const float* gamma,
                            const float* beta, int64_t rows, int D, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
+  TraceScope tr("gln_fwd", s);
   NCH_DISPATCH(D, (gln_fwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(x, y, mean, rstd, gid, gamma, beta,
                                                                             rows, D, eps)));
   return cudaGetLastError();
@@ -317,13 +318,17 @@ cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const flo
                            int64_t rows, int D, cudaStream_t s) {
   const int nb = gln_bwd_blocks(rows);
   const size_t smem = (size_t)8 * D * sizeof(float);
+  {
+  TraceScope tr("gln_bwd", s);
   NCH_DISPATCH(D, ({
                  auto k = gln_bwd_kernel<T, NCHV>;
                  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                  k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D);
                }));
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  TraceScope tr("gln_param_reduce", s);
   gln_param_reduce_kernel<<<(8 * D + 255) / 256, 256, 0, s>>>(partial, nb, D, dgamma, dbeta);
   return cudaGetLastError();
 }
@@ -332,6 +337,7 @@ template <typename TU, typename TY>
 cudaError_t launch_ln_gate_fwd(const float* O, const TU* U, int64_t ldu, TY* Y, float* mean, float* rstd,
                                int64_t rows, int n, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
+  TraceScope tr("gate_fwd", s);
   NCH_DISPATCH(n, (ln_gate_fwd_kernel<TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd,
                                                                                      rows, n, eps)));
   return cudaGetLastError();
@@ -342,6 +348,7 @@ cudaError_t launch_ln_gate_bwd(const TG* dY, const float* O, const TU* U, int64_
                                const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* z, int64_t rows, int n,
                                cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
+  TraceScope tr("gate_bwd", s);
   NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
                       dY, O, U, ldu, mean, rstd, dO, dU, ldg, z, rows, n)));
   return cudaGetLastError();
@@ -365,6 +372,7 @@ cudaError_t launch_bf16_to_f16(const __nv_bfloat16* src, int64_t lds, __half* ds
                                int n, cudaStream_t s) {
   const int64_t n8 = rows * n / 8;
   if (n8 == 0) return cudaSuccess;
+  TraceScope tr("to_f16", s);
   convert_rows_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(src, lds, dst, ldd, rows, n);
   return cudaGetLastError();
 }

@@ -166,6 +166,7 @@ cudaError_t launch_user_info(const int32_t* offsets, int32_t B, const uint8_t* g
   if (B <= 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (int)(((int64_t)B * 32 + threads - 1) / threads);
+  TraceScope tr("plan_users", s);
   user_info_kernel<<<blocks, threads, 0, s>>>(offsets, B, gid, T, users, status);
   return cudaGetLastError();
 }
@@ -176,6 +177,7 @@ cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, i
   UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
   cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s);
   if (e != cudaSuccess) return e;
+  TraceScope tr("plan_items", s);
   plan_items_kernel<<<1, 1024, 0, s>>>(users, B, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.bwd_items), L.max_items, status);
   return cudaGetLastError();
@@ -186,6 +188,7 @@ cudaError_t launch_visible_counts(const int32_t* offsets, int32_t B, const uint8
   cudaError_t e = cudaMemsetAsync(total, 0, sizeof(int64_t), s);
   if (e != cudaSuccess) return e;
   if (B <= 0) return cudaSuccess;
+  TraceScope tr("visible_counts", s);
   visible_counts_kernel<<<B, 256, 0, s>>>(offsets, gid, ts, T, cnt, reinterpret_cast<unsigned long long*>(total));
   return cudaGetLastError();
 }

@@ -47,6 +47,9 @@ EXPORTS = {
     # name: (restype, argtypes)
     "mtgr_last_error": (C.c_char_p, []),
     "mtgr_version": (C.c_int, []),
+    "mtgr_trace_enable": (None, [C.c_int]),
+    "mtgr_trace_reset": (None, []),
+    "mtgr_trace_report": (C.c_int, [C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]),
     "mtgr_validate_batch": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
     "mtgr_debug_visible_counts": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64,
                                             C.c_void_p, C.c_void_p, C.c_void_p]),
@@ -122,6 +125,31 @@ def mtgr_last_error() -> str:
 
 def mtgr_version() -> int:
     return lib().mtgr_version()
+
+
+def mtgr_trace_enable(on: bool = True):
+    lib().mtgr_trace_enable(1 if on else 0)
+
+
+def mtgr_trace_reset():
+    lib().mtgr_trace_reset()
+
+
+def mtgr_trace_report(max_entries: int = 64) -> dict:
+    """{kernel name: (total device ms, launches)} since the last reset."""
+    name_len = 48
+    names = C.create_string_buffer(max_entries * name_len)
+    ms = (C.c_double * max_entries)()
+    cnt = (C.c_int32 * max_entries)()
+    n = lib().mtgr_trace_report(max_entries, C.cast(names, C.c_void_p), name_len, C.cast(ms, C.c_void_p),
+                                C.cast(cnt, C.c_void_p))
+    if n < 0:
+        raise MtgrError("mtgr_trace_report", n, "CUDA error while reading trace events")
+    out = {}
+    for k in range(min(n, max_entries)):
+        nm = names.raw[k * name_len:(k + 1) * name_len].split(b"\0", 1)[0].decode()
+        out[nm] = (float(ms[k]), int(cnt[k]))
+    return out
 
 
 def mtgr_validate_batch(offsets, gid, T, status_word, stream=None):

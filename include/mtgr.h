@@ -82,6 +82,17 @@ MTGR_API const char* mtgr_last_error(void);
 /* Library version (major*10000 + minor*100 + patch). */
 MTGR_API int mtgr_version(void);
 
+/* Kernel tracing (host side).  While enabled, every kernel launch of the
+ * library is bracketed by two CUDA events recorded on the launching stream.
+ * mtgr_trace_report() waits for the recorded events, then writes per kernel
+ * name (up to max_entries, each name truncated to name_len-1 bytes into
+ * names[k*name_len]) the summed device time in ms and the launch count, and
+ * returns the number of distinct names (-1 on a CUDA error).  The events are
+ * pooled and reused after mtgr_trace_reset(). */
+MTGR_API void mtgr_trace_enable(int on);
+MTGR_API void mtgr_trace_reset(void);
+MTGR_API int mtgr_trace_report(int max_entries, char* names, int name_len, double* total_ms, int32_t* launches);
+
 /* ------------------------------------------------------------------------- */
 /* Batch metadata                                                             */
 /* ------------------------------------------------------------------------- */
