@@ -8,6 +8,8 @@
 //  * Gate (paper-daily "模型怎么搭": normalise the aggregate, multiply by U):
 //      Y = LayerNorm(O) ⊙ U over the H·d_h features of a token, no affine
 //      (O is kept in fp32 in both precision paths).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace mtgr {
@@ -404,3 +406,112 @@ template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half>(const bf16_t*, c
                                                                 int64_t, const bf16_t*, int64_t, int, cudaStream_t);
 
 }  // namespace mtgr
+
+// ---------------------------------------------------------------------------
+// Group LayerNorm backward for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------
+// Some callers of this library cannot call cudaMalloc at the point where they
+// run the backward: a host framework that owns every allocation through its own
+// pool, a process whose device memory is fully reserved up front, or code that
+// must not allocate inside a latency-critical step.  They also cannot size and
+// pass the workspace that mtgr_group_layernorm_bwd needs for its per-block
+// partial sums of dγ / dβ.  mtgr_group_layernorm_bwd_noalloc keeps those partial
+// sums in the fixed array below instead.
+namespace mtgr {
+
+constexpr int64_t kGlnNoAllocFloats = int64_t(1) << 20;  // 4 MiB of fp32 partial sums
+static __device__ __align__(256) float g_gln_noalloc_partial[kGlnNoAllocFloats];
+
+namespace {
+// Device address of the array on the current device.  In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per device
+// with that device current and cached.
+float* gln_noalloc_scratch() {
+  static std::mutex mu;
+  static float* cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_gln_noalloc_partial);
+    if (e != cudaSuccess || p == nullptr) return nullptr;
+    cached[dev] = static_cast<float*>(p);
+  }
+  return cached[dev];
+}
+
+template <typename T>
+cudaError_t launch_gln_bwd_noalloc(const T* dy, const T* x, const float* mean, const float* rstd, const uint8_t* gid,
+                                   const float* gamma, const T* dres, T* dx, float* dgamma, float* dbeta,
+                                   float* partial, int64_t rows, int D, cudaStream_t s) {
+  // each block writes all 8*D of its partial sums, so fewer blocks than the
+  // workspace variant may run, but nothing has to be cleared beforehand
+  int nb = gln_bwd_blocks(rows);
+  const int64_t fit = kGlnNoAllocFloats / (8 * (int64_t)D);
+  if (nb > fit) nb = (int)fit;
+  const size_t smem = (size_t)8 * D * sizeof(float);
+  {
+    TraceScope tr("gln_bwd", s);
+    NCH_DISPATCH(D, ({
+                   auto k = gln_bwd_kernel<T, NCHV>;
+                   cudaError_t ea = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                   if (ea != cudaSuccess) return ea;
+                   k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D);
+                 }));
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  TraceScope tr("gln_param_reduce", s);
+  gln_param_reduce_kernel<<<(8 * D + 255) / 256, 256, 0, s>>>(partial, nb, D, dgamma, dbeta);
+  return cudaGetLastError();
+}
+}  // namespace
+}  // namespace mtgr
+
+extern "C" MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy, const void* x, const float* mean,
+                                                                 const float* rstd, const uint8_t* gid,
+                                                                 const float* gamma, const void* dx_residual,
+                                                                 void* dx, float* dgamma, float* dbeta, int64_t T,
+                                                                 int32_t D, mtgr_dtype dtype, mtgr_stream_t stream) {
+  using namespace mtgr;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!(T >= 0 && D > 0 && D % 8 == 0)) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: D must be a positive multiple of 8 and T >= 0");
+    return MTGR_ERR_UNSUPPORTED;
+  }
+  if (D > 4096) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: D = %d is above its maximum of 4096 (fixed 4 MiB device scratch)",
+              (int)D);
+    return MTGR_ERR_UNSUPPORTED;
+  }
+  if (dtype != MTGR_F32 && dtype != MTGR_BF16) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: bad dtype");
+    return MTGR_ERR_INVALID_ARG;
+  }
+  if (!dgamma || !dbeta || (T > 0 && !(dy && x && mean && rstd && gid && gamma && dx))) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: NULL pointer");
+    return MTGR_ERR_INVALID_ARG;
+  }
+  if (!(a16(dy) && a16(x) && a16(dx) && a16(gamma) && a16(dx_residual))) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: tensors must be 16-byte aligned");
+    return MTGR_ERR_INVALID_ARG;
+  }
+  float* partial = gln_noalloc_scratch();
+  if (!partial) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: cudaGetSymbolAddress of the device scratch failed: %s",
+              cudaGetErrorString(cudaGetLastError()));
+    return MTGR_ERR_CUDA;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == MTGR_BF16
+          ? launch_gln_bwd_noalloc(static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean,
+                                   rstd, gid, gamma, static_cast<const __nv_bfloat16*>(dx_residual),
+                                   static_cast<__nv_bfloat16*>(dx), dgamma, dbeta, partial, T, D, s)
+          : launch_gln_bwd_noalloc(static_cast<const float*>(dy), static_cast<const float*>(x), mean, rstd, gid,
+                                   gamma, static_cast<const float*>(dx_residual), static_cast<float*>(dx), dgamma,
+                                   dbeta, partial, T, D, s);
+  if (e != cudaSuccess) return cuda_status(e, "group_layernorm_bwd_noalloc");
+  return MTGR_OK;
+}

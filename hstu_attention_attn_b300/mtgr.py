@@ -58,6 +58,7 @@ EXPORTS = {
     "mtgr_group_layernorm_bwd_workspace_size": (C.c_size_t, [C.c_int64, C.c_int32]),
     "mtgr_group_layernorm_bwd": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p,
                                                                 C.c_size_t, C.c_void_p]),
+    "mtgr_group_layernorm_bwd_noalloc": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p]),
     "mtgr_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int]),
     "mtgr_hstu_attn_fwd": (C.c_int, [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
                                                          C.c_int64, C.c_int32, C.c_int32, C.c_float]
@@ -180,6 +181,17 @@ def mtgr_group_layernorm_bwd(dy, x, mean, rstd, gid, gamma, dx_residual, dx, dga
            lib().mtgr_group_layernorm_bwd(_p(dy), _p(x), _p(mean), _p(rstd), _p(gid), _p(gamma), _p(dx_residual),
                                           _p(dx), _p(dgamma), _p(dbeta), T, D, _dtype(x), _p(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_group_layernorm_bwd_noalloc(dy, x, mean, rstd, gid, gamma, dx_residual, dx, dgamma, dbeta, stream=None):
+    """Group LayerNorm backward without a workspace argument, for callers that
+    cannot allocate device memory; the library keeps its partial sums in a fixed
+    device array, so calls must not overlap on the GPU."""
+    T, D = x.shape
+    _check("mtgr_group_layernorm_bwd_noalloc",
+           lib().mtgr_group_layernorm_bwd_noalloc(_p(dy), _p(x), _p(mean), _p(rstd), _p(gid), _p(gamma),
+                                                  _p(dx_residual), _p(dx), _p(dgamma), _p(dbeta), T, D, _dtype(x),
+                                                  _stream(stream)))
 
 
 def mtgr_attn_workspace_size(B, T, n_heads, d_h, dtype) -> int:

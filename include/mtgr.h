@@ -9,7 +9,8 @@
  * Ownership.  Every pointer argument is caller-owned.  Tensor arguments are
  *   DEVICE pointers (current device) unless the comment says "host".  The
  *   library allocates no device memory of its own: scratch comes from the
- *   caller's `workspace`, sized by the matching *_workspace_size() query.
+ *   caller's `workspace`, sized by the matching *_workspace_size() query
+ *   (mtgr_group_layernorm_bwd_noalloc uses a fixed array inside the library).
  * Streams.  Every call enqueues work on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream) and returns without synchronising.
  * Layout.  Row-major.  T tokens of B users, user b owning rows
@@ -135,6 +136,26 @@ MTGR_API mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, con
                                      const uint8_t* gid, const float* gamma, const void* dx_residual, void* dx,
                                      float* dgamma, float* dbeta, int64_t T, int32_t D, mtgr_dtype dtype,
                                      void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
+
+/* Same result as mtgr_group_layernorm_bwd, for callers that cannot allocate
+ * device memory when they call it (a framework whose allocator owns all device
+ * memory, a process that reserved its memory up front, a latency-critical step
+ * that must not allocate) and so cannot pass a workspace.  The pages have no
+ * counterpart: this is a packaging variant, not a step of the method.
+ * The per-block dγ/dβ partial sums go to one fixed 4 MiB device array inside
+ * the library (held by every device that loads the library until the process
+ * exits).  Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ * call.  Limit: D <= 4096 (a launch uses at most 1,048,576 / (8*D) blocks);
+ * larger D returns MTGR_ERR_UNSUPPORTED with a message.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  Every call
+ * shares the array and overwrites the part it reads, so no clearing is needed,
+ * but calls that overlap on the GPU (other streams, other host threads) race on
+ * it: serialise them.  Arguments, layouts and errors as mtgr_group_layernorm_bwd. */
+MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy, const void* x, const float* mean,
+                                             const float* rstd, const uint8_t* gid, const float* gamma,
+                                             const void* dx_residual, void* dx, float* dgamma, float* dbeta,
+                                             int64_t T, int32_t D, mtgr_dtype dtype, mtgr_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* HSTU attention (marovi.ai "Métodos" block formula; paper-daily "模型怎么搭")  */
