@@ -13,13 +13,22 @@
 // rescaling: the accumulator simply sums, and 1/n_u is one per-row scale at
 // the end (n_u is constant over a user's rows).
 //
-// CTA = one (user, query tile, head) work item from the longest-first list.
-//   warp 0      TMA: Q once, then K_j / V_j (one buffer each)
-//   warp 1      MMA issuer (one thread) + TMEM owner
-//   warps 2..5  P epilogue (thread = query row = TMEM lane) and the O store
-// TMEM: S at columns [0,128) (P aliases its first 64 columns as packed f16),
-// O at [128, 128+d_h).  96 KB of shared memory and 256 TMEM columns per CTA,
-// so two CTAs share an SM and interleave their MMA and epilogue phases.
+// Persistent kernel, one CTA per SM.  A work item is a pair of consecutive
+// query tiles (slots a and b) of one (user, head); both slots share one stream
+// of K/V tiles (the union of their key lists) through a TMA ring, and the two
+// slots ping-pong: while the epilogue of one slot turns S into P, the tensor
+// core works on the other slot.
+//   warp 0       TMA: Q_a/Q_b per item, then K_j, V_j into a 4-stage ring
+//   warp 1       MMA issuer (one thread) + TMEM owner
+//   warps 2..9   slot a epilogue: two warpgroups, one per half of the 128 key
+//                columns (thread = query row = TMEM lane), then the O store
+//   warps 10..17 slot b epilogue
+// TMEM (512 columns): S_a [0,128), S_b [128,256), O_a [256, 256+d_h),
+// O_b [256+d_h, 256+2 d_h).  P overwrites S as packed f16: the keys of column
+// half g go to columns 64g .. 64g+31 of the slot's S region, so each
+// warpgroup only ever writes the columns it has already read.
+// The fp32 O rows leave through a per-warp shared-memory transpose so that the
+// global stores are coalesced.
 #include "common.cuh"
 #include "plan.cuh"
 
@@ -27,26 +36,34 @@ namespace mtgr {
 namespace {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 576;  // 18 warps
+constexpr int EPI_WARPS = 8;      // per slot
+constexpr int RING = 4;
+constexpr int STG_FLOATS = 32 * 16;  // per-warp O staging: 32 rows x 16 fp32
 
 template <int D>
 struct FwdCfg {
-  static constexpr int TILE_BYTES = BQ * D * 2;  // one Q / K / V tile
-  // at least ~100 KB so that no more than two CTAs (2 x 256 TMEM columns) share an SM
-  static constexpr int SMEM = (3 * TILE_BYTES + 1152) > 102400 ? (3 * TILE_BYTES + 1152) : 102400;
-  static constexpr uint32_t TMEM_COLS = 256;
-  static constexpr uint32_t S_COL = 0, O_COL = 128;
+  static constexpr int TILE = BQ * D * 2;  // one Q / K / V tile (f16)
+  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int STG_OFF = RING_OFF + RING * TILE;  // O staging, one buffer per epilogue warp
+  static constexpr int BAR_OFF = STG_OFF + 2 * EPI_WARPS * STG_FLOATS * 4;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  // TMEM columns of slot sl: S (and P) at s_col, the O accumulator at o_col
+  __device__ static constexpr uint32_t s_col(int sl) { return (uint32_t)sl * 128u; }
+  __device__ static constexpr uint32_t o_col(int sl) { return 256u + (uint32_t)sl * D; }
 };
 
-struct FwdSmem {
-  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, o_full, pv_done;
+struct FwdBars {
+  uint64_t q_full, q_empty;
+  uint64_t ring_full[RING], ring_empty[RING];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_full[2], o_free[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct FwdParams {
   const UserInfo* users;
-  const WorkItem* items;
+  const WorkItem* items;  // (user, first query tile of the pair), longest first
   const int32_t* counts;
   const int64_t* ts;
   float* O;  // [T, H*D] fp32
@@ -58,7 +75,6 @@ struct FwdParams {
 
 // Shared-memory descriptors of a [128 rows][D] 16-bit tile staged as D/64 boxes
 // of [128][64] with 128-byte swizzle (16 KB per box).
-template <int D>
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {  // K = d, step 16
   return smem_desc_sw128(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
 }
@@ -66,43 +82,110 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {  // K 
   return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
 }
 
+// Item sequence of one CTA: rounds of gridDim.x items, serpentine so that the
+// longest-first order is dealt out evenly.
+__device__ __forceinline__ int item_at(int round) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+struct ItemCtx {
+  UserInfo u;
+  PairKeys pk;
+  int h;
+};
+__device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
+  ItemCtx c;
+  const int pi = idx / p.H;
+  c.h = idx - pi * p.H;
+  const WorkItem wi = p.items[pi];
+  c.u = p.users[wi.b];
+  c.pk = pair_keys(c.u, wi.t);
+  return c;
+}
+
+// silu(x) with h = x/2: h + h tanh(h)
+__device__ __forceinline__ float silu_half(float h) { return fmaf(h, tanh_approx(h), h); }
+
+// N scores of one query row (keys j0 .. j0+N-1 of the segment) -> N/2 packed
+// f16 P values under the dynamic mixed mask.  The chunk class depends only on
+// j0, so it is uniform across the warp.
+template <int N>
+__device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const UserInfo& u, int ri, bool row_ok,
+                                        bool cand, int64_t thr, const int64_t* ts_u, float hs,
+                                        uint32_t (&pk)[N / 2]) {
+  if (j0 + N <= u.eS) {
+    // every key is User/Seq: visible to every row
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e)
+      pk[e] = pack_f16x2(silu_half(__uint_as_float(r[2 * e]) * hs), silu_half(__uint_as_float(r[2 * e + 1]) * hs));
+  } else if (j0 >= u.eR) {
+    // candidate keys (or keys past the segment): only the diagonal is visible
+    const int ed = ri - j0;
+    const bool diag = cand && row_ok && ed >= 0 && ed < N;
+    float sd = 0.f;
+#pragma unroll
+    for (int e = 0; e < N; ++e) sd = (e == ed) ? __uint_as_float(r[e]) : sd;
+    const float pd = diag ? silu_half(sd * hs) : 0.f;
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) pk[e] = pack_f16x2((2 * e == ed) ? pd : 0.f, (2 * e + 1 == ed) ? pd : 0.f);
+  } else {
+    // the chunk overlaps the RealTime keys: full predicate
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) {
+      float pv[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int jj = j0 + 2 * e + t;
+        bool vis;
+        if (jj < u.eS)
+          vis = true;
+        else if (jj < u.eR)
+          vis = __ldg(ts_u + jj) < thr;
+        else
+          vis = cand && jj == ri;
+        const float v = silu_half(__uint_as_float(r[2 * e + t]) * hs);
+        pv[t] = vis ? v : 0.f;
+      }
+      pk[e] = pack_f16x2(pv[0], pv[1]);
+    }
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 2)
+__global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers each (5 warps on some SMSPs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Cfg = FwdCfg<D>;
-  const int item_idx = blockIdx.x / p.H;
-  const int h = blockIdx.x - item_idx * p.H;
-  if (item_idx >= p.counts[0]) return;
-  const WorkItem wi = p.items[item_idx];
-  const UserInfo u = p.users[wi.b];
-  const int qt = wi.t;
-  const QTileKeys keys = qtile_keys(u, qt);
-  const int nk = keys.count();
+  const int total = p.counts[0] * p.H;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sK = base + Cfg::TILE_BYTES;
-  uint8_t* sV = base + 2 * Cfg::TILE_BYTES;
-  FwdSmem& S = *reinterpret_cast<FwdSmem*>(base + 3 * Cfg::TILE_BYTES);
+  uint8_t* sQ = base;  // Q_a, Q_b
+  uint8_t* sRing = base + Cfg::RING_OFF;
+  float* sStg = reinterpret_cast<float*>(base + Cfg::STG_OFF);
+  FwdBars& S = *reinterpret_cast<FwdBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&S.q_full, 1);
-    mbar_init(&S.k_full, 1);
-    mbar_init(&S.k_empty, 1);
-    mbar_init(&S.v_full, 1);
-    mbar_init(&S.v_empty, 1);
-    mbar_init(&S.s_full, 1);
-    mbar_init(&S.p_full, 4);
-    mbar_init(&S.o_full, 1);
-    mbar_init(&S.pv_done, 1);
+    mbar_init(&S.q_empty, 1);
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&S.ring_full[i], 1);
+      mbar_init(&S.ring_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.s_full[i], 1);
+      mbar_init(&S.p_full[i], EPI_WARPS);
+      mbar_init(&S.pv_done[i], 1);
+      mbar_init(&S.o_full[i], 1);
+      mbar_init(&S.o_free[i], EPI_WARPS);
+    }
     S.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, Cfg::TMEM_COLS);
+    tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -116,25 +199,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
   bool ok = true;
-  const int col_h = h * D;  // column of this head inside q / k / v
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_arrive_expect_tx(&S.q_full, Cfg::TILE_BYTES);
+      int stage = 0;
+      uint32_t ph = 0;
+      int n_items = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const ItemCtx c = item_ctx(p, idx);
+        const int col_h = c.h * D;
+        if (!mbar_wait(&S.q_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        const bool two = c.pk.qb >= 0;
+        mbar_arrive_expect_tx(&S.q_full, (two ? 2 : 1) * Cfg::TILE);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sQ + c * 16384, &tmQ, &S.q_full, col_h + 64 * c, u.start + qt * BQ);
-      for (int i = 0; i < nk && ok; ++i) {
-        const int row = u.start + keys.kt(i, qt) * BKV;
-        if (!mbar_wait(&S.k_empty, (i & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&S.k_full, Cfg::TILE_BYTES);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          tma_load_2d(sQ + cc * 16384, &tmQ, &S.q_full, col_h + 64 * cc, c.u.start + c.pk.qa * BQ);
+          if (two) tma_load_2d(sQ + Cfg::TILE + cc * 16384, &tmQ, &S.q_full, col_h + 64 * cc,
+                               c.u.start + c.pk.qb * BQ);
+        }
+        const int nk = c.pk.count();
+        for (int i = 0; i < nk && ok; ++i) {
+          const int row = c.u.start + c.pk.kt(i) * BKV;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_2d(sK + c * 16384, &tmK, &S.k_full, col_h + 64 * c, row);
-        if (!mbar_wait(&S.v_empty, (i & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&S.v_full, Cfg::TILE_BYTES);
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!mbar_wait(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* dst = sRing + stage * Cfg::TILE;
+            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_2d(sV + c * 16384, &tmV, &S.v_full, col_h + 64 * c, row);
+            for (int cc = 0; cc < D / 64; ++cc)
+              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
+            if (++stage == RING) { stage = 0; ph ^= 1; }
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -142,107 +242,207 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BQ, BKV, false, false);
       constexpr uint32_t idesc_o = idesc_f16_f32(BQ, D, false, true);
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint32_t t_s = tmem + Cfg::S_COL, t_o = tmem + Cfg::O_COL;
-      if (!mbar_wait(&S.q_full, 0, abort_flag)) ok = false;
-      for (int i = 0; i < nk && ok; ++i) {
-        const uint32_t par = i & 1;
-        if (!mbar_wait(&S.k_full, par, abort_flag)) { ok = false; break; }
-        // S_i overwrites the columns that hold P_{i-1}: wait until P_{i-1} V_{i-1} has read them
-        if (i > 0 && !mbar_wait(&S.pv_done, par ^ 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      const uint32_t q_addr[2] = {smem_u32(sQ), smem_u32(sQ + Cfg::TILE)};
+      const uint32_t ring_addr = smem_u32(sRing);
+      int stage = 0;
+      uint32_t ph = 0;
+      int n_items = 0;
+      bool pv_pending[2] = {false, false}, o_pending[2] = {false, false};
+      uint32_t pv_waits[2] = {0, 0}, p_waits[2] = {0, 0}, o_waits[2] = {0, 0};
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const ItemCtx c = item_ctx(p, idx);
+        if (!mbar_wait(&S.q_full, n_items & 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        bool first[2] = {true, true};
+        const int nk = c.pk.count();
+        // Issue order per key tile i: PV_a(i), S_a(i+1), PV_b(i), S_b(i+1), so the
+        // two epilogues alternate: slot a's P(i+1) is computed while the tensor
+        // core runs PV_b(i) and S_b(i+1), and the other way round.  S_slot(i+1)
+        // overwrites the columns P_slot(i) is read from, so it waits for PV_slot(i).
+        auto issue_s = [&](int sl, uint32_t k_addr) -> bool {
+          if (pv_pending[sl]) {
+            if (!mbar_wait(&S.pv_done[sl], pv_waits[sl] & 1, abort_flag)) return false;
+            ++pv_waits[sl];
+            pv_pending[sl] = false;
+            tc_fence_after();
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(t_s, kmajor_desc<D>(q_addr, kk), kmajor_desc<D>(k_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.k_empty);
-        tc_commit(&S.s_full);
-        if (!mbar_wait(&S.p_full, par, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&S.v_full, par, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tmem + Cfg::s_col(sl), kmajor_desc(q_addr[sl], kk), kmajor_desc(k_addr, kk), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          tc_commit(&S.s_full[sl]);
+          return true;
+        };
+        auto issue_pv = [&](int sl, uint32_t v_addr) -> bool {
+          if (!mbar_wait(&S.p_full[sl], p_waits[sl] & 1, abort_flag)) return false;
+          ++p_waits[sl];
+          if (first[sl] && o_pending[sl]) {  // O_slot still holds the previous item's result
+            if (!mbar_wait(&S.o_free[sl], o_waits[sl] & 1, abort_flag)) return false;
+            ++o_waits[sl];
+            o_pending[sl] = false;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          tc_mma_ts(t_o, t_s + kk * 8, mnmajor_desc(v_addr, kk), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&S.v_empty);
-        tc_commit(&S.pv_done);
+          for (int kk = 0; kk < BKV / 16; ++kk)  // keys 16kk..16kk+15: column half kk/4, packed columns
+            tc_mma_ts(tmem + Cfg::o_col(sl), tmem + Cfg::s_col(sl) + (kk >> 2) * 64 + (kk & 3) * 8,
+                      mnmajor_desc(v_addr, kk), idesc_o, (!first[sl] || kk > 0) ? 1u : 0u);
+          tc_commit(&S.pv_done[sl]);
+          pv_pending[sl] = true;
+          first[sl] = false;
+          return true;
+        };
+        // prologue: S of the first key tile
+        {
+          const int kt = c.pk.kt(0);
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = ring_addr + stage * Cfg::TILE;
+          if (c.pk.in_a(kt) && !issue_s(0, k_addr)) { ok = false; break; }
+          if (c.pk.in_b(kt) && !issue_s(1, k_addr)) { ok = false; break; }
+          tc_commit(&S.ring_empty[stage]);
+          if (nk == 1) tc_commit(&S.q_empty);
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+        }
+        for (int i = 0; i < nk && ok; ++i) {
+          const int kt = c.pk.kt(i);
+          const bool in[2] = {c.pk.in_a(kt), c.pk.in_b(kt)};
+          const bool more = i + 1 < nk;
+          const int kt1 = more ? c.pk.kt(i + 1) : 0;
+          const bool in1[2] = {more && c.pk.in_a(kt1), more && c.pk.in_b(kt1)};
+          // V_i, then K_{i+1} (ring order)
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          const int v_stage = stage;
+          const uint32_t v_addr = ring_addr + stage * Cfg::TILE;
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+          int k_stage = -1;
+          uint32_t k_addr = 0;
+          if (more) {
+            if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+            k_stage = stage;
+            k_addr = ring_addr + stage * Cfg::TILE;
+            if (++stage == RING) { stage = 0; ph ^= 1; }
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int sl = 0; sl < 2; ++sl) {
+            if (in[sl] && !issue_pv(sl, v_addr)) { ok = false; break; }
+            if (in1[sl] && !issue_s(sl, k_addr)) { ok = false; break; }
+          }
+          if (!ok) break;
+          tc_commit(&S.ring_empty[v_stage]);
+          if (more) {
+            tc_commit(&S.ring_empty[k_stage]);
+            if (i + 2 == nk) tc_commit(&S.q_empty);  // the item's last S has been issued
+          }
+        }
+        if (!ok) break;
+        for (int sl = 0; sl < 2; ++sl) {
+          if (!first[sl]) {
+            tc_commit(&S.o_full[sl]);
+            o_pending[sl] = true;
+          }
+        }
       }
-      tc_commit(&S.o_full);
     }
   } else {
-    // ---------------- P epilogue (warps 2..5) ----------------
-    const int quarter = warp & 3;
+    // ---------------- epilogue warpgroups ----------------
+    const int ew = warp - 2;             // 0..15
+    const int sl = ew >> 3;              // slot
+    const int g = (ew >> 2) & 1;         // column half of S (and of O)
+    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    const int ri = qt * BQ + quarter * 32 + lane;  // segment-relative query row
-    const bool row_ok = ri < u.n;
-    const int row_cls = ri < u.eS ? 0 : (ri < u.eR ? 1 : 2);  // 0 User/Seq, 1 RealTime, 2 Cand
-    const int64_t ts_i = (row_ok && row_cls > 0) ? p.ts[u.start + ri] : 0;
-    const float hs = 0.5f * p.scale;  // silu(x) = h + h tanh(h), h = x/2
-    for (int i = 0; i < nk && ok; ++i) {
-      const int kt = keys.kt(i, qt);
-      if (!mbar_wait(&S.s_full, i & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int k0 = kt * BKV;
-      const bool all_static = k0 + BKV <= u.eS;
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + Cfg::S_COL + c * 32 + lane_sel, r);
+    const int r_in = quarter * 32 + lane;
+    const float hs = 0.5f * p.scale;
+    float* stg = sStg + ew * STG_FLOATS;
+    uint32_t s_waits = 0, o_waits = 0;
+    for (int r = 0; ok; ++r) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const ItemCtx c = item_ctx(p, idx);
+      const int qt = sl == 0 ? c.pk.qa : c.pk.qb;
+      if (qt < 0) continue;
+      const UserInfo& u = c.u;
+      const int ri = qt * BQ + r_in;  // segment-relative query row
+      const bool row_ok = ri < u.n;
+      const bool cand = ri >= u.eR;
+      // RealTime key j is visible to this row iff ts_j < thr (User/Seq rows: never)
+      int64_t thr = INT64_MIN;
+      if (row_ok && ri >= u.eS) thr = p.ts[u.start + ri] + (cand ? 0 : 1);
+      const int64_t* ts_u = p.ts + u.start;
+      bool any = false;
+      const int nk = c.pk.count();
+      for (int i = 0; i < nk && ok; ++i) {
+        const int kt = c.pk.kt(i);
+        if (!(sl == 0 ? c.pk.in_a(kt) : c.pk.in_b(kt))) continue;
+        any = true;
+        if (!mbar_wait(&S.s_full[sl], s_waits & 1, abort_flag)) { ok = false; break; }
+        ++s_waits;
+        tc_fence_after();
+        const uint32_t t_s = tmem + Cfg::s_col(sl) + g * 64 + lane_sel;
+        const int jg = kt * BKV + g * 64;  // first key of this warp's column half
+        // 4 chunks of 16 keys; the load of chunk c+1 is in flight while chunk c
+        // is computed.  P of chunk c goes to columns 8c..8c+7 of this half,
+        // which chunk c/2 has already read.
+        uint32_t rc[2][16], pk[8];
+        tmem_ld16(t_s, rc[0]);
         tmem_wait_ld();
-        uint32_t pk[16];
-        if (all_static) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float h0 = __uint_as_float(r[2 * e]) * hs, h1 = __uint_as_float(r[2 * e + 1]) * hs;
-            pk[e] = pack_f16x2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pv[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int rj = k0 + c * 32 + 2 * e + t;
-              bool vis;
-              if (rj < u.eS) {
-                vis = true;
-              } else if (rj < u.eR) {
-                const int64_t ts_j = p.ts[u.start + rj];
-                vis = row_cls == 1 ? (ts_j <= ts_i) : (row_cls == 2 && ts_j < ts_i);
-              } else {
-                vis = (rj == ri) && rj < u.n;
-              }
-              const float hh = __uint_as_float(r[2 * e + t]) * hs;
-              pv[t] = vis ? fmaf(hh, tanh_approx(hh), hh) : 0.f;
-            }
-            pk[e] = pack_f16x2(pv[0], pv[1]);
-          }
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch < 3) tmem_ld16(t_s + 16 * (ch + 1), rc[(ch + 1) & 1]);
+          p_chunk<16>(rc[ch & 1], jg + 16 * ch, u, ri, row_ok, cand, thr, ts_u, hs, pk);
+          tmem_st8(t_s + 8 * ch, pk);
+          if (ch < 3) tmem_wait_ld();
         }
-        tmem_st16(tmem + Cfg::S_COL + c * 16 + lane_sel, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[sl]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full);
-    }
-    // ---------------- O = acc / n_u -> global ----------------
-    if (ok && mbar_wait(&S.o_full, 0, abort_flag)) {
+      if (!ok || !any) {
+        if (!any) continue;
+        break;
+      }
+      // ---------------- O = acc / n_u -> global (columns g*D/2 .. of this head) ----------------
+      if (!mbar_wait(&S.o_full[sl], o_waits & 1, abort_flag)) { ok = false; break; }
+      ++o_waits;
       tc_fence_after();
       const float inv_n = 1.0f / (float)u.n;
-      float* orow = p.O + (int64_t)(u.start + ri) * p.ldo + col_h;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + Cfg::O_COL + c * 32 + lane_sel, r);
+      const int row0 = qt * BQ + quarter * 32;  // segment-relative first row of this warp
+      float* obase = p.O + (int64_t)(u.start + row0) * p.ldo + c.h * D + g * (D / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + Cfg::o_col(sl) + g * (D / 2) + cc * 32 + lane_sel, rr);
         tmem_wait_ld();
-        if (row_ok) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<float4*>(orow + c * 32 + 4 * v) =
-                make_float4(__uint_as_float(r[4 * v + 0]) * inv_n, __uint_as_float(r[4 * v + 1]) * inv_n,
-                            __uint_as_float(r[4 * v + 2]) * inv_n, __uint_as_float(r[4 * v + 3]) * inv_n);
+        for (int sub = 0; sub < 2; ++sub) {
+          // row r_in's 16 values -> stg[lane][16], 16-byte slots XOR-swizzled by row
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int slot = v ^ ((lane >> 1) & 3);
+            *reinterpret_cast<float4*>(stg + lane * 16 + slot * 4) =
+                make_float4(__uint_as_float(rr[sub * 16 + 4 * v + 0]) * inv_n,
+                            __uint_as_float(rr[sub * 16 + 4 * v + 1]) * inv_n,
+                            __uint_as_float(rr[sub * 16 + 4 * v + 2]) * inv_n,
+                            __uint_as_float(rr[sub * 16 + 4 * v + 3]) * inv_n);
+          }
+          __syncwarp();
+          // 8 rows x 64 bytes per store instruction
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int rw = it * 8 + (lane >> 2), c4 = lane & 3;
+            const float4 val = *reinterpret_cast<const float4*>(stg + rw * 16 + (c4 ^ ((rw >> 1) & 3)) * 4);
+            if (row0 + rw < u.n)
+              *reinterpret_cast<float4*>(obase + (int64_t)rw * p.ldo + cc * 32 + sub * 16 + c4 * 4) = val;
+          }
         }
       }
-    } else {
-      ok = false;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.o_free[sl]);
     }
   }
 
@@ -254,16 +454,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 }  // namespace
 
 // q, k, v: [T, *] f16 with row stride ld; O: [T, H*d] fp32.
-cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* v,
-                                 int64_t ld, int64_t T, int H, int d, const int32_t* plan, int32_t B,
-                                 const int64_t* ts, float* O, int32_t* status, cudaStream_t s) {
+cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, int64_t T, int H,
+                                int d, const int32_t* plan, int32_t B, const int64_t* ts, float* O, int32_t* status,
+                                cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T);
   const int HD = H * d;
@@ -281,19 +481,20 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
   p.H = H;
   p.scale = 1.0f / sqrtf((float)d);
   p.status = status;
-  const int64_t grid = L.max_items * H;
-  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  // persistent: one CTA per SM (the item count lives on the device; CTAs without an item exit at once)
+  const int64_t max_items = L.max_items * H;
+  const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
   TraceScope tr("attn_fwd", s);
   if (d == 128) {
     auto kern = attn_fwd_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<128>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, p);
   } else if (d == 64) {
     auto kern = attn_fwd_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<64>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, p);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -45,8 +45,18 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
   }
 }
 
-// One block: bucket every query tile (forward) and key tile (backward) by the
-// number of tiles it pairs with, then scatter into lists ordered longest first.
+// Cost of a forward work item (query tiles qa and qa + 1 of a user): tensor
+// tiles of both, i.e. key tiles visited by each.
+__device__ __forceinline__ int fwd_cost(const UserInfo& u, int qa) {
+  const PairKeys pk = pair_keys(u, qa);
+  int c = 0;
+  for (int i = 0; i < pk.count(); ++i) c += (pk.in_a(pk.kt(i)) ? 1 : 0) + (pk.in_b(pk.kt(i)) ? 1 : 0);
+  return min(c, kBuckets - 1);
+}
+
+// One block: bucket every forward item (pair of query tiles) and backward item
+// (key tile) by its number of tile products, then scatter into lists ordered
+// longest first.
 __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B,
                                                           int32_t* __restrict__ counts,
                                                           WorkItem* __restrict__ fwd_items,
@@ -61,10 +71,8 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
     for (int t = 0; t < nt; ++t) {
-      const int cf = min(qtile_keys(u, t).count(), kBuckets - 1);
-      const int cb = min(ktile_queries(u, t).count(), kBuckets - 1);
-      atomicAdd(&hist[0][cf], 1);
-      atomicAdd(&hist[1][cb], 1);
+      if ((t & 1) == 0) atomicAdd(&hist[0][fwd_cost(u, t)], 1);
+      atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
     }
   }
   __syncthreads();
@@ -91,11 +99,11 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
     for (int t = 0; t < nt; ++t) {
-      const int cf = min(qtile_keys(u, t).count(), kBuckets - 1);
-      const int cb = min(ktile_queries(u, t).count(), kBuckets - 1);
-      const int pf = atomicAdd(&hist[0][cf], 1);
-      const int pb = atomicAdd(&hist[1][cb], 1);
-      if (pf < max_items) fwd_items[pf] = WorkItem{b, t};
+      if ((t & 1) == 0) {
+        const int pf = atomicAdd(&hist[0][fwd_cost(u, t)], 1);
+        if (pf < max_items) fwd_items[pf] = WorkItem{b, t};
+      }
+      const int pb = atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
       if (pb < max_items) bwd_items[pb] = WorkItem{b, t};
     }
   }

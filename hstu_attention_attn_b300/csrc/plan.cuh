@@ -49,6 +49,46 @@ __host__ __device__ __forceinline__ QTileKeys qtile_keys(const UserInfo& u, int 
   return k;
 }
 
+// Key tiles of a pair of consecutive query tiles (qa, qb = qa + 1, or qb = -1
+// when qa is the user's last tile) processed together by the forward kernel:
+// the union of both key lists, in increasing order, with per-tile membership.
+// Rows of qa precede rows of qb, so hi_a <= hi_b and the union is [0, hi_b)
+// plus the diagonal tiles that lie at or beyond it.
+struct PairKeys {
+  int qa, qb;
+  int hi_a, ea, hi_b, eb;  // key list of each tile: [0, hi) plus the diagonal when e
+  int hi;                  // max(hi_a, hi_b)
+  __host__ __device__ __forceinline__ bool xa() const { return ea && qa >= hi; }
+  __host__ __device__ __forceinline__ bool xb() const { return eb && qb >= hi; }
+  __host__ __device__ __forceinline__ int count() const { return hi + (xa() ? 1 : 0) + (xb() ? 1 : 0); }
+  __host__ __device__ __forceinline__ int kt(int i) const {
+    if (i < hi) return i;
+    return (i == hi && xa()) ? qa : qb;
+  }
+  __host__ __device__ __forceinline__ bool in_a(int k) const { return k < hi_a || (ea && k == qa); }
+  __host__ __device__ __forceinline__ bool in_b(int k) const { return qb >= 0 && (k < hi_b || (eb && k == qb)); }
+};
+
+__host__ __device__ __forceinline__ PairKeys pair_keys(const UserInfo& u, int qa) {
+  PairKeys p;
+  const int nt = ceil_div(u.n, kTile);
+  p.qa = qa;
+  p.qb = qa + 1 < nt ? qa + 1 : -1;
+  const QTileKeys a = qtile_keys(u, qa);
+  p.hi_a = a.hi;
+  p.ea = a.extra;
+  if (p.qb >= 0) {
+    const QTileKeys b = qtile_keys(u, p.qb);
+    p.hi_b = b.hi;
+    p.eb = b.extra;
+  } else {
+    p.hi_b = 0;
+    p.eb = 0;
+  }
+  p.hi = p.hi_a > p.hi_b ? p.hi_a : p.hi_b;
+  return p;
+}
+
 // Query tiles visiting key tile kt: tiles [lo, nq) then (if extra) tile kt.
 struct KTileQueries {
   int lo, nq;
@@ -75,8 +115,8 @@ __host__ __device__ __forceinline__ KTileQueries ktile_queries(const UserInfo& u
 // Workspace layout of a plan (all int32), offsets in elements.
 struct PlanLayout {
   int64_t users;      // UserInfo[B]
-  int64_t counts;     // [4]: fwd items, bwd items, (reserved)
-  int64_t fwd_items;  // WorkItem[max_items]
+  int64_t counts;     // [4]: fwd query-tile pairs, bwd key tiles, (reserved)
+  int64_t fwd_items;  // WorkItem[max_items]: (user, first query tile of the pair)
   int64_t bwd_items;  // WorkItem[max_items]
   int64_t hist;       // [2][kBuckets] histograms / cursors
   int64_t total;      // int32 count
