@@ -41,7 +41,7 @@ cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int
                                 const int32_t*, int32_t, const int64_t*, float*, int32_t*, cudaStream_t);
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
-                                float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
+                                __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
                                 const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
                                 int32_t* status, cudaStream_t s);
 
@@ -156,11 +156,11 @@ bool make_tmap_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static size_t esize(mtgr_dtype dt) { return dt == MTGR_BF16 ? 2 : 4; }
 
-// Attention workspace.  In the bf16 path the tensor-core operands are f16:
-// q, k, v are converted once (exactly) into f16 copies, and dO, P, dS are
-// produced in f16 (11 significand bits instead of 8).
+// Attention workspace: status word, jagged tile plan, dO; in the bf16 path the
+// tensor-core operands are f16: q, k, v are converted once (exactly) into f16
+// copies, and dO, P, dS are produced in f16 (11 significand bits instead of 8).
 struct AttnWs {
-  size_t status, plan, dO, dq_acc, qkv16, total;
+  size_t status, plan, dO, qkv16, total;
 };
 static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt, bool convert_qkv = true) {
   AttnWs w;
@@ -172,8 +172,6 @@ static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt,
   o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T).total);
   w.dO = o;
   o += align256(THD * (dt == MTGR_BF16 ? 2 : 4));
-  w.dq_acc = o;
-  if (dt == MTGR_BF16) o += align256(THD * sizeof(float));
   w.qkv16 = o;
   if (dt == MTGR_BF16 && convert_qkv) o += 3 * align256(THD * 2);
   w.total = o;
@@ -277,8 +275,7 @@ static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16
                         : launch_ln_gate_bwd(dy, o, static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du,
                                              ldg, z, T, (int)HD, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd gate");
-  MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts,
-                                    reinterpret_cast<float*>(ws + w.dq_acc), dq, dk, dv, ldg,
+  MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts, dq, dk, dv, ldg,
                                     z ? z + HD : nullptr, z ? z + 2 * HD : nullptr, z ? z + 3 * HD : nullptr, status,
                                     s),
                 "attn_bwd tcgen05");

@@ -8,117 +8,201 @@
 //   dQ = dS K,   dK = dSᵀ Q,   silu'(s) = σ(s)(1 + s(1 - σ(s))).
 // There is no softmax, so no row statistics are needed: S is recomputed.
 //
-// CTA = one (user, key tile, head) work item from the longest-first list; it
-// loops over the query tiles that see the key tile (dynamic mixed mask,
-// fun-rec chapter 7.3, §7.3.4).  Per query tile:
-//   Sᵀ  = K Qᵀ            -> TMEM [0,128)
-//   dPᵀ = V dOᵀ           -> TMEM [128,256)
-//   epilogue (thread = key row): Pᵀ (f16) into TMEM [0,64), dSᵀ (f16) into
-//   shared memory (128-byte swizzled, written by threads)
-//   dV += Pᵀ dO           (A from TMEM)            -> TMEM [256, 256+D)
-//   dK += dSᵀ Q           (A K-major from smem)    -> TMEM [256+D, 256+2D)
-//   dQ  = dS K            (A MN-major: same smem)  -> TMEM [128,128+D)
-//   epilogue (thread = query row): dQ added into an fp32 accumulator in global
-//   memory with vector atomics; a final pass applies silu'(z) and rounds to
-//   bf16.  P is kept without the 1/n_u factor (dV is scaled once at the end).
-// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..5 epilogue.
-#include "common.cuh"
-#include "plan.cuh"
+// Two persistent kernels, neither of which needs atomics:
+//  * dK/dV (key-tile major): one item = (user, key tile, head), looping over
+//    the query tiles that see the key tile (dynamic mixed mask, fun-rec
+//    chapter 7.3, §7.3.4).  Per query tile:  Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (TMEM);
+//    the epilogue writes Pᵀ (f16) over Sᵀ and dSᵀ (f16) over dPᵀ in TMEM; then
+//    dV += Pᵀ dO and dK += dSᵀ Q with the A operand read from TMEM.
+//  * dQ (query-tile major): one item = (user, query tile, head), looping over
+//    the key tiles the query tile sees.  Per key tile: S = Q Kᵀ, dP = dO Vᵀ;
+//    the epilogue writes dS (f16) over dP; dQ += dS K from TMEM.  dQ lives in
+//    one of two TMEM accumulators, so the store of one item overlaps the next.
+// Recomputing S and dP in the dQ kernel costs 3 extra MMAs per tile pair but
+// avoids accumulating dQ across CTAs through L2 reductions (64 KB of fp32
+// read-modify-write per tile pair).
+//
+// In both, the epilogue of a 128x128 tile is handed to the tensor core in
+// four quarters of 32 columns, so the MMAs of one quarter run while the next
+// is computed.  Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..9 epilogue (two
+// warpgroups, each taking 16 of the 32 columns of a quarter), 10..13 output
+// (TMEM -> bf16).
+#include "attn_sm103.cuh"
 
 namespace mtgr {
 namespace {
+using attn::BT;
+using attn::item_at;
+using attn::kmajor_desc;
+using attn::mnmajor_desc;
+using attn::packed_col;
+using attn::silu_and_grad_half;
 
-constexpr int BT = 128;  // key tile = query tile = 128 rows
-constexpr int NUM_THREADS = 192;
-
-template <int D>
-struct BwdCfg {
-  static constexpr int TILE = BT * D * 2;  // K / V / Q / dO tile bytes
-  static constexpr int DS_BYTES = BT * BT * 2;
-  static constexpr int SMEM = 4 * TILE + DS_BYTES + 1024 + 256;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t ST = 0, DPT = 128, DQ = 128, DV = 256, DK = 256 + D;
-};
-
-struct BwdSmem {
-  uint64_t kv_full, q_full, q_empty, do_full, do_empty, sdp_full, p_ready, dq_full, dq_free, dkdv_full, dv_done;
-  uint32_t tmem_base;
-  int abort_flag;
-};
+constexpr int NUM_THREADS = 448;  // 14 warps
+constexpr int EPI_WARPS = 8;
+constexpr int RING = 4;
 
 struct BwdParams {
   const UserInfo* users;
   const WorkItem* items;
-  const int32_t* counts;
+  const int32_t* count;  // number of items in the list
   const int64_t* ts;
-  float* dq_acc;  // [T, H*D] fp32 (row stride ldacc), zeroed before the launch
-  int64_t ldacc;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  __nv_bfloat16* g0;  // dkdv kernel: dk; dq kernel: dq
+  __nv_bfloat16* g1;  // dkdv kernel: dv
   int64_t ldg;
-  const __nv_bfloat16* zk;  // optional pre-activations (row stride ldz)
-  const __nv_bfloat16* zv;
+  const __nv_bfloat16* z0;  // optional pre-activations (row stride ldz) matching g0 / g1
+  const __nv_bfloat16* z1;
   int64_t ldz;
   int H;
-  float scale;
+  float scale;  // 1/sqrt(d_h)
   int32_t* status;
 };
 
-template <int D>
-__device__ __forceinline__ uint64_t kmaj(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
+// ---------------------------------------------------------------------------
+// Mask helpers.  Rows / keys are segment-relative; eS, eR: first RealTime and
+// first candidate token; n: tokens of the user.
+// ---------------------------------------------------------------------------
+// Query row ri sees key rj (dynamic mixed mask, fun-rec §7.3.4): User/Seq keys
+// always; a RealTime key if ts_j < thr (thr = ts_i + 1 for a RealTime row,
+// ts_i for a candidate row, INT64_MIN for a User/Seq row); a candidate key only
+// on the diagonal.
+struct RowMask {
+  int ri;
+  bool row_ok, cand;
+  int64_t thr;
+};
+__device__ __forceinline__ RowMask row_mask(const UserInfo& u, const int64_t* ts, int ri) {
+  RowMask m;
+  m.ri = ri;
+  m.row_ok = ri < u.n;
+  m.cand = ri >= u.eR;
+  m.thr = INT64_MIN;
+  if (m.row_ok && ri >= u.eS) m.thr = ts[u.start + ri] + (m.cand ? 0 : 1);
+  return m;
 }
 
-__device__ __forceinline__ float silu_grad_bf(float z) {
-  const float sg = sigmoid_f(z);
-  return sg * (1.f + z * (1.f - sg));
+// =============================================================================
+// dQ kernel
+// =============================================================================
+template <int D>
+struct DqCfg {
+  static constexpr int TILE = BT * D * 2;
+  static constexpr int Q_OFF = 0, DO_OFF = TILE, RING_OFF = 2 * TILE;
+  static constexpr int STG_OFF = RING_OFF + RING * TILE;  // 4 output warps x 2 KB
+  static constexpr int BAR_OFF = STG_OFF + 4 * 2048;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t S_COL = 0, DP_COL = 128;
+  __device__ static constexpr uint32_t dq_col(int b) { return 256u + (uint32_t)b * D; }
+};
+
+struct DqBars {
+  uint64_t qdo_full, qdo_empty;
+  uint64_t ring_full[RING], ring_empty[RING];
+  uint64_t s_full, ds_full[4], dsr_free, dq_full[2], dq_free[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct DqItem {
+  UserInfo u;
+  QTileKeys keys;
+  int qt, h;
+};
+__device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
+  DqItem c;
+  const int pi = idx / p.H;
+  c.h = idx - pi * p.H;
+  const WorkItem wi = p.items[pi];
+  c.u = p.users[wi.b];
+  c.qt = wi.t;
+  c.keys = qtile_keys(c.u, c.qt);
+  return c;
+}
+
+// 16 (s, dp) pairs of one query row, keys j0 .. j0+15 -> 8 packed f16 dS values.
+__device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int j0,
+                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc, float cn,
+                                           uint32_t (&pk)[8]) {
+  if (j0 + 16 <= u.eS) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float v[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        v[t] = __uint_as_float(dr[2 * e + t]) * ds * cn;
+      }
+      pk[e] = pack_f16x2(v[0], v[1]);
+    }
+  } else if (j0 >= u.eR) {
+    const int ed = m.ri - j0;
+    const bool diag = m.cand && m.row_ok && ed >= 0 && ed < 16;
+    float s_d = 0.f, dp_d = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      s_d = (e == ed) ? __uint_as_float(sr[e]) : s_d;
+      dp_d = (e == ed) ? __uint_as_float(dr[e]) : dp_d;
+    }
+    float sl, ds;
+    silu_and_grad_half(s_d * hc, sl, ds);
+    const float vd = diag ? dp_d * ds * cn : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pk[e] = pack_f16x2((2 * e == ed) ? vd : 0.f, (2 * e + 1 == ed) ? vd : 0.f);
+  } else {
+    // the chunk overlaps the RealTime keys: branch-free predicate; tk holds the
+    // stamp of key j0 + (lane & 15) (attn::rt_key_stamp), broadcast
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float v[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int jj = j0 + 2 * e + t;
+        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        v[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds * cn : 0.f;
+      }
+      pk[e] = pack_f16x2(v[0], v[1]);
+    }
+  }
 }
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdParams p) {
-  using Cfg = BwdCfg<D>;
-  const int item_idx = blockIdx.x / p.H;
-  const int h = blockIdx.x - item_idx * p.H;
-  if (item_idx >= p.counts[1]) return;
-  const WorkItem wi = p.items[item_idx];
-  const UserInfo u = p.users[wi.b];
-  const int kt = wi.t;
-  const KTileQueries qs = ktile_queries(u, kt);
-  const int nq = qs.count();
-
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+  using Cfg = DqCfg<D>;
+  const int total = p.count[0] * p.H;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = base;
-  uint8_t* sV = base + Cfg::TILE;
-  uint8_t* sQ = base + 2 * Cfg::TILE;
-  uint8_t* sdO = base + 3 * Cfg::TILE;
-  uint8_t* sdS = base + 4 * Cfg::TILE;
-  BwdSmem& S = *reinterpret_cast<BwdSmem*>(base + 4 * Cfg::TILE + Cfg::DS_BYTES);
+  uint8_t* sQ = base + Cfg::Q_OFF;
+  uint8_t* sdO = base + Cfg::DO_OFF;
+  uint8_t* sRing = base + Cfg::RING_OFF;
+  uint8_t* sStg = base + Cfg::STG_OFF;
+  DqBars& S = *reinterpret_cast<DqBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&S.kv_full, 1);
-    mbar_init(&S.q_full, 1);
-    mbar_init(&S.q_empty, 1);
-    mbar_init(&S.do_full, 1);
-    mbar_init(&S.do_empty, 1);
-    mbar_init(&S.sdp_full, 1);
-    mbar_init(&S.p_ready, 4);
-    mbar_init(&S.dq_full, 1);
-    mbar_init(&S.dq_free, 4);
-    mbar_init(&S.dkdv_full, 1);
-    mbar_init(&S.dv_done, 1);
+    mbar_init(&S.qdo_full, 1);
+    mbar_init(&S.qdo_empty, 1);
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&S.ring_full[i], 1);
+      mbar_init(&S.ring_empty[i], 1);
+    }
+    mbar_init(&S.s_full, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&S.ds_full[i], EPI_WARPS);
+    mbar_init(&S.dsr_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.dq_full[i], 1);
+      mbar_init(&S.dq_free[i], 4);
+    }
     S.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, Cfg::TMEM_COLS);
+    tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -133,208 +217,203 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
   bool ok = true;
-  const int col_h = h * D;
-  const int key_row0 = u.start + kt * BT;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
+      int stage = 0, n_items = 0;
+      uint32_t ph = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DqItem c = dq_item(p, idx);
+        const int col_h = c.h * D;
+        if (!mbar_wait_sleepy(&S.qdo_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        mbar_arrive_expect_tx(&S.qdo_full, 2 * Cfg::TILE);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(sK + c * 16384, &tmK, &S.kv_full, col_h + 64 * c, key_row0);
-        tma_load_2d(sV + c * 16384, &tmV, &S.kv_full, col_h + 64 * c, key_row0);
-      }
-      for (int i = 0; i < nq && ok; ++i) {
-        const int qrow = u.start + qs.qt(i, kt) * BT;
-        if (!mbar_wait(&S.q_empty, (i & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&S.q_full, Cfg::TILE);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          tma_load_2d(sQ + cc * 16384, &tmQ, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+          tma_load_2d(sdO + cc * 16384, &tmdO, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+        }
+        const int nk = c.keys.count();
+        for (int i = 0; i < nk && ok; ++i) {
+          const int row = c.u.start + c.keys.kt(i, c.qt) * BT;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_2d(sQ + c * 16384, &tmQ, &S.q_full, col_h + 64 * c, qrow);
-        if (!mbar_wait(&S.do_empty, (i & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&S.do_full, Cfg::TILE);
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* dst = sRing + stage * Cfg::TILE;
+            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_2d(sdO + c * 16384, &tmdO, &S.do_full, col_h + 64 * c, qrow);
+            for (int cc = 0; cc < D / 64; ++cc)
+              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
+            if (++stage == RING) { stage = 0; ph ^= 1; }
+          }
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t id_sq = idesc_f16_f32(BT, BT, false, false);  // Sᵀ, dPᵀ
-      constexpr uint32_t id_dv = idesc_f16_f32(BT, D, false, true);    // dV (A tmem), dK (A K-major)
-      constexpr uint32_t id_dq = idesc_f16_f32(BT, D, true, true);     // dQ: A = dS MN-major
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
-                     adS = smem_u32(sdS);
-      if (!mbar_wait(&S.kv_full, 0, abort_flag)) ok = false;
-      for (int i = 0; i < nq && ok; ++i) {
-        const uint32_t par = i & 1;
-        if (!mbar_wait(&S.q_full, par, abort_flag)) { ok = false; break; }
-        // Sᵀ_i overwrites the columns holding Pᵀ_{i-1}: wait until dV_{i-1} has read them
-        if (i > 0 && !mbar_wait(&S.dv_done, par ^ 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), ring_addr = smem_u32(sRing);
+      int stage = 0, n_items = 0;
+      uint32_t ph = 0, ds_waits[4] = {0, 0, 0, 0}, dsr_waits = 0, dqf_waits[2] = {0, 0};
+      bool dsr_pending = false, dq_pending[2] = {false, false};
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DqItem c = dq_item(p, idx);
+        const int qb = n_items & 1;
+        if (!mbar_wait(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        const int nk = c.keys.count();
+        for (int i = 0; i < nk && ok; ++i) {
+          // S = Q K_iᵀ (S columns are free: the epilogue read them before ds_full[1])
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          const int k_stage = stage;
+          const uint32_t k_addr = ring_addr + stage * Cfg::TILE;
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tmem + Cfg::ST, kmaj<D>(aK, kk), kmaj<D>(aQ, kk), id_sq, kk > 0 ? 1u : 0u);
-        if (i > 0 && !mbar_wait(&S.dq_free, par ^ 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&S.do_full, par, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tmem + Cfg::S_COL, kmajor_desc(q_addr, kk), kmajor_desc(k_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+          // dP = dO V_iᵀ overwrites the dS the previous dQ MMAs read
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          const int v_stage = stage;
+          const uint32_t v_addr = ring_addr + stage * Cfg::TILE;
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+          if (dsr_pending) {
+            if (!mbar_wait(&S.dsr_free, dsr_waits & 1, abort_flag)) { ok = false; break; }
+            ++dsr_waits;
+            dsr_pending = false;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tmem + Cfg::DPT, kmaj<D>(aV, kk), kmaj<D>(adO, kk), id_sq, kk > 0 ? 1u : 0u);
-        tc_commit(&S.sdp_full);
-        if (!mbar_wait(&S.p_ready, par, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tmem + Cfg::DP_COL, kmajor_desc(do_addr, kk), kmajor_desc(v_addr, kk), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          tc_commit(&S.s_full);
+          tc_commit(&S.ring_empty[v_stage]);
+          if (i == nk - 1) tc_commit(&S.qdo_empty);
+          // dQ += dS K_i, one quarter of the keys at a time
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)  // dV += Pᵀ dO, K = query rows
-          tc_mma_ts(tmem + Cfg::DV, tmem + Cfg::ST + kk * 8, mnmaj(adO, kk), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&S.dv_done);
+          for (int qr = 0; qr < 4; ++qr) {
+            if (!mbar_wait(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
+            ++ds_waits[qr];
+            if (i == 0 && qr == 0 && dq_pending[qb]) {  // accumulator still holds an older item's dQ
+              if (!mbar_wait(&S.dq_free[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
+              ++dqf_waits[qb];
+              dq_pending[qb] = false;
+            }
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)  // dK += dSᵀ Q
-          tc_mma_ss(tmem + Cfg::DK, kmaj<BT>(adS, kk), mnmaj(aQ, kk), id_dv, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)  // dQ = dS K, K = key rows
-          tc_mma_ss(tmem + Cfg::DQ, mnmaj(adS, kk), mnmaj(aK, kk), id_dq, kk > 0 ? 1u : 0u);
-        tc_commit(&S.dq_full);
-        tc_commit(&S.q_empty);
-        tc_commit(&S.do_empty);
+            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+              tc_mma_ts(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), mnmajor_desc(k_addr, kk),
+                        idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          tc_commit(&S.dsr_free);
+          dsr_pending = true;
+          tc_commit(&S.ring_empty[k_stage]);
+        }
+        if (!ok) break;
+        if (nk == 0) tc_commit(&S.qdo_empty);
+        tc_commit(&S.dq_full[qb]);
+        dq_pending[qb] = true;
       }
-      tc_commit(&S.dkdv_full);
     }
-  } else {
-    // ---------------- epilogue warps 2..5 ----------------
+  } else if (warp < 2 + EPI_WARPS) {
+    // ---------------- dS epilogue (thread = query row) ----------------
+    const int ew = warp - 2;
+    const int g = ew >> 2;  // 32-column block of each 64-column half
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    const int r_in = quarter * 32 + lane;  // TMEM lane
-    const int rj = kt * BT + r_in;         // this thread's key row (segment-relative)
-    const int key_cls = rj < u.eS ? 0 : (rj < u.eR ? 1 : 2);
-    const int64_t ts_j = (key_cls == 1 && rj < u.n) ? p.ts[u.start + rj] : 0;
-    const float c = p.scale, inv_n = 1.0f / (float)u.n;
-    const float cds = c * inv_n;
-    const bool all_static = kt * BT + BT <= u.eS;
-    for (int i = 0; i < nq && ok; ++i) {
-      const int qt = qs.qt(i, kt);
-      const int q0 = qt * BT;
-      if (!mbar_wait(&S.sdp_full, i & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll 1
-      for (int ch = 0; ch < BT / 32; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + Cfg::ST + ch * 32 + lane_sel, sr);
-        tmem_ld32(tmem + Cfg::DPT + ch * 32 + lane_sel, dr);
+    const float hc = 0.5f * p.scale;
+    uint32_t s_waits = 0;
+    for (int r = 0; ok; ++r) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const DqItem c = dq_item(p, idx);
+      const UserInfo& u = c.u;
+      const RowMask m = row_mask(u, p.ts, c.qt * BT + quarter * 32 + lane);
+      const int64_t* ts_u = p.ts + u.start;
+      const float cn = p.scale / (float)u.n;
+      const int nk = c.keys.count();
+      for (int i = 0; i < nk && ok; ++i) {
+        const int k0 = c.keys.kt(i, c.qt) * BT;
+        // stamps of the keys this lane broadcasts, loaded before the wait
+        int64_t tk[4];
+#pragma unroll
+        for (int qr = 0; qr < 4; ++qr) tk[qr] = attn::rt_key_stamp(u, ts_u, k0 + 32 * qr + 16 * g, lane);
+        if (!mbar_wait(&S.s_full, s_waits & 1, abort_flag)) { ok = false; break; }
+        ++s_waits;
+        tc_fence_after();
+        // four quarters of 32 key columns; this warp takes 16 of each (block
+        // 2*qr + g); the next quarter's loads are in flight during the math
+        uint32_t sr[2][16], dr[2][16], pk[8];
+        tmem_ld16(tmem + Cfg::S_COL + 16 * g + lane_sel, sr[0]);
+        tmem_ld16(tmem + Cfg::DP_COL + 16 * g + lane_sel, dr[0]);
         tmem_wait_ld();
-        uint32_t pk[16], dk[16];
+#pragma unroll 1
+        for (int q2 = 0; q2 < 4; q2 += 2) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int col = ch * 32 + 2 * e + t;
-            const int ri = q0 + col;
-            bool vis;
-            if (all_static || key_cls == 0) {
-              vis = ri < u.n;
-            } else if (key_cls == 1) {
-              if (ri < u.eS || ri >= u.n) {
-                vis = false;
-              } else {
-                const int64_t ts_i = p.ts[u.start + ri];
-                vis = ri < u.eR ? (ts_j <= ts_i) : (ts_j < ts_i);
-              }
-            } else {
-              vis = (ri == rj) && ri < u.n;
+          for (int b = 0; b < 2; ++b) {
+            const int qr = q2 + b;
+            const int cb = 32 * qr + 16 * g;
+            if (qr < 3) {
+              tmem_ld16(tmem + Cfg::S_COL + cb + 32 + lane_sel, sr[b ^ 1]);
+              tmem_ld16(tmem + Cfg::DP_COL + cb + 32 + lane_sel, dr[b ^ 1]);
             }
-            const float s = __uint_as_float(sr[2 * e + t]) * c;
-            const float sg = fmaf(0.5f, tanh_approx(0.5f * s), 0.5f);
-            const float silu = s * sg;
-            const float dsil = sg * fmaf(s, 1.f - sg, 1.f);
-            pv[t] = vis ? silu : 0.f;
-            dsv[t] = vis ? __uint_as_float(dr[2 * e + t]) * dsil * cds : 0.f;
+            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, cn, pk);
+            tmem_st8(tmem + Cfg::DP_COL + cb + lane_sel, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.ds_full[qr]);
+            if (qr < 3) tmem_wait_ld();
           }
-          pk[e] = pack_f16x2(pv[0], pv[1]);
-          dk[e] = pack_f16x2(dsv[0], dsv[1]);
-        }
-        tmem_st16(tmem + Cfg::ST + ch * 16 + lane_sel, pk);
-        // dSᵀ row r_in, query columns ch*32 .. ch*32+31 -> 4 swizzled 16-byte chunks
-        uint8_t* box = sdS + (ch >> 1) * 16384 + r_in * 128;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int chunk = ((ch & 1) * 4 + v) ^ (r_in & 7);
-          *reinterpret_cast<uint4*>(box + chunk * 16) = make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
         }
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_ready);
-      // ---- dQ partial of this key tile -> fp32 accumulator ----
-      if (!mbar_wait(&S.dq_full, i & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int ri = q0 + r_in;  // TMEM lane = query row for the dQ product
-      float* dq_row = p.dq_acc + (int64_t)(u.start + ri) * p.ldacc + col_h;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + Cfg::DQ + ch * 32 + lane_sel, r);
-        tmem_wait_ld();
-        if (ri < u.n) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            atomicAdd(reinterpret_cast<float4*>(dq_row + ch * 32 + 4 * v),
-                      make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.dq_free);
     }
-    // ---- dK, dV of this key tile -> global (bf16) ----
-    if (ok && mbar_wait(&S.dkdv_full, 0, abort_flag)) {
+  } else {
+    // ---------------- dQ output (thread = query row) ----------------
+    const int quarter = warp & 3;
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
+    uint32_t dqf_waits[2] = {0, 0};
+    int n_items = 0;
+    for (int r = 0; ok; ++r) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const DqItem c = dq_item(p, idx);
+      const int qb = n_items & 1;
+      ++n_items;
+      if (!mbar_wait_sleepy(&S.dq_full[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
+      ++dqf_waits[qb];
       tc_fence_after();
-      const bool row_ok = rj < u.n;
-      const int64_t grow = (int64_t)(u.start + rj);
+      const int row0 = c.qt * BT + quarter * 32;  // segment-relative first row of this warp
+      const int nvalid = c.u.n - row0;
+      const bool any = c.keys.count() > 0;
+      const int64_t grow = (int64_t)c.u.start + row0 + lane;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = (which == 0 ? p.dk : p.dv) + grow * p.ldg + col_h;
-        const __nv_bfloat16* z = which == 0 ? p.zk : p.zv;
-        const uint32_t col = which == 0 ? Cfg::DK : Cfg::DV;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tmem + col + ch * 32 + lane_sel, r);
-          tmem_wait_ld();
-          if (!row_ok) continue;
-          float x[32];
-          const float sc = nq > 0 ? (which == 0 ? 1.f : inv_n) : 0.f;  // P carries no 1/n_u
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * sc;
-          if (z) {
-            const uint4* zp = reinterpret_cast<const uint4*>(z + grow * p.ldz + col_h + ch * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 zz = zp[v];
-              const uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                x[8 * v + 2 * t] *= silu_grad_bf(bf16_lo(w[t]));
-                x[8 * v + 2 * t + 1] *= silu_grad_bf(bf16_hi(w[t]));
-              }
-            }
-          }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(x[8 * v + 0], x[8 * v + 1]);
-            o.y = pack_bf16x2(x[8 * v + 2], x[8 * v + 3]);
-            o.z = pack_bf16x2(x[8 * v + 4], x[8 * v + 5]);
-            o.w = pack_bf16x2(x[8 * v + 6], x[8 * v + 7]);
-            *reinterpret_cast<uint4*>(out + ch * 32 + 8 * v) = o;
-          }
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + Cfg::dq_col(qb) + cc * 32 + lane_sel, rr);
+        tmem_wait_ld();
+        if (cc == D / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.dq_free[qb]);
         }
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) : 0.f;
+        if (p.z0 && lane < nvalid) attn::mul_silu_grad_32(x, p.z0 + grow * p.ldz + c.h * D + cc * 32);
+        attn::store_rows_bf16_32(x, stg, p.g0 + ((int64_t)c.u.start + row0) * p.ldg + c.h * D + cc * 32, p.ldg,
+                                 nvalid, lane);
       }
-    } else {
-      ok = false;
     }
   }
 
@@ -346,97 +425,461 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-// dq = bf16(dq_acc [* silu'(z)]) for every row that belongs to a segment.
-__global__ void dq_finish_kernel(const float* __restrict__ acc, int64_t T, int HD, __nv_bfloat16* __restrict__ dq,
-                                 int64_t ldg, const __nv_bfloat16* __restrict__ z, int64_t ldz) {
-  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (i >= T * HD) return;
-  const int64_t row = i / HD;
-  const int col = (int)(i - row * HD);
-  const float4 a0 = *reinterpret_cast<const float4*>(acc + i);
-  const float4 a1 = *reinterpret_cast<const float4*>(acc + i + 4);
-  float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  if (z) {
-    const uint4 zz = *reinterpret_cast<const uint4*>(z + row * ldz + col);
-    const uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
+// =============================================================================
+// dK/dV kernel
+// =============================================================================
+template <int D>
+struct DkvCfg {
+  static constexpr int TILE = BT * D * 2;
+  static constexpr int K_OFF = 0, V_OFF = TILE, RING_OFF = 2 * TILE;
+  static constexpr int STG_OFF = RING_OFF + RING * TILE;
+  static constexpr int BAR_OFF = STG_OFF + 4 * 2048;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+};
+
+struct DkvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t ring_full[RING], ring_empty[RING];
+  uint64_t s_full, ds_full[4], pt_free, dst_free, dkdv_full, dkdv_free;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct DkvItem {
+  UserInfo u;
+  KTileQueries qs;
+  int kt, h;
+};
+__device__ __forceinline__ DkvItem dkv_item(const BwdParams& p, int idx) {
+  DkvItem c;
+  const int pi = idx / p.H;
+  c.h = idx - pi * p.H;
+  const WorkItem wi = p.items[pi];
+  c.u = p.users[wi.b];
+  c.kt = wi.t;
+  c.qs = ktile_queries(c.u, c.kt);
+  return c;
+}
+
+// Key row rj as seen by query rows (the transposed mask): User/Seq keys by
+// every row of the segment; a RealTime key by RealTime rows stamped at or after
+// it and candidate rows stamped after it; a candidate key only by itself.
+struct KeyMask {
+  int rj;
+  int cls;  // 0 User/Seq, 1 RealTime, 2 candidate, 3 past the segment
+  int64_t ts_j;
+};
+
+// Stamp threshold of query row rq for the RealTime test of the transposed mask:
+// ts_i + 1 for a RealTime row, ts_i for a candidate row, INT64_MIN for a
+// User/Seq row or a row past the segment.
+__device__ __forceinline__ int64_t query_adj(const UserInfo& u, const int64_t* ts_u, int rq) {
+  return (rq >= u.eS && rq < u.n) ? __ldg(ts_u + rq) + (rq < u.eR ? 1 : 0) : INT64_MIN;
+}
+
+// 16 (sᵀ, dpᵀ) pairs of one key row, query rows q0 .. q0+15 -> 8 packed f16
+// Pᵀ values (silu, without 1/n_u) and 8 packed dSᵀ values.  warp_us: every
+// key of the warp is User/Seq; any_rt: some key of the warp is RealTime (both
+// warp-uniform).
+__device__ __forceinline__ void pds_chunk_k(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int q0,
+                                            const UserInfo& u, const KeyMask& k, bool warp_us, bool any_rt,
+                                            int64_t adj, float hc, float cn, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
+  if (warp_us && q0 + 16 <= u.n) {
+    // every key of the warp is User/Seq and every query row lies in the segment
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      x[2 * t] *= silu_grad_bf(bf16_lo(w[t]));
-      x[2 * t + 1] *= silu_grad_bf(bf16_hi(w[t]));
+    for (int e = 0; e < 8; ++e) {
+      float a[2], b[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        a[t] = sl;
+        b[t] = __uint_as_float(dr[2 * e + t]) * ds * cn;
+      }
+      pp[e] = pack_f16x2(a[0], a[1]);
+      pd[e] = pack_f16x2(b[0], b[1]);
+    }
+  } else {
+    // Query row ri sees a RealTime key stamped ts_j iff ts_j < adj_i (see
+    // query_adj); adj holds adj_{q0 + (lane & 15)} and is broadcast.
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float a[2], b[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int ri = q0 + 2 * e + t;
+        const int64_t adj_i = attn::shfl_i64(adj, 2 * e + t);
+        const bool vis = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        a[t] = vis ? sl : 0.f;
+        b[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds * cn : 0.f;
+      }
+      pp[e] = pack_f16x2(a[0], a[1]);
+      pd[e] = pack_f16x2(b[0], b[1]);
     }
   }
-  uint4 o;
-  o.x = pack_bf16x2(x[0], x[1]);
-  o.y = pack_bf16x2(x[2], x[3]);
-  o.z = pack_bf16x2(x[4], x[5]);
-  o.w = pack_bf16x2(x[6], x[7]);
-  *reinterpret_cast<uint4*>(dq + row * ldg + col) = o;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const BwdParams p) {
+  using Cfg = DkvCfg<D>;
+  const int total = p.count[0] * p.H;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = base + Cfg::K_OFF;
+  uint8_t* sV = base + Cfg::V_OFF;
+  uint8_t* sRing = base + Cfg::RING_OFF;
+  uint8_t* sStg = base + Cfg::STG_OFF;
+  DkvBars& S = *reinterpret_cast<DkvBars*>(base + Cfg::BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&S.kv_full, 1);
+    mbar_init(&S.kv_empty, 1);
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&S.ring_full[i], 1);
+      mbar_init(&S.ring_empty[i], 1);
+    }
+    mbar_init(&S.s_full, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&S.ds_full[i], EPI_WARPS);
+    mbar_init(&S.pt_free, 1);
+    mbar_init(&S.dst_free, 1);
+    mbar_init(&S.dkdv_full, 1);
+    mbar_init(&S.dkdv_free, 4);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0, n_items = 0;
+      uint32_t ph = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DkvItem c = dkv_item(p, idx);
+        const int col_h = c.h * D;
+        if (!mbar_wait_sleepy(&S.kv_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          tma_load_2d(sK + cc * 16384, &tmK, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+          tma_load_2d(sV + cc * 16384, &tmV, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+        }
+        const int nq = c.qs.count();
+        for (int i = 0; i < nq && ok; ++i) {
+          const int row = c.u.start + c.qs.qt(i, c.kt) * BT;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {  // Q_i, then dO_i
+            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* dst = sRing + stage * Cfg::TILE;
+            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc)
+              tma_load_2d(dst + cc * 16384, which == 0 ? &tmQ : &tmdO, &S.ring_full[stage], col_h + 64 * cc, row);
+            if (++stage == RING) { stage = 0; ph ^= 1; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_g = idesc_f16_f32(BT, D, false, true);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ring_addr = smem_u32(sRing);
+      int stage = 0, n_items = 0;
+      uint32_t ph = 0, ds_waits[4] = {0, 0, 0, 0}, pt_waits = 0, dst_waits = 0, free_waits = 0;
+      bool pt_pending = false, dst_pending = false, dkdv_pending = false;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DkvItem c = dkv_item(p, idx);
+        if (!mbar_wait(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        const int nq = c.qs.count();
+        for (int i = 0; i < nq && ok; ++i) {
+          // Sᵀ = K Q_iᵀ overwrites the Pᵀ the previous dV MMAs read
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          const int q_stage = stage;
+          const uint32_t q_addr = ring_addr + stage * Cfg::TILE;
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+          if (pt_pending) {
+            if (!mbar_wait(&S.pt_free, pt_waits & 1, abort_flag)) { ok = false; break; }
+            ++pt_waits;
+            pt_pending = false;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tmem + Cfg::ST_COL, kmajor_desc(k_addr, kk), kmajor_desc(q_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+          // dPᵀ = V dO_iᵀ overwrites the dSᵀ the previous dK MMAs read
+          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          const int do_stage = stage;
+          const uint32_t do_addr = ring_addr + stage * Cfg::TILE;
+          if (++stage == RING) { stage = 0; ph ^= 1; }
+          if (dst_pending) {
+            if (!mbar_wait(&S.dst_free, dst_waits & 1, abort_flag)) { ok = false; break; }
+            ++dst_waits;
+            dst_pending = false;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tmem + Cfg::DPT_COL, kmajor_desc(v_addr, kk), kmajor_desc(do_addr, kk), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          tc_commit(&S.s_full);
+          if (i == nq - 1) tc_commit(&S.kv_empty);
+          // dV += Pᵀ dO_i, dK += dSᵀ Q_i, one quarter of the query rows at a time
+#pragma unroll
+          for (int qr = 0; qr < 4; ++qr) {
+            if (!mbar_wait(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
+            ++ds_waits[qr];
+            if (i == 0 && qr == 0 && dkdv_pending) {  // accumulators still hold the previous item
+              if (!mbar_wait(&S.dkdv_free, free_waits & 1, abort_flag)) { ok = false; break; }
+              ++free_waits;
+              dkdv_pending = false;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+              tc_mma_ts(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), mnmajor_desc(do_addr, kk), idesc_g,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            if (qr == 3) {
+              tc_commit(&S.pt_free);
+              pt_pending = true;
+            }
+#pragma unroll
+            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+              tc_mma_ts(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), mnmajor_desc(q_addr, kk), idesc_g,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            if (qr == 3) {
+              tc_commit(&S.dst_free);
+              dst_pending = true;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&S.ring_empty[q_stage]);
+          tc_commit(&S.ring_empty[do_stage]);
+        }
+        if (!ok) break;
+        if (nq == 0) tc_commit(&S.kv_empty);
+        tc_commit(&S.dkdv_full);
+        dkdv_pending = true;
+      }
+    }
+  } else if (warp < 2 + EPI_WARPS) {
+    // ---------------- Pᵀ / dSᵀ epilogue (thread = key row) ----------------
+    const int ew = warp - 2;
+    const int g = ew >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const float hc = 0.5f * p.scale;
+    uint32_t s_waits = 0;
+    for (int r = 0; ok; ++r) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const DkvItem c = dkv_item(p, idx);
+      const UserInfo& u = c.u;
+      KeyMask km;
+      km.rj = c.kt * BT + quarter * 32 + lane;
+      km.cls = km.rj < u.eS ? 0 : (km.rj < u.eR ? 1 : (km.rj < u.n ? 2 : 3));
+      km.ts_j = km.cls == 1 ? p.ts[u.start + km.rj] : 0;
+      const bool warp_us = __all_sync(0xffffffffu, km.cls == 0);
+      const bool any_rt = __any_sync(0xffffffffu, km.cls == 1);
+      const int64_t* ts_u = p.ts + u.start;
+      const float cn = p.scale / (float)u.n;
+      const int nq = c.qs.count();
+      for (int i = 0; i < nq && ok; ++i) {
+        const int q0 = c.qs.qt(i, c.kt) * BT;
+        // stamps of the query rows this lane broadcasts in the masked chunks,
+        // loaded before the wait so that their latency is hidden
+        int64_t adj[4];
+#pragma unroll
+        for (int qr = 0; qr < 4; ++qr)
+          adj[qr] = any_rt ? query_adj(u, ts_u, q0 + 32 * qr + 16 * g + (lane & 15)) : INT64_MIN;
+        if (!mbar_wait(&S.s_full, s_waits & 1, abort_flag)) { ok = false; break; }
+        ++s_waits;
+        tc_fence_after();
+        // four quarters of 32 query columns; this warp takes 16 of each
+        // (pairs of quarters per loop trip keep the code small enough for the
+        // instruction cache; the buffer index stays static)
+        uint32_t sr[2][16], dr[2][16], pp[8], pd[8];
+        tmem_ld16(tmem + Cfg::ST_COL + 16 * g + lane_sel, sr[0]);
+        tmem_ld16(tmem + Cfg::DPT_COL + 16 * g + lane_sel, dr[0]);
+        tmem_wait_ld();
+#pragma unroll 1
+        for (int q2 = 0; q2 < 4; q2 += 2) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int qr = q2 + b;
+            const int cb = 32 * qr + 16 * g;
+            if (qr < 3) {
+              tmem_ld16(tmem + Cfg::ST_COL + cb + 32 + lane_sel, sr[b ^ 1]);
+              tmem_ld16(tmem + Cfg::DPT_COL + cb + 32 + lane_sel, dr[b ^ 1]);
+            }
+            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, any_rt, q2 == 0 ? adj[b] : adj[2 + b], hc, cn, pp,
+                        pd);
+            tmem_st8(tmem + Cfg::ST_COL + cb + lane_sel, pp);
+            tmem_st8(tmem + Cfg::DPT_COL + cb + lane_sel, pd);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.ds_full[qr]);
+            if (qr < 3) tmem_wait_ld();
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------- dK / dV output (thread = key row) ----------------
+    const int quarter = warp & 3;
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
+    uint32_t full_waits = 0;
+    for (int r = 0; ok; ++r) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const DkvItem c = dkv_item(p, idx);
+      if (!mbar_wait_sleepy(&S.dkdv_full, full_waits & 1, abort_flag)) { ok = false; break; }
+      ++full_waits;
+      tc_fence_after();
+      const int row0 = c.kt * BT + quarter * 32;
+      const int nvalid = c.u.n - row0;
+      const bool any = c.qs.count() > 0;
+      const int64_t grow = (int64_t)c.u.start + row0 + lane;
+      const float inv_n = 1.0f / (float)c.u.n;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {  // dV (P carries no 1/n_u), then dK
+        const uint32_t col = which == 0 ? Cfg::DV_COL : Cfg::DK_COL;
+        const float sc = which == 0 ? inv_n : 1.f;
+        const __nv_bfloat16* z = which == 0 ? p.z1 : p.z0;
+        __nv_bfloat16* out = which == 0 ? p.g1 : p.g0;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + col + cc * 32 + lane_sel, rr);
+          tmem_wait_ld();
+          if (which == 1 && cc == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.dkdv_free);
+          }
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
+          if (z && lane < nvalid) attn::mul_silu_grad_32(x, z + grow * p.ldz + c.h * D + cc * 32);
+          attn::store_rows_bf16_32(x, stg, out + ((int64_t)c.u.start + row0) * p.ldg + c.h * D + cc * 32, p.ldg,
+                                   nvalid, lane);
+        }
+      }
+    }
+  }
+
+  if (!ok) {
+    *abort_flag = 1;
+    if (p.status) atomicOr(p.status, DEV_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                         BwdParams pa, BwdParams pq, int grid, cudaStream_t s) {
+  cudaError_t e;
+  {
+    TraceScope tr("attn_bwd", s);
+    auto kern = attn_bwd_dkdv_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
+  TraceScope tr("attn_bwd_dq", s);
+  auto kern = attn_bwd_dq_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NUM_THREADS, DqCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pq);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v,
-                                 int64_t ld, const __half* dO, int64_t T, int H, int d, const int32_t* plan,
-                                 int32_t B, const int64_t* ts, float* dq_acc, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                                 __nv_bfloat16* dv, int64_t ldg, const __nv_bfloat16* zq, const __nv_bfloat16* zk,
-                                 const __nv_bfloat16* zv, int32_t* status, cudaStream_t s) {
+// q, k, v: [T, *] f16 with row stride ld; dO: [T, H*d] f16.  dq, dk, dv: bf16
+// with row stride ldg (times silu'(z) of the matching pre-activation block
+// when zq/zk/zv are given, row stride 4*H*d).  Every row of every segment is
+// written.
+cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
+                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
+                                __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
+                                const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
+                                int32_t* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T);
   const int HD = H * d;
-  cudaError_t e;
-  {
-    TraceScope tr("dq_zero", s);
-    e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * HD, s);
-  }
-  if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BT) ||
       !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tdo, dO, T, HD, HD, 64, BT))
     return cudaErrorInvalidValue;
-  BwdParams p;
-  p.users = reinterpret_cast<const UserInfo*>(plan + L.users);
-  p.items = reinterpret_cast<const WorkItem*>(plan + L.bwd_items);
-  p.counts = plan + L.counts;
-  p.ts = ts;
-  p.dq_acc = dq_acc;
-  p.dk = dk;
-  p.dv = dv;
-  p.ldg = ldg;
-  p.zk = zk;
-  p.zv = zv;
-  p.ldz = 4 * (int64_t)HD;
-  p.H = H;
-  p.scale = 1.0f / sqrtf((float)d);
-  p.status = status;
-  p.ldacc = HD;
-  const int64_t grid = L.max_items * H;
-  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  {
-  TraceScope tr("attn_bwd", s);
-  if (d == 128) {
-    auto kern = attn_bwd_kernel<128>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<128>::SMEM);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, NUM_THREADS, BwdCfg<128>::SMEM, s>>>(tq, tk, tv, tdo, p);
-  } else if (d == 64) {
-    auto kern = attn_bwd_kernel<64>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<64>::SMEM);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, NUM_THREADS, BwdCfg<64>::SMEM, s>>>(tq, tk, tv, tdo, p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) return e;
-  const int64_t n8 = (int64_t)T * HD / 8;
-  TraceScope tr2("dq_finish", s);
-  dq_finish_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(dq_acc, T, HD, dq, ldg, zq, 4 * (int64_t)HD);
-  return cudaGetLastError();
+  BwdParams pa{};
+  pa.users = reinterpret_cast<const UserInfo*>(plan + L.users);
+  pa.ts = ts;
+  pa.ldg = ldg;
+  pa.ldz = 4 * (int64_t)HD;
+  pa.H = H;
+  pa.scale = 1.0f / sqrtf((float)d);
+  pa.status = status;
+  BwdParams pq = pa;
+  pa.items = reinterpret_cast<const WorkItem*>(plan + L.bwd_items);
+  pa.count = plan + L.counts + 1;
+  pa.g0 = dk;
+  pa.g1 = dv;
+  pa.z0 = zk;
+  pa.z1 = zv;
+  pq.items = reinterpret_cast<const WorkItem*>(plan + L.dq_items);
+  pq.count = plan + L.counts + 2;
+  pq.g0 = dq;
+  pq.g1 = nullptr;
+  pq.z0 = zq;
+  pq.z1 = nullptr;
+  const int64_t max_items = L.max_items * H;
+  const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, pa, pq, grid, s);
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, pa, pq, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mtgr

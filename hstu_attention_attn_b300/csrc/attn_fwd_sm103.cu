@@ -29,11 +29,14 @@
 // warpgroup only ever writes the columns it has already read.
 // The fp32 O rows leave through a per-warp shared-memory transpose so that the
 // global stores are coalesced.
-#include "common.cuh"
-#include "plan.cuh"
+#include "attn_sm103.cuh"
 
 namespace mtgr {
 namespace {
+using attn::item_at;
+using attn::kmajor_desc;
+using attn::mnmajor_desc;
+using attn::silu_half;
 
 constexpr int BQ = 128, BKV = 128;
 constexpr int NUM_THREADS = 576;  // 18 warps
@@ -73,22 +76,6 @@ struct FwdParams {
   int32_t* status;
 };
 
-// Shared-memory descriptors of a [128 rows][D] 16-bit tile staged as D/64 boxes
-// of [128][64] with 128-byte swizzle (16 KB per box).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {  // K = d, step 16
-  return smem_desc_sw128(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {  // K = rows, step 16
-  return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
-}
-
-// Item sequence of one CTA: rounds of gridDim.x items, serpentine so that the
-// longest-first order is dealt out evenly.
-__device__ __forceinline__ int item_at(int round) {
-  const int G = gridDim.x, c = blockIdx.x;
-  return round * G + ((round & 1) ? (G - 1 - c) : c);
-}
-
 struct ItemCtx {
   UserInfo u;
   PairKeys pk;
@@ -104,16 +91,12 @@ __device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
   return c;
 }
 
-// silu(x) with h = x/2: h + h tanh(h)
-__device__ __forceinline__ float silu_half(float h) { return fmaf(h, tanh_approx(h), h); }
-
 // N scores of one query row (keys j0 .. j0+N-1 of the segment) -> N/2 packed
 // f16 P values under the dynamic mixed mask.  The chunk class depends only on
 // j0, so it is uniform across the warp.
 template <int N>
 __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const UserInfo& u, int ri, bool row_ok,
-                                        bool cand, int64_t thr, const int64_t* ts_u, float hs,
-                                        uint32_t (&pk)[N / 2]) {
+                                        bool cand, int64_t thr, int64_t tk, float hs, uint32_t (&pk)[N / 2]) {
   if (j0 + N <= u.eS) {
     // every key is User/Seq: visible to every row
 #pragma unroll
@@ -130,20 +113,16 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const Us
 #pragma unroll
     for (int e = 0; e < N / 2; ++e) pk[e] = pack_f16x2((2 * e == ed) ? pd : 0.f, (2 * e + 1 == ed) ? pd : 0.f);
   } else {
-    // the chunk overlaps the RealTime keys: full predicate
+    // the chunk overlaps the RealTime keys: full predicate, branch-free; tk
+    // holds the stamp of key j0 + (lane & 15) (attn::rt_key_stamp), broadcast
+    static_assert(N == 16, "stamp broadcast covers 16 keys");
 #pragma unroll
     for (int e = 0; e < N / 2; ++e) {
       float pv[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int jj = j0 + 2 * e + t;
-        bool vis;
-        if (jj < u.eS)
-          vis = true;
-        else if (jj < u.eR)
-          vis = __ldg(ts_u + jj) < thr;
-        else
-          vis = cand && jj == ri;
+        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < thr) | (cand & (jj == ri));
         const float v = silu_half(__uint_as_float(r[2 * e + t]) * hs);
         pv[t] = vis ? v : 0.f;
       }
@@ -377,11 +356,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
         const int kt = c.pk.kt(i);
         if (!(sl == 0 ? c.pk.in_a(kt) : c.pk.in_b(kt))) continue;
         any = true;
+        const int jg = kt * BKV + g * 64;  // first key of this warp's column half
+        // stamps of the keys this lane broadcasts in masked chunks, loaded before the wait
+        int64_t tk[4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tk[ch] = attn::rt_key_stamp(u, ts_u, jg + 16 * ch, lane);
         if (!mbar_wait(&S.s_full[sl], s_waits & 1, abort_flag)) { ok = false; break; }
         ++s_waits;
         tc_fence_after();
         const uint32_t t_s = tmem + Cfg::s_col(sl) + g * 64 + lane_sel;
-        const int jg = kt * BKV + g * 64;  // first key of this warp's column half
         // 4 chunks of 16 keys; the load of chunk c+1 is in flight while chunk c
         // is computed.  P of chunk c goes to columns 8c..8c+7 of this half,
         // which chunk c/2 has already read.
@@ -391,7 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           if (ch < 3) tmem_ld16(t_s + 16 * (ch + 1), rc[(ch + 1) & 1]);
-          p_chunk<16>(rc[ch & 1], jg + 16 * ch, u, ri, row_ok, cand, thr, ts_u, hs, pk);
+          p_chunk<16>(rc[ch & 1], jg + 16 * ch, u, ri, row_ok, cand, thr, tk[ch], hs, pk);
           tmem_st8(t_s + 8 * ch, pk);
           if (ch < 3) tmem_wait_ld();
         }

@@ -1,0 +1,112 @@
+// attn_sm103.cuh -- device helpers shared by the tcgen05 attention kernels
+// (forward, dK/dV backward, dQ backward): shared-memory operand descriptors of
+// the 128-row tiles, the persistent item order, SiLU in tanh form and the
+// coalesced bf16 row store through a small per-warp staging buffer.
+#pragma once
+#include "common.cuh"
+#include "plan.cuh"
+
+namespace mtgr {
+namespace attn {
+
+constexpr int BT = 128;  // rows of every query / key tile
+
+// Shared-memory descriptors of a [128 rows][D] 16-bit tile staged as D/64
+// TMA boxes of [128][64] with 128-byte swizzle (16 KB per box).
+// K-major use (the reduction runs along the D columns), k-step kk of 16:
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+}
+// MN-major use (the reduction runs along the 128 rows), k-step kk of 16 rows:
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
+}
+
+// TMEM column (relative to the 128-column region of a score tile) of the
+// packed f16 operand for reduction step kk (rows/keys 16kk .. 16kk+15), when
+// the epilogue writes the 8 packed words of every 16-column chunk into the
+// first 8 columns of that chunk (so that no warp overwrites columns another
+// warp has yet to read).
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(16 * kk); }
+
+// 64-bit warp broadcast from lane src.
+__device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
+  const int lo = __shfl_sync(0xffffffffu, (int)(uint32_t)(uint64_t)v, src);
+  const int hi = __shfl_sync(0xffffffffu, (int)(uint32_t)((uint64_t)v >> 32), src);
+  return (int64_t)(((uint64_t)(uint32_t)hi << 32) | (uint64_t)(uint32_t)lo);
+}
+
+// Stamps of 16 keys j0 .. j0+15 for the RealTime test, one per lane (lane & 15):
+// the key's stamp when it is a RealTime key of the segment, else INT64_MAX
+// (never visible through the stamp test).  Read back with shfl_i64(.., e).
+__device__ __forceinline__ int64_t rt_key_stamp(const UserInfo& u, const int64_t* ts_u, int j0, int lane) {
+  const int j = j0 + (lane & 15);
+  return (j >= u.eS && j < u.eR) ? __ldg(ts_u + j) : INT64_MAX;
+}
+
+// Persistent item order of one CTA: rounds of gridDim.x items, serpentine so
+// that a longest-first list is dealt out evenly.
+__device__ __forceinline__ int item_at(int round) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+// silu(x) with h = x/2: h + h tanh(h)  (σ(x) = (1 + tanh(x/2)) / 2)
+__device__ __forceinline__ float silu_half(float h) { return fmaf(h, tanh_approx(h), h); }
+
+// For h = x/2: silu(x) and silu'(x) = σ(x)(1 + x(1 - σ(x))) = σ + silu (1 - σ).
+__device__ __forceinline__ void silu_and_grad_half(float h, float& silu, float& dsilu) {
+  const float t = tanh_approx(h);
+  const float sg = fmaf(0.5f, t, 0.5f);
+  silu = fmaf(h, t, h);
+  dsilu = fmaf(silu, 1.0f - sg, sg);
+}
+
+// silu'(z) of a pre-activation in fp32 (accurate exponential).
+__device__ __forceinline__ float silu_grad_f(float z) {
+  const float sg = sigmoid_f(z);
+  return sg * (1.f + z * (1.f - sg));
+}
+
+// A warp holds 32 consecutive rows (lane = row) x 32 values; write them as
+// bf16 to rows row0 .. row0+31 of out (row stride ld elements), skipping rows
+// >= nvalid, through a 2 KB staging buffer so that each store instruction
+// writes 8 rows x 64 contiguous bytes.
+__device__ __forceinline__ void store_rows_bf16_32(const float (&x)[32], uint8_t* stg, __nv_bfloat16* out,
+                                                   int64_t ld, int nvalid, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 w;
+    w.x = pack_bf16x2(x[8 * v + 0], x[8 * v + 1]);
+    w.y = pack_bf16x2(x[8 * v + 2], x[8 * v + 3]);
+    w.z = pack_bf16x2(x[8 * v + 4], x[8 * v + 5]);
+    w.w = pack_bf16x2(x[8 * v + 6], x[8 * v + 7]);
+    *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16));
+    if (r < nvalid) *reinterpret_cast<uint4*>(out + (int64_t)r * ld + c4 * 8) = w;
+  }
+}
+
+// 32 bf16 pre-activations z[0..31] of one row -> silu'(z) multiplied into x.
+__device__ __forceinline__ void mul_silu_grad_32(float (&x)[32], const __nv_bfloat16* z) {
+  const uint4* zp = reinterpret_cast<const uint4*>(z);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 zz = zp[v];
+    const uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[8 * v + 2 * t] *= silu_grad_f(bf16_lo(w[t]));
+      x[8 * v + 2 * t + 1] *= silu_grad_f(bf16_hi(w[t]));
+    }
+  }
+}
+
+}  // namespace attn
+}  // namespace mtgr

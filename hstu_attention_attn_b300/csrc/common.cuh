@@ -83,6 +83,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Same, for waiters off the critical path (TMA producers, output warps): after
+// a short spin the thread sleeps between polls, so that it does not take issue
+// slots from the warps doing the arithmetic.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 32;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (it > 4) {
+      __nanosleep(ns);
+      if (ns < 256) ns <<= 1;
+    }
+    if ((it & 15u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA (tensor maps are built on the host with cuTensorMapEncodeTiled)
 // ----------------------------------------------------------------------------

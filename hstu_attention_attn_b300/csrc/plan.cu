@@ -60,12 +60,13 @@ __device__ __forceinline__ int fwd_cost(const UserInfo& u, int qa) {
 __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B,
                                                           int32_t* __restrict__ counts,
                                                           WorkItem* __restrict__ fwd_items,
-                                                          WorkItem* __restrict__ bwd_items, int64_t max_items,
+                                                          WorkItem* __restrict__ bwd_items,
+                                                          WorkItem* __restrict__ dq_items, int64_t max_items,
                                                           int32_t* __restrict__ status) {
-  __shared__ int32_t hist[2][kBuckets];
-  __shared__ int32_t tot[2];
+  __shared__ int32_t hist[3][kBuckets];
+  __shared__ int32_t tot[3];
   const int tid = threadIdx.x;
-  for (int i = tid; i < 2 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
+  for (int i = tid; i < 3 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
   for (int b = tid; b < B; b += blockDim.x) {
     const UserInfo u = users[b];
@@ -73,11 +74,12 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     for (int t = 0; t < nt; ++t) {
       if ((t & 1) == 0) atomicAdd(&hist[0][fwd_cost(u, t)], 1);
       atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
+      atomicAdd(&hist[2][min(qtile_keys(u, t).count(), kBuckets - 1)], 1);
     }
   }
   __syncthreads();
-  // exclusive scan from the most expensive bucket down (two warps, one per list)
-  if (tid < 64) {
+  // exclusive scan from the most expensive bucket down (one warp per list)
+  if (tid < 96) {
     const int list = tid >> 5, lane = tid & 31;
     int running = 0;
     for (int base = kBuckets - 1; base >= 0; base -= 32) {
@@ -105,13 +107,16 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
       }
       const int pb = atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
       if (pb < max_items) bwd_items[pb] = WorkItem{b, t};
+      const int pq = atomicAdd(&hist[2][min(qtile_keys(u, t).count(), kBuckets - 1)], 1);
+      if (pq < max_items) dq_items[pq] = WorkItem{b, t};
     }
   }
   __syncthreads();
   if (tid == 0) {
     counts[0] = tot[0];
     counts[1] = tot[1];
-    if ((tot[0] > max_items || tot[1] > max_items) && status) atomicOr(status, DEV_ERR_PLAN);
+    counts[2] = tot[2];
+    if ((tot[0] > max_items || tot[1] > max_items || tot[2] > max_items) && status) atomicOr(status, DEV_ERR_PLAN);
   }
 }
 
@@ -187,7 +192,8 @@ cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, i
   if (e != cudaSuccess) return e;
   TraceScope tr("plan_items", s);
   plan_items_kernel<<<1, 1024, 0, s>>>(users, B, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
-                                       reinterpret_cast<WorkItem*>(ws + L.bwd_items), L.max_items, status);
+                                       reinterpret_cast<WorkItem*>(ws + L.bwd_items),
+                                       reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items, status);
   return cudaGetLastError();
 }
 

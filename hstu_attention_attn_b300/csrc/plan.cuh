@@ -115,10 +115,10 @@ __host__ __device__ __forceinline__ KTileQueries ktile_queries(const UserInfo& u
 // Workspace layout of a plan (all int32), offsets in elements.
 struct PlanLayout {
   int64_t users;      // UserInfo[B]
-  int64_t counts;     // [4]: fwd query-tile pairs, bwd key tiles, (reserved)
+  int64_t counts;     // [4]: fwd query-tile pairs, bwd key tiles, bwd query tiles, (reserved)
   int64_t fwd_items;  // WorkItem[max_items]: (user, first query tile of the pair)
-  int64_t bwd_items;  // WorkItem[max_items]
-  int64_t hist;       // [2][kBuckets] histograms / cursors
+  int64_t bwd_items;  // WorkItem[max_items]: (user, key tile)
+  int64_t dq_items;   // WorkItem[max_items]: (user, query tile)
   int64_t total;      // int32 count
   int64_t max_items;
 };
@@ -136,8 +136,8 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T) {
   o += 2 * L.max_items;
   L.bwd_items = o;
   o += 2 * L.max_items;
-  L.hist = o;
-  o += 4 * kBuckets;
+  L.dq_items = o;
+  o += 2 * L.max_items;
   L.total = o;
   return L;
 }
