@@ -15,7 +15,7 @@ namespace mtgr {
 
 // ---- launchers defined in the other translation units ----
 cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, UserInfo*, int32_t*, cudaStream_t);
-cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
                                   int64_t*, cudaStream_t);
 template <typename T>
@@ -169,7 +169,7 @@ static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt,
   w.status = o;
   o += 256;
   w.plan = o;
-  o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T).total);
+  o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T, H).total);
   w.dO = o;
   o += align256(THD * (dt == MTGR_BF16 ? 2 : 4));
   w.qkv16 = o;
@@ -246,7 +246,7 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_fwd plan");
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_fwd plan");
   MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
   const int HD = H * d;
   cudaError_t e = u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, y, mean, rstd, T, HD, eps, s)
@@ -267,7 +267,7 @@ static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_bwd plan");
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_bwd plan");
   const int64_t HD = (int64_t)H * d;
   __half* dO = reinterpret_cast<__half*>(ws + w.dO);
   cudaError_t e = u_f16 ? launch_ln_gate_bwd(dy, o, static_cast<const __half*>(u), ldu, mean, rstd, dO, du, ldg, z,
@@ -464,8 +464,8 @@ mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, cons
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_fwd plan");
-  const PlanLayout L = plan_layout(B, T);
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, n_heads, plan, status, s), "attn_fwd plan");
+  const PlanLayout L = plan_layout(B, T, n_heads);
   MTGR_CUDA_TRY(launch_attn_f32_fwd(static_cast<const float*>(q), static_cast<const float*>(k),
                                     static_cast<const float*>(v), ld_in,
                                     reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
@@ -514,8 +514,8 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, plan, status, s), "attn_bwd plan");
-  const PlanLayout L = plan_layout(B, T);
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, n_heads, plan, status, s), "attn_bwd plan");
+  const PlanLayout L = plan_layout(B, T, n_heads);
   const float* z = static_cast<const float*>(z_uqkv);
   float* dO = reinterpret_cast<float*>(ws + w.dO);
   MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const float*>(dy), static_cast<const float*>(o_saved),

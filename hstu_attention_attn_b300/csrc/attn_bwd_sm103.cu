@@ -110,11 +110,10 @@ struct DqItem {
 };
 __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
   DqItem c;
-  const int pi = idx / p.H;
-  c.h = idx - pi * p.H;
-  const WorkItem wi = p.items[pi];
+  const WorkItem wi = p.items[idx];
+  c.h = wi.h();
   c.u = p.users[wi.b];
-  c.qt = wi.t;
+  c.qt = wi.t();
   c.keys = qtile_keys(c.u, c.qt);
   return c;
 }
@@ -174,7 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdParams p) {
   using Cfg = DqCfg<D>;
-  const int total = p.count[0] * p.H;
+  const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + Cfg::Q_OFF;
@@ -219,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   bool ok = true;
 
   if (warp == 0) {
-    if (lane == 0) {
+    {  // whole warp; lane 0 issues
       // ---------------- TMA producer ----------------
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
@@ -228,32 +227,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
         const int col_h = c.h * D;
-        if (!mbar_wait_sleepy(&S.qdo_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp_sleepy(&S.qdo_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
         ++n_items;
-        mbar_arrive_expect_tx(&S.qdo_full, 2 * Cfg::TILE);
+        if (lane == 0) mbar_arrive_expect_tx(&S.qdo_full, 2 * Cfg::TILE);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          tma_load_2d(sQ + cc * 16384, &tmQ, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
-          tma_load_2d(sdO + cc * 16384, &tmdO, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+          if (lane == 0) tma_load_2d(sQ + cc * 16384, &tmQ, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+          if (lane == 0) tma_load_2d(sdO + cc * 16384, &tmdO, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
         }
         const int nk = c.keys.count();
         for (int i = 0; i < nk && ok; ++i) {
           const int row = c.u.start + c.keys.kt(i, c.qt) * BT;
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
-            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
             uint8_t* dst = sRing + stage * Cfg::TILE;
-            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+            if (lane == 0) mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
+              if (lane == 0) tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
             if (++stage == RING) { stage = 0; ph ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {  // whole warp; lane 0 issues
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
       constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
@@ -266,61 +265,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
         const int qb = n_items & 1;
-        if (!mbar_wait(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         const int nk = c.keys.count();
         for (int i = 0; i < nk && ok; ++i) {
           // S = Q K_iᵀ (S columns are free: the epilogue read them before ds_full[1])
-          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int k_stage = stage;
           const uint32_t k_addr = ring_addr + stage * Cfg::TILE;
           if (++stage == RING) { stage = 0; ph ^= 1; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tmem + Cfg::S_COL, kmajor_desc(q_addr, kk), kmajor_desc(k_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+            if (lane == 0) tc_mma_ss(tmem + Cfg::S_COL, kmajor_desc(q_addr, kk), kmajor_desc(k_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
           // dP = dO V_iᵀ overwrites the dS the previous dQ MMAs read
-          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int v_stage = stage;
           const uint32_t v_addr = ring_addr + stage * Cfg::TILE;
           if (++stage == RING) { stage = 0; ph ^= 1; }
           if (dsr_pending) {
-            if (!mbar_wait(&S.dsr_free, dsr_waits & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&S.dsr_free, dsr_waits & 1, abort_flag)) { ok = false; break; }
             ++dsr_waits;
             dsr_pending = false;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tmem + Cfg::DP_COL, kmajor_desc(do_addr, kk), kmajor_desc(v_addr, kk), idesc_s,
+            if (lane == 0) tc_mma_ss(tmem + Cfg::DP_COL, kmajor_desc(do_addr, kk), kmajor_desc(v_addr, kk), idesc_s,
                       kk > 0 ? 1u : 0u);
-          tc_commit(&S.s_full);
-          tc_commit(&S.ring_empty[v_stage]);
-          if (i == nk - 1) tc_commit(&S.qdo_empty);
+          if (lane == 0) tc_commit(&S.s_full);
+          if (lane == 0) tc_commit(&S.ring_empty[v_stage]);
+          if (i == nk - 1) if (lane == 0) tc_commit(&S.qdo_empty);
           // dQ += dS K_i, one quarter of the keys at a time
 #pragma unroll
           for (int qr = 0; qr < 4; ++qr) {
-            if (!mbar_wait(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
             ++ds_waits[qr];
             if (i == 0 && qr == 0 && dq_pending[qb]) {  // accumulator still holds an older item's dQ
-              if (!mbar_wait(&S.dq_free[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
+              if (!mbar_wait_warp(&S.dq_free[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
               ++dqf_waits[qb];
               dq_pending[qb] = false;
             }
             tc_fence_after();
 #pragma unroll
             for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              tc_mma_ts(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), mnmajor_desc(k_addr, kk),
+              if (lane == 0) tc_mma_ts(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), mnmajor_desc(k_addr, kk),
                         idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
-          tc_commit(&S.dsr_free);
+          if (lane == 0) tc_commit(&S.dsr_free);
           dsr_pending = true;
-          tc_commit(&S.ring_empty[k_stage]);
+          if (lane == 0) tc_commit(&S.ring_empty[k_stage]);
         }
         if (!ok) break;
-        if (nk == 0) tc_commit(&S.qdo_empty);
-        tc_commit(&S.dq_full[qb]);
+        if (nk == 0) if (lane == 0) tc_commit(&S.qdo_empty);
+        if (lane == 0) tc_commit(&S.dq_full[qb]);
         dq_pending[qb] = true;
       }
     }
@@ -457,11 +456,10 @@ struct DkvItem {
 };
 __device__ __forceinline__ DkvItem dkv_item(const BwdParams& p, int idx) {
   DkvItem c;
-  const int pi = idx / p.H;
-  c.h = idx - pi * p.H;
-  const WorkItem wi = p.items[pi];
+  const WorkItem wi = p.items[idx];
+  c.h = wi.h();
   c.u = p.users[wi.b];
-  c.kt = wi.t;
+  c.kt = wi.t();
   c.qs = ktile_queries(c.u, c.kt);
   return c;
 }
@@ -532,7 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const BwdParams p) {
   using Cfg = DkvCfg<D>;
-  const int total = p.count[0] * p.H;
+  const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = base + Cfg::K_OFF;
@@ -576,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   bool ok = true;
 
   if (warp == 0) {
-    if (lane == 0) {
+    {  // whole warp; lane 0 issues
       // ---------------- TMA producer ----------------
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
@@ -585,32 +583,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
         const int col_h = c.h * D;
-        if (!mbar_wait_sleepy(&S.kv_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp_sleepy(&S.kv_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
         ++n_items;
-        mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
+        if (lane == 0) mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          tma_load_2d(sK + cc * 16384, &tmK, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
-          tma_load_2d(sV + cc * 16384, &tmV, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+          if (lane == 0) tma_load_2d(sK + cc * 16384, &tmK, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+          if (lane == 0) tma_load_2d(sV + cc * 16384, &tmV, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
         }
         const int nq = c.qs.count();
         for (int i = 0; i < nq && ok; ++i) {
           const int row = c.u.start + c.qs.qt(i, c.kt) * BT;
 #pragma unroll
           for (int which = 0; which < 2; ++which) {  // Q_i, then dO_i
-            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
             uint8_t* dst = sRing + stage * Cfg::TILE;
-            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+            if (lane == 0) mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-              tma_load_2d(dst + cc * 16384, which == 0 ? &tmQ : &tmdO, &S.ring_full[stage], col_h + 64 * cc, row);
+              if (lane == 0) tma_load_2d(dst + cc * 16384, which == 0 ? &tmQ : &tmdO, &S.ring_full[stage], col_h + 64 * cc, row);
             if (++stage == RING) { stage = 0; ph ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {  // whole warp; lane 0 issues
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
       constexpr uint32_t idesc_g = idesc_f16_f32(BT, D, false, true);
@@ -622,76 +620,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int idx = item_at(r);
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
-        if (!mbar_wait(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         const int nq = c.qs.count();
         for (int i = 0; i < nq && ok; ++i) {
           // Sᵀ = K Q_iᵀ overwrites the Pᵀ the previous dV MMAs read
-          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int q_stage = stage;
           const uint32_t q_addr = ring_addr + stage * Cfg::TILE;
           if (++stage == RING) { stage = 0; ph ^= 1; }
           if (pt_pending) {
-            if (!mbar_wait(&S.pt_free, pt_waits & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&S.pt_free, pt_waits & 1, abort_flag)) { ok = false; break; }
             ++pt_waits;
             pt_pending = false;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tmem + Cfg::ST_COL, kmajor_desc(k_addr, kk), kmajor_desc(q_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+            if (lane == 0) tc_mma_ss(tmem + Cfg::ST_COL, kmajor_desc(k_addr, kk), kmajor_desc(q_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
           // dPᵀ = V dO_iᵀ overwrites the dSᵀ the previous dK MMAs read
-          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int do_stage = stage;
           const uint32_t do_addr = ring_addr + stage * Cfg::TILE;
           if (++stage == RING) { stage = 0; ph ^= 1; }
           if (dst_pending) {
-            if (!mbar_wait(&S.dst_free, dst_waits & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&S.dst_free, dst_waits & 1, abort_flag)) { ok = false; break; }
             ++dst_waits;
             dst_pending = false;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tmem + Cfg::DPT_COL, kmajor_desc(v_addr, kk), kmajor_desc(do_addr, kk), idesc_s,
+            if (lane == 0) tc_mma_ss(tmem + Cfg::DPT_COL, kmajor_desc(v_addr, kk), kmajor_desc(do_addr, kk), idesc_s,
                       kk > 0 ? 1u : 0u);
-          tc_commit(&S.s_full);
-          if (i == nq - 1) tc_commit(&S.kv_empty);
+          if (lane == 0) tc_commit(&S.s_full);
+          if (i == nq - 1) if (lane == 0) tc_commit(&S.kv_empty);
           // dV += Pᵀ dO_i, dK += dSᵀ Q_i, one quarter of the query rows at a time
 #pragma unroll
           for (int qr = 0; qr < 4; ++qr) {
-            if (!mbar_wait(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
             ++ds_waits[qr];
             if (i == 0 && qr == 0 && dkdv_pending) {  // accumulators still hold the previous item
-              if (!mbar_wait(&S.dkdv_free, free_waits & 1, abort_flag)) { ok = false; break; }
+              if (!mbar_wait_warp(&S.dkdv_free, free_waits & 1, abort_flag)) { ok = false; break; }
               ++free_waits;
               dkdv_pending = false;
             }
             tc_fence_after();
 #pragma unroll
             for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              tc_mma_ts(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), mnmajor_desc(do_addr, kk), idesc_g,
+              if (lane == 0) tc_mma_ts(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), mnmajor_desc(do_addr, kk), idesc_g,
                         (i > 0 || kk > 0) ? 1u : 0u);
             if (qr == 3) {
-              tc_commit(&S.pt_free);
+              if (lane == 0) tc_commit(&S.pt_free);
               pt_pending = true;
             }
 #pragma unroll
             for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              tc_mma_ts(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), mnmajor_desc(q_addr, kk), idesc_g,
+              if (lane == 0) tc_mma_ts(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), mnmajor_desc(q_addr, kk), idesc_g,
                         (i > 0 || kk > 0) ? 1u : 0u);
             if (qr == 3) {
-              tc_commit(&S.dst_free);
+              if (lane == 0) tc_commit(&S.dst_free);
               dst_pending = true;
             }
           }
           if (!ok) break;
-          tc_commit(&S.ring_empty[q_stage]);
-          tc_commit(&S.ring_empty[do_stage]);
+          if (lane == 0) tc_commit(&S.ring_empty[q_stage]);
+          if (lane == 0) tc_commit(&S.ring_empty[do_stage]);
         }
         if (!ok) break;
-        if (nq == 0) tc_commit(&S.kv_empty);
-        tc_commit(&S.dkdv_full);
+        if (nq == 0) if (lane == 0) tc_commit(&S.kv_empty);
+        if (lane == 0) tc_commit(&S.dkdv_full);
         dkdv_pending = true;
       }
     }
@@ -848,7 +846,7 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
                                 const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
                                 int32_t* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
-  const PlanLayout L = plan_layout(B, T);
+  const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BT) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BT) ||
@@ -875,7 +873,7 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   pq.g1 = nullptr;
   pq.z0 = zq;
   pq.z1 = nullptr;
-  const int64_t max_items = L.max_items * H;
+  const int64_t max_items = L.max_items;
   const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
   if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, pa, pq, grid, s);
   if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, pa, pq, grid, s);

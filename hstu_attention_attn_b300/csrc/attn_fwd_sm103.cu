@@ -83,11 +83,10 @@ struct ItemCtx {
 };
 __device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
   ItemCtx c;
-  const int pi = idx / p.H;
-  c.h = idx - pi * p.H;
-  const WorkItem wi = p.items[pi];
+  const WorkItem wi = p.items[idx];
+  c.h = wi.h();
   c.u = p.users[wi.b];
-  c.pk = pair_keys(c.u, wi.t);
+  c.pk = pair_keys(c.u, wi.t());
   return c;
 }
 
@@ -136,7 +135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Cfg = FwdCfg<D>;
-  const int total = p.counts[0] * p.H;
+  const int total = p.counts[0];
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -448,7 +447,7 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
                                 int d, const int32_t* plan, int32_t B, const int64_t* ts, float* O, int32_t* status,
                                 cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
-  const PlanLayout L = plan_layout(B, T);
+  const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BKV) ||
@@ -465,7 +464,7 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
   p.scale = 1.0f / sqrtf((float)d);
   p.status = status;
   // persistent: one CTA per SM (the item count lives on the device; CTAs without an item exit at once)
-  const int64_t max_items = L.max_items * H;
+  const int64_t max_items = L.max_items;
   const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
   TraceScope tr("attn_fwd", s);
   if (d == 128) {

@@ -1,6 +1,6 @@
 // plan.cu -- batch metadata on the device: validation, per-user group
-// boundaries, integer visible-pair counts, and the longest-first ordered list
-// of jagged attention tiles (see plan.cuh for the tile rule).
+// boundaries, integer visible-pair counts, and the work lists of the jagged
+// attention kernels (see plan.cuh for the tile rule).
 #include "common.cuh"
 #include "plan.cuh"
 
@@ -45,37 +45,35 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
   }
 }
 
-// Cost of a forward work item (query tiles qa and qa + 1 of a user): tensor
-// tiles of both, i.e. key tiles visited by each.
-__device__ __forceinline__ int fwd_cost(const UserInfo& u, int qa) {
-  const PairKeys pk = pair_keys(u, qa);
-  int c = 0;
-  for (int i = 0; i < pk.count(); ++i) c += (pk.in_a(pk.kt(i)) ? 1 : 0) + (pk.in_b(pk.kt(i)) ? 1 : 0);
-  return min(c, kBuckets - 1);
-}
-
-// One block: bucket every forward item (pair of query tiles) and backward item
-// (key tile) by its number of tile products, then scatter into lists ordered
-// longest first.
-__global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B,
+// One block: order users by their work (tile products), largest first, then
+// write each list user by user, head by head, tile by tile.  A user's items
+// for one head are consecutive, so the persistent kernels (which deal items
+// out to CTAs in order) work on one user's tiles at the same time and its
+// streamed operands are read from HBM about once.
+__global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B, int32_t H,
                                                           int32_t* __restrict__ counts,
                                                           WorkItem* __restrict__ fwd_items,
                                                           WorkItem* __restrict__ bwd_items,
                                                           WorkItem* __restrict__ dq_items, int64_t max_items,
                                                           int32_t* __restrict__ status) {
-  __shared__ int32_t hist[3][kBuckets];
+  __shared__ int32_t hist[3][kBuckets];  // items of each list per cost bucket, then cursors
   __shared__ int32_t tot[3];
   const int tid = threadIdx.x;
   for (int i = tid; i < 3 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
+  auto user_cost = [](const UserInfo& u) {
+    const int nt = ceil_div(u.n, kTile);
+    int c = 0;
+    for (int t = 0; t < nt; ++t) c += qtile_keys(u, t).count();
+    return min(c, kBuckets - 1);
+  };
   for (int b = tid; b < B; b += blockDim.x) {
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
-    for (int t = 0; t < nt; ++t) {
-      if ((t & 1) == 0) atomicAdd(&hist[0][fwd_cost(u, t)], 1);
-      atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
-      atomicAdd(&hist[2][min(qtile_keys(u, t).count(), kBuckets - 1)], 1);
-    }
+    const int c = user_cost(u);
+    atomicAdd(&hist[0][c], ((nt + 1) / 2) * H);
+    atomicAdd(&hist[1][c], nt * H);
+    atomicAdd(&hist[2][c], nt * H);
   }
   __syncthreads();
   // exclusive scan from the most expensive bucket down (one warp per list)
@@ -100,15 +98,21 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
   for (int b = tid; b < B; b += blockDim.x) {
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
-    for (int t = 0; t < nt; ++t) {
-      if ((t & 1) == 0) {
-        const int pf = atomicAdd(&hist[0][fwd_cost(u, t)], 1);
-        if (pf < max_items) fwd_items[pf] = WorkItem{b, t};
+    const int np = (nt + 1) / 2;
+    const int c = user_cost(u);
+    const int pf = atomicAdd(&hist[0][c], np * H);
+    const int pb = atomicAdd(&hist[1][c], nt * H);
+    const int pq = atomicAdd(&hist[2][c], nt * H);
+    for (int h = 0; h < H; ++h) {
+      for (int i = 0; i < np; ++i) {
+        const int64_t o = (int64_t)pf + h * np + i;
+        if (o < max_items) fwd_items[o] = WorkItem{b, (2 * i) | (h << 16)};
       }
-      const int pb = atomicAdd(&hist[1][min(ktile_queries(u, t).count(), kBuckets - 1)], 1);
-      if (pb < max_items) bwd_items[pb] = WorkItem{b, t};
-      const int pq = atomicAdd(&hist[2][min(qtile_keys(u, t).count(), kBuckets - 1)], 1);
-      if (pq < max_items) dq_items[pq] = WorkItem{b, t};
+      for (int t = 0; t < nt; ++t) {
+        const int64_t ob = (int64_t)pb + h * nt + t, oq = (int64_t)pq + h * nt + t;
+        if (ob < max_items) bwd_items[ob] = WorkItem{b, t | (h << 16)};
+        if (oq < max_items) dq_items[oq] = WorkItem{b, t | (h << 16)};
+      }
     }
   }
   __syncthreads();
@@ -184,14 +188,14 @@ cudaError_t launch_user_info(const int32_t* offsets, int32_t B, const uint8_t* g
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, int32_t* ws,
+cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, int32_t H, int32_t* ws,
                         int32_t* status, cudaStream_t s) {
-  const PlanLayout L = plan_layout(B, T);
+  const PlanLayout L = plan_layout(B, T, H);
   UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
   cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s);
   if (e != cudaSuccess) return e;
   TraceScope tr("plan_items", s);
-  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
+  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, H, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.bwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items, status);
   return cudaGetLastError();

@@ -27,8 +27,10 @@ struct UserInfo {
 };
 
 struct WorkItem {
-  int32_t b;  // user
-  int32_t t;  // tile index inside the user (query tile fwd, key tile bwd)
+  int32_t b;   // user
+  int32_t th;  // tile index inside the user (low 16 bits) | head << 16
+  __host__ __device__ __forceinline__ int t() const { return th & 0xFFFF; }
+  __host__ __device__ __forceinline__ int h() const { return th >> 16; }
 };
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -112,21 +114,24 @@ __host__ __device__ __forceinline__ KTileQueries ktile_queries(const UserInfo& u
   return q;
 }
 
-// Workspace layout of a plan (all int32), offsets in elements.
+// Workspace layout of a plan (all int32), offsets in elements.  Each list
+// holds one item per (tile, head), grouped by user (users in decreasing order
+// of work, a user's items for one head consecutive) so that concurrently
+// running CTAs share the user's streamed operands through L2.
 struct PlanLayout {
   int64_t users;      // UserInfo[B]
-  int64_t counts;     // [4]: fwd query-tile pairs, bwd key tiles, bwd query tiles, (reserved)
-  int64_t fwd_items;  // WorkItem[max_items]: (user, first query tile of the pair)
-  int64_t bwd_items;  // WorkItem[max_items]: (user, key tile)
-  int64_t dq_items;   // WorkItem[max_items]: (user, query tile)
+  int64_t counts;     // [4]: items of the fwd / bwd key-tile / bwd query-tile lists, (reserved)
+  int64_t fwd_items;  // WorkItem[max_items]: (user, first query tile of a pair, head)
+  int64_t bwd_items;  // WorkItem[max_items]: (user, key tile, head)
+  int64_t dq_items;   // WorkItem[max_items]: (user, query tile, head)
   int64_t total;      // int32 count
   int64_t max_items;
 };
 constexpr int kBuckets = 1024;
 
-__host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T) {
+__host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T, int32_t H) {
   PlanLayout L;
-  L.max_items = T / kTile + (int64_t)B + 1;
+  L.max_items = (T / kTile + (int64_t)B + 1) * (H > 0 ? H : 1);
   int64_t o = 0;
   L.users = o;
   o += 4 * (int64_t)B;
