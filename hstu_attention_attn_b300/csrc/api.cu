@@ -42,7 +42,7 @@ cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
                                 __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
-                                const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
+                                const __nv_bfloat16* mq, const __nv_bfloat16* mk, const __nv_bfloat16* mv,
                                 int32_t* status, cudaStream_t s);
 
 // ---- kernel tracing ----
@@ -189,7 +189,7 @@ static int choose_splits(int64_t M, int64_t N, int64_t K) {
   int64_t s = (2 * (int64_t)num_sms() + tiles - 1) / tiles;
   if (s > 16) s = 16;
   if (s > nk) s = nk;
-  return (int)(s < 1 ? 1 : s);
+  return gemm_splits(K, (int)(s < 1 ? 1 : s));
 }
 static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, mtgr_dtype dt) {
   LayerWs w;
@@ -261,7 +261,7 @@ static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16
                                       const float* o, const float* mean, const float* rstd, const int32_t* offsets,
                                       int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
                                       __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, __nv_bfloat16* du,
-                                      int64_t ldg, const __nv_bfloat16* z, uint8_t* ws, const AttnWs& w,
+                                      int64_t ldg, const __nv_bfloat16* dsilu, uint8_t* ws, const AttnWs& w,
                                       cudaStream_t s) {
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
@@ -270,14 +270,14 @@ static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_bwd plan");
   const int64_t HD = (int64_t)H * d;
   __half* dO = reinterpret_cast<__half*>(ws + w.dO);
-  cudaError_t e = u_f16 ? launch_ln_gate_bwd(dy, o, static_cast<const __half*>(u), ldu, mean, rstd, dO, du, ldg, z,
+  cudaError_t e = u_f16 ? launch_ln_gate_bwd(dy, o, static_cast<const __half*>(u), ldu, mean, rstd, dO, du, ldg, dsilu,
                                              T, (int)HD, s)
                         : launch_ln_gate_bwd(dy, o, static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du,
-                                             ldg, z, T, (int)HD, s);
+                                             ldg, dsilu, T, (int)HD, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd gate");
   MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts, dq, dk, dv, ldg,
-                                    z ? z + HD : nullptr, z ? z + 2 * HD : nullptr, z ? z + 3 * HD : nullptr, status,
-                                    s),
+                                    dsilu ? dsilu + HD : nullptr, dsilu ? dsilu + 2 * HD : nullptr,
+                                    dsilu ? dsilu + 3 * HD : nullptr, status, s),
                 "attn_bwd tcgen05");
   return MTGR_OK;
 }
@@ -481,7 +481,7 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
                                int64_t ld_in, const void* o_saved, const float* ln_mean, const float* ln_rstd,
                                const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
                                int64_t T, int32_t n_heads, int32_t d_h, void* dq, void* dk, void* dv, void* du,
-                               int64_t ld_grad, const void* z_uqkv, mtgr_dtype dtype, void* workspace,
+                               int64_t ld_grad, const void* dsilu_uqkv, mtgr_dtype dtype, void* workspace,
                                size_t workspace_bytes, mtgr_stream_t stream) {
   mtgr_status st = check_attn(q, k, v, u, ld_in, offsets, B, gid, ts, T, n_heads, d_h, dtype, workspace,
                               workspace_bytes);
@@ -491,9 +491,10 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
           "NULL pointer");
   REQUIRE(ld_grad >= HD && ld_grad % 8 == 0, MTGR_ERR_INVALID_ARG, "ld_grad must be >= H*d_h and a multiple of 8");
   REQUIRE(aligned16(dy) && aligned16(o_saved) && aligned16(dq) && aligned16(dk) && aligned16(dv) &&
-              aligned16(du) && aligned16(z_uqkv),
+              aligned16(du) && aligned16(dsilu_uqkv),
           MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
-  REQUIRE(z_uqkv == nullptr || ld_grad == 4 * HD, MTGR_ERR_INVALID_ARG, "with z_uqkv, ld_grad must be 4*H*d_h");
+  REQUIRE(dsilu_uqkv == nullptr || ld_grad == 4 * HD, MTGR_ERR_INVALID_ARG,
+          "with dsilu_uqkv, ld_grad must be 4*H*d_h");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const AttnWs w = attn_ws(B, T, n_heads, d_h, dtype);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -508,7 +509,7 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
     return attn_bwd_bf16_core(static_cast<const bf*>(dy), q16, k16, v16, HD, u, false, ld_in,
                               static_cast<const float*>(o_saved), ln_mean, ln_rstd, offsets, B, gid, ts, T, n_heads,
                               d_h, static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv),
-                              static_cast<bf*>(du), ld_grad, static_cast<const bf*>(z_uqkv), ws, w, s);
+                              static_cast<bf*>(du), ld_grad, static_cast<const bf*>(dsilu_uqkv), ws, w, s);
   }
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
@@ -516,18 +517,18 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
   if (T == 0 || B == 0) return MTGR_OK;
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, n_heads, plan, status, s), "attn_bwd plan");
   const PlanLayout L = plan_layout(B, T, n_heads);
-  const float* z = static_cast<const float*>(z_uqkv);
+  const float* m = static_cast<const float*>(dsilu_uqkv);
   float* dO = reinterpret_cast<float*>(ws + w.dO);
   MTGR_CUDA_TRY(launch_ln_gate_bwd(static_cast<const float*>(dy), static_cast<const float*>(o_saved),
                                    static_cast<const float*>(u), ld_in, ln_mean, ln_rstd, dO,
-                                   static_cast<float*>(du), ld_grad, z, T, (int)HD, s),
+                                   static_cast<float*>(du), ld_grad, m, T, (int)HD, s),
                 "attn_bwd gate");
   MTGR_CUDA_TRY(launch_attn_f32_bwd(static_cast<const float*>(q), static_cast<const float*>(k),
                                     static_cast<const float*>(v), ld_in, dO,
                                     reinterpret_cast<const UserInfo*>(plan + L.users), B, ts, T, n_heads, d_h,
                                     static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
-                                    ld_grad, z ? z + HD : nullptr, z ? z + 2 * HD : nullptr,
-                                    z ? z + 3 * HD : nullptr, s),
+                                    ld_grad, m ? m + HD : nullptr, m ? m + 2 * HD : nullptr,
+                                    m ? m + 3 * HD : nullptr, s),
                 "attn_bwd fp32");
   return MTGR_OK;
 }
@@ -567,10 +568,10 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
   mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
   if (st != MTGR_OK) return st;
   REQUIRE(sv != nullptr, MTGR_ERR_INVALID_ARG, "saved is NULL");
-  REQUIRE(T == 0 || (x && x_out && sv->xn && sv->z && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
+  REQUIRE(T == 0 || (x && x_out && sv->xn && sv->dsilu && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
                      sv->gln_rstd && sv->ln_mean && sv->ln_rstd && ts),
           MTGR_ERR_INVALID_ARG, "NULL tensor");
-  REQUIRE(aligned16(x) && aligned16(x_out) && aligned16(sv->xn) && aligned16(sv->z) && aligned16(sv->uqkv) &&
+  REQUIRE(aligned16(x) && aligned16(x_out) && aligned16(sv->xn) && aligned16(sv->dsilu) && aligned16(sv->uqkv) &&
               aligned16(sv->o) && aligned16(sv->y),
           MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   const int D = w->d_model, H = w->n_heads, d = w->d_h;
@@ -590,14 +591,15 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
     g.M = T; g.N = N4; g.K = D;
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
-    // [U|Q|K|V] = silu(z) is written in f16: the attention's tensor-core operands
-    g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->z); g.ldz = N4;
+    // [U|Q|K|V] = silu(z) is written in f16 (the attention's tensor-core operands),
+    // silu'(z) in bf16 (the factor of the SiLU backward)
+    g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->dsilu); g.ldz = N4;
     g.splits = 1; g.status = status; g.name = "gemm_uqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_SILU, T, N4, D, static_cast<const float*>(sv->xn), D, 1,
                                   static_cast<const float*>(w->w_uqkv), N4, 1, static_cast<float*>(sv->uqkv), N4,
-                                  nullptr, 0, static_cast<float*>(sv->z), N4, s),
+                                  nullptr, 0, static_cast<float*>(sv->dsilu), N4, s),
                   "layer_fwd uqkv gemm");
   }
   if (dtype == MTGR_BF16) {
@@ -637,7 +639,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   if (st != MTGR_OK) return st;
   REQUIRE(sv && gr && gr->dw_uqkv && gr->dw_o && gr->dgamma && gr->dbeta, MTGR_ERR_INVALID_ARG,
           "NULL saved / grads");
-  REQUIRE(T == 0 || (x && dx_out && dx && sv->xn && sv->z && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
+  REQUIRE(T == 0 || (x && dx_out && dx && sv->xn && sv->dsilu && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
                      sv->gln_rstd && sv->ln_mean && sv->ln_rstd && ts),
           MTGR_ERR_INVALID_ARG, "NULL tensor");
   REQUIRE(aligned16(x) && aligned16(dx_out) && aligned16(dx), MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
@@ -696,12 +698,12 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     bf* dz = static_cast<bf*>(dZ);
     r = attn_bwd_bf16_core(static_cast<const bf*>(dY), a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, sv->o,
                            sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
-                           dz, N4, static_cast<const bf*>(sv->z), ws + L.attn_base, L.attn, s);
+                           dz, N4, static_cast<const bf*>(sv->dsilu), ws + L.attn_base, L.attn, s);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     float* dz = static_cast<float*>(dZ);
     r = mtgr_hstu_attn_bwd(dY, a + HD, a + 2 * HD, a + 3 * HD, a, N4, sv->o, sv->ln_mean, sv->ln_rstd, offsets, B,
-                           gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD, dz, N4, sv->z, dtype,
+                           gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD, dz, N4, sv->dsilu, dtype,
                            ws + L.attn_base, L.attn.total, stream);
   }
   if (r != MTGR_OK) return r;

@@ -37,6 +37,12 @@ using attn::kmajor_desc;
 using attn::mnmajor_desc;
 using attn::packed_col;
 using attn::silu_and_grad_half;
+using attn::MRING;
+using attn::MSLOT;
+using attn::cp_async_commit;
+using attn::cp_async_wait;
+using attn::prefetch_l2;
+using attn::mslot_fetch;
 
 constexpr int NUM_THREADS = 448;  // 14 warps
 constexpr int EPI_WARPS = 8;
@@ -50,9 +56,9 @@ struct BwdParams {
   __nv_bfloat16* g0;  // dkdv kernel: dk; dq kernel: dq
   __nv_bfloat16* g1;  // dkdv kernel: dv
   int64_t ldg;
-  const __nv_bfloat16* z0;  // optional pre-activations (row stride ldz) matching g0 / g1
-  const __nv_bfloat16* z1;
-  int64_t ldz;
+  const __nv_bfloat16* m0;  // optional bf16 multipliers of g0 / g1 (row stride ldm)
+  const __nv_bfloat16* m1;
+  int64_t ldm;
   int H;
   float scale;  // 1/sqrt(d_h)
   int32_t* status;
@@ -89,7 +95,8 @@ struct DqCfg {
   static constexpr int TILE = BT * D * 2;
   static constexpr int Q_OFF = 0, DO_OFF = TILE, RING_OFF = 2 * TILE;
   static constexpr int STG_OFF = RING_OFF + RING * TILE;  // 4 output warps x 2 KB
-  static constexpr int BAR_OFF = STG_OFF + 4 * 2048;
+  static constexpr int MR_OFF = STG_OFF + 4 * 2048;         // 4 output warps x multiplier ring
+  static constexpr int BAR_OFF = MR_OFF + 4 * MRING * MSLOT;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL = 0, DP_COL = 128;
   __device__ static constexpr uint32_t dq_col(int b) { return 256u + (uint32_t)b * D; }
@@ -180,6 +187,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sdO = base + Cfg::DO_OFF;
   uint8_t* sRing = base + Cfg::RING_OFF;
   uint8_t* sStg = base + Cfg::STG_OFF;
+  uint8_t* sMr = base + Cfg::MR_OFF;
   DqBars& S = *reinterpret_cast<DqBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -381,6 +389,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
+    uint8_t* mr = sMr + (warp - 2 - EPI_WARPS) * (MRING * MSLOT);
+    const bool has_m = p.m0 != nullptr;
+    constexpr int NC = D / 32;
     uint32_t dqf_waits[2] = {0, 0};
     int n_items = 0;
     for (int r = 0; ok; ++r) {
@@ -389,19 +400,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const DqItem c = dq_item(p, idx);
       const int qb = n_items & 1;
       ++n_items;
-      if (!mbar_wait_sleepy(&S.dq_full[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
-      ++dqf_waits[qb];
-      tc_fence_after();
       const int row0 = c.qt * BT + quarter * 32;  // segment-relative first row of this warp
       const int nvalid = c.u.n - row0;
       const bool any = c.keys.count() > 0;
-      const int64_t grow = (int64_t)c.u.start + row0 + lane;
+      const int64_t rbase = (int64_t)c.u.start + row0;
+      const __nv_bfloat16* mb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
+      if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
+#pragma unroll
+        for (int s = 0; s < MRING; ++s) {
+          if (s < NC) mslot_fetch(mr + s * MSLOT, mb + s * 32, p.ldm, nvalid, lane);
+          cp_async_commit();
+        }
+        if (NC > MRING && lane < nvalid) prefetch_l2(mb + lane * p.ldm + MRING * 32, (NC - MRING) * 64);
+      }
+      if (!mbar_wait_sleepy(&S.dq_full[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
+      ++dqf_waits[qb];
+      tc_fence_after();
+      int slot = 0;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < NC; ++cc) {
         uint32_t rr[32];
         tmem_ld32(tmem + Cfg::dq_col(qb) + cc * 32 + lane_sel, rr);
         tmem_wait_ld();
-        if (cc == D / 32 - 1) {
+        if (cc == NC - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.dq_free[qb]);
@@ -409,11 +430,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) : 0.f;
-        if (p.z0 && lane < nvalid) attn::mul_silu_grad_32(x, p.z0 + grow * p.ldz + c.h * D + cc * 32);
-        attn::store_rows_bf16_32(x, stg, p.g0 + ((int64_t)c.u.start + row0) * p.ldg + c.h * D + cc * 32, p.ldg,
-                                 nvalid, lane);
+        if (has_m) {
+          cp_async_wait<MRING - 1>();
+          __syncwarp();
+          attn::mul_slot_32(x, mr + slot * MSLOT, lane);
+          __syncwarp();
+          if (cc + MRING < NC) mslot_fetch(mr + slot * MSLOT, mb + (cc + MRING) * 32, p.ldm, nvalid, lane);
+          cp_async_commit();
+          slot = slot == MRING - 1 ? 0 : slot + 1;
+        }
+        attn::store_rows_bf16_32(x, stg, p.g0 + rbase * p.ldg + c.h * D + cc * 32, p.ldg, nvalid, lane);
       }
     }
+    if (has_m) cp_async_wait<0>();
   }
 
   if (!ok) {
@@ -436,7 +465,8 @@ struct DkvCfg {
   static constexpr int TILE = BT * D * 2;
   static constexpr int K_OFF = 0, V_OFF = TILE, RING_OFF = 2 * TILE;
   static constexpr int STG_OFF = RING_OFF + RING * TILE;
-  static constexpr int BAR_OFF = STG_OFF + 4 * 2048;
+  static constexpr int MR_OFF = STG_OFF + 4 * 2048;
+  static constexpr int BAR_OFF = MR_OFF + 4 * MRING * MSLOT;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
 };
@@ -537,6 +567,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sV = base + Cfg::V_OFF;
   uint8_t* sRing = base + Cfg::RING_OFF;
   uint8_t* sStg = base + Cfg::STG_OFF;
+  uint8_t* sMr = base + Cfg::MR_OFF;
   DkvBars& S = *reinterpret_cast<DkvBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -761,44 +792,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
+    uint8_t* mr = sMr + (warp - 2 - EPI_WARPS) * (MRING * MSLOT);
+    const bool has_m = p.m0 != nullptr && p.m1 != nullptr;
+    constexpr int NC = D / 32, NCH = 2 * NC;  // chunks: dV 0 .. NC-1, then dK
     uint32_t full_waits = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
       if (idx >= total) break;
       const DkvItem c = dkv_item(p, idx);
-      if (!mbar_wait_sleepy(&S.dkdv_full, full_waits & 1, abort_flag)) { ok = false; break; }
-      ++full_waits;
-      tc_fence_after();
       const int row0 = c.kt * BT + quarter * 32;
       const int nvalid = c.u.n - row0;
       const bool any = c.qs.count() > 0;
-      const int64_t grow = (int64_t)c.u.start + row0 + lane;
+      const int64_t rbase = (int64_t)c.u.start + row0;
       const float inv_n = 1.0f / (float)c.u.n;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {  // dV (P carries no 1/n_u), then dK
-        const uint32_t col = which == 0 ? Cfg::DV_COL : Cfg::DK_COL;
-        const float sc = which == 0 ? inv_n : 1.f;
-        const __nv_bfloat16* z = which == 0 ? p.z1 : p.z0;
-        __nv_bfloat16* out = which == 0 ? p.g1 : p.g0;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + col + cc * 32 + lane_sel, rr);
-          tmem_wait_ld();
-          if (which == 1 && cc == D / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.dkdv_free);
-          }
-          float x[32];
+      const __nv_bfloat16* mvb = has_m ? p.m1 + rbase * p.ldm + c.h * D : nullptr;
+      const __nv_bfloat16* mkb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
+      if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
-          if (z && lane < nvalid) attn::mul_silu_grad_32(x, z + grow * p.ldz + c.h * D + cc * 32);
-          attn::store_rows_bf16_32(x, stg, out + ((int64_t)c.u.start + row0) * p.ldg + c.h * D + cc * 32, p.ldg,
-                                   nvalid, lane);
+        for (int s = 0; s < MRING; ++s) {
+          mslot_fetch(mr + s * MSLOT, s < NC ? mvb + s * 32 : mkb + (s - NC) * 32, p.ldm, nvalid, lane);
+          cp_async_commit();
+        }
+        if (lane < nvalid) {
+          if (NC > MRING) prefetch_l2(mvb + lane * p.ldm + MRING * 32, (NC - MRING) * 64);
+          const int k0 = MRING > NC ? MRING - NC : 0;
+          prefetch_l2(mkb + lane * p.ldm + k0 * 32, (NC - k0) * 64);
         }
       }
+      if (!mbar_wait_sleepy(&S.dkdv_full, full_waits & 1, abort_flag)) { ok = false; break; }
+      ++full_waits;
+      tc_fence_after();
+      int slot = 0;
+#pragma unroll 1
+      for (int ch = 0; ch < NCH; ++ch) {  // dV (P carries no 1/n_u), then dK
+        const bool is_k = ch >= NC;
+        const int cc = is_k ? ch - NC : ch;
+        uint32_t rr[32];
+        tmem_ld32(tmem + (is_k ? Cfg::DK_COL : Cfg::DV_COL) + cc * 32 + lane_sel, rr);
+        tmem_wait_ld();
+        if (ch == NCH - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.dkdv_free);
+        }
+        const float sc = is_k ? 1.f : inv_n;
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
+        if (has_m) {
+          cp_async_wait<MRING - 1>();
+          __syncwarp();
+          attn::mul_slot_32(x, mr + slot * MSLOT, lane);
+          __syncwarp();
+          const int nx = ch + MRING;
+          if (nx < NCH) mslot_fetch(mr + slot * MSLOT, nx < NC ? mvb + nx * 32 : mkb + (nx - NC) * 32, p.ldm, nvalid, lane);
+          cp_async_commit();
+          slot = slot == MRING - 1 ? 0 : slot + 1;
+        }
+        attn::store_rows_bf16_32(x, stg, (is_k ? p.g0 : p.g1) + rbase * p.ldg + c.h * D + cc * 32, p.ldg, nvalid,
+                                 lane);
+      }
     }
+    if (has_m) cp_async_wait<0>();
   }
 
   if (!ok) {
@@ -837,13 +892,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 // q, k, v: [T, *] f16 with row stride ld; dO: [T, H*d] f16.  dq, dk, dv: bf16
-// with row stride ldg (times silu'(z) of the matching pre-activation block
-// when zq/zk/zv are given, row stride 4*H*d).  Every row of every segment is
-// written.
+// with row stride ldg, each multiplied elementwise by the bf16 multiplier
+// block mq / mk / mv when given (row stride 4*H*d; the layer passes silu'(z)
+// of its UQKV projection).  Every row of every segment is written.
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
                                 __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
-                                const __nv_bfloat16* zq, const __nv_bfloat16* zk, const __nv_bfloat16* zv,
+                                const __nv_bfloat16* mq, const __nv_bfloat16* mk, const __nv_bfloat16* mv,
                                 int32_t* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
@@ -856,7 +911,7 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   pa.users = reinterpret_cast<const UserInfo*>(plan + L.users);
   pa.ts = ts;
   pa.ldg = ldg;
-  pa.ldz = 4 * (int64_t)HD;
+  pa.ldm = 4 * (int64_t)HD;
   pa.H = H;
   pa.scale = 1.0f / sqrtf((float)d);
   pa.status = status;
@@ -865,14 +920,14 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   pa.count = plan + L.counts + 1;
   pa.g0 = dk;
   pa.g1 = dv;
-  pa.z0 = zk;
-  pa.z1 = zv;
+  pa.m0 = mk;
+  pa.m1 = mv;
   pq.items = reinterpret_cast<const WorkItem*>(plan + L.dq_items);
   pq.count = plan + L.counts + 2;
   pq.g0 = dq;
   pq.g1 = nullptr;
-  pq.z0 = zq;
-  pq.z1 = nullptr;
+  pq.m0 = mq;
+  pq.m1 = nullptr;
   const int64_t max_items = L.max_items;
   const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
   if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, pa, pq, grid, s);

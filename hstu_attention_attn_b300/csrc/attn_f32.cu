@@ -95,7 +95,7 @@ template <int NV>
 __global__ void __launch_bounds__(128) attn_f32_bwd_dq_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v, int64_t ld,
     const float* __restrict__ dO, const UserInfo* __restrict__ users, int B, const int64_t* __restrict__ ts,
-    int64_t T, int H, int dh, float* __restrict__ dq, int64_t ldg, const float* __restrict__ z) {
+    int64_t T, int H, int dh, float* __restrict__ dq, int64_t ldg, const float* __restrict__ mq) {
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= T * H) return;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(128) attn_f32_bwd_dq_kernel(
     const int d = lane + 32 * m;
     if (d < dh) {
       float g = acc[m];
-      if (z) g *= silu_grad_acc(z[i * ldg + h * dh + d]);
+      if (mq) g *= mq[i * ldg + h * dh + d];
       dq[i * ldg + h * dh + d] = g;
     }
   }
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(128) attn_f32_bwd_dkdv_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v, int64_t ld,
     const float* __restrict__ dO, const UserInfo* __restrict__ users, int B, const int64_t* __restrict__ ts,
     int64_t T, int H, int dh, float* __restrict__ dk, float* __restrict__ dv, int64_t ldg,
-    const float* __restrict__ zk, const float* __restrict__ zv) {
+    const float* __restrict__ mk, const float* __restrict__ mv) {
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= T * H) return;
@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(128) attn_f32_bwd_dkdv_kernel(
     const int d = lane + 32 * m;
     if (d < dh) {
       float gk = ak[m], gv = av[m];
-      if (zk) gk *= silu_grad_acc(zk[j * ldg + h * dh + d]);
-      if (zv) gv *= silu_grad_acc(zv[j * ldg + h * dh + d]);
+      if (mk) gk *= mk[j * ldg + h * dh + d];
+      if (mv) gv *= mv[j * ldg + h * dh + d];
       dk[j * ldg + h * dh + d] = gk;
       dv[j * ldg + h * dh + d] = gv;
     }
@@ -229,18 +229,18 @@ cudaError_t launch_attn_f32_fwd(const float* q, const float* k, const float* v, 
 
 cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, int64_t ld, const float* dO,
                                 const UserInfo* users, int B, const int64_t* ts, int64_t T, int H, int dh,
-                                float* dq, float* dk, float* dv, int64_t ldg, const float* zq, const float* zk,
-                                const float* zv, cudaStream_t s) {
+                                float* dq, float* dk, float* dv, int64_t ldg, const float* mq, const float* mk,
+                                const float* mv, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const int64_t warps = T * H;
   const int blocks = (int)((warps * 32 + 127) / 128);
   TraceScope tr("attn_f32_bwd", s);
   if (dh <= 64) {
-    attn_f32_bwd_dq_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dq, ldg, zq);
-    attn_f32_bwd_dkdv_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dk, dv, ldg, zk, zv);
+    attn_f32_bwd_dq_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dq, ldg, mq);
+    attn_f32_bwd_dkdv_kernel<2><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dk, dv, ldg, mk, mv);
   } else {
-    attn_f32_bwd_dq_kernel<4><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dq, ldg, zq);
-    attn_f32_bwd_dkdv_kernel<4><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dk, dv, ldg, zk, zv);
+    attn_f32_bwd_dq_kernel<4><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dq, ldg, mq);
+    attn_f32_bwd_dkdv_kernel<4><<<blocks, 128, 0, s>>>(q, k, v, ld, dO, users, B, ts, T, H, dh, dk, dv, ldg, mk, mv);
   }
   return cudaGetLastError();
 }

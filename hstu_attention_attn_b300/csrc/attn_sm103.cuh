@@ -75,12 +75,6 @@ __device__ __forceinline__ void silu_and_grad_half(float h, float& silu, float& 
   dsilu = fmaf(silu, 1.0f - sg, sg);
 }
 
-// silu'(z) of a pre-activation in fp32 (accurate exponential).
-__device__ __forceinline__ float silu_grad_f(float z) {
-  const float sg = sigmoid_f(z);
-  return sg * (1.f + z * (1.f - sg));
-}
-
 // A warp holds 32 consecutive rows (lane = row) x 32 values; write them as
 // bf16 to rows row0 .. row0+31 of out (row stride ld elements), skipping rows
 // >= nvalid, through a 2 KB staging buffer so that each store instruction
@@ -106,17 +100,54 @@ __device__ __forceinline__ void store_rows_bf16_32(const float (&x)[32], uint8_t
   }
 }
 
-// 32 bf16 pre-activations z[0..31] of one row -> silu'(z) multiplied into x.
-__device__ __forceinline__ void mul_silu_grad_32(float (&x)[32], const __nv_bfloat16* z) {
-  const uint4* zp = reinterpret_cast<const uint4*>(z);
+// ---------------------------------------------------------------------------
+// Multiplier chunks of an output warp, fetched ahead of use.  The output warps
+// may multiply each [32 rows][32 columns] gradient chunk elementwise by the
+// same block of a bf16 multiplier (the layer passes silu'(z) of its UQKV
+// projection); a plain per-chunk load would put one HBM round trip per chunk
+// on the path that frees the TMEM accumulators, so the chunks go through a
+// ring of MRING shared slots (2 KB each, rows of 64 bytes with the 16-byte
+// pieces XOR-swizzled by (row >> 1) & 3, conflict-free for both the coalesced
+// fill and the row-per-lane read) filled with cp.async.
+// ---------------------------------------------------------------------------
+constexpr int MRING = 3;
+constexpr int MSLOT = 2048;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Copy rows 0 .. nvalid-1 (at most 32) of a [32][32] bf16 block (row stride ld
+// elements) into a ring slot; one commit group per call is left to the caller.
+__device__ __forceinline__ void mslot_fetch(uint8_t* slot, const __nv_bfloat16* src, int64_t ld, int nvalid,
+                                            int lane) {
+  const uint32_t s = smem_u32(slot);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
+    if (r < nvalid) cp_async16(s + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16), src + (int64_t)r * ld + c4 * 8);
+  }
+}
+
+// x[0..31] *= the 32 bf16 multipliers of row `lane` in a ring slot.
+__device__ __forceinline__ void mul_slot_32(float (&x)[32], const uint8_t* slot, int lane) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const uint4 zz = zp[v];
-    const uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
+    const uint4 mm = *reinterpret_cast<const uint4*>(slot + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
+    const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      x[8 * v + 2 * t] *= silu_grad_f(bf16_lo(w[t]));
-      x[8 * v + 2 * t + 1] *= silu_grad_f(bf16_hi(w[t]));
+      x[8 * v + 2 * t] *= bf16_lo(w[t]);
+      x[8 * v + 2 * t + 1] *= bf16_hi(w[t]);
     }
   }
 }

@@ -400,6 +400,81 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
+// ----------------------------------------------------------------------------
+// Coalesced row-block I/O of an epilogue warp.  The warp holds 32 consecutive
+// rows (lane = row) x 32 consecutive columns in fp32 registers.  Going through
+// a small per-warp shared-memory buffer (16-byte slots XOR-swizzled by row, so
+// both passes are bank-conflict free) turns 32 row-strided accesses per
+// instruction into a few contiguous row segments.  Rows >= nrows and columns
+// >= ncols (a multiple of 8) are not touched.
+// ----------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  uint4 w;
+  w.x = pack2<T>(x[0], x[1]);
+  w.y = pack2<T>(x[2], x[3]);
+  w.z = pack2<T>(x[4], x[5]);
+  w.w = pack2<T>(x[6], x[7]);
+  return w;
+}
+// 16-bit T: 64 bytes per row, staging 2 KB.
+template <typename T>
+__device__ __forceinline__ void store_rows16_32(const float (&x)[32], uint8_t* stg, T* out, int64_t ld, int nrows,
+                                                int ncols, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = pack8<T>(x + 8 * v);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16));
+    if (r < nrows && c4 * 8 < ncols) *reinterpret_cast<uint4*>(out + (int64_t)r * ld + c4 * 8) = w;
+  }
+}
+// fp32: 128 bytes per row, staging 4 KB.
+__device__ __forceinline__ void store_rows32_32(const float (&x)[32], uint8_t* stg, float* out, int64_t ld, int nrows,
+                                                int ncols, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    *reinterpret_cast<float4*>(stg + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+        make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3), c8 = lane & 7;
+    const float4 w = *reinterpret_cast<const float4*>(stg + r * 128 + ((c8 ^ (r & 7)) * 16));
+    if (r < nrows && c8 * 4 < ncols) *reinterpret_cast<float4*>(out + (int64_t)r * ld + c8 * 4) = w;
+  }
+}
+// Load 32 rows x 32 16-bit values of `in` (row stride ld) into x (lane = row);
+// out-of-range rows / columns read as 0.
+template <typename T>
+__device__ __forceinline__ void load_rows16_32(const T* in, int64_t ld, int nrows, int ncols, uint8_t* stg,
+                                               float (&x)[32], int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (r < nrows && c4 * 8 < ncols) w = *reinterpret_cast<const uint4*>(in + (int64_t)r * ld + c4 * 8);
+    *reinterpret_cast<uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[8 * v + 2 * t] = lo16<T>(ww[t]);
+      x[8 * v + 2 * t + 1] = hi16<T>(ww[t]);
+    }
+  }
+}
+
 }  // namespace mtgr
 
 // ----------------------------------------------------------------------------

@@ -8,7 +8,7 @@ namespace mtgr {
 
 enum GemmEpilogue : int {
   EPI_PLAIN = 0,     // C = acc
-  EPI_SILU = 1,      // Z = acc, C = silu(acc)
+  EPI_SILU = 1,      // C = silu(acc), Z = silu'(acc)
   EPI_RESIDUAL = 2,  // C = R + acc
   EPI_F32 = 3,       // fp32 C = acc (split-K slices go to C + split*M*ldc)
 };
@@ -36,13 +36,25 @@ struct GemmArgs {
   int64_t ldc;
   const __nv_bfloat16* R;  // residual (EPI_RESIDUAL)
   int64_t ldr;
-  __nv_bfloat16* Z;  // pre-activation (EPI_SILU)
+  __nv_bfloat16* Z;  // silu'(acc) (EPI_SILU)
   int64_t ldz;
   int splits;  // split-K slices (EPI_F32 only); slice s covers its own K range
   int32_t* status;
   const char* name;  // trace label
 };
 cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s);
+// Split-K slices that launch_gemm_bf16 writes for a request of `splits` over K:
+// every slice covers a whole number of 64-wide K blocks and at least one, so
+// the count can come out below the request.  A caller that reduces the slices
+// must size the reduction with this number.
+inline int gemm_splits(int64_t K, int splits) {
+  const int64_t nk = (K + 63) / 64;
+  int64_t s = splits > 0 ? splits : 1;
+  if (s > nk) s = nk > 0 ? nk : 1;
+  const int64_t per = nk > 0 ? (nk + s - 1) / s : 1;
+  s = nk > 0 ? (nk + per - 1) / per : 1;
+  return (int)s;
+}
 // fp32 out[i] = sum_s parts[s*stride + i] for i < n
 cudaError_t launch_split_reduce(const float* parts, int splits, int64_t stride, int64_t n, float* out,
                                 cudaStream_t s);

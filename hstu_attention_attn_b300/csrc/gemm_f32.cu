@@ -55,8 +55,9 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int64_t M, int64_t N, int
       if (gn >= N) continue;
       const float x = acc[i][j];
       if (EPI == EPI_SILU) {
-        Z[gm * ldz + gn] = x;
-        C[gm * ldc + gn] = x / (1.0f + expf(-x));
+        const float sg = 1.0f / (1.0f + expf(-x));  // C = silu(x), Z = silu'(x)
+        Z[gm * ldz + gn] = sg * (1.0f + x * (1.0f - sg));
+        C[gm * ldc + gn] = x * sg;
       } else if (EPI == EPI_RESIDUAL) {
         C[gm * ldc + gn] = R[gm * ldr + gn] + x;
       } else {

@@ -17,13 +17,15 @@ namespace mtgr {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+static_assert(BK == 64, "gemm_splits counts K in blocks of 64");
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;           // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int STG_BYTES = 4096;  // per epilogue warp: 32 rows x 32 fp32
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Smem {
   uint64_t full[STAGES];
@@ -63,7 +65,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned staging area (128-byte swizzle atoms), then the barriers
   uint8_t* stage_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& S = *reinterpret_cast<Smem*>(stage_base + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = stage_base + STAGES * STAGE_BYTES;
+  Smem& S = *reinterpret_cast<Smem*>(stg_base + 4 * STG_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.splits * p.m_tiles * p.n_tiles;
 
@@ -95,18 +98,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   bool ok = true;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int split, mt, nt;
-        tile_coords(p, t, split, mt, nt);
-        const int kb0 = split * p.kb_per_split;
-        const int kb1 = min(kb0 + p.kb_per_split, p.nk);
-        const int m0 = mt * BM, n0 = nt * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&S.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+    // ---------------- TMA producer (whole warp polls, lane 0 issues) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int split, mt, nt;
+      tile_coords(p, t, split, mt, nt);
+      const int kb0 = split * p.kb_per_split;
+      const int kb1 = min(kb0 + p.kb_per_split, p.nk);
+      const int m0 = mt * BM, n0 = nt * BN;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_warp(&S.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+        if (lane == 0) {
           uint8_t* sa = stage_base + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
@@ -121,53 +124,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(sb, &tmB, &S.full[stage], k0, n0);
           } else {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * (B_BYTES / 4), &tmB, &S.full[stage], n0 + 64 * i, k0);
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * (B_BYTES / 4), &tmB, &S.full[stage], n0 + 64 * i, k0);
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
-        int split, mt, nt;
-        tile_coords(p, t, split, mt, nt);
-        const int kb0 = split * p.kb_per_split;
-        const int kb1 = min(kb0 + p.kb_per_split, p.nk);
-        const int buf = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&S.acc_empty[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+    // ---------------- MMA issuer (whole warp polls, lane 0 issues) ----------------
+    const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      int split, mt, nt;
+      tile_coords(p, t, split, mt, nt);
+      const int kb0 = split * p.kb_per_split;
+      const int kb1 = min(kb0 + p.kb_per_split, p.nk);
+      const int buf = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_warp(&S.acc_empty[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + buf * ACC_COLS;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_warp(&S.full[stage], phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * ACC_COLS;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&S.full[stage], phase, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t sa = smem_u32(stage_base + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
+          const SmemDesc ad = p.a_mn ? smem_desc_sw128_h(sa, A_BYTES / 2, 1024) : smem_desc_sw128_h(sa, 16, 1024);
+          const SmemDesc bd = p.b_mn ? smem_desc_sw128_h(sb, B_BYTES / 4, 1024) : smem_desc_sw128_h(sb, 16, 1024);
+          const uint32_t a_step = p.a_mn ? 2048u >> 4 : 32u >> 4, b_step = p.b_mn ? 2048u >> 4 : 32u >> 4;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + kk * 2048, A_BYTES / 2, 1024)
-                                       : smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + kk * 2048, B_BYTES / 4, 1024)
-                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_ss(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_ss_h(d_tmem, ad.lo + kk * a_step, ad.hi, bd.lo + kk * b_step, bd.hi, idesc,
+                        (kb > kb0 || kk > 0) ? 1u : 0u);
           tc_commit(&S.empty[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
-        tc_commit(&S.acc_full[buf]);
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&S.acc_full[buf]);
+      __syncwarp();
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    uint8_t* stg = stg_base + (warp - 2) * STG_BYTES;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int split, mt, nt;
@@ -176,72 +183,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!mbar_wait(&S.acc_full[buf], acc_phase, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int64_t row = (int64_t)mt * BM + row_in_tile;
-      const bool row_ok = row < p.M;
+      const int64_t row0 = (int64_t)mt * BM + quarter * 32;
+      const int nrows = (int)(p.M - row0 < 32 ? p.M - row0 : 32);
+#pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + buf * ACC_COLS + c * 32 + ((uint32_t)(quarter * 32) << 16), r);
+        tmem_ld32(tmem + buf * ACC_COLS + c * 32 + lane_sel, r);
         tmem_wait_ld();
+        if (c == BN / 32 - 1) {  // the accumulator is free once read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
+        }
         const int64_t col0 = (int64_t)nt * BN + c * 32;
-        if (!row_ok) continue;
-        if (p.epi == EPI_F32) {
-          float* C = reinterpret_cast<float*>(p.C) + (int64_t)split * p.M * p.ldc + row * p.ldc;
+        const int ncols = (int)(p.N - col0 < 32 ? p.N - col0 : 32);
+        if (ncols <= 0 || nrows <= 0) continue;
+        float x[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            if (col0 + 4 * v < p.N)
-              *reinterpret_cast<float4*>(C + col0 + 4 * v) =
-                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+        if (p.epi == EPI_F32) {
+          float* C = reinterpret_cast<float*>(p.C) + (int64_t)split * p.M * p.ldc + row0 * p.ldc + col0;
+          store_rows32_32(x, stg, C, p.ldc, nrows, ncols, lane);
           continue;
         }
-        __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.ldc;
+        if (p.epi == EPI_SILU) {
+          // C = silu(z); Z = silu'(z) = σ(z)(1 + z(1 - σ(z))), the factor that
+          // the backward applies to the gradient of silu(z)
+          float dz[32];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          if (col0 + 8 * v >= p.N) continue;
-          float x[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(r[8 * v + i]);
-          if (p.epi == EPI_SILU) {
-            uint4 zz;
-            zz.x = pack_bf16x2(x[0], x[1]);
-            zz.y = pack_bf16x2(x[2], x[3]);
-            zz.z = pack_bf16x2(x[4], x[5]);
-            zz.w = pack_bf16x2(x[6], x[7]);
-            *reinterpret_cast<uint4*>(p.Z + row * p.ldz + col0 + 8 * v) = zz;
-            // silu of the bf16-rounded pre-activation, so that z and silu(z) agree
-            const uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              x[2 * i] = silu_f(bf16_lo(w[i]));
-              x[2 * i + 1] = silu_f(bf16_hi(w[i]));
-            }
-          } else if (p.epi == EPI_RESIDUAL) {
-            const uint4 rr = *reinterpret_cast<const uint4*>(p.R + row * p.ldr + col0 + 8 * v);
-            const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              x[2 * i] += bf16_lo(w[i]);
-              x[2 * i + 1] += bf16_hi(w[i]);
-            }
+          for (int i = 0; i < 32; ++i) {
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-x[i]));
+            dz[i] = sg * fmaf(x[i], 1.0f - sg, 1.0f);
+            x[i] *= sg;
           }
-          uint4 o;
-          if (p.c_f16) {
-            o.x = pack_f16x2(x[0], x[1]);
-            o.y = pack_f16x2(x[2], x[3]);
-            o.z = pack_f16x2(x[4], x[5]);
-            o.w = pack_f16x2(x[6], x[7]);
-          } else {
-            o.x = pack_bf16x2(x[0], x[1]);
-            o.y = pack_bf16x2(x[2], x[3]);
-            o.z = pack_bf16x2(x[4], x[5]);
-            o.w = pack_bf16x2(x[6], x[7]);
-          }
-          *reinterpret_cast<uint4*>(C + col0 + 8 * v) = o;
+          store_rows16_32(dz, stg, p.Z + row0 * p.ldz + col0, p.ldz, nrows, ncols, lane);
+        } else if (p.epi == EPI_RESIDUAL) {
+          float res[32];
+          load_rows16_32(p.R + row0 * p.ldr + col0, p.ldr, nrows, ncols, stg, res, lane);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] += res[i];
         }
+        if (p.c_f16)
+          store_rows16_32(x, stg, reinterpret_cast<__half*>(p.C) + row0 * p.ldc + col0, p.ldc, nrows, ncols, lane);
+        else
+          store_rows16_32(x, stg, reinterpret_cast<__nv_bfloat16*>(p.C) + row0 * p.ldc + col0, p.ldc, nrows, ncols,
+                          lane);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
     }
   }
 
@@ -292,11 +279,8 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   p.m_tiles = (int)((a.M + BM - 1) / BM);
   p.n_tiles = (int)((a.N + BN - 1) / BN);
   p.nk = (int)((a.K + BK - 1) / BK);
-  int splits = a.epi == EPI_F32 ? (a.splits > 0 ? a.splits : 1) : 1;
-  if (splits > p.nk) splits = p.nk > 0 ? p.nk : 1;
+  const int splits = a.epi == EPI_F32 ? gemm_splits(a.K, a.splits) : 1;
   p.kb_per_split = (p.nk + splits - 1) / splits;
-  splits = (p.nk + p.kb_per_split - 1) / p.kb_per_split;  // every slice gets >= 1 K block
-  if (splits < 1) splits = 1;
   p.splits = splits;
   p.a_mn = a.a_mn_major;
   p.b_mn = a.b_mn_major;

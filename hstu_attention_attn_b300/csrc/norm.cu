@@ -220,14 +220,14 @@ __global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const float* __restric
   }
 }
 
-// dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ silu'(z_u) when z given).
+// dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ dsilu when given: silu'(z_u)).
 template <typename TG, typename TU, typename TO, int NCH>
 __global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__ dY, const float* __restrict__ O,
                                                           const TU* __restrict__ U, int64_t ldu,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ rstd, TO* __restrict__ dO,
                                                           TG* __restrict__ dU, int64_t ldg,
-                                                          const TG* __restrict__ z, int64_t rows, int n) {
+                                                          const TG* __restrict__ dsilu, int64_t rows, int n) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
@@ -247,14 +247,11 @@ __global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__
         s2 += g[m][i] * oh[m][i];
         du[i] = dv[i] * oh[m][i];
       }
-      if (z) {
-        float zv[8];
-        load8(z + r * ldg + 8 * c, zv);
+      if (dsilu) {
+        float mv[8];
+        load8(dsilu + r * ldg + 8 * c, mv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float sg = sigmoid_f(zv[i]);
-          du[i] *= sg * (1.f + zv[i] * (1.f - sg));
-        }
+        for (int i = 0; i < 8; ++i) du[i] *= mv[i];
       }
       store8(dU + r * ldg + 8 * c, du);
     }
@@ -347,12 +344,12 @@ cudaError_t launch_ln_gate_fwd(const float* O, const TU* U, int64_t ldu, TY* Y, 
 
 template <typename TG, typename TU, typename TO>
 cudaError_t launch_ln_gate_bwd(const TG* dY, const float* O, const TU* U, int64_t ldu, const float* mean,
-                               const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* z, int64_t rows, int n,
+                               const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* dsilu, int64_t rows, int n,
                                cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gate_bwd", s);
   NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
-                      dY, O, U, ldu, mean, rstd, dO, dU, ldg, z, rows, n)));
+                      dY, O, U, ldu, mean, rstd, dO, dU, ldg, dsilu, rows, n)));
   return cudaGetLastError();
 }
 

@@ -66,7 +66,7 @@ class HstuAttention:
                                 mean, rstd, self._workspace(db))
         return y, (o, mean, rstd)
 
-    def backward(self, dy, q, k, v, u, saved, db: DeviceBatch, ld=None, z_uqkv=None, grads=None):
+    def backward(self, dy, q, k, v, u, saved, db: DeviceBatch, ld=None, dsilu_uqkv=None, grads=None):
         T, HD = db.T, self.H * self.dh
         ld = ld if ld is not None else q.stride(0)
         o, mean, rstd = saved
@@ -76,7 +76,7 @@ class HstuAttention:
         else:
             dq, dk, dv, du = grads
         mtgr.mtgr_hstu_attn_bwd(dy, q, k, v, u, ld, o, mean, rstd, db.offsets, db.gid, db.ts, T, self.H, self.dh,
-                                dq, dk, dv, du, dq.stride(0), z_uqkv, self._workspace(db))
+                                dq, dk, dv, du, dq.stride(0), dsilu_uqkv, self._workspace(db))
         return dq, dk, dv, du
 
 
@@ -106,7 +106,7 @@ class HstuLayer:
         e = lambda *s: torch.empty(*s, dtype=self.dtype, device=self.device)
         f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
         u16 = torch.float16 if self.dtype == torch.bfloat16 else self.dtype   # attention operands
-        return dict(xn=e(T, self.D), z=e(T, 4 * HD), uqkv=torch.empty(T, 4 * HD, dtype=u16, device=self.device),
+        return dict(xn=e(T, self.D), dsilu=e(T, 4 * HD), uqkv=torch.empty(T, 4 * HD, dtype=u16, device=self.device),
                     o=f(T, HD), y=e(T, HD),
                     gln_mean=f(T), gln_rstd=f(T), ln_mean=f(T), ln_rstd=f(T))
 

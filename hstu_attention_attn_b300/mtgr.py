@@ -35,7 +35,7 @@ class LayerWeights(C.Structure):
 
 
 class LayerSaved(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in ("xn", "z", "uqkv", "o", "y", "gln_mean", "gln_rstd",
+    _fields_ = [(n, C.c_void_p) for n in ("xn", "dsilu", "uqkv", "o", "y", "gln_mean", "gln_rstd",
                                           "ln_mean", "ln_rstd")]
 
 
@@ -208,11 +208,11 @@ def mtgr_hstu_attn_fwd(q, k, v, u, ld_in, offsets, gid, ts, T, n_heads, d_h, eps
 
 
 def mtgr_hstu_attn_bwd(dy, q, k, v, u, ld_in, o_saved, ln_mean, ln_rstd, offsets, gid, ts, T, n_heads, d_h,
-                       dq, dk, dv, du, ld_grad, z_uqkv, workspace, stream=None):
+                       dq, dk, dv, du, ld_grad, dsilu_uqkv, workspace, stream=None):
     _check("mtgr_hstu_attn_bwd",
            lib().mtgr_hstu_attn_bwd(_p(dy), _p(q), _p(k), _p(v), _p(u), ld_in, _p(o_saved), _p(ln_mean),
                                     _p(ln_rstd), _p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, n_heads,
-                                    d_h, _p(dq), _p(dk), _p(dv), _p(du), ld_grad, _p(z_uqkv), _dtype(dy),
+                                    d_h, _p(dq), _p(dk), _p(dv), _p(du), ld_grad, _p(dsilu_uqkv), _dtype(dy),
                                     _p(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)))
 

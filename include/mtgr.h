@@ -188,15 +188,17 @@ MTGR_API mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void
 
 /* Backward of mtgr_hstu_attn_fwd for upstream dy [T, H*d_h].  Writes dq, dk,
  * dv, du (row stride ld_grad elements; every row of every segment is
- * overwritten).  silu'(s) = σ(s)(1 + s(1 - σ(s))).  When z_uqkv is not NULL it
- * is the [T, 4*H*d_h] pre-activation of the layer's UQKV projection (column
- * blocks U, Q, K, V, each head-major) and every gradient is also multiplied by
- * silu'(z) of its block (this fuses the SiLU backward of the projection). */
+ * overwritten).  silu'(s) = σ(s)(1 + s(1 - σ(s))).  When dsilu_uqkv is not
+ * NULL it is a [T, 4*H*d_h] multiplier (dtype, row stride ld_grad, which must
+ * then be 4*H*d_h; column blocks U, Q, K, V, each head-major) and every
+ * gradient is also multiplied elementwise by its block.  The layer passes
+ * silu'(z) of its UQKV pre-activation z, which fuses the SiLU backward of the
+ * projection into this call. */
 MTGR_API mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, const void* v, const void* u,
                                int64_t ld_in, const void* o_saved, const float* ln_mean, const float* ln_rstd,
                                const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
                                int64_t T, int32_t n_heads, int32_t d_h, void* dq, void* dk, void* dv, void* du,
-                               int64_t ld_grad, const void* z_uqkv, mtgr_dtype dtype, void* workspace,
+                               int64_t ld_grad, const void* dsilu_uqkv, mtgr_dtype dtype, void* workspace,
                                size_t workspace_bytes, mtgr_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
@@ -219,7 +221,8 @@ typedef struct {
 
 typedef struct {        /* written by the forward, read by the backward (dtype unless noted) */
   void* xn;             /* [T, D] GLN output */
-  void* z;              /* [T, 4*H*d_h] pre-activation */
+  void* dsilu;          /* [T, 4*H*d_h] silu'(z) at the UQKV pre-activation z: the only
+                           use the backward makes of z */
   void* uqkv;           /* [T, 4*H*d_h] silu(z); f16 in the MTGR_BF16 path (the attention's
                            tensor-core operands, 11 significand bits), fp32 in MTGR_F32 */
   float* o;             /* [T, H*d_h] attention output before the gate (fp32) */

@@ -97,7 +97,7 @@ def test_layer_f32(orc, seed):
     ref = orc.layer_fwd(b, L.D, L.H, L.dh, L.x, L.w_uqkv, L.w_o, L.gamma, L.beta)
     torch.cuda.synchronize()
     assert_close(to_np(saved["xn"]), ref["xn"], TOL_F32, "xn")
-    assert_close(to_np(saved["z"]), ref["z"], TOL_F32, "z")
+    assert_close(to_np(saved["dsilu"]), orc.silu_grad(ref["z"]), TOL_F32, "silu'(z)")
     assert_close(to_np(saved["o"]), ref["o"], TOL_F32, "o")
     assert_close(to_np(saved["y"]), ref["y"], TOL_F32, "y")
     assert_close(to_np(x_out), ref["x_out"], TOL_F32, "x_out")
