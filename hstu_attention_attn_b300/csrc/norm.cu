@@ -110,47 +110,120 @@ __global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T
   }
 }
 
+// 8 consecutive elements of a row kept in their stored form (one 16-byte
+// vector for bf16, two for fp32) and widened to fp32 on use.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 w;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { w = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = bf16_lo(u[i]);
+      v[2 * i + 1] = bf16_hi(u[i]);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
 // dx = rstd (dŷ - mean(dŷ) - x̂ mean(dŷ x̂)) (+ dres), dŷ = dy ⊙ γ_g;
-// per-block partial sums of dy ⊙ x̂ and dy per group go to `partial`
+// per-block sums of dy ⊙ x̂ and dy per group go to `partial`
 // ([gridDim.x][2][4][D] fp32), reduced by gln_param_reduce_kernel.
+// Each warp takes a contiguous range of rows.  Tokens of a user are sorted by
+// group, so the group id changes rarely along the range: for bf16 rows up to
+// 1024 features (fp32 up to 512) every lane keeps the sums of its own columns
+// in registers and adds them to the block's shared sums only when the group
+// changes; for wider rows the registers do not suffice and every row adds
+// into the shared sums directly.
 template <typename T, int NCH>
-__global__ void __launch_bounds__(256) gln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
-                                                      const float* __restrict__ mean,
-                                                      const float* __restrict__ rstd,
-                                                      const uint8_t* __restrict__ gid,
-                                                      const float* __restrict__ gamma,
-                                                      const T* __restrict__ dres, T* __restrict__ dx,
-                                                      float* __restrict__ partial, int64_t rows, int D) {
+__global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
+    gln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ mean,
+                   const float* __restrict__ rstd, const uint8_t* __restrict__ gid, const float* __restrict__ gamma,
+                   const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ partial, int64_t rows,
+                   int D) {
+  constexpr bool REG = NCH * sizeof(T) <= 8;  // bf16 rows up to 1024, fp32 rows up to 512
   extern __shared__ float acc[];  // [2][4][D]
   for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) acc[i] = 0.f;
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    const float mu = mean[r], rs = rstd[r];
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t per = (rows + nw - 1) / nw;
+  const int64_t r0 = w * per, r1 = r0 + per < rows ? r0 + per : rows;
+  float sg[REG ? NCH : 1][8], sb[REG ? NCH : 1][8];  // Σ dy x̂, Σ dy of the current group
+  if constexpr (REG) {
+#pragma unroll
+    for (int m = 0; m < NCH; ++m)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sg[m][i] = sb[m][i] = 0.f;
+  }
+  int gcur = -1;
+  auto flush = [&]() {
+    if constexpr (REG) {
+      ROW_CHUNKS_FOR(m, c, lane, D) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          atomicAdd(&acc[gcur * D + 8 * c + i], sg[m][i]);
+          atomicAdd(&acc[(4 + gcur) * D + 8 * c + i], sb[m][i]);
+          sg[m][i] = sb[m][i] = 0.f;
+        }
+      }
+    }
+  };
+  for (int64_t r = r0; r < r1; ++r) {
     const int g = min((int)gid[r], 3);
-    float xh[NCH][8], gy[NCH][8];
+    if (g != gcur) {
+      if (gcur >= 0) flush();
+      gcur = g;
+    }
+    const float mu = mean[r], rs = rstd[r];
+    Raw8<T> xr[NCH], dr[NCH];
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      xr[m].load(x + r * D + 8 * c);
+      dr[m].load(dy + r * D + 8 * c);
+    }
     float s1 = 0.f, s2 = 0.f;
     ROW_CHUNKS_FOR(m, c, lane, D) {
       float xv[8], dv[8], ga[8];
-      load8(x + r * D + 8 * c, xv);
-      load8(dy + r * D + 8 * c, dv);
+      xr[m].get(xv);
+      dr[m].get(dv);
       load8(gamma + (int64_t)g * D + 8 * c, ga);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        xh[m][i] = (xv[i] - mu) * rs;
-        gy[m][i] = dv[i] * ga[i];
-        s1 += gy[m][i];
-        s2 += gy[m][i] * xh[m][i];
-        atomicAdd(&acc[(0 * 4 + g) * D + 8 * c + i], dv[i] * xh[m][i]);
-        atomicAdd(&acc[(1 * 4 + g) * D + 8 * c + i], dv[i]);
+        const float xh = (xv[i] - mu) * rs, gy = dv[i] * ga[i];
+        s1 += gy;
+        s2 += gy * xh;
+        if constexpr (REG) {
+          sg[m][i] += dv[i] * xh;
+          sb[m][i] += dv[i];
+        } else {
+          atomicAdd(&acc[g * D + 8 * c + i], dv[i] * xh);
+          atomicAdd(&acc[(4 + g) * D + 8 * c + i], dv[i]);
+        }
       }
     }
     const float m1 = warp_sum(s1) / (float)D, m2 = warp_sum(s2) / (float)D;
     ROW_CHUNKS_FOR(m, c, lane, D) {
-      float o[8];
+      float xv[8], dv[8], ga[8], o[8];
+      xr[m].get(xv);
+      dr[m].get(dv);
+      load8(gamma + (int64_t)g * D + 8 * c, ga);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = rs * (gy[m][i] - m1 - xh[m][i] * m2);
+      for (int i = 0; i < 8; ++i) o[i] = rs * (dv[i] * ga[i] - m1 - (xv[i] - mu) * rs * m2);
       if (dres) {
         float rv[8];
         load8(dres + r * D + 8 * c, rv);
@@ -160,6 +233,7 @@ __global__ void __launch_bounds__(256) gln_bwd_kernel(const T* __restrict__ dy, 
       store8(dx + r * D + 8 * c, o);
     }
   }
+  if (gcur >= 0) flush();
   __syncthreads();
   float* out = partial + (int64_t)blockIdx.x * 8 * D;
   for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) out[i] = acc[i];
