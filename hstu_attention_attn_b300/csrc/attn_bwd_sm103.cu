@@ -39,9 +39,6 @@ using attn::packed_col;
 using attn::silu_and_grad_half;
 using attn::MRING;
 using attn::MSLOT;
-using attn::cp_async_commit;
-using attn::cp_async_wait;
-using attn::prefetch_l2;
 using attn::mslot_fetch;
 
 constexpr int NUM_THREADS = 448;  // 14 warps

@@ -113,19 +113,6 @@ __device__ __forceinline__ void store_rows_bf16_32(const float (&x)[32], uint8_t
 constexpr int MRING = 3;
 constexpr int MSLOT = 2048;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Copy rows 0 .. nvalid-1 (at most 32) of a [32][32] bf16 block (row stride ld
 // elements) into a ring slot; one commit group per call is left to the caller.
 __device__ __forceinline__ void mslot_fetch(uint8_t* slot, const __nv_bfloat16* src, int64_t ld, int nvalid,

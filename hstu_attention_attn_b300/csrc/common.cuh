@@ -449,6 +449,49 @@ __device__ __forceinline__ void store_rows32_32(const float (&x)[32], uint8_t* s
     if (r < nrows && c8 * 4 < ncols) *reinterpret_cast<float4*>(out + (int64_t)r * ld + c8 * 4) = w;
   }
 }
+// Asynchronous global -> shared copies (cp.async, 16 bytes, cached in L2
+// only) and their commit groups; a bulk L2 prefetch.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The two halves of load_rows16_32 for a copy issued ahead of use: start the
+// copy of rows < nrows, columns < ncols of a [32][32] 16-bit block into a 2 KB
+// staging slot (same swizzle as below); after the copy's group has completed
+// and a __syncwarp, read row `lane` back as floats.
+__device__ __forceinline__ void fetch_rows16_32(uint8_t* slot, const void* in, int64_t ld, int nrows, int ncols,
+                                                int lane) {
+  const uint32_t s = smem_u32(slot);
+  const uint16_t* src = static_cast<const uint16_t*>(in);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
+    if (r < nrows && c4 * 8 < ncols) cp_async16(s + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16), src + r * ld + c4 * 8);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void read_rows16_32(const uint8_t* slot, float (&x)[32], int lane) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 w = *reinterpret_cast<const uint4*>(slot + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[8 * v + 2 * t] = lo16<T>(ww[t]);
+      x[8 * v + 2 * t + 1] = hi16<T>(ww[t]);
+    }
+  }
+}
+
 // Load 32 rows x 32 16-bit values of `in` (row stride ld) into x (lane = row);
 // out-of-range rows / columns read as 0.
 template <typename T>

@@ -25,7 +25,9 @@ constexpr int ACC_COLS = BN;           // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_THREADS = 192;
 constexpr int STG_BYTES = 4096;  // per epilogue warp: 32 rows x 32 fp32
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int RES_BYTES = 2 * 2048;  // per epilogue warp: 2 residual chunks of 32 rows x 32 bf16
+constexpr int SMEM_BYTES =
+    STAGES * STAGE_BYTES + 4 * STG_BYTES + 4 * RES_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Smem {
   uint64_t full[STAGES];
@@ -66,7 +68,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // 1024-byte aligned staging area (128-byte swizzle atoms), then the barriers
   uint8_t* stage_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg_base = stage_base + STAGES * STAGE_BYTES;
-  Smem& S = *reinterpret_cast<Smem*>(stg_base + 4 * STG_BYTES);
+  uint8_t* res_base = stg_base + 4 * STG_BYTES;
+  Smem& S = *reinterpret_cast<Smem*>(res_base + 4 * RES_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.splits * p.m_tiles * p.n_tiles;
 
@@ -175,16 +178,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     uint8_t* stg = stg_base + (warp - 2) * STG_BYTES;
+    // Residual chunks (EPI_RESIDUAL) go through a 2-slot cp.async ring: chunks
+    // 0 and 1 are requested before the accumulator wait and the rest of the
+    // warp's rows of the tile are prefetched into L2, so no chunk waits for a
+    // full HBM round trip while the accumulator is held.
+    uint8_t* rres = res_base + (warp - 2) * RES_BYTES;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int split, mt, nt;
       tile_coords(p, t, split, mt, nt);
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&S.acc_full[buf], acc_phase, abort_flag)) { ok = false; break; }
-      tc_fence_after();
       const int64_t row0 = (int64_t)mt * BM + quarter * 32;
       const int nrows = (int)(p.M - row0 < 32 ? p.M - row0 : 32);
+      if (p.epi == EPI_RESIDUAL && nrows > 0) {
+        const int64_t n0 = (int64_t)nt * BN;
+        const __nv_bfloat16* Rt = p.R + row0 * p.ldr + n0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int64_t cq = n0 + 32 * q;
+          if (cq < p.N) fetch_rows16_32(rres + q * 2048, Rt + 32 * q, p.ldr, nrows, (int)(p.N - cq < 32 ? p.N - cq : 32), lane);
+          cp_async_commit();
+        }
+        const int64_t tcols = p.N - n0 < BN ? p.N - n0 : BN;
+        if (lane < nrows && tcols > 64) prefetch_l2(Rt + (int64_t)lane * p.ldr + 64, (uint32_t)(tcols - 64) * 2u);
+      }
+      if (!mbar_wait(&S.acc_full[buf], acc_phase, abort_flag)) { ok = false; break; }
+      tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -218,8 +238,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           store_rows16_32(dz, stg, p.Z + row0 * p.ldz + col0, p.ldz, nrows, ncols, lane);
         } else if (p.epi == EPI_RESIDUAL) {
+          cp_async_wait<1>();
+          __syncwarp();
           float res[32];
-          load_rows16_32(p.R + row0 * p.ldr + col0, p.ldr, nrows, ncols, stg, res, lane);
+          read_rows16_32<__nv_bfloat16>(rres + (c & 1) * 2048, res, lane);
+          __syncwarp();
+          const int64_t cx = col0 + 64;  // chunk c + 2 into the slot just read
+          if (c + 2 < BN / 32 && cx < p.N)
+            fetch_rows16_32(rres + (c & 1) * 2048, p.R + row0 * p.ldr + cx, p.ldr, nrows,
+                            (int)(p.N - cx < 32 ? p.N - cx : 32), lane);
+          cp_async_commit();
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[i] += res[i];
         }
@@ -230,6 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           lane);
       }
     }
+    cp_async_wait<0>();
   }
 
   if (!ok) {
