@@ -149,6 +149,25 @@ bool make_tmap_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
                       uint32_t box_cols, uint32_t box_rows) {
   return make_tmap_16bit_2d(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, base, rows, cols, ld, box_cols, box_rows);
 }
+bool make_tmap_out(CUtensorMap* m, OutType t, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                   uint64_t slices, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0 || cols == 0) return false;
+  const CUtensorMapDataType dt = t == OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : t == OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t es = t == OUT_F32 ? 4 : 2;
+  const uint64_t inner = box_cols * es;
+  if (inner != 64 && inner != 128) return false;
+  const CUtensorMapSwizzle sw = inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  cuuint64_t dims[3] = {cols, rows, slices > 0 ? slices : 1};
+  cuuint64_t strides[2] = {ld * es, rows * ld * es};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, slices > 0 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // ---------------------------------------------------------------------------
 // Workspace carving
@@ -183,13 +202,24 @@ struct LayerWs {
   size_t attn_base, dY, dZ, dxn, gln_part, wpart, total;
   int splits_uqkv, splits_o;
 };
+// Split-K count for a weight-gradient GEMM (M x N output, K = tokens): the
+// persistent kernel runs tiles x splits work units over the SMs, and each
+// slice costs one fp32 M x N partial in the reduction, so take the fewest
+// splits (at most 16) whose waves are within 2% as full as the fullest.
 static int choose_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-  const int64_t nk = (K + 63) / 64;
-  int64_t s = (2 * (int64_t)num_sms() + tiles - 1) / tiles;
-  if (s > 16) s = 16;
-  if (s > nk) s = nk;
-  return gemm_splits(K, (int)(s < 1 ? 1 : s));
+  const int64_t sms = num_sms();
+  auto fill = [&](int s) {
+    const int64_t units = tiles * s;
+    return (double)units / (double)(((units + sms - 1) / sms) * sms);
+  };
+  double best = 0.0;
+  for (int req = 1; req <= 16; ++req) best = fmax(best, fill(gemm_splits(K, req)));
+  for (int req = 1; req <= 16; ++req) {
+    const int s = gemm_splits(K, req);  // the count the GEMM actually runs
+    if (fill(s) >= best - 0.02) return s;
+  }
+  return 1;
 }
 static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, mtgr_dtype dt) {
   LayerWs w;

@@ -137,7 +137,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed bulk stores still read shared memory.
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read_n() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -533,6 +544,14 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 // Same for an f16 matrix.
 bool make_tmap_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                       uint32_t box_cols, uint32_t box_rows);
+// Tensor map for TMA stores of an output matrix [rows, cols] (row stride ld
+// elements): a 2-D map when slices == 0, else a 3-D map over `slices` such
+// matrices laid out back to back (a box clipped at `rows` then never spills
+// into the next slice).  The box row is 64 or 128 bytes and uses the 64- or
+// 128-byte swizzle of that width.
+enum OutType { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
+bool make_tmap_out(CUtensorMap* m, OutType t, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                   uint64_t slices, uint32_t box_cols, uint32_t box_rows);
 int num_sms();
 
 // Kernel tracing: when enabled (mtgr_trace_enable), every launch inside a

@@ -23,11 +23,15 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;           // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;
-constexpr int NUM_THREADS = 192;
-constexpr int STG_BYTES = 4096;  // per epilogue warp: 32 rows x 32 fp32
-constexpr int RES_BYTES = 2 * 2048;  // per epilogue warp: 2 residual chunks of 32 rows x 32 bf16
-constexpr int SMEM_BYTES =
-    STAGES * STAGE_BYTES + 4 * STG_BYTES + 4 * RES_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// warp 0 TMA, warp 1 MMA, then 4 epilogue warps (EPI_RESIDUAL) or 8 (two per
+// TMEM lane quarter, each draining half of the tile's columns)
+constexpr int MAX_THREADS = 320;
+// 32 KB of epilogue staging in 2 KB slots (each a [32][32] 16-bit TMA box).
+// With 4 epilogue warps each has 8 KB: 2 residual slots + 2 output slots
+// (EPI_RESIDUAL).  With 8 warps each has 4 KB: a ring of 2 output slots, or
+// one fp32 box of 4 KB (EPI_F32).
+constexpr int EP_TOTAL = 32768;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EP_TOTAL + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Smem {
   uint64_t full[STAGES];
@@ -53,6 +57,42 @@ struct Params {
   int32_t* status;
 };
 
+// Stage 32 rows x 32 values (lane = row) as 16-bit T in the 64-byte-swizzled
+// layout of a [32][32] TMA box and store the box at (x0, y0).
+template <typename T>
+__device__ __forceinline__ void stage_store16(const float (&x)[32], uint8_t* slot, const CUtensorMap* m, int x0,
+                                              int y0, int lane) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    *reinterpret_cast<uint4*>(slot + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = pack8<T>(x + 8 * v);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(m, slot, x0, y0);
+    tma_store_commit();
+  }
+}
+// fp32: 128-byte rows with the 128-byte swizzle, box [1][32][32] of a 3-D map.
+__device__ __forceinline__ void stage_store32(const float (&x)[32], uint8_t* slot, const CUtensorMap* m, int x0,
+                                              int y0, int z0, int lane) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    *reinterpret_cast<float4*>(slot + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+        make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(m, slot, x0, y0, z0);
+    tma_store_commit();
+  }
+}
+// Before restaging a slot: at most N newer stores of this warp may still be reading theirs.
+template <int N>
+__device__ __forceinline__ void slot_free(int lane) {
+  if (lane == 0) tma_store_wait_read_n<N>();
+  __syncwarp();
+}
+
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int& split, int& mt, int& nt) {
   const int per_split = p.m_tiles * p.n_tiles;
   split = t / per_split;
@@ -61,15 +101,16 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& split, 
   nt = r - mt * p.n_tiles;
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(MAX_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ,
                      const Params p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned staging area (128-byte swizzle atoms), then the barriers
   uint8_t* stage_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stg_base = stage_base + STAGES * STAGE_BYTES;
-  uint8_t* res_base = stg_base + 4 * STG_BYTES;
-  Smem& S = *reinterpret_cast<Smem*>(res_base + 4 * RES_BYTES);
+  uint8_t* ep_base = stage_base + STAGES * STAGE_BYTES;
+  Smem& S = *reinterpret_cast<Smem*>(ep_base + EP_TOTAL);
+  const int n_epi = (int)(blockDim.x >> 5) - 2;  // 4 or 8
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.splits * p.m_tiles * p.n_tiles;
 
@@ -80,7 +121,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.acc_full[i], 1);
-      mbar_init(&S.acc_empty[i], 4);  // one arrival per epilogue warp
+      mbar_init(&S.acc_empty[i], n_epi);  // one arrival per epilogue warp
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -92,6 +133,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmZ);
   }
   tc_fence_before();
   __syncthreads();
@@ -174,15 +217,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2 .. 2 + n_epi - 1) ----------------
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    uint8_t* stg = stg_base + (warp - 2) * STG_BYTES;
-    // Residual chunks (EPI_RESIDUAL) go through a 2-slot cp.async ring: chunks
-    // 0 and 1 are requested before the accumulator wait and the rest of the
-    // warp's rows of the tile are prefetched into L2, so no chunk waits for a
-    // full HBM round trip while the accumulator is held.
-    uint8_t* rres = res_base + (warp - 2) * RES_BYTES;
+    const int e = warp - 2;
+    const int cpw = (BN / 32) * 4 / n_epi;  // 32-column chunks per warp: 8 or 4
+    const int c0 = (e >> 2) * cpw;          // this warp's first chunk of the tile
+    // Outputs leave through TMA stores from the warp's staging slots, so the
+    // warp never waits on global stores.  Residual chunks (EPI_RESIDUAL, 4
+    // epilogue warps) come in through a 2-slot cp.async ring: chunks 0 and 1
+    // are requested before the accumulator wait and the rest of the warp's
+    // rows of the tile are prefetched into L2, so no chunk waits for a full
+    // HBM round trip while the accumulator is held.
+    uint8_t* wbuf = ep_base + e * (EP_TOTAL / n_epi);
+    uint8_t* rres = wbuf;  // EPI_RESIDUAL: residual slots 0, 1; output slots 2, 3
+    const bool wide = n_epi == 4;
+    int ns = 0;            // stores issued by this warp
+    // staging slot for the next 16-bit output box
+    auto out_slot = [&]() -> uint8_t* {
+      uint8_t* sl;
+      if (p.epi == EPI_RESIDUAL) {
+        slot_free<1>(lane);
+        sl = wbuf + 4096 + (ns & 1) * 2048;
+      } else if (wide) {
+        slot_free<3>(lane);
+        sl = wbuf + (ns & 3) * 2048;
+      } else {
+        slot_free<1>(lane);
+        sl = wbuf + (ns & 1) * 2048;
+      }
+      ++ns;
+      return sl;
+    };
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int split, mt, nt;
@@ -206,11 +272,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(&S.acc_full[buf], acc_phase, abort_flag)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int j = 0; j < cpw; ++j) {
+        const int c = c0 + j;
         uint32_t r[32];
         tmem_ld32(tmem + buf * ACC_COLS + c * 32 + lane_sel, r);
         tmem_wait_ld();
-        if (c == BN / 32 - 1) {  // the accumulator is free once read
+        if (j == cpw - 1) {  // the accumulator is free once read
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
@@ -222,8 +289,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
         if (p.epi == EPI_F32) {
-          float* C = reinterpret_cast<float*>(p.C) + (int64_t)split * p.M * p.ldc + row0 * p.ldc + col0;
-          store_rows32_32(x, stg, C, p.ldc, nrows, ncols, lane);
+          uint8_t* sl;
+          if (wide) {
+            slot_free<1>(lane);
+            sl = wbuf + (ns & 1) * 4096;
+          } else {
+            slot_free<0>(lane);
+            sl = wbuf;
+          }
+          ++ns;
+          stage_store32(x, sl, &tmC, (int)col0, (int)row0, split, lane);
           continue;
         }
         if (p.epi == EPI_SILU) {
@@ -236,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dz[i] = sg * fmaf(x[i], 1.0f - sg, 1.0f);
             x[i] *= sg;
           }
-          store_rows16_32(dz, stg, p.Z + row0 * p.ldz + col0, p.ldz, nrows, ncols, lane);
+          stage_store16<__nv_bfloat16>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
         } else if (p.epi == EPI_RESIDUAL) {
           cp_async_wait<1>();
           __syncwarp();
@@ -252,12 +327,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) x[i] += res[i];
         }
         if (p.c_f16)
-          store_rows16_32(x, stg, reinterpret_cast<__half*>(p.C) + row0 * p.ldc + col0, p.ldc, nrows, ncols, lane);
+          stage_store16<__half>(x, out_slot(), &tmC, (int)col0, (int)row0, lane);
         else
-          store_rows16_32(x, stg, reinterpret_cast<__nv_bfloat16*>(p.C) + row0 * p.ldc + col0, p.ldc, nrows, ncols,
-                          lane);
+          stage_store16<__nv_bfloat16>(x, out_slot(), &tmC, (int)col0, (int)row0, lane);
       }
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
     cp_async_wait<0>();
   }
 
@@ -311,6 +387,14 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   const int splits = a.epi == EPI_F32 ? gemm_splits(a.K, a.splits) : 1;
   p.kb_per_split = (p.nk + splits - 1) / splits;
   p.splits = splits;
+  // outputs: [32][32] boxes; fp32 split-K slices as a 3-D map
+  CUtensorMap tmC, tmZ;
+  const bool okC = a.epi == EPI_F32
+                       ? make_tmap_out(&tmC, OUT_F32, a.C, a.M, a.N, a.ldc, splits, 32, 32)
+                       : make_tmap_out(&tmC, a.c_f16 ? OUT_F16 : OUT_BF16, a.C, a.M, a.N, a.ldc, 0, 32, 32);
+  const bool okZ = a.epi == EPI_SILU ? make_tmap_out(&tmZ, OUT_BF16, a.Z, a.M, a.N, a.ldz, 0, 32, 32) : true;
+  if (a.epi != EPI_SILU) tmZ = tmC;
+  if (!okC || !okZ) return cudaErrorInvalidValue;
   p.a_mn = a.a_mn_major;
   p.b_mn = a.b_mn_major;
   p.epi = a.epi;
@@ -328,7 +412,9 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   const int grid = tiles < num_sms() ? tiles : num_sms();
   if (p.nk == 0) return cudaErrorInvalidValue;
   TraceScope tr(a.name ? a.name : "gemm", s);
-  gemm_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+  // the residual epilogue keeps 4 warps (its cp.async ring needs 8 KB each)
+  const int threads = a.epi == EPI_RESIDUAL ? 192 : MAX_THREADS;
+  gemm_bf16_kernel<<<grid, threads, SMEM_BYTES, s>>>(tmA, tmB, tmC, tmZ, p);
   return cudaGetLastError();
 }
 
