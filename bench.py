@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--workload", choices=["large_train", "small_attn"], default="large_train")
     ap.add_argument("--seed", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=262144,
+                    help="training-step batch: users are drawn until it holds at least this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -169,7 +171,7 @@ def run_reference(args):
     if rank != 0:
         return
     from hstu_attention_attn_b300 import synth
-    L = synth.large_train_layer(args.seed) if args.workload == "large_train" else None
+    L = synth.large_train_layer(args.seed, args.tokens) if args.workload == "large_train" else None
     if L is None:
         a = synth.small_attn(1)
         batch, H, dh = a.batch, a.H, a.dh
@@ -200,7 +202,10 @@ def workload_config(args, batch, H, dh, D=None):
                             f"{batch.T} tokens, d_model 1024, {H} heads x d_h {dh}, Seq lognormal median 300 "
                             f"in [16,1000], RealTime U[0,64], 20 candidates, grad on candidates only",
                 "tokens": int(batch.T), "users": int(batch.B), "d_model": 1024, "n_heads": H, "d_h": dh,
-                "l2": "inputs larger than L2 (x and dx_out are 512 MiB each)", "parallelism": "replicas only"}
+                "l2": (f"inputs larger than L2 (x and dx_out are {batch.T * 2048 / 2**20:.0f} MiB each)"
+                       if batch.T * 2048 > 126 * 2**20 else
+                       f"working set larger than L2 (uqkv and silu'(z) are {batch.T * 2 * 4096 * 2 / 2**20:.0f} MiB)"),
+                "parallelism": "replicas only"}
     return {"workload": f"MTGR-small-like attention fwd+bwd: {batch.B} users, {batch.T} tokens, {H} heads x d_h {dh}",
             "tokens": int(batch.T), "users": int(batch.B), "n_heads": H, "d_h": dh,
             "l2": "inputs larger than L2", "parallelism": "replicas only"}
@@ -226,7 +231,7 @@ def run_mine(args):
 
     # ---- inputs (seeded, synthetic; each replica draws its own batch) ----
     if args.workload == "large_train":
-        L = synth.large_train_layer(args.seed + rank)
+        L = synth.large_train_layer(args.seed + rank, args.tokens)
         batch, H, dh, D = L.batch, L.H, L.dh, L.D
     else:
         A = synth.small_attn(1 + rank)

@@ -133,7 +133,8 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const Us
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers each (5 warps on some SMSPs)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p) {
   using Cfg = FwdCfg<D>;
   const int total = p.counts[0];
 
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -393,6 +395,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
       const float inv_n = 1.0f / (float)u.n;
       const int row0 = qt * BQ + quarter * 32;  // segment-relative first row of this warp
       float* obase = p.O + (int64_t)(u.start + row0) * p.ldo + c.h * D + g * (D / 2);
+      // A box of 32 rows inside the segment leaves by TMA store; the warp that
+      // holds the segment's end stores its valid rows one by one (a box would
+      // also write the next user's rows).
+      const bool box = row0 + 32 <= u.n;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t rr[32];
@@ -400,7 +406,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
         tmem_wait_ld();
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
-          // row r_in's 16 values -> stg[lane][16], 16-byte slots XOR-swizzled by row
+          // row r_in's 16 values -> stg[lane][16], 16-byte slots XOR-swizzled by
+          // row (the 64-byte swizzle of a [32][16] fp32 TMA box); the previous
+          // box store must have finished reading the buffer
+          if (lane == 0) tma_store_wait_read_n<0>();
           __syncwarp();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -410,6 +419,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
                             __uint_as_float(rr[sub * 16 + 4 * v + 1]) * inv_n,
                             __uint_as_float(rr[sub * 16 + 4 * v + 2]) * inv_n,
                             __uint_as_float(rr[sub * 16 + 4 * v + 3]) * inv_n);
+          }
+          if (box) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, stg, c.h * D + g * (D / 2) + cc * 32 + sub * 16, u.start + row0);
+              tma_store_commit();
+            }
+            continue;
           }
           __syncwarp();
           // 8 rows x 64 bytes per store instruction
@@ -426,6 +444,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.o_free[sl]);
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
   }
 
   if (!ok) {
@@ -449,9 +469,9 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BKV) ||
-      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV))
+      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV) || !make_tmap_out(&to, OUT_F32, O, T, HD, HD, 0, 16, 32))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.users = reinterpret_cast<const UserInfo*>(plan + L.users);
@@ -471,12 +491,12 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
     auto kern = attn_fwd_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<128>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, to, p);
   } else if (d == 64) {
     auto kern = attn_fwd_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<64>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, to, p);
   } else {
     return cudaErrorInvalidValue;
   }

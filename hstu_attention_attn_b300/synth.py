@@ -204,5 +204,6 @@ def large_layer(seed=2):
     return layer_inputs(seed, large_users, LARGE.D, LARGE.H, LARGE.dh, "dense")
 
 
-def large_train_layer(seed=3):
-    return layer_inputs(seed, large_users_token_budget, LARGE.D, LARGE.H, LARGE.dh, "cand")
+def large_train_layer(seed=3, min_tokens=262144):
+    return layer_inputs(seed, lambda rng: large_users_token_budget(rng, min_tokens), LARGE.D, LARGE.H, LARGE.dh,
+                        "cand")
