@@ -39,7 +39,7 @@ ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--workload", choices=["large_train", "small_attn"], default="large_train")
@@ -76,7 +76,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -341,24 +341,57 @@ def run_mine(args):
         h2d = x_h.numel() * 2 + dxo_h.numel() * 2 + sum(m.numel() * m.element_size() for m in meta_h)
         d2h = sum(t.numel() * t.element_size() for t in g_h.values())
 
-        def e2e_step():
-            x.copy_(x_h, non_blocking=True)
-            dxo.copy_(dxo_h, non_blocking=True)
-            db.offsets.copy_(meta_h[0], non_blocking=True)
-            db.gid.copy_(meta_h[1], non_blocking=True)
-            db.ts.copy_(meta_h[2], non_blocking=True)
-            layer.forward(x, db, saved, x_out)
-            layer.backward(x, saved, dxo, db, dx, grads)
-            for n, t in grads.items():
-                g_h[n].copy_(t, non_blocking=True)
-        for _ in range(2):
-            e2e_step()
+        # Input prefetch as a training loop does it: two device sets of inputs,
+        # metadata and weight gradients; a copy stream brings step k+1's inputs
+        # in while step k computes, then reads step k's weight gradients out.
+        # Every step's copies are inside the timed region (the first input copy
+        # is issued in it, and nothing is copied for a step after the last).
+        comp_s = torch.cuda.current_stream(dev)
+        copy_s = torch.cuda.Stream(dev)
+        xs, dxos = [x, torch.empty_like(x)], [dxo, torch.empty_like(dxo)]
+        dbs = [db, device_batch(batch, dev)]
+        gs = [grads, {n: torch.empty_like(t) for n, t in grads.items()}]
+        ghs = [g_h, {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in grads.items()}]
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in_ready", "in_free", "out_ready", "out_free")}
+        for k in ("in_free", "out_free"):
+            for e in ev[k]:
+                e.record(comp_s)
+
+        def copy_in(b):
+            with torch.cuda.stream(copy_s):
+                copy_s.wait_event(ev["in_free"][b])
+                xs[b].copy_(x_h, non_blocking=True)
+                dxos[b].copy_(dxo_h, non_blocking=True)
+                dbs[b].offsets.copy_(meta_h[0], non_blocking=True)
+                dbs[b].gid.copy_(meta_h[1], non_blocking=True)
+                dbs[b].ts.copy_(meta_h[2], non_blocking=True)
+                ev["in_ready"][b].record(copy_s)
+
+        def compute_and_d2h(b):
+            comp_s.wait_event(ev["in_ready"][b])
+            comp_s.wait_event(ev["out_free"][b])
+            layer.forward(xs[b], dbs[b], saved, x_out)
+            layer.backward(xs[b], saved, dxos[b], dbs[b], dx, gs[b])
+            ev["in_free"][b].record(comp_s)
+            ev["out_ready"][b].record(comp_s)
+            with torch.cuda.stream(copy_s):
+                copy_s.wait_event(ev["out_ready"][b])
+                for n, t in gs[b].items():
+                    ghs[b][n].copy_(t, non_blocking=True)
+                ev["out_free"][b].record(copy_s)
+
+        def run(steps):
+            copy_in(0)
+            for k in range(steps):
+                if k + 1 < steps:
+                    copy_in((k + 1) & 1)
+                compute_and_d2h(k & 1)
+        run(2)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
-        for _ in range(K):
-            e2e_step()
+        run(K)
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / K
         if world > 1:
@@ -367,7 +400,8 @@ def run_mine(args):
             e2e_ms = float(t.item())
         e2e = {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-               "note": "whole layer step incl. pinned-host copies of x, dx_out, metadata in and weight grads out"}
+               "note": "whole layer step incl. pinned-host copies of x, dx_out, metadata in and weight grads out; "
+                       "the next step's inputs are copied in on a second stream while the current step computes"}
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
