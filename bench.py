@@ -33,6 +33,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/layer"
+# DRAM bytes per visible pair (all heads) of the dK/dV kernel: one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum = 568.65 + 148.29 MB) of the
+# 40,960-token training batch (24,977,261 visible pairs).  The kernel's traffic
+# grows with the tile pairs it visits, so a launch moves about this many bytes
+# per visible pair; to be taken again whenever that kernel changes.
+DKDV_DRAM_BYTES_PER_PAIR = (568.65e6 + 148.29e6) / 24977261
 ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", "attn_bwd", "attn_bwd_dq")
 
 
@@ -328,7 +334,10 @@ def run_mine(args):
     if algo:
         ach = algo["flops"] / (per_launch_ms * 1e-3) / 1e12
         roof = {"kernel": dname, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"], "traffic": None,
+                "frac": ach / pk["bf16_sus"],
+                "traffic": DKDV_DRAM_BYTES_PER_PAIR * npairs if dname == "attn_bwd" else None,
+                "traffic_note": "DRAM bytes per launch, from an ncu capture of the 40,960-token batch scaled by "
+                                "visible pairs" if dname == "attn_bwd" else None,
                 "peak_note": f"{pk['src']} sustained dense bf16 (f16 operands run at the same tensor rate)"}
     attn_core_ms = sum(trace.get(k, (0, 0))[0] for k in ("attn_fwd", "attn_bwd", "attn_bwd_dq")) / K
 
