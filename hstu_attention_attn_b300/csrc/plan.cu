@@ -49,7 +49,9 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
 // write each list user by user, head by head, tile by tile.  A user's items
 // for one head are consecutive, so the persistent kernels (which deal items
 // out to CTAs in order) work on one user's tiles at the same time and its
-// streamed operands are read from HBM about once.
+// streamed operands are read from HBM about once.  One warp per user: the
+// lanes sum the user's tile costs, lane 0 takes the user's place in each
+// list, and the lanes write its items to consecutive addresses.
 __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B, int32_t H,
                                                           int32_t* __restrict__ counts,
                                                           WorkItem* __restrict__ fwd_items,
@@ -58,27 +60,30 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
                                                           int32_t* __restrict__ status) {
   __shared__ int32_t hist[3][kBuckets];  // items of each list per cost bucket, then cursors
   __shared__ int32_t tot[3];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
   for (int i = tid; i < 3 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
-  auto user_cost = [](const UserInfo& u) {
+  auto user_cost = [&](const UserInfo& u) {  // whole warp; the same value on every lane
     const int nt = ceil_div(u.n, kTile);
     int c = 0;
-    for (int t = 0; t < nt; ++t) c += qtile_keys(u, t).count();
+    for (int t = lane; t < nt; t += 32) c += qtile_keys(u, t).count();
+    c = __reduce_add_sync(0xffffffffu, c);
     return min(c, kBuckets - 1);
   };
-  for (int b = tid; b < B; b += blockDim.x) {
+  for (int b = warp; b < B; b += nw) {
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
     const int c = user_cost(u);
-    atomicAdd(&hist[0][c], ((nt + 1) / 2) * H);
-    atomicAdd(&hist[1][c], nt * H);
-    atomicAdd(&hist[2][c], nt * H);
+    if (lane == 0) {
+      atomicAdd(&hist[0][c], ((nt + 1) / 2) * H);
+      atomicAdd(&hist[1][c], nt * H);
+      atomicAdd(&hist[2][c], nt * H);
+    }
   }
   __syncthreads();
   // exclusive scan from the most expensive bucket down (one warp per list)
   if (tid < 96) {
-    const int list = tid >> 5, lane = tid & 31;
+    const int list = tid >> 5;
     int running = 0;
     for (int base = kBuckets - 1; base >= 0; base -= 32) {
       const int c = base - lane;
@@ -95,24 +100,30 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     if (lane == 0) tot[list] = running;
   }
   __syncthreads();
-  for (int b = tid; b < B; b += blockDim.x) {
+  for (int b = warp; b < B; b += nw) {
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
     const int np = (nt + 1) / 2;
     const int c = user_cost(u);
-    const int pf = atomicAdd(&hist[0][c], np * H);
-    const int pb = atomicAdd(&hist[1][c], nt * H);
-    const int pq = atomicAdd(&hist[2][c], nt * H);
-    for (int h = 0; h < H; ++h) {
-      for (int i = 0; i < np; ++i) {
-        const int64_t o = (int64_t)pf + h * np + i;
-        if (o < max_items) fwd_items[o] = WorkItem{b, (2 * i) | (h << 16)};
-      }
-      for (int t = 0; t < nt; ++t) {
-        const int64_t ob = (int64_t)pb + h * nt + t, oq = (int64_t)pq + h * nt + t;
-        if (ob < max_items) bwd_items[ob] = WorkItem{b, t | (h << 16)};
-        if (oq < max_items) dq_items[oq] = WorkItem{b, t | (h << 16)};
-      }
+    int pf = 0, pb = 0, pq = 0;
+    if (lane == 0) {
+      pf = atomicAdd(&hist[0][c], np * H);
+      pb = atomicAdd(&hist[1][c], nt * H);
+      pq = atomicAdd(&hist[2][c], nt * H);
+    }
+    pf = __shfl_sync(0xffffffffu, pf, 0);
+    pb = __shfl_sync(0xffffffffu, pb, 0);
+    pq = __shfl_sync(0xffffffffu, pq, 0);
+    for (int e = lane; e < np * H; e += 32) {  // head e / np, pair e % np
+      const int h = e / np, i = e - h * np;
+      const int64_t o = (int64_t)pf + e;
+      if (o < max_items) fwd_items[o] = WorkItem{b, (2 * i) | (h << 16)};
+    }
+    for (int e = lane; e < nt * H; e += 32) {  // head e / nt, tile e % nt
+      const int h = e / nt, t = e - h * nt;
+      const int64_t ob = (int64_t)pb + e, oq = (int64_t)pq + e;
+      if (ob < max_items) bwd_items[ob] = WorkItem{b, t | (h << 16)};
+      if (oq < max_items) dq_items[oq] = WorkItem{b, t | (h << 16)};
     }
   }
   __syncthreads();

@@ -126,3 +126,68 @@ class HstuLayer:
         mtgr.mtgr_hstu_layer_bwd(self.weights, x, mtgr.make_saved(saved), dx_out, dx, mtgr.make_grads(grads),
                                  db.offsets, db.gid, db.ts, db.T, self._workspace(db))
         return dx, grads
+
+
+class HstuStack:
+    """A stack of HSTU layers run forward for ranking (22 layers at d_model 1024
+    in paper-daily deep reading §2), eagerly or replayed from one captured CUDA
+    Graph (the pages' inference path uses CUDA Graphs, paper-daily
+    "计算量涨了 65 倍…").
+
+    All layers share two activation buffers (layer l reads one and writes the
+    other), one set of saved-state buffers (inference keeps nothing between
+    layers) and one workspace, so after the first run nothing is allocated and
+    the whole stack can be captured."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        self._key = None
+        self._graph = None
+
+    def _prepare(self, x, db):
+        key = (db.B, db.T, x.dtype, x.device)
+        if self._key == key:
+            return
+        l0 = self.layers[0]
+        self._act = [torch.empty_like(x), torch.empty_like(x)]
+        self._saved = l0.alloc_saved(db.T)
+        ws = l0._workspace(db)
+        for layer in self.layers:
+            layer._ws = ws
+        self._key, self._graph = key, None
+
+    def forward(self, x, db: DeviceBatch, outs=None):
+        """Run every layer on x; returns the last output (one of the stack's own
+        buffers).  When `outs` is a list, each layer's output is appended to it
+        as a copy."""
+        self._prepare(x, db)
+        h = x
+        for i, layer in enumerate(self.layers):
+            o = self._act[i & 1]
+            layer.forward(h, db, saved=self._saved, x_out=o)
+            if outs is not None:
+                outs.append(o.clone())
+            h = o
+        return h
+
+    def capture(self, x, db: DeviceBatch):
+        """Capture the stack's forward on x (a static buffer the caller refills
+        between replays) and db; returns the static output buffer."""
+        self._prepare(x, db)
+        side = torch.cuda.Stream(device=x.device)
+        side.wait_stream(torch.cuda.current_stream(x.device))
+        with torch.cuda.stream(side):  # warm-up outside the capture
+            self.forward(x, db)
+        torch.cuda.current_stream(x.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            y = self.forward(x, db)
+        self._graph, self._y = g, y
+        return y
+
+    def replay(self):
+        """Replay the captured forward; returns the static output buffer."""
+        if self._graph is None:
+            raise RuntimeError("HstuStack.replay before capture")
+        self._graph.replay()
+        return self._y
