@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmtgr.so")
 SOURCES = ["api.cu", "plan.cu", "norm.cu", "attn_f32.cu", "gemm_f32.cu", "gemm_sm103.cu",
-           "attn_fwd_sm103.cu", "attn_bwd_sm103.cu"]
+           "attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "batching.cpp"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
          "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -30,7 +30,7 @@ def _deps():
 
 def _compile(src, force, verbose):
     s = os.path.join(CSRC, src)
-    o = os.path.join(OBJ, src.replace(".cu", ".o"))
+    o = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
     if not force and os.path.exists(o) and os.path.getmtime(o) >= max(os.path.getmtime(s), _deps()):
         return o
     cmd = [NVCC, *FLAGS, "-c", s, "-o", o]

@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes as C
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -59,6 +60,8 @@ EXPORTS = {
     "mtgr_group_layernorm_bwd": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p,
                                                                 C.c_size_t, C.c_void_p]),
     "mtgr_group_layernorm_bwd_noalloc": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p]),
+    "mtgr_stochastic_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32] + [C.c_void_p] * 4),
+    "mtgr_token_balanced_split": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32] + [C.c_void_p] * 3),
     "mtgr_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int]),
     "mtgr_hstu_attn_fwd": (C.c_int, [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
                                                          C.c_int64, C.c_int32, C.c_int32, C.c_float]
@@ -248,3 +251,36 @@ def mtgr_hstu_layer_bwd(weights: LayerWeights, x, saved: LayerSaved, dx_out, dx,
                                      _p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x),
                                      _p(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Training batches (host arrays in, host arrays out; no device work)
+# ---------------------------------------------------------------------------
+def mtgr_stochastic_length(offsets, gid, max_seq, draws):
+    """Stochastic-length selection of one batch: returns (keep, new_offsets),
+    the kept token indices (int32, ascending) and the new offsets (int32 [B+1]).
+    offsets int32 [B+1], gid uint8 [T], draws uint64 [B] (host arrays)."""
+    offsets = np.ascontiguousarray(offsets, np.int32)
+    gid = np.ascontiguousarray(gid, np.uint8)
+    draws = np.ascontiguousarray(draws, np.uint64)
+    B, T = len(offsets) - 1, len(gid)
+    keep = np.empty(max(T, 1), np.int32)
+    new_offsets = np.empty(B + 1, np.int32)
+    new_T = C.c_int64(0)
+    _check("mtgr_stochastic_length",
+           lib().mtgr_stochastic_length(offsets.ctypes.data, B, gid.ctypes.data, T, int(max_seq), draws.ctypes.data,
+                                        keep.ctypes.data, new_offsets.ctypes.data, C.addressof(new_T)))
+    return keep[:new_T.value].copy(), new_offsets
+
+
+def mtgr_token_balanced_split(tokens, n_ranks):
+    """Token-balanced contiguous split of users over n_ranks: returns
+    (rank_first int32 [n_ranks+1], rank_tokens int64 [n_ranks], grad_weight float64 [n_ranks])."""
+    tokens = np.ascontiguousarray(tokens, np.int64)
+    first = np.empty(n_ranks + 1, np.int32)
+    rank_tokens = np.empty(n_ranks, np.int64)
+    weight = np.empty(n_ranks, np.float64)
+    _check("mtgr_token_balanced_split",
+           lib().mtgr_token_balanced_split(tokens.ctypes.data, len(tokens), int(n_ranks), first.ctypes.data,
+                                           rank_tokens.ctypes.data, weight.ctypes.data))
+    return first, rank_tokens, weight

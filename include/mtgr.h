@@ -256,6 +256,43 @@ MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void
                                 int64_t T, mtgr_dtype dtype, void* workspace, size_t workspace_bytes,
                                 mtgr_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* Training batches (host side: plain host arrays, no device work, no stream). */
+/* ------------------------------------------------------------------------- */
+
+/* Stochastic length (paper-daily "MTGR：美团外卖生成式推荐Scaling Law落地实践",
+ * "计算量涨了 65 倍…": training shortens long user sequences by sampling a piece
+ * of them; scoring keeps the whole sequence).  Reading: per user the User,
+ * RealTime and candidate tokens are kept; a Seq run longer than max_seq is cut
+ * to the max_seq consecutive Seq tokens starting at Seq position
+ * draws[u] mod (n_S - max_seq + 1), so the caller supplies the randomness
+ * (one uint64 per user).  offsets (host int32 [B+1], offsets[0] = 0,
+ * offsets[B] = T) and gid (host uint8 [T], User*, Seq*, RealTime*, Cand* per
+ * segment) describe the batch.  Writes keep (host int32, capacity T: the kept
+ * token indices, ascending), new_offsets (host int32 [B+1]) and *new_T.  The
+ * caller gathers its per-token arrays with keep.  Returns
+ * MTGR_ERR_BAD_OFFSETS / MTGR_ERR_BAD_GROUP_ORDER for bad metadata,
+ * MTGR_ERR_INVALID_ARG for bad scalars or NULL pointers; nothing is written
+ * then. */
+MTGR_API mtgr_status mtgr_stochastic_length(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T,
+                                            int32_t max_seq, const uint64_t* draws, int32_t* keep,
+                                            int32_t* new_offsets, int64_t* new_T);
+
+/* Token-balanced per-GPU batches (zzxanthony.github.io "MTGR：工业级生成式推荐框架",
+ * §11.3 "Dynamic batch size 做负载均衡": each GPU's batch size follows the
+ * sequence lengths so that every GPU computes about the same, and gradients are
+ * weighted by each GPU's batch size).  Reading: users keep their arrival order
+ * and are cut into n_ranks contiguous groups whose largest token count is the
+ * smallest possible; among such cuts, each rank in turn takes as many users as
+ * fit, leaving at least one user for every later rank when B >= n_ranks (with
+ * fewer users than ranks the last ranks are empty).  tokens: host int64 [B]
+ * (tokens of each user, >= 0).  Writes rank_first (host int32 [n_ranks+1]:
+ * rank r owns users rank_first[r] .. rank_first[r+1]-1), rank_tokens (host
+ * int64 [n_ranks]) and grad_weight (host double [n_ranks] = users of the rank /
+ * B).  MTGR_ERR_INVALID_ARG for bad scalars, negative tokens or NULL pointers. */
+MTGR_API mtgr_status mtgr_token_balanced_split(const int64_t* tokens, int32_t B, int32_t n_ranks,
+                                               int32_t* rank_first, int64_t* rank_tokens, double* grad_weight);
+
 #ifdef __cplusplus
 }
 #endif
