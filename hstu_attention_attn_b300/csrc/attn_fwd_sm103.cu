@@ -86,7 +86,7 @@ __device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
   const WorkItem wi = p.items[idx];
   c.h = wi.h();
   c.u = p.users[wi.b];
-  c.pk = pair_keys(c.u, wi.t());
+  c.pk = pair_keys(c.u, wi.t() & (kSingleItem - 1), (wi.t() & kSingleItem) != 0);
   return c;
 }
 

@@ -53,7 +53,7 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
 // lanes sum the user's tile costs, lane 0 takes the user's place in each
 // list, and the lanes write its items to consecutive addresses.
 __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __restrict__ users, int32_t B, int32_t H,
-                                                          int32_t* __restrict__ counts,
+                                                          int32_t singles, int32_t* __restrict__ counts,
                                                           WorkItem* __restrict__ fwd_items,
                                                           WorkItem* __restrict__ bwd_items,
                                                           WorkItem* __restrict__ dq_items, int64_t max_items,
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     const int nt = ceil_div(u.n, kTile);
     const int c = user_cost(u);
     if (lane == 0) {
-      atomicAdd(&hist[0][c], ((nt + 1) / 2) * H);
+      atomicAdd(&hist[0][c], (singles ? nt : (nt + 1) / 2) * H);
       atomicAdd(&hist[1][c], nt * H);
       atomicAdd(&hist[2][c], nt * H);
     }
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
   for (int b = warp; b < B; b += nw) {
     const UserInfo u = users[b];
     const int nt = ceil_div(u.n, kTile);
-    const int np = (nt + 1) / 2;
+    const int np = singles ? nt : (nt + 1) / 2;  // forward items per head
     const int c = user_cost(u);
     int pf = 0, pb = 0, pq = 0;
     if (lane == 0) {
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     for (int e = lane; e < np * H; e += 32) {  // head e / np, pair e % np
       const int h = e / np, i = e - h * np;
       const int64_t o = (int64_t)pf + e;
-      if (o < max_items) fwd_items[o] = WorkItem{b, (2 * i) | (h << 16)};
+      if (o < max_items) fwd_items[o] = WorkItem{b, (singles ? (i | kSingleItem) : 2 * i) | (h << 16)};
     }
     for (int e = lane; e < nt * H; e += 32) {  // head e / nt, tile e % nt
       const int h = e / nt, t = e - h * nt;
@@ -205,8 +205,11 @@ cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, i
   UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
   cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s);
   if (e != cudaSuccess) return e;
+  // single query tiles per forward item when even (T/128 + B) / 2 pairs per
+  // head would not fill the SMs twice (short requests): twice the items
+  const int singles = (T / kTile + B) * (int64_t)H <= 4 * (int64_t)num_sms() ? 1 : 0;
   TraceScope tr("plan_items", s);
-  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, H, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
+  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, H, singles, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.bwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items, status);
   return cudaGetLastError();

@@ -71,11 +71,14 @@ struct PairKeys {
   __host__ __device__ __forceinline__ bool in_b(int k) const { return qb >= 0 && (k < hi_b || (eb && k == qb)); }
 };
 
-__host__ __device__ __forceinline__ PairKeys pair_keys(const UserInfo& u, int qa) {
+// A forward work item names qa in the low 15 bits of its tile field; bit 15
+// marks an item of qa alone (used when pairs would leave SMs idle).
+constexpr int kSingleItem = 0x8000;
+__host__ __device__ __forceinline__ PairKeys pair_keys(const UserInfo& u, int qa, bool single = false) {
   PairKeys p;
   const int nt = ceil_div(u.n, kTile);
   p.qa = qa;
-  p.qb = qa + 1 < nt ? qa + 1 : -1;
+  p.qb = (!single && qa + 1 < nt) ? qa + 1 : -1;
   const QTileKeys a = qtile_keys(u, qa);
   p.hi_a = a.hi;
   p.ea = a.extra;

@@ -47,6 +47,20 @@ def test_attention_fwd_bf16_ragged(orc, dh, ts_hi):
     assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
+def test_attention_fwd_bf16_ragged_paired_items(orc):
+    """Enough ragged users (about 41k tokens) that the forward plans pairs of
+    query tiles per item (short requests get one tile per item instead)."""
+    need_gpu()
+    rng = np.random.default_rng(31)
+    batch = synth.make_batch(rng, ragged_users() * 24, ts_hi=3000)
+    H, dh = 2, 128
+    assert (batch.T // 128 + batch.B) * H > 4 * 148
+    _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng)
+    Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
+    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
+
+
 def test_attention_fwd_bf16_packed_layout(orc):
     need_gpu()
     rng = np.random.default_rng(21)
