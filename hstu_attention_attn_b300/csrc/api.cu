@@ -271,12 +271,14 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
                                       const void* u, bool u_f16, int64_t ldu, const int32_t* offsets, int32_t B,
                                       const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d, float eps,
                                       __nv_bfloat16* y, float* o, float* mean, float* rstd, uint8_t* ws,
-                                      const AttnWs& w, cudaStream_t s) {
+                                      const AttnWs& w, cudaStream_t s, bool plan_ready = false) {
+  // plan_ready: an earlier call on the same batch left its status word and work
+  // lists in this workspace (the layers of a stack share them)
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
-  MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
+  if (!plan_ready) MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_fwd plan");
+  if (!plan_ready) MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_fwd plan");
   MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
   const int HD = H * d;
   cudaError_t e = u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, y, mean, rstd, T, HD, eps, s)
@@ -591,10 +593,10 @@ static mtgr_status check_layer(const mtgr_layer_weights* w, const int32_t* offse
   return MTGR_OK;
 }
 
-mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void* x_out,
-                                const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
-                                const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
-                                size_t workspace_bytes, mtgr_stream_t stream) {
+static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, void* x_out,
+                                  const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
+                                  const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
+                                  size_t workspace_bytes, mtgr_stream_t stream, bool plan_ready) {
   mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
   if (st != MTGR_OK) return st;
   REQUIRE(sv != nullptr, MTGR_ERR_INVALID_ARG, "saved is NULL");
@@ -636,7 +638,7 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
     const __half* a = static_cast<const __half*>(sv->uqkv);
     r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
                            static_cast<__nv_bfloat16*>(sv->y), sv->o, sv->ln_mean, sv->ln_rstd, ws + L.attn_base,
-                           L.attn, s);
+                           L.attn, s, plan_ready);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     r = mtgr_hstu_attn_fwd(a + HD, a + 2 * HD, a + 3 * HD, a, N4, offsets, B, gid, ts, T, H, d, w->eps_ln, sv->y,
@@ -657,6 +659,36 @@ mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void
                                   static_cast<const float*>(w->w_o), D, 1, static_cast<float*>(x_out), D,
                                   static_cast<const float*>(x), D, nullptr, 0, s),
                   "layer_fwd out gemm");
+  }
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void* x, void* x_out,
+                                const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
+                                const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
+                                size_t workspace_bytes, mtgr_stream_t stream) {
+  return layer_fwd_impl(w, x, x_out, sv, offsets, B, gid, ts, T, dtype, workspace, workspace_bytes, stream, false);
+}
+
+mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x, void* x_out, void* act,
+                                const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
+                                const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
+                                size_t workspace_bytes, mtgr_stream_t stream) {
+  REQUIRE(w != nullptr && n_layers >= 1, MTGR_ERR_INVALID_ARG, "weights is NULL or n_layers < 1");
+  for (int32_t l = 1; l < n_layers; ++l)
+    REQUIRE(w[l].d_model == w[0].d_model && w[l].n_heads == w[0].n_heads && w[l].d_h == w[0].d_h,
+            MTGR_ERR_INVALID_ARG, "every layer of a stack must have the same d_model, n_heads and d_h");
+  REQUIRE(T == 0 || n_layers == 1 || (act != nullptr && act != x && act != x_out), MTGR_ERR_INVALID_ARG,
+          "act must be a separate [T, d_model] buffer when n_layers > 1");
+  REQUIRE(T == 0 || x != x_out, MTGR_ERR_INVALID_ARG, "x and x_out may not alias");
+  const void* in = x;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    void* out = ((n_layers - 1 - l) & 1) ? act : x_out;  // the last layer writes x_out
+    // one work-list build serves every layer: they share the batch and the workspace
+    const mtgr_status r = layer_fwd_impl(w + l, in, out, sv, offsets, B, gid, ts, T, dtype, workspace,
+                                         workspace_bytes, stream, l > 0);
+    if (r != MTGR_OK) return r;
+    in = out;
   }
   return MTGR_OK;
 }

@@ -156,11 +156,18 @@ class HstuStack:
             layer._ws = ws
         self._key, self._graph = key, None
 
-    def forward(self, x, db: DeviceBatch, outs=None):
+    def forward(self, x, db: DeviceBatch, outs=None, native=True):
         """Run every layer on x; returns the last output (one of the stack's own
-        buffers).  When `outs` is a list, each layer's output is appended to it
-        as a copy."""
+        buffers).  By default the whole stack is one library call
+        (mtgr_hstu_stack_fwd: the attention work lists are built once); with
+        native=False, or when `outs` is a list (each layer's output is then
+        appended to it as a copy), the layers are called one by one."""
         self._prepare(x, db)
+        if native and outs is None:
+            mtgr.mtgr_hstu_stack_fwd([l.weights for l in self.layers], x, self._act[0], self._act[1],
+                                     mtgr.make_saved(self._saved), db.offsets, db.gid, db.ts, db.T,
+                                     self.layers[0]._ws)
+            return self._act[0]
         h = x
         for i, layer in enumerate(self.layers):
             o = self._act[i & 1]

@@ -74,6 +74,9 @@ EXPORTS = {
     "mtgr_hstu_layer_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.c_void_p, C.POINTER(LayerSaved),
                                       C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int,
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
+    "mtgr_hstu_stack_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.POINTER(LayerSaved), C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_int64, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
     "mtgr_hstu_layer_bwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.POINTER(LayerSaved), C.c_void_p,
                                       C.c_void_p, C.POINTER(LayerGrads), C.c_void_p, C.c_int32, C.c_void_p,
                                       C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -240,6 +243,15 @@ def mtgr_hstu_layer_fwd(weights: LayerWeights, x, x_out, saved: LayerSaved, offs
                         stream=None):
     _check("mtgr_hstu_layer_fwd",
            lib().mtgr_hstu_layer_fwd(C.byref(weights), _p(x), _p(x_out), C.byref(saved), _p(offsets),
+                                     offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_hstu_stack_fwd(weights, x, x_out, act, saved: LayerSaved, offsets, gid, ts, T, workspace, stream=None):
+    """weights: a sequence of LayerWeights (one per layer)."""
+    arr = (LayerWeights * len(weights))(*weights)
+    _check("mtgr_hstu_stack_fwd",
+           lib().mtgr_hstu_stack_fwd(arr, len(weights), _p(x), _p(x_out), _p(act), C.byref(saved), _p(offsets),
                                      offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
 

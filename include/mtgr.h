@@ -249,6 +249,21 @@ MTGR_API mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void
                                 const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
                                 void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
 
+/* A stack of n_layers layers run forward for ranking (paper-daily deep reading
+ * §2: 22 layers at d_model 1024), in one call: layer l reads layer l-1's
+ * output; the last layer writes x_out.  w: host array of n_layers weight sets,
+ * all with the same d_model, n_heads, d_h.  act: [T, D] scratch (dtype,
+ * distinct from x and x_out) when n_layers > 1.  saved: one set of buffers
+ * that every layer overwrites (inference keeps nothing between layers).  The
+ * attention work lists are built once for all layers (they depend only on the
+ * batch).  Workspace: mtgr_layer_workspace_size of one layer.  The call
+ * allocates nothing and never synchronises, so it can be captured in a CUDA
+ * Graph. */
+MTGR_API mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x, void* x_out,
+                                void* act, const mtgr_layer_saved* saved, const int32_t* offsets, int32_t B,
+                                const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
+                                void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
+
 /* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path. */
 MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* saved,
                                 const void* dx_out, void* dx, const mtgr_layer_grads* grads,

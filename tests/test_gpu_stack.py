@@ -35,7 +35,9 @@ def test_stack_graph_replay_equals_eager(orc):
     db = device_batch(base.batch)
     x = dev(base.x, BF)
     outs = []
-    y_eager = stack.forward(x, db, outs=outs).clone()
+    y_eager = stack.forward(x, db, outs=outs).clone()          # layer by layer
+    y_native = HstuStack(stack.layers).forward(x, db).clone()  # one library call, one work-list build
+    assert torch.equal(y_native, y_eager)
     stack.capture(x, db)
     torch.cuda.synchronize()
     assert torch.equal(stack.replay().clone(), y_eager)
