@@ -22,19 +22,6 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
 }
 
-// Cheap descriptor stepping for the MMA issue loops: the start-address field
-// holds addr >> 4 in the low 14 bits, and every tile here lies inside the
-// CTA's shared memory (< 256 KB), so moving the start by a multiple of 16
-// bytes is a plain 64-bit add of (bytes >> 4) with no carry out of the field.
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
-// Byte offset of k-step kk in a K-major tile made of TMA boxes of `box` bytes
-// (64 columns of 16-bit values per box, 32 bytes per k-step of 16 columns).
-__host__ __device__ constexpr uint32_t kmajor_off(int kk, uint32_t box) {
-  return (uint32_t)(kk >> 2) * box + (uint32_t)(kk & 3) * 32u;
-}
-// Byte offset of k-step kk (16 rows of 128 bytes) in an MN-major tile.
-__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return (uint32_t)kk * 2048u; }
-
 // TMEM column (relative to the 128-column region of a score tile) of the
 // packed f16 operand for reduction step kk (rows/keys 16kk .. 16kk+15), when
 // the epilogue writes the 8 packed words of every 16-column chunk into the

@@ -152,9 +152,6 @@ __device__ __forceinline__ void tma_store_wait_read_n() {
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ void tma_store_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -211,16 +208,6 @@ __device__ __forceinline__ void tc_mma_ss_h(uint32_t d_tmem, uint32_t a_lo, uint
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_mma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
-      "mov.b64 bd, {%2, %3};\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on the mbarrier when every tcgen05 op issued so far by this thread completes.
@@ -406,18 +393,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// SiLU and its derivative in fp32 (accurate exponential; used by the fp32 path
-// and by elementwise kernels).
+// SiLU in fp32 (accurate exponential).
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
 // ----------------------------------------------------------------------------
-// Coalesced row-block I/O of an epilogue warp.  The warp holds 32 consecutive
-// rows (lane = row) x 32 consecutive columns in fp32 registers.  Going through
-// a small per-warp shared-memory buffer (16-byte slots XOR-swizzled by row, so
-// both passes are bank-conflict free) turns 32 row-strided accesses per
-// instruction into a few contiguous row segments.  Rows >= nrows and columns
-// >= ncols (a multiple of 8) are not touched.
+// Row-block I/O of an epilogue warp.  The warp holds 32 consecutive rows
+// (lane = row) x 32 consecutive columns; a [32][32] 16-bit block is staged in
+// 2 KB of shared memory as rows of 64 bytes whose 16-byte pieces are
+// XOR-swizzled by (row >> 1) & 3 (bank-conflict free for the row-per-lane and
+// the coalesced passes, and the 64-byte swizzle of a TMA box).
 // ----------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ uint4 pack8(const float* x) {
@@ -427,38 +411,6 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
   w.z = pack2<T>(x[4], x[5]);
   w.w = pack2<T>(x[6], x[7]);
   return w;
-}
-// 16-bit T: 64 bytes per row, staging 2 KB.
-template <typename T>
-__device__ __forceinline__ void store_rows16_32(const float (&x)[32], uint8_t* stg, T* out, int64_t ld, int nrows,
-                                                int ncols, int lane) {
-  __syncwarp();
-#pragma unroll
-  for (int v = 0; v < 4; ++v)
-    *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = pack8<T>(x + 8 * v);
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
-    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16));
-    if (r < nrows && c4 * 8 < ncols) *reinterpret_cast<uint4*>(out + (int64_t)r * ld + c4 * 8) = w;
-  }
-}
-// fp32: 128 bytes per row, staging 4 KB.
-__device__ __forceinline__ void store_rows32_32(const float (&x)[32], uint8_t* stg, float* out, int64_t ld, int nrows,
-                                                int ncols, int lane) {
-  __syncwarp();
-#pragma unroll
-  for (int v = 0; v < 8; ++v)
-    *reinterpret_cast<float4*>(stg + lane * 128 + ((v ^ (lane & 7)) * 16)) =
-        make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int r = it * 4 + (lane >> 3), c8 = lane & 7;
-    const float4 w = *reinterpret_cast<const float4*>(stg + r * 128 + ((c8 ^ (r & 7)) * 16));
-    if (r < nrows && c8 * 4 < ncols) *reinterpret_cast<float4*>(out + (int64_t)r * ld + c8 * 4) = w;
-  }
 }
 // Asynchronous global -> shared copies (cp.async, 16 bytes, cached in L2
 // only) and their commit groups; a bulk L2 prefetch.
@@ -475,10 +427,10 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// The two halves of load_rows16_32 for a copy issued ahead of use: start the
-// copy of rows < nrows, columns < ncols of a [32][32] 16-bit block into a 2 KB
-// staging slot (same swizzle as below); after the copy's group has completed
-// and a __syncwarp, read row `lane` back as floats.
+// A block load issued ahead of use: start the copy (cp.async) of rows < nrows,
+// columns < ncols (a multiple of 8) of a [32][32] 16-bit block into a 2 KB
+// staging slot; after the copy's group has completed and a __syncwarp, read
+// row `lane` back as floats.
 __device__ __forceinline__ void fetch_rows16_32(uint8_t* slot, const void* in, int64_t ld, int nrows, int ncols,
                                                 int lane) {
   const uint32_t s = smem_u32(slot);
@@ -494,32 +446,6 @@ __device__ __forceinline__ void read_rows16_32(const uint8_t* slot, float (&x)[3
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint4 w = *reinterpret_cast<const uint4*>(slot + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      x[8 * v + 2 * t] = lo16<T>(ww[t]);
-      x[8 * v + 2 * t + 1] = hi16<T>(ww[t]);
-    }
-  }
-}
-
-// Load 32 rows x 32 16-bit values of `in` (row stride ld) into x (lane = row);
-// out-of-range rows / columns read as 0.
-template <typename T>
-__device__ __forceinline__ void load_rows16_32(const T* in, int64_t ld, int nrows, int ncols, uint8_t* stg,
-                                               float (&x)[32], int lane) {
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (r < nrows && c4 * 8 < ncols) w = *reinterpret_cast<const uint4*>(in + (int64_t)r * ld + c4 * 8);
-    *reinterpret_cast<uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16)) = w;
-  }
-  __syncwarp();
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 w = *reinterpret_cast<const uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
