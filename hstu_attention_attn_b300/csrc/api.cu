@@ -18,6 +18,7 @@ cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, U
 cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
                                   int64_t*, cudaStream_t);
+cudaError_t launch_expand_rows(const void*, const int32_t*, int64_t, void*, int64_t, int64_t, cudaStream_t);
 template <typename T>
 cudaError_t launch_gln_fwd(const T*, T*, float*, float*, const uint8_t*, const float*, const float*, int64_t, int,
                            float, cudaStream_t);
@@ -386,6 +387,21 @@ mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const u
   MTGR_CUDA_TRY(launch_visible_counts(offsets, B, gid, ts, T, cnt, total_pairs,
                                       reinterpret_cast<cudaStream_t>(stream)),
                 "visible_counts");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_expand_rows(const void* src, const int32_t* rows, int64_t n, void* dst, int64_t T, int32_t D,
+                             mtgr_dtype dtype, mtgr_stream_t stream) {
+  REQUIRE(n >= 0 && T >= 0 && D > 0, MTGR_ERR_INVALID_ARG, "n, T must be >= 0 and D > 0");
+  REQUIRE(dtype == MTGR_BF16 || dtype == MTGR_F32, MTGR_ERR_UNSUPPORTED, "dtype");
+  const int64_t row_bytes = (int64_t)D * (dtype == MTGR_BF16 ? 2 : 4);
+  REQUIRE(row_bytes % 16 == 0, MTGR_ERR_INVALID_ARG, "a row must be a multiple of 16 bytes (D %% 8 == 0 for bf16)");
+  REQUIRE(T == 0 || dst != nullptr, MTGR_ERR_INVALID_ARG, "dst is NULL");
+  REQUIRE(n == 0 || (src != nullptr && rows != nullptr), MTGR_ERR_INVALID_ARG, "src / rows is NULL");
+  REQUIRE(aligned16(src) && aligned16(dst), MTGR_ERR_INVALID_ARG, "src and dst must be 16-byte aligned");
+  if (T == 0) return MTGR_OK;
+  MTGR_CUDA_TRY(launch_expand_rows(src, rows, n, dst, T, row_bytes, reinterpret_cast<cudaStream_t>(stream)),
+                "expand_rows");
   return MTGR_OK;
 }
 

@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmtgr.so")
 
 MTGR_F32, MTGR_BF16 = 0, 1
+MTGR_OK, MTGR_ERR_INVALID_ARG, MTGR_ERR_UNSUPPORTED = 0, -1, -4
 STATUS_BAD_OFFSETS, STATUS_BAD_GROUP_ORDER, STATUS_BAD_GROUP_ID, STATUS_TIMEOUT = 1, 2, 4, 8
 
 _lib = None
@@ -60,6 +61,8 @@ EXPORTS = {
     "mtgr_group_layernorm_bwd": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p,
                                                                 C.c_size_t, C.c_void_p]),
     "mtgr_group_layernorm_bwd_noalloc": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p]),
+    "mtgr_expand_rows": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int32, C.c_int,
+                                   C.c_void_p]),
     "mtgr_stochastic_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32] + [C.c_void_p] * 4),
     "mtgr_token_balanced_split": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32] + [C.c_void_p] * 3),
     "mtgr_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int]),
@@ -296,3 +299,10 @@ def mtgr_token_balanced_split(tokens, n_ranks):
            lib().mtgr_token_balanced_split(tokens.ctypes.data, len(tokens), int(n_ranks), first.ctypes.data,
                                            rank_tokens.ctypes.data, weight.ctypes.data))
     return first, rank_tokens, weight
+
+
+def mtgr_expand_rows(src, rows, dst, stream=None):
+    """dst [T, D] <- zeros, then dst[rows[k]] = src[k] (device tensors; rows int32)."""
+    _check("mtgr_expand_rows",
+           lib().mtgr_expand_rows(_p(src), _p(rows), rows.numel(), _p(dst), dst.shape[0], dst.shape[1], _dtype(dst),
+                                  _stream(stream)))

@@ -271,6 +271,16 @@ MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void
                                 int64_t T, mtgr_dtype dtype, void* workspace, size_t workspace_bytes,
                                 mtgr_stream_t stream);
 
+/* Dense upstream gradient from its nonzero rows.  A loss on the candidate tokens
+ * only (fun-rec §7.3.1: every candidate is scored from its own position) makes
+ * dx' zero on every other row, so a training step need only move the
+ * candidates' rows to the GPU.  dst [T, D] (dtype, device) is zeroed, then
+ * dst[rows[k], :] = src[k, :] for k < n; src [n, D] (dtype, device), rows
+ * (device int32 [n], distinct); a row outside [0, T) is skipped.  D * element
+ * size must be a multiple of 16 bytes; src and dst 16-byte aligned. */
+MTGR_API mtgr_status mtgr_expand_rows(const void* src, const int32_t* rows, int64_t n, void* dst, int64_t T,
+                                      int32_t D, mtgr_dtype dtype, mtgr_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Training batches (host side: plain host arrays, no device work, no stream). */
 /* ------------------------------------------------------------------------- */

@@ -67,3 +67,14 @@ def test_bad_scalars_rejected_on_host(lib):
     # negative sizes
     r = L.mtgr_validate_batch(16, -1, 16, 10, 16, None)
     assert r == -1
+
+
+def test_expand_rows_rejects_bad_arguments_on_the_host(lib):
+    import ctypes as C
+    from hstu_attention_attn_b300 import mtgr
+    buf = (C.c_uint8 * 4096)()
+    p = C.addressof(buf) + (-C.addressof(buf)) % 16          # a 16-byte aligned host address, never read
+    # D = 7 bf16 values is not a multiple of 16 bytes
+    assert lib.mtgr_expand_rows(p, p, 1, p, 4, 7, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
+    assert lib.mtgr_expand_rows(None, None, 1, p, 4, 8, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
+    assert lib.mtgr_expand_rows(p, p, -1, p, 4, 8, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
