@@ -26,11 +26,11 @@ template <typename T>
 cudaError_t launch_gln_bwd(const T*, const T*, const float*, const float*, const uint8_t*, const float*, const T*,
                            T*, float*, float*, float*, int64_t, int, cudaStream_t);
 int gln_bwd_blocks(int64_t rows);
-template <typename TU, typename TY>
-cudaError_t launch_ln_gate_fwd(const float*, const TU*, int64_t, TY*, float*, float*, int64_t, int, float,
+template <typename TOi, typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd(const TOi*, const TU*, int64_t, TY*, float*, float*, int64_t, int, float,
                                cudaStream_t);
-template <typename TG, typename TU, typename TO>
-cudaError_t launch_ln_gate_bwd(const TG*, const float*, const TU*, int64_t, const float*, const float*, TO*, TG*,
+template <typename TG, typename TOi, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TG*, const TOi*, const TU*, int64_t, const float*, const float*, TO*, TG*,
                                int64_t, const TG*, int64_t, int, cudaStream_t);
 cudaError_t launch_bf16_to_f16(const __nv_bfloat16*, int64_t, __half*, int64_t, int64_t, int, cudaStream_t);
 cudaError_t launch_attn_f32_fwd(const float*, const float*, const float*, int64_t, const UserInfo*, int,
@@ -39,7 +39,7 @@ cudaError_t launch_attn_f32_bwd(const float*, const float*, const float*, int64_
                                 int, const int64_t*, int64_t, int, int, float*, float*, float*, int64_t,
                                 const float*, const float*, const float*, cudaStream_t);
 cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int64_t, int64_t, int, int,
-                                const int32_t*, int32_t, const int64_t*, float*, int32_t*, cudaStream_t);
+                                const int32_t*, int32_t, const int64_t*, __half*, int32_t*, cudaStream_t);
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
                                 __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
@@ -271,7 +271,7 @@ static mtgr_status check_meta(const int32_t* offsets, int32_t B, const uint8_t* 
 static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, const __half* v16, int64_t ld16,
                                       const void* u, bool u_f16, int64_t ldu, const int32_t* offsets, int32_t B,
                                       const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d, float eps,
-                                      __nv_bfloat16* y, float* o, float* mean, float* rstd, uint8_t* ws,
+                                      __nv_bfloat16* y, __half* o, float* mean, float* rstd, uint8_t* ws,
                                       const AttnWs& w, cudaStream_t s, bool plan_ready = false) {
   // plan_ready: an earlier call on the same batch left its status word and work
   // lists in this workspace (the layers of a stack share them)
@@ -291,7 +291,7 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
 
 static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16, const __half* k16,
                                       const __half* v16, int64_t ld16, const void* u, bool u_f16, int64_t ldu,
-                                      const float* o, const float* mean, const float* rstd, const int32_t* offsets,
+                                      const __half* o, const float* mean, const float* rstd, const int32_t* offsets,
                                       int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
                                       __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, __nv_bfloat16* du,
                                       int64_t ldg, const __nv_bfloat16* dsilu, uint8_t* ws, const AttnWs& w,
@@ -506,7 +506,7 @@ mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, cons
     MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(k), ld_in, k16, HD, T, (int)HD, s), "attn_fwd f16 k");
     MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(v), ld_in, v16, HD, T, (int)HD, s), "attn_fwd f16 v");
     return attn_fwd_bf16_core(q16, k16, v16, HD, u, false, ld_in, offsets, B, gid, ts, T, n_heads, d_h, eps,
-                              static_cast<bf*>(y), static_cast<float*>(o_saved), ln_mean, ln_rstd, ws, w, s);
+                              static_cast<bf*>(y), static_cast<__half*>(o_saved), ln_mean, ln_rstd, ws, w, s);
   }
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
@@ -555,7 +555,7 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
     MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(k), ld_in, k16, HD, T, (int)HD, s), "attn_bwd f16 k");
     MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(v), ld_in, v16, HD, T, (int)HD, s), "attn_bwd f16 v");
     return attn_bwd_bf16_core(static_cast<const bf*>(dy), q16, k16, v16, HD, u, false, ld_in,
-                              static_cast<const float*>(o_saved), ln_mean, ln_rstd, offsets, B, gid, ts, T, n_heads,
+                              static_cast<const __half*>(o_saved), ln_mean, ln_rstd, offsets, B, gid, ts, T, n_heads,
                               d_h, static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv),
                               static_cast<bf*>(du), ld_grad, static_cast<const bf*>(dsilu_uqkv), ws, w, s);
   }
@@ -653,7 +653,8 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
   if (dtype == MTGR_BF16) {
     const __half* a = static_cast<const __half*>(sv->uqkv);
     r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
-                           static_cast<__nv_bfloat16*>(sv->y), sv->o, sv->ln_mean, sv->ln_rstd, ws + L.attn_base,
+                           static_cast<__nv_bfloat16*>(sv->y), static_cast<__half*>(sv->o), sv->ln_mean, sv->ln_rstd,
+                           ws + L.attn_base,
                            L.attn, s, plan_ready);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
@@ -774,7 +775,8 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   if (dtype == MTGR_BF16) {
     const __half* a = static_cast<const __half*>(sv->uqkv);
     bf* dz = static_cast<bf*>(dZ);
-    r = attn_bwd_bf16_core(static_cast<const bf*>(dY), a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, sv->o,
+    r = attn_bwd_bf16_core(static_cast<const bf*>(dY), a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4,
+                           static_cast<const __half*>(sv->o),
                            sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
                            dz, N4, static_cast<const bf*>(sv->dsilu), ws + L.attn_base, L.attn, s);
   } else {

@@ -42,7 +42,7 @@ constexpr int BQ = 128, BKV = 128;
 constexpr int NUM_THREADS = 576;  // 18 warps
 constexpr int EPI_WARPS = 8;      // per slot
 constexpr int RING = 4;
-constexpr int STG_FLOATS = 32 * 16;  // per-warp O staging: 32 rows x 16 fp32
+constexpr int STG_FLOATS = 32 * 16;  // per-warp O staging, 2 KB: one [32][32] f16 box
 
 template <int D>
 struct FwdCfg {
@@ -69,7 +69,7 @@ struct FwdParams {
   const WorkItem* items;  // (user, first query tile of the pair), longest first
   const int32_t* counts;
   const int64_t* ts;
-  float* O;  // [T, H*D] fp32
+  __half* O;  // [T, H*D] f16
   int64_t ldo;
   int H;
   float scale;  // 1/sqrt(d_h)
@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
       tc_fence_after();
       const float inv_n = 1.0f / (float)u.n;
       const int row0 = qt * BQ + quarter * 32;  // segment-relative first row of this warp
-      float* obase = p.O + (int64_t)(u.start + row0) * p.ldo + c.h * D + g * (D / 2);
+      __half* obase = p.O + (int64_t)(u.start + row0) * p.ldo + c.h * D + g * (D / 2);
+      uint8_t* box_buf = reinterpret_cast<uint8_t*>(stg);
       // A box of 32 rows inside the segment leaves by TMA store; the warp that
       // holds the segment's end stores its valid rows one by one (a box would
       // also write the next user's rows).
@@ -404,40 +405,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
         uint32_t rr[32];
         tmem_ld32(tmem + Cfg::o_col(sl) + g * (D / 2) + cc * 32 + lane_sel, rr);
         tmem_wait_ld();
+        // row r_in's 32 values as f16 -> box_buf[lane][64 bytes], 16-byte pieces
+        // XOR-swizzled by row (the 64-byte swizzle of a [32][32] f16 TMA box);
+        // the previous box store must have finished reading the buffer
+        if (lane == 0) tma_store_wait_read_n<0>();
+        __syncwarp();
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          // row r_in's 16 values -> stg[lane][16], 16-byte slots XOR-swizzled by
-          // row (the 64-byte swizzle of a [32][16] fp32 TMA box); the previous
-          // box store must have finished reading the buffer
-          if (lane == 0) tma_store_wait_read_n<0>();
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_f16x2(__uint_as_float(rr[8 * v + 0]) * inv_n, __uint_as_float(rr[8 * v + 1]) * inv_n);
+          w.y = pack_f16x2(__uint_as_float(rr[8 * v + 2]) * inv_n, __uint_as_float(rr[8 * v + 3]) * inv_n);
+          w.z = pack_f16x2(__uint_as_float(rr[8 * v + 4]) * inv_n, __uint_as_float(rr[8 * v + 5]) * inv_n);
+          w.w = pack_f16x2(__uint_as_float(rr[8 * v + 6]) * inv_n, __uint_as_float(rr[8 * v + 7]) * inv_n);
+          *reinterpret_cast<uint4*>(box_buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
+        }
+        if (box) {
+          fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, box_buf, c.h * D + g * (D / 2) + cc * 32, u.start + row0);
+            tma_store_commit();
+          }
+          continue;
+        }
+        __syncwarp();
+        // 8 rows x 64 bytes per store instruction
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int slot = v ^ ((lane >> 1) & 3);
-            *reinterpret_cast<float4*>(stg + lane * 16 + slot * 4) =
-                make_float4(__uint_as_float(rr[sub * 16 + 4 * v + 0]) * inv_n,
-                            __uint_as_float(rr[sub * 16 + 4 * v + 1]) * inv_n,
-                            __uint_as_float(rr[sub * 16 + 4 * v + 2]) * inv_n,
-                            __uint_as_float(rr[sub * 16 + 4 * v + 3]) * inv_n);
-          }
-          if (box) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmO, stg, c.h * D + g * (D / 2) + cc * 32 + sub * 16, u.start + row0);
-              tma_store_commit();
-            }
-            continue;
-          }
-          __syncwarp();
-          // 8 rows x 64 bytes per store instruction
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int rw = it * 8 + (lane >> 2), c4 = lane & 3;
-            const float4 val = *reinterpret_cast<const float4*>(stg + rw * 16 + (c4 ^ ((rw >> 1) & 3)) * 4);
-            if (row0 + rw < u.n)
-              *reinterpret_cast<float4*>(obase + (int64_t)rw * p.ldo + cc * 32 + sub * 16 + c4 * 4) = val;
-          }
+        for (int it = 0; it < 4; ++it) {
+          const int rw = it * 8 + (lane >> 2), c4 = lane & 3;
+          const uint4 val = *reinterpret_cast<const uint4*>(box_buf + rw * 64 + ((c4 ^ ((rw >> 1) & 3)) * 16));
+          if (row0 + rw < u.n) *reinterpret_cast<uint4*>(obase + (int64_t)rw * p.ldo + cc * 32 + c4 * 8) = val;
         }
       }
       tc_fence_before();
@@ -462,16 +459,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
 
 }  // namespace
 
-// q, k, v: [T, *] f16 with row stride ld; O: [T, H*d] fp32.
+// q, k, v: [T, *] f16 with row stride ld; O: [T, H*d] f16 (scaled by 1/n_u).
 cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, int64_t T, int H,
-                                int d, const int32_t* plan, int32_t B, const int64_t* ts, float* O, int32_t* status,
+                                int d, const int32_t* plan, int32_t B, const int64_t* ts, __half* O, int32_t* status,
                                 cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BKV) ||
-      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV) || !make_tmap_out(&to, OUT_F32, O, T, HD, HD, 0, 16, 32))
+      !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV) || !make_tmap_out(&to, OUT_F16, O, T, HD, HD, 0, 32, 32))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.users = reinterpret_cast<const UserInfo*>(plan + L.users);

@@ -7,7 +7,7 @@
 //      γ_g/β_g selected by the token's group id.
 //  * Gate (paper-daily "模型怎么搭": normalise the aggregate, multiply by U):
 //      Y = LayerNorm(O) ⊙ U over the H·d_h features of a token, no affine
-//      (O is kept in fp32 in both precision paths).
+//      (O is fp32 in the fp32 path and f16 in the bf16 path; statistics fp32).
 #include <mutex>
 
 #include "common.cuh"
@@ -255,8 +255,8 @@ __global__ void gln_param_reduce_kernel(const float* __restrict__ partial, int n
 // ---------------------------------------------------------------------------
 // Gate: Y = LayerNorm(O) ⊙ U
 // ---------------------------------------------------------------------------
-template <typename TU, typename TY, int NCH>
-__global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const float* __restrict__ O, const TU* __restrict__ U,
+template <typename TOi, typename TU, typename TY, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const TOi* __restrict__ O, const TU* __restrict__ U,
                                                           int64_t ldu, TY* __restrict__ Y,
                                                           float* __restrict__ mean, float* __restrict__ rstd,
                                                           int64_t rows, int n, float eps) {
@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const float* __restric
 }
 
 // dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ dsilu when given: silu'(z_u)).
-template <typename TG, typename TU, typename TO, int NCH>
-__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__ dY, const float* __restrict__ O,
+template <typename TG, typename TOi, typename TU, typename TO, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__ dY, const TOi* __restrict__ O,
                                                           const TU* __restrict__ U, int64_t ldu,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ rstd, TO* __restrict__ dO,
@@ -406,23 +406,23 @@ cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const flo
   return cudaGetLastError();
 }
 
-template <typename TU, typename TY>
-cudaError_t launch_ln_gate_fwd(const float* O, const TU* U, int64_t ldu, TY* Y, float* mean, float* rstd,
+template <typename TOi, typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd(const TOi* O, const TU* U, int64_t ldu, TY* Y, float* mean, float* rstd,
                                int64_t rows, int n, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gate_fwd", s);
-  NCH_DISPATCH(n, (ln_gate_fwd_kernel<TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd,
+  NCH_DISPATCH(n, (ln_gate_fwd_kernel<TOi, TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd,
                                                                                      rows, n, eps)));
   return cudaGetLastError();
 }
 
-template <typename TG, typename TU, typename TO>
-cudaError_t launch_ln_gate_bwd(const TG* dY, const float* O, const TU* U, int64_t ldu, const float* mean,
+template <typename TG, typename TOi, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TG* dY, const TOi* O, const TU* U, int64_t ldu, const float* mean,
                                const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* dsilu, int64_t rows, int n,
                                cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gate_bwd", s);
-  NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
+  NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TOi, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
                       dY, O, U, ldu, mean, rstd, dO, dU, ldg, dsilu, rows, n)));
   return cudaGetLastError();
 }
@@ -460,21 +460,25 @@ INSTANTIATE(float)
 INSTANTIATE(__nv_bfloat16)
 
 using bf16_t = __nv_bfloat16;
-template cudaError_t launch_ln_gate_fwd<float, float>(const float*, const float*, int64_t, float*, float*, float*,
-                                                      int64_t, int, float, cudaStream_t);
-template cudaError_t launch_ln_gate_fwd<bf16_t, bf16_t>(const float*, const bf16_t*, int64_t, bf16_t*, float*,
-                                                        float*, int64_t, int, float, cudaStream_t);
-template cudaError_t launch_ln_gate_fwd<__half, bf16_t>(const float*, const __half*, int64_t, bf16_t*, float*,
-                                                        float*, int64_t, int, float, cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<float, float, float>(const float*, const float*, const float*, int64_t,
-                                                             const float*, const float*, float*, float*, int64_t,
-                                                             const float*, int64_t, int, cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<bf16_t, bf16_t, __half>(const bf16_t*, const float*, const bf16_t*, int64_t,
-                                                                const float*, const float*, __half*, bf16_t*,
-                                                                int64_t, const bf16_t*, int64_t, int, cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half>(const bf16_t*, const float*, const __half*, int64_t,
-                                                                const float*, const float*, __half*, bf16_t*,
-                                                                int64_t, const bf16_t*, int64_t, int, cudaStream_t);
+// O is fp32 in the fp32 path and f16 in the bf16 path
+template cudaError_t launch_ln_gate_fwd<float, float, float>(const float*, const float*, int64_t, float*, float*,
+                                                             float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd<__half, bf16_t, bf16_t>(const __half*, const bf16_t*, int64_t, bf16_t*,
+                                                                float*, float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd<__half, __half, bf16_t>(const __half*, const __half*, int64_t, bf16_t*,
+                                                                float*, float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<float, float, float, float>(const float*, const float*, const float*,
+                                                                    int64_t, const float*, const float*, float*,
+                                                                    float*, int64_t, const float*, int64_t, int,
+                                                                    cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<bf16_t, __half, bf16_t, __half>(const bf16_t*, const __half*, const bf16_t*,
+                                                                        int64_t, const float*, const float*, __half*,
+                                                                        bf16_t*, int64_t, const bf16_t*, int64_t,
+                                                                        int, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half, __half>(const bf16_t*, const __half*, const __half*,
+                                                                        int64_t, const float*, const float*, __half*,
+                                                                        bf16_t*, int64_t, const bf16_t*, int64_t,
+                                                                        int, cudaStream_t);
 
 }  // namespace mtgr
 

@@ -59,7 +59,9 @@ class HstuAttention:
         T, HD = db.T, self.H * self.dh
         ld = ld if ld is not None else q.stride(0)
         y = torch.empty(T, HD, dtype=self.dtype, device=self.device)
-        o = torch.empty(T, HD, dtype=torch.float32, device=self.device)
+        # O before the gate: f16 in the bf16 path, fp32 in the fp32 path
+        o = torch.empty(T, HD, dtype=torch.float16 if self.dtype == torch.bfloat16 else torch.float32,
+                        device=self.device)
         mean = torch.empty(T, dtype=torch.float32, device=self.device)
         rstd = torch.empty(T, dtype=torch.float32, device=self.device)
         mtgr.mtgr_hstu_attn_fwd(q, k, v, u, ld, db.offsets, db.gid, db.ts, T, self.H, self.dh, self.eps, y, o,
@@ -107,7 +109,7 @@ class HstuLayer:
         f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
         u16 = torch.float16 if self.dtype == torch.bfloat16 else self.dtype   # attention operands
         return dict(xn=e(T, self.D), dsilu=e(T, 4 * HD), uqkv=torch.empty(T, 4 * HD, dtype=u16, device=self.device),
-                    o=f(T, HD), y=e(T, HD),
+                    o=torch.empty(T, HD, dtype=u16, device=self.device), y=e(T, HD),
                     gln_mean=f(T), gln_rstd=f(T), ln_mean=f(T), ln_rstd=f(T))
 
     def forward(self, x, db: DeviceBatch, saved=None, x_out=None):

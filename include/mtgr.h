@@ -175,9 +175,10 @@ MTGR_API size_t mtgr_attn_workspace_size(int32_t B, int64_t T, int32_t n_heads, 
  * [T, 4*H*d_h] buffer).  In the MTGR_BF16 path the tensor-core operands are
  * f16: q, k, v are first copied to f16 (exact for values in the f16 normal
  * range, |x| in [6.1e-5, 65504]) and P, dO, dS are rounded to f16 (11
- * significand bits) instead of bf16 (8).  y: [T, H*d_h] dense (dtype).  o_saved: fp32
- * [T, H*d_h], O before the gate, kept in fp32 in both paths (needed by the
- * backward).  ln_mean, ln_rstd: fp32 [T].
+ * significand bits) instead of bf16 (8).  y: [T, H*d_h] dense (dtype).  o_saved:
+ * [T, H*d_h], O before the gate (needed by the backward): f16 in the MTGR_BF16
+ * path (11 significand bits; O is an average of V rows, far inside the f16
+ * range), fp32 in the MTGR_F32 path.  ln_mean, ln_rstd: fp32 [T].
  * Supported: MTGR_BF16 with d_h in {64, 128} (tcgen05 tensor-core path) and
  * MTGR_F32 with d_h <= 128, d_h % 4 == 0 (fp32 CUDA-core path). */
 MTGR_API mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void* v, const void* u, int64_t ld_in,
@@ -225,7 +226,8 @@ typedef struct {        /* written by the forward, read by the backward (dtype u
                            use the backward makes of z */
   void* uqkv;           /* [T, 4*H*d_h] silu(z); f16 in the MTGR_BF16 path (the attention's
                            tensor-core operands, 11 significand bits), fp32 in MTGR_F32 */
-  float* o;             /* [T, H*d_h] attention output before the gate (fp32) */
+  void* o;              /* [T, H*d_h] attention output before the gate: f16 in the MTGR_BF16
+                           path, fp32 in MTGR_F32 */
   void* y;              /* [T, H*d_h] gate output */
   float* gln_mean;      /* [T] */
   float* gln_rstd;      /* [T] */
