@@ -174,7 +174,7 @@ bool make_tmap_out(CUtensorMap* m, OutType t, const void* base, uint64_t rows, u
 // Workspace carving
 // ---------------------------------------------------------------------------
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-static size_t esize(mtgr_dtype dt) { return dt == MTGR_BF16 ? 2 : 4; }
+static size_t esize(mtgr_dtype dt) { return dt == MTGR_F32 ? 4 : 2; }
 
 // Attention workspace: status word, jagged tile plan, dO; in the bf16 path the
 // tensor-core operands are f16: q, k, v are converted once (exactly) into f16
@@ -191,7 +191,7 @@ static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt,
   w.plan = o;
   o += align256(sizeof(int32_t) * (size_t)plan_layout(B, T, H).total);
   w.dO = o;
-  o += align256(THD * (dt == MTGR_BF16 ? 2 : 4));
+  o += align256(THD * esize(dt));
   w.qkv16 = o;
   if (dt == MTGR_BF16 && convert_qkv) o += 3 * align256(THD * 2);
   w.total = o;
@@ -237,7 +237,7 @@ static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, m
   o += align256((size_t)T * D * esize(dt));
   w.gln_part = o;
   o += align256((size_t)gln_bwd_blocks(T) * 8 * D * sizeof(float));
-  w.splits_uqkv = dt == MTGR_BF16 ? choose_splits(D, 4 * HD, T) : 1;
+  w.splits_uqkv = dt == MTGR_BF16 ? choose_splits(D, 4 * HD, T) : 1;  // weight gradients: bf16 path only
   w.splits_o = dt == MTGR_BF16 ? choose_splits(HD, D, T) : 1;
   const size_t p1 = (size_t)w.splits_uqkv * D * 4 * HD, p2 = (size_t)w.splits_o * HD * D;
   w.wpart = o;
@@ -271,8 +271,9 @@ static mtgr_status check_meta(const int32_t* offsets, int32_t B, const uint8_t* 
 static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, const __half* v16, int64_t ld16,
                                       const void* u, bool u_f16, int64_t ldu, const int32_t* offsets, int32_t B,
                                       const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d, float eps,
-                                      __nv_bfloat16* y, __half* o, float* mean, float* rstd, uint8_t* ws,
-                                      const AttnWs& w, cudaStream_t s, bool plan_ready = false) {
+                                      void* y, __half* o, float* mean, float* rstd, uint8_t* ws,
+                                      const AttnWs& w, cudaStream_t s, bool plan_ready = false,
+                                      bool y_f16 = false) {
   // plan_ready: an earlier call on the same batch left its status word and work
   // lists in this workspace (the layers of a stack share them)
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
@@ -282,9 +283,13 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
   if (!plan_ready) MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_fwd plan");
   MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
   const int HD = H * d;
-  cudaError_t e = u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, y, mean, rstd, T, HD, eps, s)
-                        : launch_ln_gate_fwd(o, static_cast<const __nv_bfloat16*>(u), ldu, y, mean, rstd, T, HD,
-                                             eps, s);
+  cudaError_t e =
+      y_f16   ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, static_cast<__half*>(y), mean, rstd, T, HD,
+                                   eps, s)
+      : u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, static_cast<__nv_bfloat16*>(y), mean, rstd,
+                                   T, HD, eps, s)
+              : launch_ln_gate_fwd(o, static_cast<const __nv_bfloat16*>(u), ldu, static_cast<__nv_bfloat16*>(y), mean,
+                                   rstd, T, HD, eps, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_fwd gate");
   return MTGR_OK;
 }
@@ -409,17 +414,19 @@ mtgr_status mtgr_group_layernorm_fwd(const void* x, void* y, float* mean, float*
                                      const float* gamma, const float* beta, int64_t T, int32_t D, float eps,
                                      mtgr_dtype dtype, mtgr_stream_t stream) {
   REQUIRE(T >= 0 && D > 0 && D % 8 == 0 && D <= 4096, MTGR_ERR_UNSUPPORTED, "D must be a multiple of 8 in [8, 4096]");
-  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
+  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16 || dtype == MTGR_F16, MTGR_ERR_INVALID_ARG, "bad dtype");
   if (T == 0) return MTGR_OK;
   REQUIRE(x && y && gid && gamma && beta, MTGR_ERR_INVALID_ARG, "NULL pointer");
   REQUIRE(aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta), MTGR_ERR_INVALID_ARG,
           "tensors must be 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == MTGR_BF16
-                      ? launch_gln_fwd(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), mean,
-                                       rstd, gid, gamma, beta, T, D, eps, s)
-                      : launch_gln_fwd(static_cast<const float*>(x), static_cast<float*>(y), mean, rstd, gid, gamma,
-                                       beta, T, D, eps, s);
+  cudaError_t e =
+      dtype == MTGR_BF16 ? launch_gln_fwd(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y),
+                                          mean, rstd, gid, gamma, beta, T, D, eps, s)
+      : dtype == MTGR_F16 ? launch_gln_fwd(static_cast<const __half*>(x), static_cast<__half*>(y), mean, rstd, gid,
+                                           gamma, beta, T, D, eps, s)
+                          : launch_gln_fwd(static_cast<const float*>(x), static_cast<float*>(y), mean, rstd, gid,
+                                           gamma, beta, T, D, eps, s);
   if (e != cudaSuccess) return cuda_status(e, "group_layernorm_fwd");
   return MTGR_OK;
 }
@@ -433,6 +440,7 @@ mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, const float*
                                      float* dgamma, float* dbeta, int64_t T, int32_t D, mtgr_dtype dtype,
                                      void* workspace, size_t workspace_bytes, mtgr_stream_t stream) {
   REQUIRE(T >= 0 && D > 0 && D % 8 == 0 && D <= 4096, MTGR_ERR_UNSUPPORTED, "D must be a multiple of 8 in [8, 4096]");
+  REQUIRE(dtype != MTGR_F16, MTGR_ERR_UNSUPPORTED, "MTGR_F16 is supported by the forward entry points only");
   REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
   REQUIRE(dgamma && dbeta, MTGR_ERR_INVALID_ARG, "NULL dgamma/dbeta");
   REQUIRE(workspace && workspace_bytes >= mtgr_group_layernorm_bwd_workspace_size(T, D), MTGR_ERR_WORKSPACE,
@@ -471,6 +479,7 @@ static mtgr_status check_attn(const void* q, const void* k, const void* v, const
     REQUIRE(d <= 128 && d % 4 == 0, MTGR_ERR_UNSUPPORTED, "fp32 path supports d_h <= 128, d_h % 4 == 0");
     REQUIRE(ld_in % 4 == 0, MTGR_ERR_INVALID_ARG, "ld_in must be a multiple of 4");
   } else {
+    REQUIRE(dtype != MTGR_F16, MTGR_ERR_UNSUPPORTED, "MTGR_F16 is supported by the layer and stack forward only");
     REQUIRE(false, MTGR_ERR_INVALID_ARG, "bad dtype");
   }
   REQUIRE((int64_t)H * d % 8 == 0 && H * d <= 4096, MTGR_ERR_UNSUPPORTED, "H*d_h must be a multiple of 8, <= 4096");
@@ -599,8 +608,9 @@ static mtgr_status check_layer(const mtgr_layer_weights* w, const int32_t* offse
   REQUIRE(D > 0 && H > 0 && d > 0, MTGR_ERR_INVALID_ARG, "bad layer dims");
   REQUIRE(D % 64 == 0 && D <= 4096 && (H * d) % 64 == 0, MTGR_ERR_UNSUPPORTED,
           "d_model and H*d_h must be multiples of 64 (d_model <= 4096)");
-  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16, MTGR_ERR_INVALID_ARG, "bad dtype");
-  if (dtype == MTGR_BF16) REQUIRE(d == 64 || d == 128, MTGR_ERR_UNSUPPORTED, "bf16 path supports d_h in {64, 128}");
+  REQUIRE(dtype == MTGR_F32 || dtype == MTGR_BF16 || dtype == MTGR_F16, MTGR_ERR_INVALID_ARG, "bad dtype");
+  if (dtype != MTGR_F32)
+    REQUIRE(d == 64 || d == 128, MTGR_ERR_UNSUPPORTED, "the tensor-core path supports d_h in {64, 128}");
   REQUIRE(w->w_uqkv && w->w_o && w->gamma && w->beta, MTGR_ERR_INVALID_ARG, "NULL weight");
   REQUIRE(aligned16(w->w_uqkv) && aligned16(w->w_o) && aligned16(w->gamma) && aligned16(w->beta),
           MTGR_ERR_INVALID_ARG, "weights must be 16-byte aligned");
@@ -633,15 +643,18 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
   r = mtgr_group_layernorm_fwd(x, sv->xn, sv->gln_mean, sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln,
                                dtype, stream);
   if (r != MTGR_OK) return r;
-  if (dtype == MTGR_BF16) {
+  const bool h16 = dtype == MTGR_F16;  // 16-bit tensor-core path with f16 (else bf16) activations and weights
+  if (dtype != MTGR_F32) {
     using bf = __nv_bfloat16;
     GemmArgs g{};
     g.M = T; g.N = N4; g.K = D;
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
+    g.ab_f16 = h16;
     // [U|Q|K|V] = silu(z) is written in f16 (the attention's tensor-core operands),
-    // silu'(z) in bf16 (the factor of the SiLU backward)
+    // silu'(z) in the layer's dtype (the factor of the SiLU backward)
     g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->dsilu); g.ldz = N4;
+    g.z_f16 = h16;
     g.splits = 1; g.status = status; g.name = "gemm_uqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
   } else {
@@ -650,25 +663,26 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
                                   nullptr, 0, static_cast<float*>(sv->dsilu), N4, s),
                   "layer_fwd uqkv gemm");
   }
-  if (dtype == MTGR_BF16) {
+  if (dtype != MTGR_F32) {
     const __half* a = static_cast<const __half*>(sv->uqkv);
     r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
-                           static_cast<__nv_bfloat16*>(sv->y), static_cast<__half*>(sv->o), sv->ln_mean, sv->ln_rstd,
-                           ws + L.attn_base,
-                           L.attn, s, plan_ready);
+                           sv->y, static_cast<__half*>(sv->o), sv->ln_mean, sv->ln_rstd, ws + L.attn_base, L.attn, s,
+                           plan_ready, h16);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     r = mtgr_hstu_attn_fwd(a + HD, a + 2 * HD, a + 3 * HD, a, N4, offsets, B, gid, ts, T, H, d, w->eps_ln, sv->y,
                            sv->o, sv->ln_mean, sv->ln_rstd, dtype, ws + L.attn_base, L.attn.total, stream);
   }
   if (r != MTGR_OK) return r;
-  if (dtype == MTGR_BF16) {
+  if (dtype != MTGR_F32) {
     using bf = __nv_bfloat16;
     GemmArgs g{};
     g.M = T; g.N = D; g.K = HD;
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = true;
-    g.epi = EPI_RESIDUAL; g.C = x_out; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
+    g.ab_f16 = h16;
+    g.epi = EPI_RESIDUAL; g.C = x_out; g.c_f16 = h16; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
+    g.r_f16 = h16;
     g.splits = 1; g.status = status; g.name = "gemm_out";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
   } else {
@@ -714,6 +728,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
                                 const void* dx_out, void* dx, const mtgr_layer_grads* gr, const int32_t* offsets,
                                 int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
                                 void* workspace, size_t workspace_bytes, mtgr_stream_t stream) {
+  REQUIRE(dtype != MTGR_F16, MTGR_ERR_UNSUPPORTED, "MTGR_F16 is supported by the forward entry points only");
   mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
   if (st != MTGR_OK) return st;
   REQUIRE(sv && gr && gr->dw_uqkv && gr->dw_o && gr->dgamma && gr->dbeta, MTGR_ERR_INVALID_ARG,

@@ -38,6 +38,9 @@ struct GemmArgs {
   int64_t ldr;
   __nv_bfloat16* Z;  // silu'(acc) (EPI_SILU)
   int64_t ldz;
+  bool ab_f16;  // A and B are f16 (else bf16)
+  bool r_f16;   // the residual is f16 (else bf16)
+  bool z_f16;   // silu'(acc) is written in f16 (else bf16)
   int splits;  // split-K slices (EPI_F32 only); slice s covers its own K range
   int32_t* status;
   const char* name;  // trace label

@@ -46,6 +46,7 @@ struct Params {
   int64_t M, N, K;
   int m_tiles, n_tiles, splits, kb_per_split, nk;
   bool a_mn, b_mn;
+  bool ab_f16, r_f16, z_f16;
   bool c_f16;
   int epi;
   void* C;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp polls, lane 0 issues) ----------------
-    const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+    const uint32_t idesc = p.ab_f16 ? idesc_f16_f32(BM, BN, p.a_mn, p.b_mn) : idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
@@ -311,12 +312,18 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
             dz[i] = sg * fmaf(x[i], 1.0f - sg, 1.0f);
             x[i] *= sg;
           }
-          stage_store16<__nv_bfloat16>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
+          if (p.z_f16)
+            stage_store16<__half>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
+          else
+            stage_store16<__nv_bfloat16>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
         } else if (p.epi == EPI_RESIDUAL) {
           cp_async_wait<1>();
           __syncwarp();
           float res[32];
-          read_rows16_32<__nv_bfloat16>(rres + (c & 1) * 2048, res, lane);
+          if (p.r_f16)
+            read_rows16_32<__half>(rres + (c & 1) * 2048, res, lane);
+          else
+            read_rows16_32<__nv_bfloat16>(rres + (c & 1) * 2048, res, lane);
           __syncwarp();
           const int64_t cx = col0 + 64;  // chunk c + 2 into the slot just read
           if (c + 2 < BN / 32 && cx < p.N)
@@ -372,10 +379,9 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   // A: K-major -> rows M, cols K, box 64 x 128;  MN-major -> rows K, cols M, box 64 x 64
-  bool okA = a.a_mn_major ? make_tmap_bf16_2d(&tmA, a.A, a.K, a.M, a.lda, 64, 64)
-                    : make_tmap_bf16_2d(&tmA, a.A, a.M, a.K, a.lda, 64, BM);
-  bool okB = a.b_mn_major ? make_tmap_bf16_2d(&tmB, a.B, a.K, a.N, a.ldb, 64, 64)
-                          : make_tmap_bf16_2d(&tmB, a.B, a.N, a.K, a.ldb, 64, BN);
+  auto tmap16 = a.ab_f16 ? make_tmap_f16_2d : make_tmap_bf16_2d;
+  bool okA = a.a_mn_major ? tmap16(&tmA, a.A, a.K, a.M, a.lda, 64, 64) : tmap16(&tmA, a.A, a.M, a.K, a.lda, 64, BM);
+  bool okB = a.b_mn_major ? tmap16(&tmB, a.B, a.K, a.N, a.ldb, 64, 64) : tmap16(&tmB, a.B, a.N, a.K, a.ldb, 64, BN);
   if (!okA || !okB) return cudaErrorInvalidValue;
   Params p;
   p.M = a.M;
@@ -392,11 +398,15 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   const bool okC = a.epi == EPI_F32
                        ? make_tmap_out(&tmC, OUT_F32, a.C, a.M, a.N, a.ldc, splits, 32, 32)
                        : make_tmap_out(&tmC, a.c_f16 ? OUT_F16 : OUT_BF16, a.C, a.M, a.N, a.ldc, 0, 32, 32);
-  const bool okZ = a.epi == EPI_SILU ? make_tmap_out(&tmZ, OUT_BF16, a.Z, a.M, a.N, a.ldz, 0, 32, 32) : true;
+  const bool okZ =
+      a.epi == EPI_SILU ? make_tmap_out(&tmZ, a.z_f16 ? OUT_F16 : OUT_BF16, a.Z, a.M, a.N, a.ldz, 0, 32, 32) : true;
   if (a.epi != EPI_SILU) tmZ = tmC;
   if (!okC || !okZ) return cudaErrorInvalidValue;
   p.a_mn = a.a_mn_major;
   p.b_mn = a.b_mn_major;
+  p.ab_f16 = a.ab_f16;
+  p.r_f16 = a.r_f16;
+  p.z_f16 = a.z_f16;
   p.epi = a.epi;
   p.c_f16 = a.c_f16;
   p.C = a.C;

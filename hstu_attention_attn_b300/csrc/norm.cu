@@ -128,6 +128,19 @@ struct Raw8<__nv_bfloat16> {
   }
 };
 template <>
+struct Raw8<__half> {
+  uint4 w;
+  __device__ __forceinline__ void load(const __half* p) { w = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = f16_lo(u[i]);
+      v[2 * i + 1] = f16_hi(u[i]);
+    }
+  }
+};
+template <>
 struct Raw8<float> {
   float4 a, b;
   __device__ __forceinline__ void load(const float* p) {
@@ -458,6 +471,7 @@ cudaError_t launch_bf16_to_f16(const __nv_bfloat16* src, int64_t lds, __half* ds
                                          cudaStream_t);
 INSTANTIATE(float)
 INSTANTIATE(__nv_bfloat16)
+INSTANTIATE(__half)
 
 using bf16_t = __nv_bfloat16;
 // O is fp32 in the fp32 path and f16 in the bf16 path
@@ -467,6 +481,8 @@ template cudaError_t launch_ln_gate_fwd<__half, bf16_t, bf16_t>(const __half*, c
                                                                 float*, float*, int64_t, int, float, cudaStream_t);
 template cudaError_t launch_ln_gate_fwd<__half, __half, bf16_t>(const __half*, const __half*, int64_t, bf16_t*,
                                                                 float*, float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd<__half, __half, __half>(const __half*, const __half*, int64_t, __half*,
+                                                               float*, float*, int64_t, int, float, cudaStream_t);
 template cudaError_t launch_ln_gate_bwd<float, float, float, float>(const float*, const float*, const float*,
                                                                     int64_t, const float*, const float*, float*,
                                                                     float*, int64_t, const float*, int64_t, int,
@@ -561,8 +577,8 @@ extern "C" MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy,
     return MTGR_ERR_UNSUPPORTED;
   }
   if (dtype != MTGR_F32 && dtype != MTGR_BF16) {
-    set_error("mtgr_group_layernorm_bwd_noalloc: bad dtype");
-    return MTGR_ERR_INVALID_ARG;
+    set_error("mtgr_group_layernorm_bwd_noalloc: %s", dtype == MTGR_F16 ? "MTGR_F16 is forward-only" : "bad dtype");
+    return dtype == MTGR_F16 ? MTGR_ERR_UNSUPPORTED : MTGR_ERR_INVALID_ARG;
   }
   if (!dgamma || !dbeta || (T > 0 && !(dy && x && mean && rstd && gid && gamma && dx))) {
     set_error("mtgr_group_layernorm_bwd_noalloc: NULL pointer");

@@ -35,7 +35,7 @@ def device_batch(batch, device="cuda", pin=False) -> DeviceBatch:
 
 
 def _dt(dtype):
-    return mtgr.MTGR_BF16 if dtype == torch.bfloat16 else mtgr.MTGR_F32
+    return {torch.bfloat16: mtgr.MTGR_BF16, torch.float16: mtgr.MTGR_F16}.get(dtype, mtgr.MTGR_F32)
 
 
 def workspace(nbytes, device="cuda"):

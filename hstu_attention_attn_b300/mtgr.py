@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmtgr.so")
 
-MTGR_F32, MTGR_BF16 = 0, 1
+MTGR_F32, MTGR_BF16, MTGR_F16 = 0, 1, 2
 MTGR_OK, MTGR_ERR_INVALID_ARG, MTGR_ERR_UNSUPPORTED = 0, -1, -4
 STATUS_BAD_OFFSETS, STATUS_BAD_GROUP_ORDER, STATUS_BAD_GROUP_ID, STATUS_TIMEOUT = 1, 2, 4, 8
 
@@ -121,6 +121,8 @@ def _dtype(t):
         return MTGR_BF16
     if t.dtype == torch.float32:
         return MTGR_F32
+    if t.dtype == torch.float16:
+        return MTGR_F16
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 

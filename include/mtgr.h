@@ -69,7 +69,13 @@ typedef enum {
   MTGR_ERR_WORKSPACE = -7        /* workspace missing or smaller than queried */
 } mtgr_status;
 
-typedef enum { MTGR_F32 = 0, MTGR_BF16 = 1 } mtgr_dtype;
+/* MTGR_F16 is the inference variant (the pages serve in FP16, paper-daily
+ * "计算量涨了 65 倍…"): activations, weights and the layer's outputs in f16.
+ * It is accepted by mtgr_group_layernorm_fwd, mtgr_layer_workspace_size,
+ * mtgr_hstu_layer_fwd and mtgr_hstu_stack_fwd (the layer's saved state is
+ * then f16 too); the attention and backward entry points return
+ * MTGR_ERR_UNSUPPORTED for it. */
+typedef enum { MTGR_F32 = 0, MTGR_BF16 = 1, MTGR_F16 = 2 } mtgr_dtype;
 
 /* Bits of the int32 device status word written by mtgr_validate_batch and
  * OR-ed by kernels that give up a bounded wait. */

@@ -38,3 +38,8 @@ def sub_batch(batch, users):
         offs.append(offs[-1] + s1 - s0)
     rows = np.concatenate(rows) if rows else np.zeros(0, np.int64)
     return synth.Batch(np.asarray(offs, np.int32), batch.gid[rows], batch.ts[rows]), rows
+
+
+def f16_round(a):
+    """Round to f16 and back (the values an f16 tensor holds)."""
+    return np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
