@@ -2,7 +2,9 @@
  * mtgr.h -- C ABI of libmtgr.so: one MTGR HSTU layer (Group LayerNorm, UQKV
  * projection + SiLU, jagged HSTU attention under the dynamic mixed mask,
  * LayerNorm(O) ⊙ U, output projection + residual), forward and backward,
- * as hand-written CUDA kernels for B300 (sm_103a).
+ * as hand-written CUDA kernels for B300 (sm_103a); a stack of layers run
+ * forward in one call for ranking; and the host-side construction of training
+ * batches (stochastic length, token-balanced ranks).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -19,8 +21,10 @@
  *   gid[t] in {0 User, 1 Seq, 2 RealTime, 3 Cand} (uint8); ts[t] int64 seconds.
  *   Head h of a [T, H*d_h] activation occupies columns h*d_h .. h*d_h+d_h-1.
  * Types.  MTGR_BF16: activations and weights bf16, statistics fp32, weight /
- *   GLN-parameter gradients fp32, fp32 accumulation throughout.  MTGR_F32:
- *   everything fp32.  gamma/beta are fp32 in both modes.
+ *   GLN-parameter gradients fp32, fp32 accumulation throughout (the attention's
+ *   tensor-core operands and its saved output are f16).  MTGR_F16: the
+ *   forward-only inference variant, f16 activations and weights.  MTGR_F32:
+ *   everything fp32.  gamma/beta are fp32 in every mode.
  * Errors.  A non-zero mtgr_status means nothing was enqueued, except
  *   MTGR_ERR_CUDA, which reports a launch failure; mtgr_last_error() returns a
  *   thread-local message.  Malformed device metadata is not checked by the
