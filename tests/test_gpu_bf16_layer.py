@@ -108,3 +108,33 @@ def test_layer_bwd_bf16_steps(orc, D, H, dh):
     assert_close_bf16(to_np(dx), rb["dx"], 2 * TOL_BF16, "dx end-to-end")
     for n in ("dw_uqkv", "dw_o", "dgamma", "dbeta"):
         assert_close_bf16(to_np(g[n]), rb[n], 2 * TOL_BF16, n + " end-to-end")
+
+
+def test_layer_training_step_full_size_sampled_users(orc):
+    """The benchmark's own training step (262,171 tokens, d_model 1024, 8 heads
+    x 128, upstream gradient on candidates only), run whole on the GPU; a user's
+    x_out and dx rows depend on that user alone (given the weights), so sampled
+    whole users are checked against the oracle run on them alone."""
+    need_gpu()
+    from tests.gpu_common import sub_batch
+    L = synth.large_train_layer(3)
+    b = L.batch
+    db = device_batch(b)
+    layer = HstuLayer(L.D, L.H, L.dh, torch.from_numpy(L.w_uqkv), torch.from_numpy(L.w_o),
+                      torch.from_numpy(L.gamma), torch.from_numpy(L.beta), dtype=BF)
+    x = dev(L.x, BF)
+    x_out, sv = layer.forward(x, db)
+    dx, _ = layer.backward(x, sv, dev(L.dx_out, BF), db)
+    torch.cuda.synchronize()
+    n = np.diff(b.offsets)
+    rt = np.array([c[2] for c in b.counts]) if b.counts else np.zeros(b.B)
+    rng = np.random.default_rng(0)
+    users = sorted({int(np.argmax(n)), int(np.argmin(n)), int(np.argmax(rt)), *rng.choice(b.B, 2, replace=False).tolist()})
+    sb, rows = sub_batch(b, users)
+    xb, dxo = bf16_round(L.x[rows]), bf16_round(L.dx_out[rows])
+    wu, wo = bf16_round(L.w_uqkv), bf16_round(L.w_o)
+    ref = orc.layer_fwd(sb, L.D, L.H, L.dh, xb, wu, wo, L.gamma, L.beta)
+    assert_close_bf16(to_np(x_out)[rows], ref["x_out"], TOL_BF16, "x_out of sampled users")
+    rb = orc.layer_bwd(sb, L.D, L.H, L.dh, xb, wu, wo, L.gamma, L.beta, dxo)
+    # end to end through both passes: the composed bound of the step-wise test above
+    assert_close_bf16(to_np(dx)[rows], rb["dx"], 2 * TOL_BF16, "dx of sampled users")
