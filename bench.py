@@ -45,7 +45,7 @@ ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--workload", choices=["large_train", "small_attn"], default="large_train")
