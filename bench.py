@@ -449,7 +449,9 @@ def run_mine(args):
             "tokens_per_s_per_layer": T * world / (ms_step * 1e-3),
             "attention": {"visible_pairs": npairs, "useful_gflop_per_step": (uf["fwd"] + uf["bwd"]) / 1e9,
                           "op_ms_per_step": attn_ms, "core_kernels_ms_per_step": attn_core_ms,
-                          "core_tflops": (uf["fwd"] + uf["bwd"]) / (attn_core_ms * 1e-3) / 1e12},
+                          "core_tflops": (uf["fwd"] + uf["bwd"]) / (attn_core_ms * 1e-3) / 1e12,
+                          # FlashAttention-style count: the backward's recomputed S counted too (10 d_h per pair)
+                          "flash_count_tflops": (uf["fwd"] + uf["bwd"] * 10.0 / 8.0) * world / (attn_ms * 1e-3) / 1e12},
             "kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in sorted(trace.items(), key=lambda kv: -kv[1][0])},
             "gpu_launches": int(launches), "roofline": roof, "clocks": cl, "e2e": e2e}
     if rank == 0 and not args.no_cpu:
