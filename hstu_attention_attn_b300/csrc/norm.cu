@@ -167,12 +167,18 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
     gln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ mean,
                    const float* __restrict__ rstd, const uint8_t* __restrict__ gid, const float* __restrict__ gamma,
                    const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ partial, int64_t rows,
-                   int D) {
+                   int D, int stage_dres) {
   constexpr bool REG = NCH * sizeof(T) <= 8;  // bf16 rows up to 1024, fp32 rows up to 512
-  extern __shared__ float acc[];  // [2][4][D]
+  extern __shared__ float acc[];  // [2][4][D], then one dres row per warp
   for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) acc[i] = 0.f;
   __syncthreads();
   const int lane = threadIdx.x & 31;
+  // the row's dres is requested with its x and dy (cp.async into the warp's
+  // slot; each lane copies and later reads only its own chunks), so one HBM
+  // round trip per row remains on the warp's path instead of two; without
+  // room for the slots (fp32 rows above 2048) dres is loaded where it is used
+  const bool staged = dres != nullptr && stage_dres != 0;
+  uint8_t* dstage = reinterpret_cast<uint8_t*>(acc + 8 * D) + (threadIdx.x >> 5) * (D * (int)sizeof(T));
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t per = (rows + nw - 1) / nw;
@@ -203,6 +209,14 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       if (gcur >= 0) flush();
       gcur = g;
     }
+    if (staged) {
+      ROW_CHUNKS_FOR(m, c, lane, D) {
+#pragma unroll
+        for (int q = 0; q < (int)sizeof(T) / 2; ++q)
+          cp_async16(smem_u32(dstage + 8 * c * sizeof(T) + 16 * q), dres + r * D + 8 * c + q * (16 / sizeof(T)));
+      }
+      cp_async_commit();
+    }
     const float mu = mean[r], rs = rstd[r];
     Raw8<T> xr[NCH], dr[NCH];
     ROW_CHUNKS_FOR(m, c, lane, D) {
@@ -230,6 +244,7 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       }
     }
     const float m1 = warp_sum(s1) / (float)D, m2 = warp_sum(s2) / (float)D;
+    if (staged) cp_async_wait<0>();
     ROW_CHUNKS_FOR(m, c, lane, D) {
       float xv[8], dv[8], ga[8], o[8];
       xr[m].get(xv);
@@ -239,7 +254,10 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       for (int i = 0; i < 8; ++i) o[i] = rs * (dv[i] * ga[i] - m1 - (xv[i] - mu) * rs * m2);
       if (dres) {
         float rv[8];
-        load8(dres + r * D + 8 * c, rv);
+        if (staged)
+          load8(reinterpret_cast<const T*>(dstage + 8 * c * sizeof(T)), rv);
+        else
+          load8(dres + r * D + 8 * c, rv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] += rv[i];
       }
@@ -403,13 +421,15 @@ cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const flo
                            const float* gamma, const T* dres, T* dx, float* dgamma, float* dbeta, float* partial,
                            int64_t rows, int D, cudaStream_t s) {
   const int nb = gln_bwd_blocks(rows);
-  const size_t smem = (size_t)8 * D * sizeof(float);
+  const size_t stage_bytes = (size_t)8 * D * sizeof(T);  // 8 warps' dres rows
+  const int stage = (size_t)8 * D * sizeof(float) + stage_bytes <= 232448 ? 1 : 0;
+  const size_t smem = (size_t)8 * D * sizeof(float) + (stage ? stage_bytes : 0);
   {
   TraceScope tr("gln_bwd", s);
   NCH_DISPATCH(D, ({
                  auto k = gln_bwd_kernel<T, NCHV>;
                  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                 k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D);
+                 k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage);
                }));
   }
   cudaError_t e = cudaGetLastError();
@@ -541,14 +561,16 @@ cudaError_t launch_gln_bwd_noalloc(const T* dy, const T* x, const float* mean, c
   int nb = gln_bwd_blocks(rows);
   const int64_t fit = kGlnNoAllocFloats / (8 * (int64_t)D);
   if (nb > fit) nb = (int)fit;
-  const size_t smem = (size_t)8 * D * sizeof(float);
+  const size_t stage_bytes = (size_t)8 * D * sizeof(T);  // 8 warps' dres rows
+  const int stage = (size_t)8 * D * sizeof(float) + stage_bytes <= 232448 ? 1 : 0;
+  const size_t smem = (size_t)8 * D * sizeof(float) + (stage ? stage_bytes : 0);
   {
     TraceScope tr("gln_bwd", s);
     NCH_DISPATCH(D, ({
                    auto k = gln_bwd_kernel<T, NCHV>;
                    cudaError_t ea = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                    if (ea != cudaSuccess) return ea;
-                   k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D);
+                   k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage);
                  }));
   }
   cudaError_t e = cudaGetLastError();
