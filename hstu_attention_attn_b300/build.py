@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmtgr.so")
 SOURCES = ["api.cu", "plan.cu", "norm.cu", "attn_f32.cu", "gemm_f32.cu", "gemm_sm103.cu",
-           "attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "rows.cu", "batching.cpp"]
+           "attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "rows.cu", "waitcheck.cu", "batching.cpp"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
          "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

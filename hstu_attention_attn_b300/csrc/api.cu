@@ -19,6 +19,7 @@ cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_
 cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
                                   int64_t*, cudaStream_t);
 cudaError_t launch_expand_rows(const void*, const int32_t*, int64_t, void*, int64_t, int64_t, cudaStream_t);
+cudaError_t launch_wait_timeout(int32_t*, cudaStream_t);
 template <typename T>
 cudaError_t launch_gln_fwd(const T*, T*, float*, float*, const uint8_t*, const float*, const float*, int64_t, int,
                            float, cudaStream_t);
@@ -392,6 +393,12 @@ mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const u
   MTGR_CUDA_TRY(launch_visible_counts(offsets, B, gid, ts, T, cnt, total_pairs,
                                       reinterpret_cast<cudaStream_t>(stream)),
                 "visible_counts");
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_debug_wait_timeout(int32_t* status_word, mtgr_stream_t stream) {
+  REQUIRE(status_word != nullptr, MTGR_ERR_INVALID_ARG, "status_word is NULL");
+  MTGR_CUDA_TRY(launch_wait_timeout(status_word, reinterpret_cast<cudaStream_t>(stream)), "wait_timeout");
   return MTGR_OK;
 }
 

@@ -61,6 +61,7 @@ EXPORTS = {
     "mtgr_group_layernorm_bwd": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p,
                                                                 C.c_size_t, C.c_void_p]),
     "mtgr_group_layernorm_bwd_noalloc": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p]),
+    "mtgr_debug_wait_timeout": (C.c_int, [C.c_void_p, C.c_void_p]),
     "mtgr_expand_rows": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int32, C.c_int,
                                    C.c_void_p]),
     "mtgr_stochastic_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32] + [C.c_void_p] * 4),
@@ -173,6 +174,10 @@ def mtgr_debug_visible_counts(offsets, gid, ts, T, cnt, total_pairs, stream=None
     _check("mtgr_debug_visible_counts",
            lib().mtgr_debug_visible_counts(_p(offsets), offsets.numel() - 1, _p(gid), _p(ts), T, _p(cnt),
                                            _p(total_pairs), _stream(stream)))
+
+
+def mtgr_debug_wait_timeout(status_word, stream=None):
+    _check("mtgr_debug_wait_timeout", lib().mtgr_debug_wait_timeout(_p(status_word), _stream(stream)))
 
 
 def mtgr_group_layernorm_fwd(x, y, mean, rstd, gid, gamma, beta, eps=1e-5, stream=None):

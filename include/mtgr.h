@@ -125,6 +125,14 @@ MTGR_API mtgr_status mtgr_validate_batch(const int32_t* offsets, int32_t B, cons
 MTGR_API mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
                                       int64_t T, int32_t* cnt, int64_t* total_pairs, mtgr_stream_t stream);
 
+/* Self-check of the timeout path.  Launches one CTA that takes tensor memory
+ * and waits on an mbarrier that nothing completes, with the same bounded waits
+ * the tcgen05 kernels use (limit 2 s of %globaltimer).  When they give up it
+ * ORs MTGR_STATUS_TIMEOUT into *status_word (device int32, not cleared), frees
+ * its tensor memory and returns; nothing faults or hangs and the context stays
+ * usable.  Asynchronous on stream; takes about 2 s of one SM. */
+MTGR_API mtgr_status mtgr_debug_wait_timeout(int32_t* status_word, mtgr_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Group LayerNorm (fun-rec §7.3.3: GLN(x_i) = (x_i - μ)/σ · γ_g(i) + β_g(i);  */
 /* paper-daily "模型怎么搭": one set of normalisation parameters per token      */
