@@ -78,3 +78,9 @@ def test_expand_rows_rejects_bad_arguments_on_the_host(lib):
     assert lib.mtgr_expand_rows(p, p, 1, p, 4, 7, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
     assert lib.mtgr_expand_rows(None, None, 1, p, 4, 8, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
     assert lib.mtgr_expand_rows(p, p, -1, p, 4, 8, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
+
+
+def test_wait_timeout_check_rejects_null_status(lib):
+    from hstu_attention_attn_b300 import mtgr
+    assert lib.mtgr_debug_wait_timeout(None, None) == mtgr.MTGR_ERR_INVALID_ARG
+    assert "status_word" in mtgr.mtgr_last_error()
