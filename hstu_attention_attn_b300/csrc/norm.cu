@@ -67,49 +67,6 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
 // ---------------------------------------------------------------------------
 // Group LayerNorm
 // ---------------------------------------------------------------------------
-template <typename T, int NCH>
-__global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T* __restrict__ y,
-                                                      float* __restrict__ mean, float* __restrict__ rstd,
-                                                      const uint8_t* __restrict__ gid,
-                                                      const float* __restrict__ gamma,
-                                                      const float* __restrict__ beta, int64_t rows, int D,
-                                                      float eps) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    float v[NCH][8];
-    float s = 0.f;
-    ROW_CHUNKS_FOR(m, c, lane, D) {
-      load8(x + r * D + 8 * c, v[m]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s += v[m][i];
-    }
-    const float mu = warp_sum(s) / (float)D;
-    float q = 0.f;
-    ROW_CHUNKS_FOR(m, c, lane, D) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float d = v[m][i] - mu;
-        q += d * d;
-      }
-    }
-    const float rs = rsqrtf(warp_sum(q) / (float)D + eps);
-    const int g = min((int)gid[r], 3);
-    ROW_CHUNKS_FOR(m, c, lane, D) {
-      float ga[8], be[8], o[8];
-      load8(gamma + (int64_t)g * D + 8 * c, ga);
-      load8(beta + (int64_t)g * D + 8 * c, be);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = (v[m][i] - mu) * rs * ga[i] + be[i];
-      store8(y + r * D + 8 * c, o);
-    }
-    if (lane == 0) {
-      if (mean) mean[r] = mu;
-      if (rstd) rstd[r] = rs;
-    }
-  }
-}
-
 // 8 consecutive elements of a row kept in their stored form (one 16-byte
 // vector for bf16, two for fp32) and widened to fp32 on use.
 template <typename T>
@@ -152,6 +109,74 @@ struct Raw8<float> {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   }
 };
+
+// One warp per row, rows strided over the grid.  A row stays in its stored
+// form (Raw8) and is widened on each of the three passes (mean, variance,
+// output).  For 16-bit rows up to 1024 features the next row's chunks are
+// requested before the current row is reduced and written, so each warp keeps
+// a row of loads in flight through its whole loop, not only at the top of it.
+template <typename T, int NCH>
+__global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T* __restrict__ y,
+                                                      float* __restrict__ mean, float* __restrict__ rstd,
+                                                      const uint8_t* __restrict__ gid,
+                                                      const float* __restrict__ gamma,
+                                                      const float* __restrict__ beta, int64_t rows, int D,
+                                                      float eps) {
+  constexpr bool PIPE = sizeof(T) == 2 && NCH <= 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  Raw8<T> nx[PIPE ? NCH : 1];
+  if (PIPE && r < rows) {
+    ROW_CHUNKS_FOR(m, c, lane, D) nx[PIPE ? m : 0].load(x + r * D + 8 * c);
+  }
+  for (; r < rows; r += nwarps) {
+    Raw8<T> cur[NCH];
+    if constexpr (PIPE) {
+#pragma unroll
+      for (int m = 0; m < NCH; ++m) cur[m] = nx[m];
+      const int64_t rn = r + nwarps;
+      if (rn < rows) {
+        ROW_CHUNKS_FOR(m, c, lane, D) nx[m].load(x + rn * D + 8 * c);
+      }
+    } else {
+      ROW_CHUNKS_FOR(m, c, lane, D) cur[m].load(x + r * D + 8 * c);
+    }
+    float s = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float v[8];
+      cur[m].get(v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[i];
+    }
+    const float mu = warp_sum(s) / (float)D;
+    float q = 0.f;
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float v[8];
+      cur[m].get(v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d = v[i] - mu;
+        q += d * d;
+      }
+    }
+    const float rs = rsqrtf(warp_sum(q) / (float)D + eps);
+    const int g = min((int)gid[r], 3);
+    ROW_CHUNKS_FOR(m, c, lane, D) {
+      float v[8], ga[8], be[8], o[8];
+      cur[m].get(v);
+      load8(gamma + (int64_t)g * D + 8 * c, ga);
+      load8(beta + (int64_t)g * D + 8 * c, be);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (v[i] - mu) * rs * ga[i] + be[i];
+      store8(y + r * D + 8 * c, o);
+    }
+    if (lane == 0) {
+      if (mean) mean[r] = mu;
+      if (rstd) rstd[r] = rs;
+    }
+  }
+}
 
 // dx = rstd (dŷ - mean(dŷ) - x̂ mean(dŷ x̂)) (+ dres), dŷ = dy ⊙ γ_g;
 // per-block sums of dy ⊙ x̂ and dy per group go to `partial`
