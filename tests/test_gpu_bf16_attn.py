@@ -131,3 +131,25 @@ def test_attention_bwd_bf16_small_workload_sampled(orc):
     ref = orc.attn_bwd(sb, H, dh, *host, bf16_round(dY[rows]))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
         assert_close_bf16(to_np(got)[rows], r, TOL_BF16, name)
+
+
+def test_attention_bf16_longest_user(orc):
+    """One 4,112-token user (33 tiles: its tile cost passes the planner's
+    1023-bucket clamp, and each of its items streams up to 33 K/V tiles
+    through the ring) beside the ragged users; forward and backward against
+    the oracle on every user."""
+    need_gpu()
+    rng = np.random.default_rng(61)
+    batch = synth.make_batch(rng, [(8, 4020, 64, 20)] + ragged_users(), ts_hi=86400)
+    H, dh = 1, 128
+    assert int(np.diff(batch.offsets).max()) == 4112
+    op, db, (q, k, v, u), host, ld, y, saved = _run_fwd(batch, H, dh, rng)
+    Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
+    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
+    dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
+    dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
+    torch.cuda.synchronize()
+    ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
+    for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
+        assert_close_bf16(to_np(got), r, TOL_BF16, name)
