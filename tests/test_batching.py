@@ -16,7 +16,8 @@ def _batch(users, seed):
 # ---------------------------------------------------------------------------
 # oracle pins
 # ---------------------------------------------------------------------------
-def test_oracle_stochastic_length_identity_and_window():
+def pin_stochastic_length(ob):
+    """What the definition fixes for the stochastic-length oracle `ob`."""
     b = _batch([(8, 30, 5, 3), (0, 0, 2, 1), (2, 7, 0, 4)], 1)
     keep, off = ob.stochastic_length(b.offsets, b.gid, 1000, [5, 6, 7])
     assert keep == list(range(b.T)) and off == list(b.offsets)
@@ -24,11 +25,17 @@ def test_oracle_stochastic_length_identity_and_window():
     gid = [0, 0, 1, 1, 1, 1, 1, 1, 2, 3, 1, 3, 3]
     keep, off = ob.stochastic_length([0, 10, 13], gid, 3, [7, 2])
     assert keep == [0, 1, 5, 6, 7, 8, 9, 10, 11, 12] and off == [0, 7, 10]   # 7 mod (6-3+1) = 3
+    # windows at the start and in the middle of the Seq run: 0 mod 4 = 0, 5 mod 4 = 1
+    keep, off = ob.stochastic_length([0, 10, 13], gid, 3, [0, 2])
+    assert keep == [0, 1, 2, 3, 4, 8, 9, 10, 11, 12] and off == [0, 7, 10]
+    keep, off = ob.stochastic_length([0, 10, 13], gid, 3, [5, 2])
+    assert keep == [0, 1, 3, 4, 5, 8, 9, 10, 11, 12] and off == [0, 7, 10]
     keep, off = ob.stochastic_length([0, 10, 13], gid, 0, [7, 2])
     assert keep == [0, 1, 8, 9, 11, 12] and off == [0, 4, 6]
 
 
-def test_oracle_min_max_split_closed_forms():
+def pin_min_max_split(ob):
+    """Closed forms and the pages' picture for the token-balanced split oracle `ob`."""
     assert ob.min_max_split([3, 1, 4, 1, 5], 1) == 14
     assert ob.min_max_split([3, 1, 4, 1, 5], 5) == 5
     assert ob.min_max_split([3, 1, 4, 1, 5], 9) == 5       # more ranks than users: the largest user
@@ -37,6 +44,14 @@ def test_oracle_min_max_split_closed_forms():
     # the pages' two-card picture: four users per card at first; the card with the
     # shorter users takes a fifth so that both hold the same tokens
     assert ob.min_max_split([800] * 5 + [1000] * 4, 2) == 4000
+
+
+def test_oracle_stochastic_length_identity_and_window():
+    pin_stochastic_length(ob)
+
+
+def test_oracle_min_max_split_closed_forms():
+    pin_min_max_split(ob)
 
 
 # ---------------------------------------------------------------------------
