@@ -37,6 +37,18 @@ MUTANTS = {
     "layer_uqkv_order": ("a + HD, a + 2 * HD, a + 3 * HD, 4 * HD, 0.0, O);", "a + 2 * HD, a + HD, a + 3 * HD, 4 * HD, 0.0, O);"),
     "dgamma_wrong_group": ("sg[g] += dy[t * D + f] * (x[t * D + f] - mus[t]) * rs[t];",
                            "sg[0] += dy[t * D + f] * (x[t * D + f] - mus[t]) * rs[t];"),
+    "dv_without_1_over_n": ("const double a = s * sg / nu;", "const double a = s * sg;"),
+    "dv_wrong_operand": ("dv[j * ldg + h * dh + d] += a * gi[d];", "dv[j * ldg + h * dh + d] += a * qi[d];"),
+    "dq_without_scale": ("dq[i * ldg + h * dh + d] += ds * c * kj[d];", "dq[i * ldg + h * dh + d] += ds * kj[d];"),
+    "gate_eps_outside_sqrt": ("        var /= n;\n        const double r = 1.0 / sqrt(var + eps);\n        for (int f = 0; f < n; ++f) Y[",
+                              "        var /= n;\n        const double r = 1.0 / (sqrt(var) + eps);\n        for (int f = 0; f < n; ++f) Y["),
+    "gate_bwd_du_unnormalised": ("dU[t * ldg + f] = dY[t * n + f] * oh;", "dU[t * ldg + f] = dY[t * n + f] * o[f];"),
+    "gln_bwd_drops_term": ("dx[t * D + f] = r * (gx - m1 - xh * m2);", "dx[t * D + f] = r * (gx - m1);"),
+    "dbeta_wrong_group": ("sb[g] += dy[t * D + f];", "sb[0] += dy[t * D + f];"),
+    "u_block_without_silu": ("for (int64_t e = 0; e < T * 4 * HD; ++e) a[e] = silu(z[e]);",
+                             "for (int64_t e = 0; e < T * 4 * HD; ++e) a[e] = e % (4 * HD) < HD ? z[e] : silu(z[e]);"),
+    "layer_bwd_silu_grad_is_sigmoid": ("da[e] *= sg * (1.0 + z[e] * (1.0 - sg));", "da[e] *= sg;"),
+    "layer_bwd_no_residual_grad": ("for (int64_t e = 0; e < T * D; ++e) dx[e] += dx_out[e];", ""),
 }
 
 
