@@ -42,6 +42,26 @@ DKDV_DRAM_BYTES_PER_PAIR = (568.65e6 + 148.29e6) / 24977261
 ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", "attn_bwd", "attn_bwd_dq")
 
 
+def rank_totals(sums, maxes, device=None):
+    """Whole-job figures from this rank's own: the sum over the ranks of each
+    entry of `sums` (work processed) and the maximum over the ranks of each
+    entry of `maxes` (times), one all-reduce per non-empty list.  Without a
+    process group of more than one rank the values pass through unchanged."""
+    import torch
+    import torch.distributed as dist
+    sums, maxes = [float(v) for v in sums], [float(v) for v in maxes]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return sums, maxes
+    out = []
+    for vals, op in ((sums, dist.ReduceOp.SUM), (maxes, dist.ReduceOp.MAX)):
+        if vals:
+            t = torch.tensor(vals, dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=op)
+            vals = t.tolist()
+        out.append(vals)
+    return out[0], out[1]
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -296,21 +316,17 @@ def run_mine(args):
     torch.cuda.synchronize()
     mtgr.mtgr_trace_enable(False)
     ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
     cl = clocks.stop()
     trace = mtgr.mtgr_trace_report()
     K = args.steps
-    ms_step = ms_total / K
     attn_ms = sum(trace.get(k, (0.0, 0))[0] for k in ATTN_KERNELS) / K
-    if world > 1:
-        t = torch.tensor([attn_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        attn_ms = float(t.item())
+    attn_core_ms = sum(trace.get(k, (0, 0))[0] for k in ("attn_fwd", "attn_bwd", "attn_bwd_dq")) / K
     launches = sum(c for name, (_, c) in trace.items())
-    total_flops = (uf["fwd"] + uf["bwd"]) * world
+    # whole job: work and launches summed over the ranks (each drew its own batch), times of the slowest rank
+    (total_flops, flash_flops, total_tokens, total_pairs, launches), (ms_total, attn_ms, attn_core_ms) = rank_totals(
+        [uf["fwd"] + uf["bwd"], uf["fwd"] + uf["bwd"] * 10.0 / 8.0, T, npairs, launches],
+        [ms_total, attn_ms, attn_core_ms], dev)
+    ms_step = ms_total / K
     value = total_flops / (attn_ms * 1e-3) / 1e12
 
     # ---- roofline of the dominant kernel ----
@@ -339,7 +355,6 @@ def run_mine(args):
                 "traffic_note": "DRAM bytes per launch, from an ncu capture of the 40,960-token batch scaled by "
                                 "visible pairs" if dname == "attn_bwd" else None,
                 "peak_note": f"{pk['src']} sustained dense bf16 (f16 operands run at the same tensor rate)"}
-    attn_core_ms = sum(trace.get(k, (0, 0))[0] for k in ("attn_fwd", "attn_bwd", "attn_bwd_dq")) / K
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -429,11 +444,7 @@ def run_mine(args):
         t0 = time.perf_counter()
         run(K)
         torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / K
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = rank_totals([], [(time.perf_counter() - t0) * 1e3 / K], dev)[1][0]
         e2e = {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                "note": "whole layer step through the public API incl. pinned-host copies in (x, and one packed block "
@@ -446,12 +457,12 @@ def run_mine(args):
             "vs_baseline": None, "dtype": "bf16 (f16 attention operands, fp32 accumulate)", "data": "synthetic",
             "config": workload_config(args, batch, H, dh, D),
             "pct_bf16_peak": value / pk["bf16_sus"] * 100.0,
-            "tokens_per_s_per_layer": T * world / (ms_step * 1e-3),
-            "attention": {"visible_pairs": npairs, "useful_gflop_per_step": (uf["fwd"] + uf["bwd"]) / 1e9,
+            "tokens_per_s_per_layer": total_tokens / (ms_step * 1e-3),
+            "attention": {"visible_pairs": int(total_pairs), "useful_gflop_per_step": total_flops / 1e9,
                           "op_ms_per_step": attn_ms, "core_kernels_ms_per_step": attn_core_ms,
-                          "core_tflops": (uf["fwd"] + uf["bwd"]) / (attn_core_ms * 1e-3) / 1e12,
+                          "core_tflops": total_flops / (attn_core_ms * 1e-3) / 1e12,
                           # FlashAttention-style count: the backward's recomputed S counted too (10 d_h per pair)
-                          "flash_count_tflops": (uf["fwd"] + uf["bwd"] * 10.0 / 8.0) * world / (attn_ms * 1e-3) / 1e12},
+                          "flash_count_tflops": flash_flops / (attn_ms * 1e-3) / 1e12},
             "kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in sorted(trace.items(), key=lambda kv: -kv[1][0])},
             "gpu_launches": int(launches), "roofline": roof, "clocks": cl, "e2e": e2e}
     if rank == 0 and not args.no_cpu:
