@@ -104,10 +104,15 @@ def lib():
 
 # ---------------------------------------------------------------------------
 def _p(t):
+    """Address of a tensor argument: None is NULL and an int passes as a raw
+    address.  Tensor arguments of the C ABI are device memory, so a tensor in
+    host memory is refused here, before a kernel could dereference it."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
     return t.data_ptr()
 
 

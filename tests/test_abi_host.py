@@ -84,3 +84,14 @@ def test_wait_timeout_check_rejects_null_status(lib):
     from hstu_attention_attn_b300 import mtgr
     assert lib.mtgr_debug_wait_timeout(None, None) == mtgr.MTGR_ERR_INVALID_ARG
     assert "status_word" in mtgr.mtgr_last_error()
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+    from hstu_attention_attn_b300 import mtgr
+    assert mtgr._p(None) is None and mtgr._p(4096) == 4096
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mtgr._p(torch.zeros(4))
+    st = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mtgr.mtgr_validate_batch(torch.zeros(2, dtype=torch.int32), torch.zeros(1, dtype=torch.uint8), 1, st, stream=0)
