@@ -95,3 +95,17 @@ def test_binding_refuses_host_tensors(lib):
     st = torch.zeros(1, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA tensor"):
         mtgr.mtgr_validate_batch(torch.zeros(2, dtype=torch.int32), torch.zeros(1, dtype=torch.uint8), 1, st, stream=0)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """There is no CPU fallback: without libmtgr.so every entry point raises."""
+    import torch
+    from hstu_attention_attn_b300 import mtgr
+    monkeypatch.setattr(mtgr, "LIB_PATH", str(tmp_path / "libmtgr.so"))
+    monkeypatch.setattr(mtgr, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        mtgr.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        mtgr.mtgr_version()
+    with pytest.raises(RuntimeError, match="missing"):
+        mtgr.mtgr_token_balanced_split([3, 4, 5], 2)
