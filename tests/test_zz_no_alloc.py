@@ -6,8 +6,8 @@ It is called through the C ABI twice in a row, on two different batches, and
 each result is compared with the workspace entry point mtgr_group_layernorm_bwd
 on the same inputs.  The second batch is smaller than the first, so the second
 call runs on a fixed device array that still holds the first call's partial
-sums: it must not read them.  The file name sorts last so that a run stopping
-at the first failure has already run every other test."""
+sums: it must not read them.  The file name sorts after the parity tests so
+that a run stopping at the first failure has already run them."""
 import numpy as np
 import pytest
 import torch
