@@ -33,12 +33,32 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/layer"
-# DRAM bytes per visible pair (all heads) of the dK/dV kernel: one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum = 568.65 + 148.29 MB) of the
-# 40,960-token training batch (24,977,261 visible pairs).  The kernel's traffic
-# grows with the tile pairs it visits, so a launch moves about this many bytes
-# per visible pair; to be taken again whenever that kernel changes.
-DKDV_DRAM_BYTES_PER_PAIR = (568.65e6 + 148.29e6) / 24977261
+# DRAM bytes of the dominant kernel per unit of its work, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, --clock-control none; the
+# command is in profiles/).  Each entry names the source file the capture was
+# taken on and its SHA-256: a kernel whose source has changed since reports no
+# traffic until it is captured again.
+TRAFFIC = {
+    "attn_bwd": dict(file="hstu_attention_attn_b300/csrc/attn_bwd_sm103.cu",
+                     sha256="6b45b57320a07fe62324c5367b0972fd8a26ffe26c0b358dbffa838a2e6d21ff",
+                     bytes_per_pair=(568.65e6 + 148.29e6) / 24977261,
+                     note="ncu capture of the 40,960-token training batch (24,977,261 visible pairs), "
+                          "scaled by visible pairs"),
+}
+
+
+def traffic_per_launch(kernel, npairs):
+    """(bytes, note) for one launch of `kernel`, or (None, reason)."""
+    import hashlib
+    t = TRAFFIC.get(kernel)
+    if t is None:
+        return None, "no ncu capture of this kernel"
+    with open(os.path.join(ROOT, t["file"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != t["sha256"]:
+            return None, "kernel source changed since its ncu capture"
+    return t["bytes_per_pair"] * npairs, t["note"]
+
+
 ATTN_KERNELS = ("plan_users", "plan_items", "attn_fwd", "gate_fwd", "gate_bwd", "attn_bwd", "attn_bwd_dq")
 
 
@@ -349,12 +369,13 @@ def run_mine(args):
     roof = None
     if algo:
         ach = algo["flops"] / (per_launch_ms * 1e-3) / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"],
-                "traffic": DKDV_DRAM_BYTES_PER_PAIR * npairs if dname == "attn_bwd" else None,
-                "traffic_note": "DRAM bytes per launch, from an ncu capture of the 40,960-token batch scaled by "
-                                "visible pairs" if dname == "attn_bwd" else None,
-                "peak_note": f"{pk['src']} sustained dense bf16 (f16 operands run at the same tensor rate)"}
+        traffic, tnote = traffic_per_launch(dname, npairs)
+        roof = {"kernel": dname, "bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16"], "frac_sustained": ach / pk["bf16_sus"],
+                "traffic": traffic, "traffic_note": tnote,
+                "peak_note": f"{pk['src']} dense bf16 burst (the bench runs at the maximum SM clock; the sustained "
+                             f"figure, {pk['bf16_sus']} TF/s, was measured at a lower clock under the power cap); "
+                             "f16 operands run at the same tensor rate"}
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -456,7 +477,7 @@ def run_mine(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (f16 attention operands, fp32 accumulate)", "data": "synthetic",
             "config": workload_config(args, batch, H, dh, D),
-            "pct_bf16_peak": value / pk["bf16_sus"] * 100.0,
+            "pct_bf16_peak": value / pk["bf16"] * 100.0,
             "tokens_per_s_per_layer": total_tokens / (ms_step * 1e-3),
             "attention": {"visible_pairs": int(total_pairs), "useful_gflop_per_step": total_flops / 1e9,
                           "op_ms_per_step": attn_ms, "core_kernels_ms_per_step": attn_core_ms,

@@ -31,8 +31,8 @@ int gln_bwd_blocks(int64_t rows);
 template <typename TOi, typename TU, typename TY>
 cudaError_t launch_ln_gate_fwd(const TOi*, const TU*, int64_t, TY*, float*, float*, int64_t, int, float,
                                cudaStream_t);
-template <typename TG, typename TOi, typename TU, typename TO>
-cudaError_t launch_ln_gate_bwd(const TG*, const TOi*, const TU*, int64_t, const float*, const float*, TO*, TG*,
+template <typename TD, typename TG, typename TOi, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TD*, const TOi*, const TU*, int64_t, const float*, const float*, TO*, TG*,
                                int64_t, const TG*, int64_t, int, cudaStream_t);
 cudaError_t launch_bf16_to_f16(const __nv_bfloat16*, int64_t, __half*, int64_t, int64_t, int, cudaStream_t);
 cudaError_t launch_attn_f32_fwd(const float*, const float*, const float*, int64_t, const UserInfo*, int,
@@ -300,7 +300,8 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
   return MTGR_OK;
 }
 
-static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16, const __half* k16,
+// dy is f16 and u f16 when u_f16 (the layer's own dY and [U|Q|K|V]), else both bf16.
+static mtgr_status attn_bwd_bf16_core(const void* dy, const __half* q16, const __half* k16,
                                       const __half* v16, int64_t ld16, const void* u, bool u_f16, int64_t ldu,
                                       const __half* o, const float* mean, const float* rstd, const int32_t* offsets,
                                       int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
@@ -314,10 +315,11 @@ static mtgr_status attn_bwd_bf16_core(const __nv_bfloat16* dy, const __half* q16
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_bwd plan");
   const int64_t HD = (int64_t)H * d;
   __half* dO = reinterpret_cast<__half*>(ws + w.dO);
-  cudaError_t e = u_f16 ? launch_ln_gate_bwd(dy, o, static_cast<const __half*>(u), ldu, mean, rstd, dO, du, ldg, dsilu,
-                                             T, (int)HD, s)
-                        : launch_ln_gate_bwd(dy, o, static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du,
-                                             ldg, dsilu, T, (int)HD, s);
+  cudaError_t e = u_f16 ? launch_ln_gate_bwd(static_cast<const __half*>(dy), o, static_cast<const __half*>(u), ldu,
+                                             mean, rstd, dO, du, ldg, dsilu, T, (int)HD, s)
+                        : launch_ln_gate_bwd(static_cast<const __nv_bfloat16*>(dy), o,
+                                             static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du, ldg, dsilu,
+                                             T, (int)HD, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd gate");
   MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts, dq, dk, dv, ldg,
                                     dsilu ? dsilu + HD : nullptr, dsilu ? dsilu + 2 * HD : nullptr,
@@ -767,13 +769,14 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     return MTGR_OK;
   }
   using bf = __nv_bfloat16;
-  // 1. dY = dx' · W_oᵀ
+  // 1. dY = dx' · W_oᵀ (f16 in the bf16 path: 11 significand bits for the
+  // gradient that the gate and attention backward consume, as dO and dS carry)
   if (dtype == MTGR_BF16) {
     GemmArgs g{};
     g.M = T; g.N = HD; g.K = D;
     g.A = static_cast<const bf*>(dx_out); g.lda = D; g.a_mn_major = false;
     g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = false;
-    g.epi = EPI_PLAIN; g.C = dY; g.ldc = HD; g.splits = 1; g.status = status; g.name = "gemm_dY";
+    g.epi = EPI_PLAIN; g.C = dY; g.c_f16 = true; g.ldc = HD; g.splits = 1; g.status = status; g.name = "gemm_dY";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dY gemm");
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, HD, D, static_cast<const float*>(dx_out), D, 1,
@@ -802,7 +805,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   if (dtype == MTGR_BF16) {
     const __half* a = static_cast<const __half*>(sv->uqkv);
     bf* dz = static_cast<bf*>(dZ);
-    r = attn_bwd_bf16_core(static_cast<const bf*>(dY), a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4,
+    r = attn_bwd_bf16_core(dY, a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4,
                            static_cast<const __half*>(sv->o),
                            sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
                            dz, N4, static_cast<const bf*>(sv->dsilu), ws + L.attn_base, L.attn, s);

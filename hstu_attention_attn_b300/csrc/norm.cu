@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const TOi* __restrict_
 }
 
 // dO = rstd (g - mean(g) - ô mean(g ô)), g = dY ⊙ U;  dU = dY ⊙ ô (⊙ dsilu when given: silu'(z_u)).
-template <typename TG, typename TOi, typename TU, typename TO, int NCH>
-__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TG* __restrict__ dY, const TOi* __restrict__ O,
+template <typename TD, typename TG, typename TOi, typename TU, typename TO, int NCH>
+__global__ void __launch_bounds__(256) ln_gate_bwd_kernel(const TD* __restrict__ dY, const TOi* __restrict__ O,
                                                           const TU* __restrict__ U, int64_t ldu,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ rstd, TO* __restrict__ dO,
@@ -474,13 +474,13 @@ cudaError_t launch_ln_gate_fwd(const TOi* O, const TU* U, int64_t ldu, TY* Y, fl
   return cudaGetLastError();
 }
 
-template <typename TG, typename TOi, typename TU, typename TO>
-cudaError_t launch_ln_gate_bwd(const TG* dY, const TOi* O, const TU* U, int64_t ldu, const float* mean,
+template <typename TD, typename TG, typename TOi, typename TU, typename TO>
+cudaError_t launch_ln_gate_bwd(const TD* dY, const TOi* O, const TU* U, int64_t ldu, const float* mean,
                                const float* rstd, TO* dO, TG* dU, int64_t ldg, const TG* dsilu, int64_t rows, int n,
                                cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gate_bwd", s);
-  NCH_DISPATCH(n, (ln_gate_bwd_kernel<TG, TOi, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
+  NCH_DISPATCH(n, (ln_gate_bwd_kernel<TD, TG, TOi, TU, TO, NCHV><<<row_blocks(rows), 256, 0, s>>>(
                       dY, O, U, ldu, mean, rstd, dO, dU, ldg, dsilu, rows, n)));
   return cudaGetLastError();
 }
@@ -528,18 +528,18 @@ template cudaError_t launch_ln_gate_fwd<__half, __half, bf16_t>(const __half*, c
                                                                 float*, float*, int64_t, int, float, cudaStream_t);
 template cudaError_t launch_ln_gate_fwd<__half, __half, __half>(const __half*, const __half*, int64_t, __half*,
                                                                float*, float*, int64_t, int, float, cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<float, float, float, float>(const float*, const float*, const float*,
-                                                                    int64_t, const float*, const float*, float*,
-                                                                    float*, int64_t, const float*, int64_t, int,
-                                                                    cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<bf16_t, __half, bf16_t, __half>(const bf16_t*, const __half*, const bf16_t*,
-                                                                        int64_t, const float*, const float*, __half*,
-                                                                        bf16_t*, int64_t, const bf16_t*, int64_t,
-                                                                        int, cudaStream_t);
-template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half, __half>(const bf16_t*, const __half*, const __half*,
-                                                                        int64_t, const float*, const float*, __half*,
-                                                                        bf16_t*, int64_t, const bf16_t*, int64_t,
-                                                                        int, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<float, float, float, float, float>(const float*, const float*,
+                                                                           const float*, int64_t, const float*,
+                                                                           const float*, float*, float*, int64_t,
+                                                                           const float*, int64_t, int, cudaStream_t);
+// standalone attention backward: bf16 dY and U from the caller
+template cudaError_t launch_ln_gate_bwd<bf16_t, bf16_t, __half, bf16_t, __half>(
+    const bf16_t*, const __half*, const bf16_t*, int64_t, const float*, const float*, __half*, bf16_t*, int64_t,
+    const bf16_t*, int64_t, int, cudaStream_t);
+// layer backward: f16 dY (the dY GEMM's output) and the f16 U of the UQKV projection
+template cudaError_t launch_ln_gate_bwd<__half, bf16_t, __half, __half, __half>(
+    const __half*, const __half*, const __half*, int64_t, const float*, const float*, __half*, bf16_t*, int64_t,
+    const bf16_t*, int64_t, int, cudaStream_t);
 
 }  // namespace mtgr
 
@@ -555,23 +555,38 @@ template cudaError_t launch_ln_gate_bwd<bf16_t, __half, __half, __half>(const bf
 // sums in the fixed array below instead.
 namespace mtgr {
 
-constexpr int64_t kGlnNoAllocFloats = int64_t(1) << 20;  // 4 MiB of fp32 partial sums
+// 10 MiB of fp32 partial sums: 8*D floats per block, so the full grid of two
+// blocks per SM of a 148-SM part (296 blocks) fits up to D = 1107
+constexpr int64_t kGlnNoAllocFloats = int64_t(10) << 18;
 static __device__ __align__(256) float g_gln_noalloc_partial[kGlnNoAllocFloats];
 
 namespace {
 // Device address of the array on the current device.  In host code the array's
 // name is only a host-side stand-in, so the address is looked up once per device
-// with that device current and cached.
+// with that device current and cached (not valid across cudaDeviceReset).  On
+// failure returns nullptr and writes the reason to the library's error message.
 float* gln_noalloc_scratch() {
   static std::mutex mu;
   static float* cached[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const cudaError_t eg = cudaGetDevice(&dev);
+  if (eg != cudaSuccess) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(eg));
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) {
+    set_error("mtgr_group_layernorm_bwd_noalloc: device index %d is outside the 64 devices it supports", dev);
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(mu);
   if (!cached[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_gln_noalloc_partial);
-    if (e != cudaSuccess || p == nullptr) return nullptr;
+    if (e != cudaSuccess || p == nullptr) {
+      set_error("mtgr_group_layernorm_bwd_noalloc: cudaGetSymbolAddress of the device scratch failed: %s",
+                cudaGetErrorString(e));
+      return nullptr;
+    }
     cached[dev] = static_cast<float*>(p);
   }
   return cached[dev];
@@ -619,7 +634,7 @@ extern "C" MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy,
     return MTGR_ERR_UNSUPPORTED;
   }
   if (D > 4096) {
-    set_error("mtgr_group_layernorm_bwd_noalloc: D = %d is above its maximum of 4096 (fixed 4 MiB device scratch)",
+    set_error("mtgr_group_layernorm_bwd_noalloc: D = %d is above its maximum of 4096 (fixed 10 MiB device scratch)",
               (int)D);
     return MTGR_ERR_UNSUPPORTED;
   }
@@ -636,11 +651,7 @@ extern "C" MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy,
     return MTGR_ERR_INVALID_ARG;
   }
   float* partial = gln_noalloc_scratch();
-  if (!partial) {
-    set_error("mtgr_group_layernorm_bwd_noalloc: cudaGetSymbolAddress of the device scratch failed: %s",
-              cudaGetErrorString(cudaGetLastError()));
-    return MTGR_ERR_CUDA;
-  }
+  if (!partial) return MTGR_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == MTGR_BF16

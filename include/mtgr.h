@@ -160,13 +160,17 @@ MTGR_API mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, con
  * memory, a process that reserved its memory up front, a latency-critical step
  * that must not allocate) and so cannot pass a workspace.  The pages have no
  * counterpart: this is a packaging variant, not a step of the method.
- * The per-block dγ/dβ partial sums go to one fixed 4 MiB device array inside
+ * The per-block dγ/dβ partial sums go to one fixed 10 MiB device array inside
  * the library (held by every device that loads the library until the process
  * exits).  Nothing is allocated: no cudaMalloc, cudaFree or allocating library
- * call.  Limit: D <= 4096 (a launch uses at most 1,048,576 / (8*D) blocks);
+ * call.  Limit: D <= 4096 (a launch uses at most 2,621,440 / (8*D) blocks: the
+ * full grid of two blocks per SM on a 148-SM B300 up to D = 1107, fewer above);
  * larger D returns MTGR_ERR_UNSUPPORTED with a message.  The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  Every call
+ * device current) and keeps it for later calls; make that first call before any
+ * stream capture.  The kept address is not valid after cudaDeviceReset (the
+ * context that held the array is gone): do not call this again after a reset
+ * in the same process.  Every call
  * shares the array and overwrites the part it reads, so no clearing is needed,
  * but calls that overlap on the GPU (other streams, other host threads) race on
  * it: serialise them.  Arguments, layouts and errors as mtgr_group_layernorm_bwd. */
@@ -284,7 +288,9 @@ MTGR_API mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_
                                 const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
                                 void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
 
-/* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path. */
+/* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path.
+ * In the MTGR_BF16 path the gradient of the gate's output, dY = dx_out · W_oᵀ,
+ * is kept in f16 in the workspace (11 significand bits, like dO and dS). */
 MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* saved,
                                 const void* dx_out, void* dx, const mtgr_layer_grads* grads,
                                 const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,

@@ -4,8 +4,10 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It shares no code with the CUDA path.
 
 ``liboracle.so`` is compiled from ``mtgr_oracle.c`` (plain C, fp64, OpenMP);
-this module only marshals numpy arrays into it.  ``bruteforce.py`` is an
-independent NumPy restatement used to pin the C code.
+this module marshals numpy arrays into it and, for batches too large for the
+C loops' index-order products, composes the layer from the same C steps with
+numpy's matmul (``layer_fwd_blas`` / ``layer_bwd_blas``, pinned to the C layer).
+``bruteforce.py`` is an independent NumPy restatement used to pin the C code.
 """
 from __future__ import annotations
 
@@ -232,3 +234,47 @@ def silu_grad(z):
     z = _f64(z)
     s = 1.0 / (1.0 + np.exp(-z))
     return s * (1.0 + z * (1.0 - s))
+
+
+def layer_fwd_blas(batch, D, H, dh, x, w_uqkv, w_o, gamma, beta, eps_gln=EPS_GLN, eps_ln=EPS_LN):
+    """The layer forward of ``layer_fwd`` (paper-daily "模型怎么搭": GLN, UQKV +
+    SiLU, masked SiLU attention, LN(O) ⊙ U, output linear + residual) composed
+    from the same pinned steps (``gln_fwd``, ``attn_core_fwd``, ``ln_gate_fwd``),
+    with its two products taken by numpy's matmul (a library primitive).  The
+    plain C loops sum in index order and need hours for a 60k-token batch at
+    d_model 1024; this differs from ``layer_fwd`` only in summation order.
+    Returns the same dict (x_out, xn, z, o, y)."""
+    x, w_uqkv, w_o = _f64(x), _f64(w_uqkv), _f64(w_o)
+    HD = H * dh
+    xn, _, _ = gln_fwd(x, batch.gid, gamma, beta, eps_gln)
+    z = xn @ w_uqkv
+    a = silu(z)
+    O = attn_core_fwd(batch, H, dh, a[:, HD:2 * HD], a[:, 2 * HD:3 * HD], a[:, 3 * HD:])
+    Y, _, _ = ln_gate_fwd(O, a[:, :HD], eps_ln)
+    return dict(x_out=x + Y @ w_o, xn=xn, z=z, o=O, y=Y)
+
+
+def layer_bwd_blas(batch, D, H, dh, x, w_uqkv, w_o, gamma, beta, dx_out, eps_gln=EPS_GLN, eps_ln=EPS_LN):
+    """The layer backward of ``layer_bwd`` composed from the pinned steps with
+    numpy's matmul for the four products (see ``layer_fwd_blas``):
+    dY = dx'·W_oᵀ, dW_o = Yᵀ·dx', gate and attention backward,
+    dz = [dU|dQ|dK|dV] ⊙ silu'(z), dW_uqkv = xnᵀ·dz, dxn = dz·W_uqkvᵀ, GLN
+    backward plus the residual.  Returns dict dx, dw_uqkv, dw_o, dgamma, dbeta."""
+    x, w_uqkv, w_o, dx_out = _f64(x), _f64(w_uqkv), _f64(w_o), _f64(dx_out)
+    HD = H * dh
+    f = layer_fwd_blas(batch, D, H, dh, x, w_uqkv, w_o, gamma, beta, eps_gln, eps_ln)
+    a = silu(f["z"])
+    dY = dx_out @ w_o.T
+    dw_o = f["y"].T @ dx_out
+    dO, du = ln_gate_bwd(dY, f["o"], a[:, :HD], eps_ln)
+    del dY
+    dq, dk, dv = attn_core_bwd(batch, H, dh, a[:, HD:2 * HD], a[:, 2 * HD:3 * HD], a[:, 3 * HD:], dO)
+    del dO, a
+    dz = np.concatenate([du, dq, dk, dv], axis=1)
+    del du, dq, dk, dv
+    dz *= silu_grad(f["z"])
+    dw_uqkv = f["xn"].T @ dz
+    dxn = dz @ w_uqkv.T
+    del dz
+    dx, dg, db = gln_bwd(dxn, x, batch.gid, gamma, eps_gln)
+    return dict(dx=dx + dx_out, dw_uqkv=dw_uqkv, dw_o=dw_o, dgamma=dg, dbeta=db)

@@ -1,5 +1,5 @@
 """bf16 tcgen05 attention vs the fp64 oracle (fed the same bf16-rounded inputs):
-max|err|/RMS(ref) <= 2e-2 on O, Y and every gradient."""
+the 2e-2 bound on O (f16-stored), Y and every gradient (bf16-stored)."""
 import numpy as np
 import pytest
 import torch
@@ -7,7 +7,7 @@ import torch
 from hstu_attention_attn_b300 import synth
 from hstu_attention_attn_b300.layer import HstuAttention, device_batch
 from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users, sub_batch
-from tests.util import TOL_BF16, assert_close, assert_close_bf16, to_np
+from tests.util import TOL_BF16, assert_close_bf16, assert_close_f16, to_np
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
@@ -43,7 +43,7 @@ def test_attention_fwd_bf16_ragged(orc, dh, ts_hi):
     H = 2
     _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng)
     Y, O, mean, rstd = orc.attn_fwd(batch, H, dh, *host)
-    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_f16(to_np(saved[0]), O, TOL_BF16, "O")
     assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
@@ -57,7 +57,7 @@ def test_attention_fwd_bf16_ragged_paired_items(orc):
     assert (batch.T // 128 + batch.B) * H > 4 * 148
     _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng)
     Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
-    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_f16(to_np(saved[0]), O, TOL_BF16, "O")
     assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
@@ -68,7 +68,7 @@ def test_attention_fwd_bf16_packed_layout(orc):
     H, dh = 4, 128
     _, _, _, host, _, y, saved = _run_fwd(batch, H, dh, rng, packed=True)
     Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
-    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_f16(to_np(saved[0]), O, TOL_BF16, "O")
     assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
 
 
@@ -90,7 +90,7 @@ def test_attention_fwd_bf16_small_workload_sampled(orc):
     sb, rows = sub_batch(batch, pick)
     host = [bf16_round(m[rows]) for m in (a.q, a.k, a.v, a.u)]
     Y, O, _, _ = orc.attn_fwd(sb, H, dh, *host)
-    assert_close_bf16(to_np(saved[0])[rows], O, TOL_BF16, "O")
+    assert_close_f16(to_np(saved[0])[rows], O, TOL_BF16, "O")
     assert_close_bf16(to_np(y)[rows], Y, TOL_BF16, "Y")
 
 
@@ -145,7 +145,7 @@ def test_attention_bf16_longest_user(orc):
     assert int(np.diff(batch.offsets).max()) == 4112
     op, db, (q, k, v, u), host, ld, y, saved = _run_fwd(batch, H, dh, rng)
     Y, O, _, _ = orc.attn_fwd(batch, H, dh, *host)
-    assert_close_bf16(to_np(saved[0]), O, TOL_BF16, "O")
+    assert_close_f16(to_np(saved[0]), O, TOL_BF16, "O")
     assert_close_bf16(to_np(y), Y, TOL_BF16, "Y")
     dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
     dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)

@@ -387,3 +387,23 @@ def test_attention_grads_match_torch_autograd(orc):
     (Y * torch.tensor(dY)).sum().backward()
     for mine, ref in ((dq, q.grad), (dk, k.grad), (dv, v.grad), (du, u.grad)):
         assert np.allclose(mine, ref.numpy(), rtol=1e-9, atol=1e-10)
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged"])
+def test_layer_blas_composition_equals_c_layer(orc, case):
+    """``layer_fwd_blas`` / ``layer_bwd_blas`` (the pinned steps with numpy's
+    matmul for the products, used where the C layer's index-order loops are too
+    slow) equal the C layer, which the finite-difference and composition pins
+    above hold, on every output and gradient to fp64 summation-order noise."""
+    if case == "tiny":
+        L = synth.tiny_layer(8)
+    else:
+        L = synth.layer_inputs(9, lambda r: [(8, 150, 20, 20), (4, 40, 0, 3), (0, 0, 5, 2)], 64, 2, 32)
+    b = L.batch
+    args = (b, L.D, L.H, L.dh, L.x, L.w_uqkv, L.w_o, L.gamma, L.beta)
+    f_c, f_b = orc.layer_fwd(*args), orc.layer_fwd_blas(*args)
+    for k in ("x_out", "xn", "z", "o", "y"):
+        assert np.allclose(f_b[k], f_c[k], rtol=1e-11, atol=1e-12 * max(1.0, np.abs(f_c[k]).max())), k
+    g_c, g_b = orc.layer_bwd(*args, L.dx_out), orc.layer_bwd_blas(*args, L.dx_out)
+    for k in ("dx", "dw_uqkv", "dw_o", "dgamma", "dbeta"):
+        assert np.allclose(g_b[k], g_c[k], rtol=1e-10, atol=1e-11 * max(1.0, np.abs(g_c[k]).max())), k
