@@ -21,12 +21,13 @@ cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const
                                   int64_t*, cudaStream_t);
 cudaError_t launch_expand_rows(const void*, const int32_t*, int64_t, void*, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_wait_timeout(int32_t*, cudaStream_t);
-template <typename T>
-cudaError_t launch_gln_fwd(const T*, T*, float*, float*, const uint8_t*, const float*, const float*, int64_t, int,
+template <typename T, typename TY>
+cudaError_t launch_gln_fwd(const T*, TY*, float*, float*, const uint8_t*, const float*, const float*, int64_t, int,
                            float, cudaStream_t);
-template <typename T>
-cudaError_t launch_gln_bwd(const T*, const T*, const float*, const float*, const uint8_t*, const float*, const T*,
-                           T*, float*, float*, float*, int64_t, int, cudaStream_t);
+template <typename TD, typename T>
+cudaError_t launch_gln_bwd(const TD*, const T*, const float*, const float*, const uint8_t*, const float*, const T*,
+                           T*, float*, float*, float*, int64_t, int, const float*, cudaStream_t);
+cudaError_t launch_grad_to_f16(const __nv_bfloat16*, __half*, int64_t, unsigned*, float*, cudaStream_t);
 int gln_bwd_blocks(int64_t rows);
 template <typename TOi, typename TU, typename TY>
 cudaError_t launch_ln_gate_fwd(const TOi*, const TU*, int64_t, TY*, float*, float*, int64_t, int, float,
@@ -43,10 +44,9 @@ cudaError_t launch_attn_f32_bwd(const float*, const float*, const float*, int64_
 cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int64_t, int64_t, int, int,
                                 const int32_t*, int32_t, const int64_t*, __half*, int32_t*, cudaStream_t);
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
-                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
-                                __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
-                                const __nv_bfloat16* mq, const __nv_bfloat16* mk, const __nv_bfloat16* mv,
-                                int32_t* status, cudaStream_t s);
+                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts, void* dq,
+                                void* dk, void* dv, int64_t ldg, const void* mq, const void* mk, const void* mv,
+                                bool g_f16, int32_t* status, cudaStream_t s);
 
 // ---- kernel tracing ----
 namespace {
@@ -204,9 +204,13 @@ static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt,
   return w;
 }
 
+// Layer workspace.  In the MTGR_BF16 path the layer keeps its activations and
+// gradients in f16 between steps (11 significand bits): w16 holds f16 copies
+// of W_uqkv and W_o, dxo16 the upstream gradient scaled by a power of two
+// (gscale: its max-magnitude word, then the scale s and 1/s).
 struct LayerWs {
   AttnWs attn;
-  size_t attn_base, dY, dZ, dxn, gln_part, wpart, total;
+  size_t attn_base, dY, dZ, dxn, gln_part, wpart, w16, dxo16, gscale, total;
   int splits_uqkv, splits_o;
 };
 // Split-K count for a weight-gradient GEMM (M x N output, K = tokens): the
@@ -248,6 +252,12 @@ static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, m
   const size_t p1 = (size_t)w.splits_uqkv * D * 4 * HD, p2 = (size_t)w.splits_o * HD * D;
   w.wpart = o;
   o += align256((p1 > p2 ? p1 : p2) * sizeof(float));
+  w.w16 = o;
+  if (dt == MTGR_BF16) o += align256((size_t)D * 4 * HD * 2) + align256((size_t)HD * D * 2);
+  w.dxo16 = o;
+  if (dt == MTGR_BF16) o += align256((size_t)T * D * 2);
+  w.gscale = o;
+  o += 256;
   w.total = o;
   return w;
 }
@@ -300,14 +310,14 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
   return MTGR_OK;
 }
 
-// dy is f16 and u f16 when u_f16 (the layer's own dY and [U|Q|K|V]), else both bf16.
+// layer16 (the layer's own call): dy, u, the gradients dq/dk/dv/du and the
+// multiplier dsilu are f16; otherwise (the attention entry point) all bf16.
 static mtgr_status attn_bwd_bf16_core(const void* dy, const __half* q16, const __half* k16,
-                                      const __half* v16, int64_t ld16, const void* u, bool u_f16, int64_t ldu,
+                                      const __half* v16, int64_t ld16, const void* u, bool layer16, int64_t ldu,
                                       const __half* o, const float* mean, const float* rstd, const int32_t* offsets,
                                       int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
-                                      __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, __nv_bfloat16* du,
-                                      int64_t ldg, const __nv_bfloat16* dsilu, uint8_t* ws, const AttnWs& w,
-                                      cudaStream_t s) {
+                                      void* dq, void* dk, void* dv, void* du, int64_t ldg, const void* dsilu,
+                                      uint8_t* ws, const AttnWs& w, cudaStream_t s) {
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
@@ -315,15 +325,17 @@ static mtgr_status attn_bwd_bf16_core(const void* dy, const __half* q16, const _
   MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_bwd plan");
   const int64_t HD = (int64_t)H * d;
   __half* dO = reinterpret_cast<__half*>(ws + w.dO);
-  cudaError_t e = u_f16 ? launch_ln_gate_bwd(static_cast<const __half*>(dy), o, static_cast<const __half*>(u), ldu,
-                                             mean, rstd, dO, du, ldg, dsilu, T, (int)HD, s)
-                        : launch_ln_gate_bwd(static_cast<const __nv_bfloat16*>(dy), o,
-                                             static_cast<const __nv_bfloat16*>(u), ldu, mean, rstd, dO, du, ldg, dsilu,
-                                             T, (int)HD, s);
+  cudaError_t e =
+      layer16 ? launch_ln_gate_bwd(static_cast<const __half*>(dy), o, static_cast<const __half*>(u), ldu, mean, rstd,
+                                   dO, static_cast<__half*>(du), ldg, static_cast<const __half*>(dsilu), T, (int)HD, s)
+              : launch_ln_gate_bwd(static_cast<const __nv_bfloat16*>(dy), o, static_cast<const __nv_bfloat16*>(u),
+                                   ldu, mean, rstd, dO, static_cast<__nv_bfloat16*>(du), ldg,
+                                   static_cast<const __nv_bfloat16*>(dsilu), T, (int)HD, s);
   if (e != cudaSuccess) return cuda_status(e, "attn_bwd gate");
+  const uint16_t* m16 = static_cast<const uint16_t*>(dsilu);
   MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts, dq, dk, dv, ldg,
-                                    dsilu ? dsilu + HD : nullptr, dsilu ? dsilu + 2 * HD : nullptr,
-                                    dsilu ? dsilu + 3 * HD : nullptr, status, s),
+                                    m16 ? m16 + HD : nullptr, m16 ? m16 + 2 * HD : nullptr,
+                                    m16 ? m16 + 3 * HD : nullptr, layer16, status, s),
                 "attn_bwd tcgen05");
   return MTGR_OK;
 }
@@ -467,10 +479,10 @@ mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, const float*
       dtype == MTGR_BF16
           ? launch_gln_bwd(static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd,
                            gid, gamma, static_cast<const __nv_bfloat16*>(dx_residual), static_cast<__nv_bfloat16*>(dx),
-                           dgamma, dbeta, static_cast<float*>(workspace), T, D, s)
+                           dgamma, dbeta, static_cast<float*>(workspace), T, D, nullptr, s)
           : launch_gln_bwd(static_cast<const float*>(dy), static_cast<const float*>(x), mean, rstd, gid, gamma,
                            static_cast<const float*>(dx_residual), static_cast<float*>(dx), dgamma, dbeta,
-                           static_cast<float*>(workspace), T, D, s);
+                           static_cast<float*>(workspace), T, D, nullptr, s);
   if (e != cudaSuccess) return cuda_status(e, "group_layernorm_bwd");
   return MTGR_OK;
 }
@@ -654,21 +666,39 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.attn_base + L.attn.status);
   if (T == 0) return MTGR_OK;
   mtgr_status r;
-  r = mtgr_group_layernorm_fwd(x, sv->xn, sv->gln_mean, sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln,
-                               dtype, stream);
-  if (r != MTGR_OK) return r;
-  const bool h16 = dtype == MTGR_F16;  // 16-bit tensor-core path with f16 (else bf16) activations and weights
+  // 16-bit tensor-core path: every operand f16 (MTGR_F16; MTGR_BF16 with f16
+  // copies of its weights and f16 activations between the steps)
+  const bool bf_io = dtype == MTGR_BF16;
+  const __half* wu16 = static_cast<const __half*>(w->w_uqkv);
+  const __half* wo16 = static_cast<const __half*>(w->w_o);
+  if (bf_io) {
+    __half* c = reinterpret_cast<__half*>(ws + L.w16);
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_uqkv), N4, c, N4, D, (int)N4, s),
+                  "layer_fwd W_uqkv f16");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_o), D, c + align256((size_t)D * N4 * 2) / 2,
+                                     D, HD, D, s),
+                  "layer_fwd W_o f16");
+    wu16 = c;
+    wo16 = c + align256((size_t)D * N4 * 2) / 2;
+    // xn = GLN(x) in f16
+    cudaError_t e = launch_gln_fwd(static_cast<const __nv_bfloat16*>(x), static_cast<__half*>(sv->xn), sv->gln_mean,
+                                   sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln, s);
+    if (e != cudaSuccess) return cuda_status(e, "layer_fwd gln");
+  } else {
+    r = mtgr_group_layernorm_fwd(x, sv->xn, sv->gln_mean, sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln,
+                                 dtype, stream);
+    if (r != MTGR_OK) return r;
+  }
   if (dtype != MTGR_F32) {
     using bf = __nv_bfloat16;
     GemmArgs g{};
     g.M = T; g.N = N4; g.K = D;
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = false;
-    g.B = static_cast<const bf*>(w->w_uqkv); g.ldb = N4; g.b_mn_major = true;
-    g.ab_f16 = h16;
-    // [U|Q|K|V] = silu(z) is written in f16 (the attention's tensor-core operands),
-    // silu'(z) in the layer's dtype (the factor of the SiLU backward)
+    g.B = reinterpret_cast<const bf*>(wu16); g.ldb = N4; g.b_mn_major = true;
+    g.ab_f16 = true;
+    // [U|Q|K|V] = silu(z) and silu'(z), both f16
     g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->dsilu); g.ldz = N4;
-    g.z_f16 = h16;
+    g.z_f16 = true;
     g.splits = 1; g.status = status; g.name = "gemm_uqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
   } else {
@@ -681,7 +711,7 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
     const __half* a = static_cast<const __half*>(sv->uqkv);
     r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
                            sv->y, static_cast<__half*>(sv->o), sv->ln_mean, sv->ln_rstd, ws + L.attn_base, L.attn, s,
-                           plan_ready, h16);
+                           plan_ready, /*y_f16=*/true);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     r = mtgr_hstu_attn_fwd(a + HD, a + 2 * HD, a + 3 * HD, a, N4, offsets, B, gid, ts, T, H, d, w->eps_ln, sv->y,
@@ -693,10 +723,11 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
     GemmArgs g{};
     g.M = T; g.N = D; g.K = HD;
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = false;
-    g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = true;
-    g.ab_f16 = h16;
-    g.epi = EPI_RESIDUAL; g.C = x_out; g.c_f16 = h16; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
-    g.r_f16 = h16;
+    g.B = reinterpret_cast<const bf*>(wo16); g.ldb = D; g.b_mn_major = true;
+    g.ab_f16 = true;
+    // x' = x + y·W_o in the layer's dtype
+    g.epi = EPI_RESIDUAL; g.C = x_out; g.c_f16 = !bf_io; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
+    g.r_f16 = !bf_io;
     g.splits = 1; g.status = status; g.name = "gemm_out";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
   } else {
@@ -769,13 +800,37 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     return MTGR_OK;
   }
   using bf = __nv_bfloat16;
-  // 1. dY = dx' · W_oᵀ (f16 in the bf16 path: 11 significand bits for the
-  // gradient that the gate and attention backward consume, as dO and dS carry)
+  // MTGR_BF16: gradients are carried in f16 (11 significand bits) scaled by a
+  // power of two s (from max|dx'|, so that f16's range holds them whatever the
+  // loss scale); the weight gradients, dγ, dβ and dx leave multiplied by 1/s.
+  // Weights are used as exact f16 copies.
+  const __half* wu16 = nullptr;
+  const __half* wo16 = nullptr;
+  const __half* dxo16 = nullptr;
+  const float* inv_scale = nullptr;
+  if (dtype == MTGR_BF16) {
+    __half* c = reinterpret_cast<__half*>(ws + L.w16);
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(w->w_uqkv), N4, c, N4, D, (int)N4, s),
+                  "layer_bwd W_uqkv f16");
+    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(w->w_o), D, c + align256((size_t)D * N4 * 2) / 2, D, HD,
+                                     D, s),
+                  "layer_bwd W_o f16");
+    wu16 = c;
+    wo16 = c + align256((size_t)D * N4 * 2) / 2;
+    float* gs = reinterpret_cast<float*>(ws + L.gscale + 16);
+    MTGR_CUDA_TRY(launch_grad_to_f16(static_cast<const bf*>(dx_out), reinterpret_cast<__half*>(ws + L.dxo16), T * D,
+                                     reinterpret_cast<unsigned*>(ws + L.gscale), gs, s),
+                  "layer_bwd dx' f16");
+    dxo16 = reinterpret_cast<const __half*>(ws + L.dxo16);
+    inv_scale = gs + 1;
+  }
+  // 1. dY = dx' · W_oᵀ
   if (dtype == MTGR_BF16) {
     GemmArgs g{};
     g.M = T; g.N = HD; g.K = D;
-    g.A = static_cast<const bf*>(dx_out); g.lda = D; g.a_mn_major = false;
-    g.B = static_cast<const bf*>(w->w_o); g.ldb = D; g.b_mn_major = false;
+    g.A = reinterpret_cast<const bf*>(dxo16); g.lda = D; g.a_mn_major = false;
+    g.B = reinterpret_cast<const bf*>(wo16); g.ldb = D; g.b_mn_major = false;
+    g.ab_f16 = true;
     g.epi = EPI_PLAIN; g.C = dY; g.c_f16 = true; g.ldc = HD; g.splits = 1; g.status = status; g.name = "gemm_dY";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dY gemm");
   } else {
@@ -789,8 +844,9 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     GemmArgs g{};
     g.M = HD; g.N = D; g.K = T;
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = true;
-    g.B = static_cast<const bf*>(dx_out); g.ldb = D; g.b_mn_major = true;
-    g.epi = EPI_F32; g.C = L.splits_o > 1 ? (void*)wpart : (void*)gr->dw_o; g.ldc = D;
+    g.B = reinterpret_cast<const bf*>(dxo16); g.ldb = D; g.b_mn_major = true;
+    g.ab_f16 = true;
+    g.epi = EPI_F32; g.C = L.splits_o > 1 ? (void*)wpart : (void*)gr->dw_o; g.ldc = D; g.out_scale = inv_scale;
     g.splits = L.splits_o; g.status = status; g.name = "gemm_dWo";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_o gemm");
     if (L.splits_o > 1)
@@ -804,11 +860,10 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   mtgr_status r;
   if (dtype == MTGR_BF16) {
     const __half* a = static_cast<const __half*>(sv->uqkv);
-    bf* dz = static_cast<bf*>(dZ);
-    r = attn_bwd_bf16_core(dY, a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4,
-                           static_cast<const __half*>(sv->o),
+    __half* dz = static_cast<__half*>(dZ);
+    r = attn_bwd_bf16_core(dY, a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, static_cast<const __half*>(sv->o),
                            sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
-                           dz, N4, static_cast<const bf*>(sv->dsilu), ws + L.attn_base, L.attn, s);
+                           dz, N4, sv->dsilu, ws + L.attn_base, L.attn, s);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     float* dz = static_cast<float*>(dZ);
@@ -823,7 +878,9 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     g.M = D; g.N = N4; g.K = T;
     g.A = static_cast<const bf*>(sv->xn); g.lda = D; g.a_mn_major = true;
     g.B = static_cast<const bf*>(dZ); g.ldb = N4; g.b_mn_major = true;
+    g.ab_f16 = true;
     g.epi = EPI_F32; g.C = L.splits_uqkv > 1 ? (void*)wpart : (void*)gr->dw_uqkv; g.ldc = N4;
+    g.out_scale = inv_scale;
     g.splits = L.splits_uqkv; g.status = status; g.name = "gemm_dWuqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_bwd dW_uqkv gemm");
     if (L.splits_uqkv > 1)
@@ -832,18 +889,25 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     GemmArgs h{};
     h.M = T; h.N = D; h.K = N4;
     h.A = static_cast<const bf*>(dZ); h.lda = N4; h.a_mn_major = false;
-    h.B = static_cast<const bf*>(w->w_uqkv); h.ldb = N4; h.b_mn_major = false;
-    h.epi = EPI_PLAIN; h.C = dxn; h.ldc = D; h.splits = 1; h.status = status; h.name = "gemm_dxn";
+    h.B = reinterpret_cast<const bf*>(wu16); h.ldb = N4; h.b_mn_major = false;
+    h.ab_f16 = true;
+    h.epi = EPI_PLAIN; h.C = dxn; h.c_f16 = true; h.ldc = D; h.splits = 1; h.status = status; h.name = "gemm_dxn";
     MTGR_CUDA_TRY(launch_gemm_bf16(h, s), "layer_bwd dxn gemm");
-  } else {
-    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, D, N4, T, static_cast<const float*>(sv->xn), 1, D,
-                                  static_cast<const float*>(dZ), N4, 1, gr->dw_uqkv, N4, nullptr, 0, nullptr, 0, s),
-                  "layer_bwd dW_uqkv gemm");
-    MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, D, N4, static_cast<const float*>(dZ), N4, 1,
-                                  static_cast<const float*>(w->w_uqkv), 1, N4, static_cast<float*>(dxn), D, nullptr,
-                                  0, nullptr, 0, s),
-                  "layer_bwd dxn gemm");
+    // 6. GLN backward (dxn f16, scaled by s) + residual path
+    cudaError_t e = launch_gln_bwd(static_cast<const __half*>(dxn), static_cast<const bf*>(x), sv->gln_mean,
+                                   sv->gln_rstd, gid, w->gamma, static_cast<const bf*>(dx_out), static_cast<bf*>(dx),
+                                   gr->dgamma, gr->dbeta, reinterpret_cast<float*>(ws + L.gln_part), T, D, inv_scale,
+                                   s);
+    if (e != cudaSuccess) return cuda_status(e, "layer_bwd gln");
+    return MTGR_OK;
   }
+  MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, D, N4, T, static_cast<const float*>(sv->xn), 1, D,
+                                static_cast<const float*>(dZ), N4, 1, gr->dw_uqkv, N4, nullptr, 0, nullptr, 0, s),
+                "layer_bwd dW_uqkv gemm");
+  MTGR_CUDA_TRY(launch_gemm_f32(EPI_PLAIN, T, D, N4, static_cast<const float*>(dZ), N4, 1,
+                                static_cast<const float*>(w->w_uqkv), 1, N4, static_cast<float*>(dxn), D, nullptr, 0,
+                                nullptr, 0, s),
+                "layer_bwd dxn gemm");
   // 6. GLN backward + residual path
   return mtgr_group_layernorm_bwd(dxn, x, sv->gln_mean, sv->gln_rstd, gid, w->gamma, dx_out, dx, gr->dgamma,
                                   gr->dbeta, T, D, dtype, ws + L.gln_part,

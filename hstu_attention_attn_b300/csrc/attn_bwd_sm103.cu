@@ -1,6 +1,6 @@
 // attn_bwd_sm103.cu -- jagged HSTU attention backward on the 5th-generation
 // tensor cores (tcgen05 + TMEM + TMA): f16 operands (q, k, v, dO, P, dS),
-// fp32 accumulation, bf16 gradients.
+// fp32 accumulation, bf16 or f16 gradients.
 //
 // With s = q·k / sqrt(d_h), A = M ⊙ silu(s) / n_u and O = A V (marovi.ai
 // "Métodos" block formula; paper-daily "模型怎么搭"), the gradients are
@@ -50,11 +50,11 @@ struct BwdParams {
   const WorkItem* items;
   const int32_t* count;  // number of items in the list
   const int64_t* ts;
-  __nv_bfloat16* g0;  // dkdv kernel: dk; dq kernel: dq
-  __nv_bfloat16* g1;  // dkdv kernel: dv
+  uint16_t* g0;  // dkdv kernel: dk; dq kernel: dq (16-bit type TG of the kernel)
+  uint16_t* g1;  // dkdv kernel: dv
   int64_t ldg;
-  const __nv_bfloat16* m0;  // optional bf16 multipliers of g0 / g1 (row stride ldm)
-  const __nv_bfloat16* m1;
+  const uint16_t* m0;  // optional multipliers of g0 / g1 (type TG, row stride ldm)
+  const uint16_t* m1;
   int64_t ldm;
   int H;
   float scale;  // 1/sqrt(d_h)
@@ -122,21 +122,19 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
   return c;
 }
 
-// 16 (s, dp) pairs of one query row, keys j0 .. j0+15 -> 8 packed f16 dS values.
+// 16 (s, dp) pairs of one query row, keys j0 .. j0+15 -> 8 packed f16 values
+// of dS' = M ⊙ silu'(s c) ⊙ dp (dS without its factor c / n_u, which the dQ
+// output applies once per element).  Pairs go through the packed path (one
+// f16x2 tanh per pair, attn::silu_pair / dsilu_pair).
 __device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int j0,
-                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc, float cn,
+                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc, uint64_t hc2,
                                            uint32_t (&pk)[8]) {
   if (j0 + 16 <= u.eS) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float v[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        v[t] = __uint_as_float(dr[2 * e + t]) * ds * cn;
-      }
-      pk[e] = pack_f16x2(v[0], v[1]);
+      uint32_t h, t;
+      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
+      pk[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1])));
     }
   } else if (j0 >= u.eR) {
     const int ed = m.ri - j0;
@@ -149,7 +147,7 @@ __device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint3
     }
     float sl, ds;
     silu_and_grad_half(s_d * hc, sl, ds);
-    const float vd = diag ? dp_d * ds * cn : 0.f;
+    const float vd = diag ? dp_d * ds : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) pk[e] = pack_f16x2((2 * e == ed) ? vd : 0.f, (2 * e + 1 == ed) ? vd : 0.f);
   } else {
@@ -157,21 +155,21 @@ __device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint3
     // stamp of key j0 + (lane & 15) (attn::rt_key_stamp), broadcast
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float v[2];
+      bool vis[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int jj = j0 + 2 * e + t;
-        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        v[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds * cn : 0.f;
+        vis[t] = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
       }
-      pk[e] = pack_f16x2(v[0], v[1]);
+      uint32_t h, t;
+      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
+      pk[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1]))) &
+              attn::keep_mask(vis[0], vis[1]);
     }
   }
 }
 
-template <int D>
+template <int D, typename TG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -335,6 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     const float hc = 0.5f * p.scale;
+    const uint64_t hc2 = attn::f32x2(__float_as_uint(hc), __float_as_uint(hc));
     uint32_t s_waits = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
@@ -343,7 +342,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const UserInfo& u = c.u;
       const RowMask m = row_mask(u, p.ts, c.qt * BT + quarter * 32 + lane);
       const int64_t* ts_u = p.ts + u.start;
-      const float cn = p.scale / (float)u.n;
       const int nk = c.keys.count();
       for (int i = 0; i < nk && ok; ++i) {
         const int k0 = c.keys.kt(i, c.qt) * BT;
@@ -370,7 +368,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld16(tmem + Cfg::S_COL + cb + 32 + lane_sel, sr[b ^ 1]);
               tmem_ld16(tmem + Cfg::DP_COL + cb + 32 + lane_sel, dr[b ^ 1]);
             }
-            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, cn, pk);
+            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, hc2, pk);
             tmem_st8(tmem + Cfg::DP_COL + cb + lane_sel, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -400,8 +398,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row0 = c.qt * BT + quarter * 32;  // segment-relative first row of this warp
       const int nvalid = c.u.n - row0;
       const bool any = c.keys.count() > 0;
+      const float cn = p.scale / (float)c.u.n;  // the factor c / n_u left out of dS
       const int64_t rbase = (int64_t)c.u.start + row0;
-      const __nv_bfloat16* mb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
+      const uint16_t* mb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
       if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
 #pragma unroll
         for (int s = 0; s < MRING; ++s) {
@@ -426,17 +425,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         float x[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) : 0.f;
+        for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * cn : 0.f;
         if (has_m) {
           cp_async_wait<MRING - 1>();
           __syncwarp();
-          attn::mul_slot_32(x, mr + slot * MSLOT, lane);
+          attn::mul_slot_32<TG>(x, mr + slot * MSLOT, lane);
           __syncwarp();
           if (cc + MRING < NC) mslot_fetch(mr + slot * MSLOT, mb + (cc + MRING) * 32, p.ldm, nvalid, lane);
           cp_async_commit();
           slot = slot == MRING - 1 ? 0 : slot + 1;
         }
-        attn::store_rows_bf16_32(x, stg, p.g0 + rbase * p.ldg + c.h * D + cc * 32, p.ldg, nvalid, lane);
+        attn::store_rows16_32(x, stg, reinterpret_cast<TG*>(p.g0 + rbase * p.ldg + c.h * D + cc * 32), p.ldg, nvalid,
+                              lane);
       }
     }
     if (has_m) cp_async_wait<0>();
@@ -508,50 +508,43 @@ __device__ __forceinline__ int64_t query_adj(const UserInfo& u, const int64_t* t
 }
 
 // 16 (sᵀ, dpᵀ) pairs of one key row, query rows q0 .. q0+15 -> 8 packed f16
-// Pᵀ values (silu, without 1/n_u) and 8 packed dSᵀ values.  warp_us: every
-// key of the warp is User/Seq; any_rt: some key of the warp is RealTime (both
-// warp-uniform).
+// Pᵀ values (silu, without 1/n_u) and 8 packed dS'ᵀ values (silu'·dp, without
+// the factor c / n_u, which the dK output applies).  warp_us: every key of the
+// warp is User/Seq (warp-uniform).  Pairs go through the packed path.
 __device__ __forceinline__ void pds_chunk_k(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int q0,
-                                            const UserInfo& u, const KeyMask& k, bool warp_us, bool any_rt,
-                                            int64_t adj, float hc, float cn, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
+                                            const UserInfo& u, const KeyMask& k, bool warp_us, int64_t adj,
+                                            uint64_t hc2, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
   if (warp_us && q0 + 16 <= u.n) {
     // every key of the warp is User/Seq and every query row lies in the segment
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float a[2], b[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        a[t] = sl;
-        b[t] = __uint_as_float(dr[2 * e + t]) * ds * cn;
-      }
-      pp[e] = pack_f16x2(a[0], a[1]);
-      pd[e] = pack_f16x2(b[0], b[1]);
+      uint32_t h, t;
+      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
+      pp[e] = sl;
+      pd[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1])));
     }
   } else {
     // Query row ri sees a RealTime key stamped ts_j iff ts_j < adj_i (see
     // query_adj); adj holds adj_{q0 + (lane & 15)} and is broadcast.
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float a[2], b[2];
+      bool vis[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int ri = q0 + 2 * e + t;
         const int64_t adj_i = attn::shfl_i64(adj, 2 * e + t);
-        const bool vis = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        a[t] = vis ? sl : 0.f;
-        b[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds * cn : 0.f;
+        vis[t] = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
       }
-      pp[e] = pack_f16x2(a[0], a[1]);
-      pd[e] = pack_f16x2(b[0], b[1]);
+      const uint32_t mk = attn::keep_mask(vis[0], vis[1]);
+      uint32_t h, t;
+      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
+      pp[e] = sl & mk;
+      pd[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1]))) & mk;
     }
   }
 }
 
-template <int D>
+template <int D, typename TG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -728,6 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     const float hc = 0.5f * p.scale;
+    const uint64_t hc2 = attn::f32x2(__float_as_uint(hc), __float_as_uint(hc));
     uint32_t s_waits = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
@@ -741,7 +735,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool warp_us = __all_sync(0xffffffffu, km.cls == 0);
       const bool any_rt = __any_sync(0xffffffffu, km.cls == 1);
       const int64_t* ts_u = p.ts + u.start;
-      const float cn = p.scale / (float)u.n;
       const int nq = c.qs.count();
       for (int i = 0; i < nq && ok; ++i) {
         const int q0 = c.qs.qt(i, c.kt) * BT;
@@ -771,8 +764,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld16(tmem + Cfg::ST_COL + cb + 32 + lane_sel, sr[b ^ 1]);
               tmem_ld16(tmem + Cfg::DPT_COL + cb + 32 + lane_sel, dr[b ^ 1]);
             }
-            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, any_rt, q2 == 0 ? adj[b] : adj[2 + b], hc, cn, pp,
-                        pd);
+            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, q2 == 0 ? adj[b] : adj[2 + b], hc2, pp, pd);
             tmem_st8(tmem + Cfg::ST_COL + cb + lane_sel, pp);
             tmem_st8(tmem + Cfg::DPT_COL + cb + lane_sel, pd);
             tmem_wait_st();
@@ -802,8 +794,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool any = c.qs.count() > 0;
       const int64_t rbase = (int64_t)c.u.start + row0;
       const float inv_n = 1.0f / (float)c.u.n;
-      const __nv_bfloat16* mvb = has_m ? p.m1 + rbase * p.ldm + c.h * D : nullptr;
-      const __nv_bfloat16* mkb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
+      const uint16_t* mvb = has_m ? p.m1 + rbase * p.ldm + c.h * D : nullptr;
+      const uint16_t* mkb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
       if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
 #pragma unroll
         for (int s = 0; s < MRING; ++s) {
@@ -832,22 +824,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.dkdv_free);
         }
-        const float sc = is_k ? 1.f : inv_n;
+        const float sc = is_k ? p.scale * inv_n : inv_n;  // dK: the factor c / n_u left out of dSᵀ
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
         if (has_m) {
           cp_async_wait<MRING - 1>();
           __syncwarp();
-          attn::mul_slot_32(x, mr + slot * MSLOT, lane);
+          attn::mul_slot_32<TG>(x, mr + slot * MSLOT, lane);
           __syncwarp();
           const int nx = ch + MRING;
           if (nx < NCH) mslot_fetch(mr + slot * MSLOT, nx < NC ? mvb + nx * 32 : mkb + (nx - NC) * 32, p.ldm, nvalid, lane);
           cp_async_commit();
           slot = slot == MRING - 1 ? 0 : slot + 1;
         }
-        attn::store_rows_bf16_32(x, stg, (is_k ? p.g0 : p.g1) + rbase * p.ldg + c.h * D + cc * 32, p.ldg, nvalid,
-                                 lane);
+        attn::store_rows16_32(x, stg, reinterpret_cast<TG*>((is_k ? p.g0 : p.g1) + rbase * p.ldg + c.h * D + cc * 32),
+                              p.ldg, nvalid, lane);
       }
     }
     if (has_m) cp_async_wait<0>();
@@ -865,13 +857,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, typename TG>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                          BwdParams pa, BwdParams pq, int grid, cudaStream_t s) {
   cudaError_t e;
   {
     TraceScope tr("attn_bwd", s);
-    auto kern = attn_bwd_dkdv_kernel<D>;
+    auto kern = attn_bwd_dkdv_kernel<D, TG>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, NUM_THREADS, DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
@@ -879,7 +871,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   }
   if (e != cudaSuccess) return e;
   TraceScope tr("attn_bwd_dq", s);
-  auto kern = attn_bwd_dq_kernel<D>;
+  auto kern = attn_bwd_dq_kernel<D, TG>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, NUM_THREADS, DqCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pq);
@@ -888,15 +880,15 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 }  // namespace
 
-// q, k, v: [T, *] f16 with row stride ld; dO: [T, H*d] f16.  dq, dk, dv: bf16
-// with row stride ldg, each multiplied elementwise by the bf16 multiplier
-// block mq / mk / mv when given (row stride 4*H*d; the layer passes silu'(z)
-// of its UQKV projection).  Every row of every segment is written.
+// q, k, v: [T, *] f16 with row stride ld; dO: [T, H*d] f16.  dq, dk, dv: f16
+// (g_f16) or bf16 with row stride ldg, each multiplied elementwise by the
+// multiplier block mq / mk / mv of the same type when given (row stride
+// 4*H*d; the layer passes silu'(z) of its UQKV projection).  Every row of
+// every segment is written.
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
-                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts,
-                                __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t ldg,
-                                const __nv_bfloat16* mq, const __nv_bfloat16* mk, const __nv_bfloat16* mv,
-                                int32_t* status, cudaStream_t s) {
+                                int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts, void* dq,
+                                void* dk, void* dv, int64_t ldg, const void* mq, const void* mk, const void* mv,
+                                bool g_f16, int32_t* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
@@ -915,20 +907,24 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   BwdParams pq = pa;
   pa.items = reinterpret_cast<const WorkItem*>(plan + L.bwd_items);
   pa.count = plan + L.counts + 1;
-  pa.g0 = dk;
-  pa.g1 = dv;
-  pa.m0 = mk;
-  pa.m1 = mv;
+  pa.g0 = static_cast<uint16_t*>(dk);
+  pa.g1 = static_cast<uint16_t*>(dv);
+  pa.m0 = static_cast<const uint16_t*>(mk);
+  pa.m1 = static_cast<const uint16_t*>(mv);
   pq.items = reinterpret_cast<const WorkItem*>(plan + L.dq_items);
   pq.count = plan + L.counts + 2;
-  pq.g0 = dq;
+  pq.g0 = static_cast<uint16_t*>(dq);
   pq.g1 = nullptr;
-  pq.m0 = mq;
+  pq.m0 = static_cast<const uint16_t*>(mq);
   pq.m1 = nullptr;
   const int64_t max_items = L.max_items;
   const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
-  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, pa, pq, grid, s);
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, pa, pq, grid, s);
+  if (d == 128)
+    return g_f16 ? launch_bwd_d<128, __half>(tq, tk, tv, tdo, pa, pq, grid, s)
+                 : launch_bwd_d<128, __nv_bfloat16>(tq, tk, tv, tdo, pa, pq, grid, s);
+  if (d == 64)
+    return g_f16 ? launch_bwd_d<64, __half>(tq, tk, tv, tdo, pa, pq, grid, s)
+                 : launch_bwd_d<64, __nv_bfloat16>(tq, tk, tv, tdo, pa, pq, grid, s);
   return cudaErrorInvalidValue;
 }
 

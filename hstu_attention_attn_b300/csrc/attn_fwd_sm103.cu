@@ -92,15 +92,19 @@ __device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
 
 // N scores of one query row (keys j0 .. j0+N-1 of the segment) -> N/2 packed
 // f16 P values under the dynamic mixed mask.  The chunk class depends only on
-// j0, so it is uniform across the warp.
+// j0, so it is uniform across the warp.  Pairs of scores go through the packed
+// path (attn::silu_pair: one f16x2 tanh per pair).
 template <int N>
 __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const UserInfo& u, int ri, bool row_ok,
-                                        bool cand, int64_t thr, int64_t tk, float hs, uint32_t (&pk)[N / 2]) {
+                                        bool cand, int64_t thr, int64_t tk, float hs, uint64_t hs2,
+                                        uint32_t (&pk)[N / 2]) {
   if (j0 + N <= u.eS) {
     // every key is User/Seq: visible to every row
 #pragma unroll
-    for (int e = 0; e < N / 2; ++e)
-      pk[e] = pack_f16x2(silu_half(__uint_as_float(r[2 * e]) * hs), silu_half(__uint_as_float(r[2 * e + 1]) * hs));
+    for (int e = 0; e < N / 2; ++e) {
+      uint32_t h, t;
+      pk[e] = attn::silu_pair(r[2 * e], r[2 * e + 1], hs2, h, t);
+    }
   } else if (j0 >= u.eR) {
     // candidate keys (or keys past the segment): only the diagonal is visible
     const int ed = ri - j0;
@@ -117,15 +121,14 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const Us
     static_assert(N == 16, "stamp broadcast covers 16 keys");
 #pragma unroll
     for (int e = 0; e < N / 2; ++e) {
-      float pv[2];
+      bool vis[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int jj = j0 + 2 * e + t;
-        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < thr) | (cand & (jj == ri));
-        const float v = silu_half(__uint_as_float(r[2 * e + t]) * hs);
-        pv[t] = vis ? v : 0.f;
+        vis[t] = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < thr) | (cand & (jj == ri));
       }
-      pk[e] = pack_f16x2(pv[0], pv[1]);
+      uint32_t h, t;
+      pk[e] = attn::silu_pair(r[2 * e], r[2 * e + 1], hs2, h, t) & attn::keep_mask(vis[0], vis[1]);
     }
   }
 }
@@ -335,6 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     const int r_in = quarter * 32 + lane;
     const float hs = 0.5f * p.scale;
+    const uint64_t hs2 = attn::f32x2(__float_as_uint(hs), __float_as_uint(hs));
     float* stg = sStg + ew * STG_FLOATS;
     uint32_t s_waits = 0, o_waits = 0;
     for (int r = 0; ok; ++r) {
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           if (ch < 3) tmem_ld16(t_s + 16 * (ch + 1), rc[(ch + 1) & 1]);
-          p_chunk<16>(rc[ch & 1], jg + 16 * ch, u, ri, row_ok, cand, thr, tk[ch], hs, pk);
+          p_chunk<16>(rc[ch & 1], jg + 16 * ch, u, ri, row_ok, cand, thr, tk[ch], hs, hs2, pk);
           tmem_st8(t_s + 8 * ch, pk);
           if (ch < 3) tmem_wait_ld();
         }

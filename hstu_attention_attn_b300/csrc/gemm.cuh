@@ -42,6 +42,7 @@ struct GemmArgs {
   bool r_f16;   // the residual is f16 (else bf16)
   bool z_f16;   // silu'(acc) is written in f16 (else bf16)
   int splits;  // split-K slices (EPI_F32 only); slice s covers its own K range
+  const float* out_scale;  // EPI_F32: device scalar the output is multiplied by (nullable)
   int32_t* status;
   const char* name;  // trace label
 };

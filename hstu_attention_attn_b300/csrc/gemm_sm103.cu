@@ -55,6 +55,7 @@ struct Params {
   int64_t ldr;
   __nv_bfloat16* Z;
   int64_t ldz;
+  const float* out_scale;  // EPI_F32: multiply by *out_scale when set
   int32_t* status;
 };
 
@@ -290,6 +291,11 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
         if (p.epi == EPI_F32) {
+          if (p.out_scale) {
+            const float sc = *p.out_scale;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= sc;
+          }
           uint8_t* sl;
           if (wide) {
             slot_free<1>(lane);
@@ -415,6 +421,7 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
   p.ldr = a.ldr;
   p.Z = a.Z;
   p.ldz = a.ldz;
+  p.out_scale = a.out_scale;
   p.status = a.status;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;

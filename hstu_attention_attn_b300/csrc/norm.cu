@@ -115,8 +115,8 @@ struct Raw8<float> {
 // output).  For 16-bit rows up to 1024 features the next row's chunks are
 // requested before the current row is reduced and written, so each warp keeps
 // a row of loads in flight through its whole loop, not only at the top of it.
-template <typename T, int NCH>
-__global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T* __restrict__ y,
+template <typename T, typename TY, int NCH>
+__global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, TY* __restrict__ y,
                                                       float* __restrict__ mean, float* __restrict__ rstd,
                                                       const uint8_t* __restrict__ gid,
                                                       const float* __restrict__ gamma,
@@ -178,7 +178,9 @@ __global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T
   }
 }
 
-// dx = rstd (dŷ - mean(dŷ) - x̂ mean(dŷ x̂)) (+ dres), dŷ = dy ⊙ γ_g;
+// dx = rstd (dŷ - mean(dŷ) - x̂ mean(dŷ x̂)) (+ dres), dŷ = dy ⊙ γ_g, with dy
+// read as stored times *dy_scale when dy_scale is given (an upstream gradient
+// kept scaled by a power of two);
 // per-block sums of dy ⊙ x̂ and dy per group go to `partial`
 // ([gridDim.x][2][4][D] fp32), reduced by gln_param_reduce_kernel.
 // Each warp takes a contiguous range of rows.  Tokens of a user are sorted by
@@ -187,12 +189,13 @@ __global__ void __launch_bounds__(256) gln_fwd_kernel(const T* __restrict__ x, T
 // in registers and adds them to the block's shared sums only when the group
 // changes; for wider rows the registers do not suffice and every row adds
 // into the shared sums directly.
-template <typename T, int NCH>
+template <typename TD, typename T, int NCH>
 __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
-    gln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ mean,
+    gln_bwd_kernel(const TD* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ mean,
                    const float* __restrict__ rstd, const uint8_t* __restrict__ gid, const float* __restrict__ gamma,
                    const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ partial, int64_t rows,
-                   int D, int stage_dres) {
+                   int D, int stage_dres, const float* __restrict__ dy_scale) {
+  const float dsc = dy_scale ? *dy_scale : 1.f;
   constexpr bool REG = NCH * sizeof(T) <= 8;  // bf16 rows up to 1024, fp32 rows up to 512
   extern __shared__ float acc[];  // [2][4][D], then one dres row per warp
   for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) acc[i] = 0.f;
@@ -243,7 +246,8 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       cp_async_commit();
     }
     const float mu = mean[r], rs = rstd[r];
-    Raw8<T> xr[NCH], dr[NCH];
+    Raw8<T> xr[NCH];
+    Raw8<TD> dr[NCH];
     ROW_CHUNKS_FOR(m, c, lane, D) {
       xr[m].load(x + r * D + 8 * c);
       dr[m].load(dy + r * D + 8 * c);
@@ -253,6 +257,8 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       float xv[8], dv[8], ga[8];
       xr[m].get(xv);
       dr[m].get(dv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dv[i] *= dsc;
       load8(gamma + (int64_t)g * D + 8 * c, ga);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -274,6 +280,8 @@ __global__ void __launch_bounds__(256, NCH * sizeof(T) <= 8 ? 2 : 1)
       float xv[8], dv[8], ga[8], o[8];
       xr[m].get(xv);
       dr[m].get(dv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dv[i] *= dsc;
       load8(gamma + (int64_t)g * D + 8 * c, ga);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = rs * (dv[i] * ga[i] - m1 - (xv[i] - mu) * rs * m2);
@@ -425,12 +433,12 @@ static int row_blocks(int64_t rows) {
     }                                                  \
   } while (0)
 
-template <typename T>
-cudaError_t launch_gln_fwd(const T* x, T* y, float* mean, float* rstd, const uint8_t* gid, const float* gamma,
+template <typename T, typename TY>
+cudaError_t launch_gln_fwd(const T* x, TY* y, float* mean, float* rstd, const uint8_t* gid, const float* gamma,
                            const float* beta, int64_t rows, int D, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gln_fwd", s);
-  NCH_DISPATCH(D, (gln_fwd_kernel<T, NCHV><<<row_blocks(rows), 256, 0, s>>>(x, y, mean, rstd, gid, gamma, beta,
+  NCH_DISPATCH(D, (gln_fwd_kernel<T, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(x, y, mean, rstd, gid, gamma, beta,
                                                                             rows, D, eps)));
   return cudaGetLastError();
 }
@@ -441,10 +449,10 @@ int gln_bwd_blocks(int64_t rows) {
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
-template <typename T>
-cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const float* rstd, const uint8_t* gid,
+template <typename TD, typename T>
+cudaError_t launch_gln_bwd(const TD* dy, const T* x, const float* mean, const float* rstd, const uint8_t* gid,
                            const float* gamma, const T* dres, T* dx, float* dgamma, float* dbeta, float* partial,
-                           int64_t rows, int D, cudaStream_t s) {
+                           int64_t rows, int D, const float* dy_scale, cudaStream_t s) {
   const int nb = gln_bwd_blocks(rows);
   const size_t stage_bytes = (size_t)8 * D * sizeof(T);  // 8 warps' dres rows
   const int stage = (size_t)8 * D * sizeof(float) + stage_bytes <= 232448 ? 1 : 0;
@@ -452,9 +460,10 @@ cudaError_t launch_gln_bwd(const T* dy, const T* x, const float* mean, const flo
   {
   TraceScope tr("gln_bwd", s);
   NCH_DISPATCH(D, ({
-                 auto k = gln_bwd_kernel<T, NCHV>;
+                 auto k = gln_bwd_kernel<TD, T, NCHV>;
                  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                 k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage);
+                 k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage,
+                                         dy_scale);
                }));
   }
   cudaError_t e = cudaGetLastError();
@@ -508,15 +517,17 @@ cudaError_t launch_bf16_to_f16(const __nv_bfloat16* src, int64_t lds, __half* ds
   return cudaGetLastError();
 }
 
-#define INSTANTIATE(T)                                                                                        \
-  template cudaError_t launch_gln_fwd<T>(const T*, T*, float*, float*, const uint8_t*, const float*,           \
-                                         const float*, int64_t, int, float, cudaStream_t);                    \
-  template cudaError_t launch_gln_bwd<T>(const T*, const T*, const float*, const float*, const uint8_t*,       \
-                                         const float*, const T*, T*, float*, float*, float*, int64_t, int,     \
-                                         cudaStream_t);
-INSTANTIATE(float)
-INSTANTIATE(__nv_bfloat16)
-INSTANTIATE(__half)
+#define INSTANTIATE(T, TY)                                                                                    \
+  template cudaError_t launch_gln_fwd<T, TY>(const T*, TY*, float*, float*, const uint8_t*, const float*,       \
+                                             const float*, int64_t, int, float, cudaStream_t);                \
+  template cudaError_t launch_gln_bwd<TY, T>(const TY*, const T*, const float*, const float*, const uint8_t*,   \
+                                             const float*, const T*, T*, float*, float*, float*, int64_t, int,  \
+                                             const float*, cudaStream_t);
+INSTANTIATE(float, float)
+INSTANTIATE(__nv_bfloat16, __nv_bfloat16)
+INSTANTIATE(__half, __half)
+// the bf16 layer: bf16 x and dx, f16 normalised activations and their gradient
+INSTANTIATE(__nv_bfloat16, __half)
 
 using bf16_t = __nv_bfloat16;
 // O is fp32 in the fp32 path and f16 in the bf16 path
@@ -537,9 +548,76 @@ template cudaError_t launch_ln_gate_bwd<bf16_t, bf16_t, __half, bf16_t, __half>(
     const bf16_t*, const __half*, const bf16_t*, int64_t, const float*, const float*, __half*, bf16_t*, int64_t,
     const bf16_t*, int64_t, int, cudaStream_t);
 // layer backward: f16 dY (the dY GEMM's output) and the f16 U of the UQKV projection
-template cudaError_t launch_ln_gate_bwd<__half, bf16_t, __half, __half, __half>(
-    const __half*, const __half*, const __half*, int64_t, const float*, const float*, __half*, bf16_t*, int64_t,
-    const bf16_t*, int64_t, int, cudaStream_t);
+template cudaError_t launch_ln_gate_bwd<__half, __half, __half, __half, __half>(
+    const __half*, const __half*, const __half*, int64_t, const float*, const float*, __half*, __half*, int64_t,
+    const __half*, int64_t, int, cudaStream_t);
+
+// ---------------------------------------------------------------------------
+// f16 copy of an upstream gradient, scaled by a power of two
+// ---------------------------------------------------------------------------
+// The bf16 layer backward carries its gradients in f16 (11 significand bits);
+// f16's range is narrower than bf16's, so the upstream gradient is first scaled
+// by s = 2^-e, e = ceil(log2 max|g|), which puts its largest magnitude in
+// (1/2, 1] whatever the loss scale (s = 1 for an all-zero or non-finite
+// gradient).  The results that leave the layer are multiplied by 1/s.
+
+// max |g| over n bf16 values (n a multiple of 8, 16-byte aligned), as the bit
+// pattern of a non-negative bf16 (such patterns order like the values), into
+// *out (cleared before).
+__global__ void absmax_bf16_kernel(const __nv_bfloat16* __restrict__ g, int64_t n8, unsigned* __restrict__ out) {
+  unsigned m = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 w = reinterpret_cast<const uint4*>(g)[i];
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, max(u[k] & 0x7FFFu, (u[k] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(out, m);
+}
+
+// s from the max bits (see above)
+__device__ __forceinline__ float grad_scale_from_max(unsigned bits) {
+  const float m = __uint_as_float(bits << 16);
+  if (!(m > 0.f) || !isfinite(m)) return 1.f;
+  int ex;
+  const float f = frexpf(m, &ex);  // m = f 2^ex, f in [1/2, 1)
+  const int c = f > 0.5f ? ex : ex - 1;  // ceil(log2 m)
+  return ldexpf(1.f, -c);
+}
+
+// dst (f16) = src (bf16) * s; scale[0] = s, scale[1] = 1/s (written by thread 0).
+__global__ void scale_to_f16_kernel(const __nv_bfloat16* __restrict__ src, __half* __restrict__ dst, int64_t n8,
+                                    const unsigned* __restrict__ maxbits, float* __restrict__ scale) {
+  const float sc = grad_scale_from_max(*maxbits);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    scale[0] = sc;
+    scale[1] = 1.f / sc;
+  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    load8(src + 8 * i, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] *= sc;
+    store8(dst + 8 * i, v);
+  }
+}
+
+// n (a multiple of 8) elements; ws_max: one device word; scale: two device floats
+cudaError_t launch_grad_to_f16(const __nv_bfloat16* src, __half* dst, int64_t n, unsigned* ws_max, float* scale,
+                               cudaStream_t s) {
+  TraceScope tr("grad_f16", s);
+  cudaError_t e = cudaMemsetAsync(ws_max, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = n / 8;
+  const int blocks = (int)(n8 / 256 < (int64_t)num_sms() * 8 ? (n8 + 255) / 256 : (int64_t)num_sms() * 8);
+  absmax_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(src, n8, ws_max);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scale_to_f16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(src, dst, n8, ws_max, scale);
+  return cudaGetLastError();
+}
 
 }  // namespace mtgr
 
@@ -607,10 +685,11 @@ cudaError_t launch_gln_bwd_noalloc(const T* dy, const T* x, const float* mean, c
   {
     TraceScope tr("gln_bwd", s);
     NCH_DISPATCH(D, ({
-                   auto k = gln_bwd_kernel<T, NCHV>;
+                   auto k = gln_bwd_kernel<T, T, NCHV>;
                    cudaError_t ea = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                    if (ea != cudaSuccess) return ea;
-                   k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage);
+                   k<<<nb, 256, smem, s>>>(dy, x, mean, rstd, gid, gamma, dres, dx, partial, rows, D, stage,
+                                           nullptr);
                  }));
   }
   cudaError_t e = cudaGetLastError();

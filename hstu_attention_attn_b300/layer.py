@@ -104,12 +104,14 @@ class HstuLayer:
         return self._ws
 
     def alloc_saved(self, T):
+        """Buffers the forward saves for the backward.  The bf16 layer keeps its
+        activations between steps in f16 (xn, silu'(z), [U|Q|K|V], O, y);
+        the fp32 layer in fp32."""
         HD = self.H * self.dh
-        e = lambda *s: torch.empty(*s, dtype=self.dtype, device=self.device)
+        a16 = torch.float16 if self.dtype == torch.bfloat16 else self.dtype
+        e = lambda *s: torch.empty(*s, dtype=a16, device=self.device)
         f = lambda *s: torch.empty(*s, dtype=torch.float32, device=self.device)
-        u16 = torch.float16 if self.dtype == torch.bfloat16 else self.dtype   # attention operands
-        return dict(xn=e(T, self.D), dsilu=e(T, 4 * HD), uqkv=torch.empty(T, 4 * HD, dtype=u16, device=self.device),
-                    o=torch.empty(T, HD, dtype=u16, device=self.device), y=e(T, HD),
+        return dict(xn=e(T, self.D), dsilu=e(T, 4 * HD), uqkv=e(T, 4 * HD), o=e(T, HD), y=e(T, HD),
                     gln_mean=f(T), gln_rstd=f(T), ln_mean=f(T), ln_rstd=f(T))
 
     def forward(self, x, db: DeviceBatch, saved=None, x_out=None):

@@ -20,9 +20,11 @@
  *   offsets[B] = T), ordered User*, Seq*, RealTime*, Cand* inside a user;
  *   gid[t] in {0 User, 1 Seq, 2 RealTime, 3 Cand} (uint8); ts[t] int64 seconds.
  *   Head h of a [T, H*d_h] activation occupies columns h*d_h .. h*d_h+d_h-1.
- * Types.  MTGR_BF16: activations and weights bf16, statistics fp32, weight /
- *   GLN-parameter gradients fp32, fp32 accumulation throughout (the attention's
- *   tensor-core operands and its saved output are f16).  MTGR_F16: the
+ * Types.  MTGR_BF16: the layer's inputs, outputs and weights bf16, statistics
+ *   fp32, weight / GLN-parameter gradients fp32, fp32 accumulation throughout;
+ *   inside the layer the tensor-core operands and everything saved or passed
+ *   between steps are f16 (11 significand bits against bf16's 8; see
+ *   mtgr_hstu_layer_bwd for the gradients' scaling).  MTGR_F16: the
  *   forward-only inference variant, f16 activations and weights.  MTGR_F32:
  *   everything fp32.  gamma/beta are fp32 in every mode.
  * Errors.  A non-zero mtgr_status means nothing was enqueued, except
@@ -242,14 +244,13 @@ typedef struct {
   float eps_ln;         /* 1e-5 */
 } mtgr_layer_weights;
 
-typedef struct {        /* written by the forward, read by the backward (dtype unless noted) */
+typedef struct {        /* written by the forward, read by the backward: f16 in the MTGR_BF16 and
+                           MTGR_F16 paths (11 significand bits between the steps), fp32 in MTGR_F32 */
   void* xn;             /* [T, D] GLN output */
   void* dsilu;          /* [T, 4*H*d_h] silu'(z) at the UQKV pre-activation z: the only
                            use the backward makes of z */
-  void* uqkv;           /* [T, 4*H*d_h] silu(z); f16 in the MTGR_BF16 path (the attention's
-                           tensor-core operands, 11 significand bits), fp32 in MTGR_F32 */
-  void* o;              /* [T, H*d_h] attention output before the gate: f16 in the MTGR_BF16
-                           path, fp32 in MTGR_F32 */
+  void* uqkv;           /* [T, 4*H*d_h] silu(z) (the attention's tensor-core operands) */
+  void* o;              /* [T, H*d_h] attention output before the gate */
   void* y;              /* [T, H*d_h] gate output */
   float* gln_mean;      /* [T] */
   float* gln_rstd;      /* [T] */
@@ -289,8 +290,11 @@ MTGR_API mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_
                                 void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
 
 /* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path.
- * In the MTGR_BF16 path the gradient of the gate's output, dY = dx_out · W_oᵀ,
- * is kept in f16 in the workspace (11 significand bits, like dO and dS). */
+ * MTGR_BF16: the layer runs its products on f16 operands (exact f16 copies of
+ * the bf16 weights, f16 activations) and carries its gradients in f16 scaled
+ * by a power of two s chosen from max|dx_out| (so that f16's range holds them
+ * whatever the loss scale; an all-zero or non-finite dx_out uses s = 1); dx,
+ * dw_*, dgamma and dbeta leave scaled back.  The scaling is exact. */
 MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* saved,
                                 const void* dx_out, void* dx, const mtgr_layer_grads* grads,
                                 const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
