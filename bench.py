@@ -94,6 +94,8 @@ def parse():
                     help="training-step batch: users are drawn until it holds at least this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads (MTGR-small attention, 22-layer stacks, inference sweep)")
     return ap.parse_args()
 
 
@@ -256,6 +258,118 @@ def workload_config(args, batch, H, dh, D=None):
             "tokens": int(batch.T), "users": int(batch.B), "n_heads": H, "d_h": dh,
             "l2": "inputs larger than L2", "parallelism": "replicas only"}
 
+
+
+# ---------------------------------------------------------------------------
+# The other workloads, measured after the headline timed region
+# ---------------------------------------------------------------------------
+def _event_ms(fn, iters, warmup=3):
+    import torch
+    for _ in range(warmup):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def _stack_weights(rng, n_layers, shape):
+    from hstu_attention_attn_b300 import synth
+    out = []
+    for _ in range(n_layers):
+        w_uqkv = synth.xavier(rng, shape.D, 4 * shape.H * shape.dh)
+        w_o = synth.xavier(rng, shape.H * shape.dh, shape.D)
+        gamma, beta = synth.gln_params(rng, shape.D)
+        out.append((w_uqkv, w_o, gamma, beta))
+    return out
+
+
+def _stack_graph_ms(weights, dtype, batch, x32, iters, dev):
+    """22-layer stack forward replayed from one CUDA Graph: (ms per replay, ms of one eager layer call)."""
+    import torch
+    from hstu_attention_attn_b300 import synth
+    from hstu_attention_attn_b300.layer import HstuLayer, HstuStack, device_batch
+    sh = synth.LARGE
+    layers = [HstuLayer(sh.D, sh.H, sh.dh, *(torch.from_numpy(w) for w in ws), dtype=dtype, device=dev)
+              for ws in weights]
+    db = device_batch(batch, dev)
+    x = x32.to(dtype)
+    stack = HstuStack(layers)
+    stack.forward(x, db)
+    stack.capture(x, db)
+    graph_ms = _event_ms(stack.replay, iters)
+    out = torch.empty_like(x)
+    layer_ms = _event_ms(lambda: layers[0].forward(x, db, stack._saved, out), iters)
+    return graph_ms, layer_ms
+
+
+def run_extras(dev, pk):
+    """MTGR-small-like attention fwd+bwd; the MTGR-large-like 22-layer stack
+    forward (128 users); the inference sweep over K candidates at batch 1 and 64
+    (22 layers, one user = 8 User + 1000 Seq + 64 RealTime + K candidates).
+    Device time by CUDA events on the launching stream, after warm-up."""
+    import torch
+    from hstu_attention_attn_b300 import mtgr, synth
+    from hstu_attention_attn_b300.layer import HstuAttention, device_batch
+    out = {}
+    # MTGR-small-like attention (64 users, 4 heads x 128), forward + backward
+    A = synth.small_attn(1)
+    db = device_batch(A.batch, dev)
+    cnt = torch.empty(A.batch.T, dtype=torch.int32, device=dev)
+    tot = torch.zeros(1, dtype=torch.int64, device=dev)
+    mtgr.mtgr_debug_visible_counts(db.offsets, db.gid, db.ts, A.batch.T, cnt, tot)
+    pairs = int(tot.item())
+    op = HstuAttention(A.H, A.dh, torch.bfloat16, device=dev)
+    q, k, v, u = (torch.from_numpy(m).to(dev).to(torch.bfloat16) for m in (A.q, A.k, A.v, A.u))
+    dy = torch.randn(A.batch.T, A.H * A.dh, device=dev, dtype=torch.bfloat16,
+                     generator=torch.Generator(dev).manual_seed(5))
+
+    def attn_step():
+        y, sv = op.forward(q, k, v, u, db)
+        op.backward(dy, q, k, v, u, sv, db)
+    ms = _event_ms(attn_step, 10)
+    fl = attention_useful_flops(pairs, A.H, A.dh)
+    out["small_attn"] = {"workload": f"MTGR-small-like attention fwd+bwd: {A.batch.B} users, {A.batch.T} tokens, "
+                                     f"{A.H} heads x d_h {A.dh}, bf16",
+                         "visible_pairs": pairs, "ms_per_step": ms,
+                         "useful_tflops": (fl["fwd"] + fl["bwd"]) / (ms * 1e-3) / 1e12,
+                         "frac_of_bf16_peak": (fl["fwd"] + fl["bwd"]) / (ms * 1e-3) / 1e12 / pk["bf16"]}
+    del op, q, k, v, u, dy
+    # MTGR-large-like 22-layer stack forward, 128 users
+    rng = np.random.default_rng(4)
+    sh = synth.LARGE
+    weights = _stack_weights(rng, 22, sh)
+    Lg = synth.large_layer(2)
+    x32 = torch.from_numpy(Lg.x).to(dev)
+    res = {}
+    for name, dt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        g_ms, l_ms = _stack_graph_ms(weights, dt, Lg.batch, x32, 10, dev)
+        res[name] = {"stack_ms": g_ms, "stack_tokens_per_s": Lg.batch.T / (g_ms * 1e-3), "layer_ms": l_ms,
+                     "tokens_per_s_per_layer": Lg.batch.T / (l_ms * 1e-3)}
+    out["large_stack_fwd"] = {"workload": f"MTGR-large-like 22-layer HSTU stack forward (CUDA Graph replay): "
+                                          f"{Lg.batch.B} users, {Lg.batch.T} tokens, d_model 1024, 8 heads x 128",
+                              **res}
+    del x32
+    # inference sweep: K candidates, batch 1 and 64 requests, 22 layers
+    sweep = []
+    for nb in (1, 64):
+        for K in (20, 50, 100, 200, 500):
+            batch = synth.make_batch(rng, synth.inference_users(K, nb))
+            x32 = torch.from_numpy(synth.normal(rng, (batch.T, sh.D))).to(dev)
+            row = {"requests": nb, "candidates_per_request": K, "tokens": int(batch.T)}
+            for name, dt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+                g_ms, _ = _stack_graph_ms(weights, dt, batch, x32, 10 if nb == 64 else 30, dev)
+                row[name] = {"latency_ms": g_ms, "candidates_per_s": nb * K / (g_ms * 1e-3)}
+            sweep.append(row)
+            del x32
+    out["inference_sweep"] = {"workload": "22-layer stack forward per request of 8 User + 1000 Seq + 64 RealTime "
+                                          "tokens + K candidates (CUDA Graph replay), d_model 1024, 8 heads x 128",
+                              "points": sweep}
+    return out
 
 # ---------------------------------------------------------------------------
 def run_mine(args):
@@ -486,6 +600,10 @@ def run_mine(args):
                           "flash_count_tflops": flash_flops / (attn_ms * 1e-3) / 1e12},
             "kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in sorted(trace.items(), key=lambda kv: -kv[1][0])},
             "gpu_launches": int(launches), "roofline": roof, "clocks": cl, "e2e": e2e}
+    if rank == 0 and not args.no_extras and args.workload == "large_train":
+        del layer, saved, x_out, dx, grads
+        torch.cuda.empty_cache()
+        line["other_workloads"] = run_extras(dev, pk)
     if rank == 0 and not args.no_cpu:
         try:
             line["cpu_baseline"] = {k: v for k, v in cpu_baseline(batch, H, dh).items() if k != "wall_s"}

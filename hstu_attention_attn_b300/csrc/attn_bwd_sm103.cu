@@ -33,8 +33,6 @@ namespace mtgr {
 namespace {
 using attn::BT;
 using attn::item_at;
-using attn::kmajor_desc;
-using attn::mnmajor_desc;
 using attn::packed_col;
 using attn::silu_and_grad_half;
 using attn::MRING;
@@ -124,17 +122,21 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
 
 // 16 (s, dp) pairs of one query row, keys j0 .. j0+15 -> 8 packed f16 values
 // of dS' = M ⊙ silu'(s c) ⊙ dp (dS without its factor c / n_u, which the dQ
-// output applies once per element).  Pairs go through the packed path (one
-// f16x2 tanh per pair, attn::silu_pair / dsilu_pair).
+// output applies once per element).
 __device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int j0,
-                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc, uint64_t hc2,
+                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc,
                                            uint32_t (&pk)[8]) {
   if (j0 + 16 <= u.eS) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      uint32_t h, t;
-      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
-      pk[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1])));
+      float v[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        v[t] = __uint_as_float(dr[2 * e + t]) * ds;
+      }
+      pk[e] = pack_f16x2(v[0], v[1]);
     }
   } else if (j0 >= u.eR) {
     const int ed = m.ri - j0;
@@ -155,16 +157,16 @@ __device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint3
     // stamp of key j0 + (lane & 15) (attn::rt_key_stamp), broadcast
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      bool vis[2];
+      float v[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int jj = j0 + 2 * e + t;
-        vis[t] = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
+        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        v[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds : 0.f;
       }
-      uint32_t h, t;
-      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
-      pk[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1]))) &
-              attn::keep_mask(vis[0], vis[1]);
+      pk[e] = pack_f16x2(v[0], v[1]);
     }
   }
 }
@@ -278,9 +280,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t k_addr = ring_addr + stage * Cfg::TILE;
           if (++stage == RING) { stage = 0; ph ^= 1; }
           tc_fence_after();
+          if (lane == 0) {
+            const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(k_addr);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            if (lane == 0) tc_mma_ss(tmem + Cfg::S_COL, kmajor_desc(q_addr, kk), kmajor_desc(k_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::S_COL, qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk), kd.hi,
+                          idesc_s, kk > 0 ? 1u : 0u);
+          }
           // dP = dO V_iᵀ overwrites the dS the previous dQ MMAs read
           if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int v_stage = stage;
@@ -292,10 +298,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dsr_pending = false;
           }
           tc_fence_after();
+          if (lane == 0) {
+            const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(v_addr);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            if (lane == 0) tc_mma_ss(tmem + Cfg::DP_COL, kmajor_desc(do_addr, kk), kmajor_desc(v_addr, kk), idesc_s,
-                      kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::DP_COL, od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk),
+                          vd.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
           if (lane == 0) tc_commit(&S.s_full);
           if (lane == 0) tc_commit(&S.ring_empty[v_stage]);
           if (i == nk - 1) if (lane == 0) tc_commit(&S.qdo_empty);
@@ -310,10 +319,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               dq_pending[qb] = false;
             }
             tc_fence_after();
+            if (lane == 0) {
+              const SmemDesc kd = attn::mnmajor_base(k_addr);
 #pragma unroll
-            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              if (lane == 0) tc_mma_ts(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), mnmajor_desc(k_addr, kk),
-                        idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+                tc_mma_ts_h(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), kd.lo + attn::mnmajor_step(kk),
+                            kd.hi, idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           if (!ok) break;
           if (lane == 0) tc_commit(&S.dsr_free);
@@ -333,7 +345,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     const float hc = 0.5f * p.scale;
-    const uint64_t hc2 = attn::f32x2(__float_as_uint(hc), __float_as_uint(hc));
     uint32_t s_waits = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
@@ -368,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld16(tmem + Cfg::S_COL + cb + 32 + lane_sel, sr[b ^ 1]);
               tmem_ld16(tmem + Cfg::DP_COL + cb + 32 + lane_sel, dr[b ^ 1]);
             }
-            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, hc2, pk);
+            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, pk);
             tmem_st8(tmem + Cfg::DP_COL + cb + lane_sel, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -510,36 +521,43 @@ __device__ __forceinline__ int64_t query_adj(const UserInfo& u, const int64_t* t
 // 16 (sᵀ, dpᵀ) pairs of one key row, query rows q0 .. q0+15 -> 8 packed f16
 // Pᵀ values (silu, without 1/n_u) and 8 packed dS'ᵀ values (silu'·dp, without
 // the factor c / n_u, which the dK output applies).  warp_us: every key of the
-// warp is User/Seq (warp-uniform).  Pairs go through the packed path.
+// warp is User/Seq (warp-uniform).
 __device__ __forceinline__ void pds_chunk_k(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int q0,
                                             const UserInfo& u, const KeyMask& k, bool warp_us, int64_t adj,
-                                            uint64_t hc2, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
+                                            float hc, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
   if (warp_us && q0 + 16 <= u.n) {
     // every key of the warp is User/Seq and every query row lies in the segment
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      uint32_t h, t;
-      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
-      pp[e] = sl;
-      pd[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1])));
+      float a[2], b[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        a[t] = sl;
+        b[t] = __uint_as_float(dr[2 * e + t]) * ds;
+      }
+      pp[e] = pack_f16x2(a[0], a[1]);
+      pd[e] = pack_f16x2(b[0], b[1]);
     }
   } else {
     // Query row ri sees a RealTime key stamped ts_j iff ts_j < adj_i (see
     // query_adj); adj holds adj_{q0 + (lane & 15)} and is broadcast.
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      bool vis[2];
+      float a[2], b[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int ri = q0 + 2 * e + t;
         const int64_t adj_i = attn::shfl_i64(adj, 2 * e + t);
-        vis[t] = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
+        const bool vis = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
+        float sl, ds;
+        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
+        a[t] = vis ? sl : 0.f;
+        b[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds : 0.f;
       }
-      const uint32_t mk = attn::keep_mask(vis[0], vis[1]);
-      uint32_t h, t;
-      const uint32_t sl = attn::silu_pair(sr[2 * e], sr[2 * e + 1], hc2, h, t);
-      pp[e] = sl & mk;
-      pd[e] = attn::hmul2(attn::dsilu_pair(sl, t), attn::cvt_f16x2(attn::f32x2(dr[2 * e], dr[2 * e + 1]))) & mk;
+      pp[e] = pack_f16x2(a[0], a[1]);
+      pd[e] = pack_f16x2(b[0], b[1]);
     }
   }
 }
@@ -656,9 +674,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             pt_pending = false;
           }
           tc_fence_after();
+          if (lane == 0) {
+            const SmemDesc kd = attn::kmajor_base(k_addr), qd = attn::kmajor_base(q_addr);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            if (lane == 0) tc_mma_ss(tmem + Cfg::ST_COL, kmajor_desc(k_addr, kk), kmajor_desc(q_addr, kk), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::ST_COL, kd.lo + attn::kmajor_step(kk), kd.hi, qd.lo + attn::kmajor_step(kk), qd.hi,
+                          idesc_s, kk > 0 ? 1u : 0u);
+          }
           // dPᵀ = V dO_iᵀ overwrites the dSᵀ the previous dK MMAs read
           if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
           const int do_stage = stage;
@@ -670,10 +692,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dst_pending = false;
           }
           tc_fence_after();
+          if (lane == 0) {
+            const SmemDesc vd = attn::kmajor_base(v_addr), od = attn::kmajor_base(do_addr);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            if (lane == 0) tc_mma_ss(tmem + Cfg::DPT_COL, kmajor_desc(v_addr, kk), kmajor_desc(do_addr, kk), idesc_s,
-                      kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::DPT_COL, vd.lo + attn::kmajor_step(kk), vd.hi, od.lo + attn::kmajor_step(kk),
+                          od.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
           if (lane == 0) tc_commit(&S.s_full);
           if (i == nq - 1) if (lane == 0) tc_commit(&S.kv_empty);
           // dV += Pᵀ dO_i, dK += dSᵀ Q_i, one quarter of the query rows at a time
@@ -687,18 +712,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               dkdv_pending = false;
             }
             tc_fence_after();
+            if (lane == 0) {
+              const SmemDesc od = attn::mnmajor_base(do_addr);
 #pragma unroll
-            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              if (lane == 0) tc_mma_ts(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), mnmajor_desc(do_addr, kk), idesc_g,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+                tc_mma_ts_h(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), od.lo + attn::mnmajor_step(kk),
+                            od.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            }
             if (qr == 3) {
               if (lane == 0) tc_commit(&S.pt_free);
               pt_pending = true;
             }
+            if (lane == 0) {
+              const SmemDesc qd = attn::mnmajor_base(q_addr);
 #pragma unroll
-            for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-              if (lane == 0) tc_mma_ts(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), mnmajor_desc(q_addr, kk), idesc_g,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
+                tc_mma_ts_h(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), qd.lo + attn::mnmajor_step(kk),
+                            qd.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            }
             if (qr == 3) {
               if (lane == 0) tc_commit(&S.dst_free);
               dst_pending = true;
@@ -721,7 +752,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
     const float hc = 0.5f * p.scale;
-    const uint64_t hc2 = attn::f32x2(__float_as_uint(hc), __float_as_uint(hc));
     uint32_t s_waits = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
@@ -764,7 +794,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld16(tmem + Cfg::ST_COL + cb + 32 + lane_sel, sr[b ^ 1]);
               tmem_ld16(tmem + Cfg::DPT_COL + cb + 32 + lane_sel, dr[b ^ 1]);
             }
-            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, q2 == 0 ? adj[b] : adj[2 + b], hc2, pp, pd);
+            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, q2 == 0 ? adj[b] : adj[2 + b], hc, pp, pd);
             tmem_st8(tmem + Cfg::ST_COL + cb + lane_sel, pp);
             tmem_st8(tmem + Cfg::DPT_COL + cb + lane_sel, pd);
             tmem_wait_st();

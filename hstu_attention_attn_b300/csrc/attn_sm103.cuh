@@ -22,6 +22,15 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
   return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
 }
 
+// The same descriptors as 32-bit halves, for issue loops that spend one add
+// per operand per MMA (the MMA warp shares its sub-partition with epilogue
+// warps, so every instruction of the issue loop competes for issue slots):
+// the base of a tile, plus the low-half step of k-step kk.
+__device__ __forceinline__ SmemDesc kmajor_base(uint32_t tile) { return smem_desc_sw128_h(tile, 16, 1024); }
+__device__ __forceinline__ SmemDesc mnmajor_base(uint32_t tile) { return smem_desc_sw128_h(tile, 16384, 1024); }
+__host__ __device__ constexpr uint32_t kmajor_step(int kk) { return (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2); }
+__host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return (uint32_t)(kk * 128); }
+
 // TMEM column (relative to the 128-column region of a score tile) of the
 // packed f16 operand for reduction step kk (rows/keys 16kk .. 16kk+15), when
 // the epilogue writes the 8 packed words of every 16-column chunk into the
@@ -53,67 +62,6 @@ __device__ __forceinline__ int item_at(int round) {
 
 // silu(x) with h = x/2: h + h tanh(h)  (σ(x) = (1 + tanh(x/2)) / 2)
 __device__ __forceinline__ float silu_half(float h) { return fmaf(h, tanh_approx(h), h); }
-
-// ---------------------------------------------------------------------------
-// Packed arithmetic of the score epilogues: two scores per instruction.  A
-// tcgen05.ld leaves the fp32 scores of consecutive columns in consecutive
-// registers; f32x2 operations (sm_100+) scale a pair at once, the pair is
-// rounded to one f16x2 word, and tanh.approx.f16x2 evaluates both hyperbolic
-// tangents in one MUFU operation, so a pair of scores costs one transcendental
-// instead of two.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t f32x2(uint32_t lo_bits, uint32_t hi_bits) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// (a.lo, a.hi) -> one f16x2 word, element 0 in the low half
-__device__ __forceinline__ uint32_t cvt_f16x2(uint64_t a) {
-  uint32_t lo, hi, r;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(a));
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
-  return r;
-}
-__device__ __forceinline__ uint32_t tanh_h2(uint32_t x) {
-  uint32_t y;
-  asm("tanh.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-constexpr uint32_t kH2Half = 0x38003800u;      // (0.5, 0.5) in f16x2
-constexpr uint32_t kH2MinusHalf = 0xB800B800u; // (-0.5, -0.5)
-
-// For two raw scores s (fp32 bits) and hs2 = (c/2, c/2) as f32x2 (c the score
-// scale): h = c s / 2 as f16x2, and silu(c s) = h + h tanh(h) as f16x2.
-__device__ __forceinline__ uint32_t silu_pair(uint32_t s0, uint32_t s1, uint64_t hs2, uint32_t& h, uint32_t& t) {
-  h = cvt_f16x2(mul_f32x2(f32x2(s0, s1), hs2));
-  t = tanh_h2(h);
-  return hfma2(h, t, h);
-}
-// With t = tanh(h) and the pair's silu: silu' = σ + silu (1 - σ), σ = (1 + t)/2.
-__device__ __forceinline__ uint32_t dsilu_pair(uint32_t silu, uint32_t t) {
-  const uint32_t sg = hfma2(t, kH2Half, kH2Half);
-  const uint32_t omsg = hfma2(t, kH2MinusHalf, kH2Half);
-  return hfma2(silu, omsg, sg);
-}
-// 32-bit mask word keeping element 0 (low half) and/or element 1 (high half)
-__device__ __forceinline__ uint32_t keep_mask(bool v0, bool v1) {
-  return (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
-}
 
 // For h = x/2: silu(x) and silu'(x) = σ(x)(1 + x(1 - σ(x))) = σ + silu (1 - σ).
 __device__ __forceinline__ void silu_and_grad_half(float h, float& silu, float& dsilu) {
