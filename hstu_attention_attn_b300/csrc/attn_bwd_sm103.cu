@@ -468,21 +468,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // =============================================================================
 // dK/dV kernel
 // =============================================================================
+// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue (thread = key
+// row; 4 lane quarters x 4 groups of 32 query columns), 18..21 output (TMEM ->
+// 16-bit dV then dK, one warp per lane quarter).
+constexpr int DKV_THREADS = 704;
+constexpr int DKV_EPI = 16;
+constexpr int DKV_OUT = 4;
+
 template <int D>
 struct DkvCfg {
   static constexpr int TILE = BT * D * 2;
-  static constexpr int K_OFF = 0, V_OFF = TILE, RING_OFF = 2 * TILE;
-  static constexpr int STG_OFF = RING_OFF + RING * TILE;
-  static constexpr int MR_OFF = STG_OFF + 4 * 2048;
-  static constexpr int BAR_OFF = MR_OFF + 4 * MRING * MSLOT;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
-  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  static constexpr int RING = D == 128 ? 4 : 8;  // Q / dO tiles in flight
+  static constexpr int K_OFF = 0, V_OFF = TILE, DS_OFF = 2 * TILE;
+  static constexpr int RING_OFF = DS_OFF + BT * BT * 2;  // dSᵀ: [128 keys][128 queries] f16
+  static constexpr int BAR_OFF = RING_OFF + RING * TILE;
+  static constexpr int SMEM = BAR_OFF + 512 + 1024;
+  // two 128-column score regions: Sᵀ (then Pᵀ) of query tile g in region g & 1,
+  // dPᵀ of tile g in the other one
+  __device__ static constexpr uint32_t r_col(int b) { return (uint32_t)b * 128u; }
+  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
 
 struct DkvBars {
   uint64_t kv_full, kv_empty;
-  uint64_t ring_full[RING], ring_empty[RING];
-  uint64_t s_full, ds_full[4], pt_free, dst_free, dkdv_full, dkdv_free;
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t s_full, dp_full, ds_ready, pv_done, dk_done, dkdv_full, dkdv_free;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -518,64 +528,63 @@ __device__ __forceinline__ int64_t query_adj(const UserInfo& u, const int64_t* t
   return (rq >= u.eS && rq < u.n) ? __ldg(ts_u + rq) + (rq < u.eR ? 1 : 0) : INT64_MIN;
 }
 
-// 16 (sᵀ, dpᵀ) pairs of one key row, query rows q0 .. q0+15 -> 8 packed f16
-// Pᵀ values (silu, without 1/n_u) and 8 packed dS'ᵀ values (silu'·dp, without
-// the factor c / n_u, which the dK output applies).  warp_us: every key of the
-// warp is User/Seq (warp-uniform).
-__device__ __forceinline__ void pds_chunk_k(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int q0,
-                                            const UserInfo& u, const KeyMask& k, bool warp_us, int64_t adj,
-                                            float hc, uint32_t (&pp)[8], uint32_t (&pd)[8]) {
+// 16 scores sᵀ of one key row, query rows q0 .. q0+15 -> 8 packed f16 Pᵀ
+// values (silu, without 1/n_u) and 8 packed f16 values of M ⊙ silu' (the
+// factor that dS'ᵀ = M ⊙ silu' ⊙ dPᵀ takes once dPᵀ is there; dS' leaves out
+// c / n_u, which the dK output applies).  warp_us: every key of the warp is
+// User/Seq (warp-uniform).  hc2: (c/2, c/2) as an f32 pair.
+__device__ __forceinline__ void p_chunk_k(const uint32_t (&sr)[16], int q0, const UserInfo& u, const KeyMask& k,
+                                          bool warp_us, int64_t adj, uint64_t hc2, uint32_t (&pp)[8],
+                                          uint32_t (&dsl)[8]) {
   if (warp_us && q0 + 16 <= u.n) {
     // every key of the warp is User/Seq and every query row lies in the segment
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float a[2], b[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        a[t] = sl;
-        b[t] = __uint_as_float(dr[2 * e + t]) * ds;
-      }
-      pp[e] = pack_f16x2(a[0], a[1]);
-      pd[e] = pack_f16x2(b[0], b[1]);
-    }
+    for (int e = 0; e < 8; ++e) attn::silu_pair_split(sr[2 * e], sr[2 * e + 1], hc2, pp[e], dsl[e]);
   } else {
     // Query row ri sees a RealTime key stamped ts_j iff ts_j < adj_i (see
     // query_adj); adj holds adj_{q0 + (lane & 15)} and is broadcast.
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float a[2], b[2];
+      bool vis[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int ri = q0 + 2 * e + t;
         const int64_t adj_i = attn::shfl_i64(adj, 2 * e + t);
-        const bool vis = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        a[t] = vis ? sl : 0.f;
-        b[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds : 0.f;
+        vis[t] = ((k.cls == 0) & (ri < u.n)) | ((k.cls == 1) & (k.ts_j < adj_i)) | ((k.cls == 2) & (ri == k.rj));
       }
-      pp[e] = pack_f16x2(a[0], a[1]);
-      pd[e] = pack_f16x2(b[0], b[1]);
+      attn::silu_pair_split(sr[2 * e], sr[2 * e + 1], hc2, pp[e], dsl[e]);
+      const uint32_t mk = attn::keep_mask(vis[0], vis[1]);
+      pp[e] &= mk;
+      dsl[e] &= mk;
     }
   }
 }
 
+// One item = (user, key tile, head): K and V stay in shared memory while the
+// query tiles that see the key tile stream through a ring (Q_i, then dO_i).
+// Per query tile g (counted over the CTA's items) the tensor core computes
+//   Sᵀ = K Q_gᵀ into TMEM region g & 1,  dPᵀ = V dO_gᵀ into region (g+1) & 1;
+// the epilogue writes Pᵀ = M ⊙ silu(Sᵀ c) (f16) over Sᵀ as soon as Sᵀ is there
+// (keeping M ⊙ silu' in registers), then, once dPᵀ is there, dS'ᵀ = M ⊙ silu'
+// ⊙ dPᵀ (f16) to shared memory; the tensor core adds
+//   dV += Pᵀ dO_g  (A from TMEM),  dK += dS'ᵀ Q_g  (A from shared memory).
+// Issue order per tile: S(g+1) into the region dPᵀ(g) has just left, dV(g),
+// dP(g+1) into the region Pᵀ(g) leaves once dV(g) has read it, then dK(g), so
+// the SiLU of tile g+1 runs while the tensor core works on tile g.
 template <int D, typename TG>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const BwdParams p) {
   using Cfg = DkvCfg<D>;
+  constexpr int RING = Cfg::RING;
   const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = base + Cfg::K_OFF;
   uint8_t* sV = base + Cfg::V_OFF;
+  uint8_t* sDS = base + Cfg::DS_OFF;
   uint8_t* sRing = base + Cfg::RING_OFF;
-  uint8_t* sStg = base + Cfg::STG_OFF;
-  uint8_t* sMr = base + Cfg::MR_OFF;
   DkvBars& S = *reinterpret_cast<DkvBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -587,11 +596,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&S.ring_empty[i], 1);
     }
     mbar_init(&S.s_full, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&S.ds_full[i], EPI_WARPS);
-    mbar_init(&S.pt_free, 1);
-    mbar_init(&S.dst_free, 1);
+    mbar_init(&S.dp_full, 1);
+    mbar_init(&S.ds_ready, DKV_EPI);
+    mbar_init(&S.pv_done, 1);
+    mbar_init(&S.dk_done, 1);
     mbar_init(&S.dkdv_full, 1);
-    mbar_init(&S.dkdv_free, 4);
+    mbar_init(&S.dkdv_free, DKV_OUT);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -613,8 +623,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   bool ok = true;
 
   if (warp == 0) {
-    {  // whole warp; lane 0 issues
-      // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      // ---------------- TMA producer: K, V per item; Q_i, dO_i per query tile ----------------
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
       for (int r = 0; ok; ++r) {
@@ -622,144 +632,155 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
         const int col_h = c.h * D;
-        if (!mbar_wait_warp_sleepy(&S.kv_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_sleepy(&S.kv_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
         ++n_items;
-        if (lane == 0) mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
+        mbar_arrive_expect_tx(&S.kv_full, 2 * Cfg::TILE);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          if (lane == 0) tma_load_2d(sK + cc * 16384, &tmK, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
-          if (lane == 0) tma_load_2d(sV + cc * 16384, &tmV, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+          tma_load_2d(sK + cc * 16384, &tmK, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
+          tma_load_2d(sV + cc * 16384, &tmV, &S.kv_full, col_h + 64 * cc, c.u.start + c.kt * BT);
         }
         const int nq = c.qs.count();
         for (int i = 0; i < nq && ok; ++i) {
           const int row = c.u.start + c.qs.qt(i, c.kt) * BT;
 #pragma unroll
           for (int which = 0; which < 2; ++which) {  // Q_i, then dO_i
-            if (!mbar_wait_warp_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
             uint8_t* dst = sRing + stage * Cfg::TILE;
-            if (lane == 0) mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-              if (lane == 0) tma_load_2d(dst + cc * 16384, which == 0 ? &tmQ : &tmdO, &S.ring_full[stage], col_h + 64 * cc, row);
+              tma_load_2d(dst + cc * 16384, which == 0 ? &tmQ : &tmdO, &S.ring_full[stage], col_h + 64 * cc, row);
             if (++stage == RING) { stage = 0; ph ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
-    {  // whole warp; lane 0 issues
+    if (lane == 0) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
       constexpr uint32_t idesc_g = idesc_f16_f32(BT, D, false, true);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ring_addr = smem_u32(sRing);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+      const uint32_t ring_addr = smem_u32(sRing);
       int stage = 0, n_items = 0;
-      uint32_t ph = 0, ds_waits[4] = {0, 0, 0, 0}, pt_waits = 0, dst_waits = 0, free_waits = 0;
-      bool pt_pending = false, dst_pending = false, dkdv_pending = false;
+      uint32_t ph = 0;
+      int g = 0;  // global query-tile count of this CTA
+      bool dkdv_pending = false;
+      // next ring stage (address, index), waiting until it is full
+      auto next_stage = [&](uint32_t& addr, int& st) -> bool {
+        if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
+        addr = ring_addr + stage * Cfg::TILE;
+        st = stage;
+        if (++stage == RING) { stage = 0; ph ^= 1; }
+        return true;
+      };
+      // Sᵀ(gt) = K Qᵀ into region gt & 1 (which held dPᵀ(gt - 1), already read)
+      auto issue_s = [&](int gt, uint32_t q_a) {
+        tc_fence_after();
+        const SmemDesc kd = attn::kmajor_base(k_addr), qd = attn::kmajor_base(q_a);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss_h(tmem + Cfg::r_col(gt & 1), kd.lo + attn::kmajor_step(kk), kd.hi, qd.lo + attn::kmajor_step(kk),
+                      qd.hi, idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&S.s_full);
+      };
+      // dPᵀ(gt) = V dOᵀ into region (gt + 1) & 1, once dV(gt - 1) has read Pᵀ(gt - 1) there
+      auto issue_dp = [&](int gt, uint32_t do_a) -> bool {
+        if (gt >= 1 && !mbar_wait(&S.pv_done, (gt - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const SmemDesc vd = attn::kmajor_base(v_addr), od = attn::kmajor_base(do_a);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss_h(tmem + Cfg::r_col((gt + 1) & 1), vd.lo + attn::kmajor_step(kk), vd.hi,
+                      od.lo + attn::kmajor_step(kk), od.hi, idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&S.dp_full);
+        return true;
+      };
       for (int r = 0; ok; ++r) {
         const int idx = item_at(r);
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
-        if (!mbar_wait_warp(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         const int nq = c.qs.count();
+        uint32_t q_a = 0, do_a = 0;
+        int q_s = 0, do_s = 0;
+        if (nq > 0) {
+          if (!next_stage(q_a, q_s)) { ok = false; break; }
+          issue_s(g, q_a);
+          if (!next_stage(do_a, do_s) || !issue_dp(g, do_a)) { ok = false; break; }
+        }
         for (int i = 0; i < nq && ok; ++i) {
-          // Sᵀ = K Q_iᵀ overwrites the Pᵀ the previous dV MMAs read
-          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
-          const int q_stage = stage;
-          const uint32_t q_addr = ring_addr + stage * Cfg::TILE;
-          if (++stage == RING) { stage = 0; ph ^= 1; }
-          if (pt_pending) {
-            if (!mbar_wait_warp(&S.pt_free, pt_waits & 1, abort_flag)) { ok = false; break; }
-            ++pt_waits;
-            pt_pending = false;
+          const int gi = g + i;
+          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag)) { ok = false; break; }
+          uint32_t q_n = 0, do_n = 0;
+          int q_ns = 0, do_ns = 0;
+          if (i + 1 < nq) {  // the next tile's scores while the epilogue starts on them
+            if (!next_stage(q_n, q_ns)) { ok = false; break; }
+            issue_s(gi + 1, q_n);
+          }
+          if (i == 0 && dkdv_pending) {  // the accumulators still hold the previous item
+            if (!mbar_wait(&S.dkdv_free, (n_items - 2) & 1, abort_flag)) { ok = false; break; }
+            dkdv_pending = false;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const SmemDesc kd = attn::kmajor_base(k_addr), qd = attn::kmajor_base(q_addr);
+          {  // dV += Pᵀ dO_g: Pᵀ packed in region g & 1 (query rows 16kk..: column 32(kk/2) + 8(kk%2))
+            const SmemDesc od = attn::mnmajor_base(do_a);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss_h(tmem + Cfg::ST_COL, kd.lo + attn::kmajor_step(kk), kd.hi, qd.lo + attn::kmajor_step(kk), qd.hi,
-                          idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < BT / 16; ++kk)
+              tc_mma_ts_h(tmem + Cfg::DV_COL, tmem + Cfg::r_col(gi & 1) + 32 * (kk >> 1) + 8 * (kk & 1),
+                          od.lo + attn::mnmajor_step(kk), od.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          // dPᵀ = V dO_iᵀ overwrites the dSᵀ the previous dK MMAs read
-          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
-          const int do_stage = stage;
-          const uint32_t do_addr = ring_addr + stage * Cfg::TILE;
-          if (++stage == RING) { stage = 0; ph ^= 1; }
-          if (dst_pending) {
-            if (!mbar_wait_warp(&S.dst_free, dst_waits & 1, abort_flag)) { ok = false; break; }
-            ++dst_waits;
-            dst_pending = false;
+          tc_commit(&S.pv_done);
+          // dP of the next tile goes into the region Pᵀ(g) leaves, as soon as dV(g)
+          // has read it, before dK(g), so that the epilogue gets it early
+          if (i + 1 < nq && (!next_stage(do_n, do_ns) || !issue_dp(gi + 1, do_n))) { ok = false; break; }
+          {  // dK += dS'ᵀ Q_g
+            const SmemDesc sd = attn::kmajor_base(ds_addr), qd = attn::mnmajor_base(q_a);
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::DK_COL, sd.lo + attn::kmajor_step(kk), sd.hi, qd.lo + attn::mnmajor_step(kk),
+                          qd.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const SmemDesc vd = attn::kmajor_base(v_addr), od = attn::kmajor_base(do_addr);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss_h(tmem + Cfg::DPT_COL, vd.lo + attn::kmajor_step(kk), vd.hi, od.lo + attn::kmajor_step(kk),
-                          od.hi, idesc_s, kk > 0 ? 1u : 0u);
+          tc_commit(&S.dk_done);
+          tc_commit(&S.ring_empty[q_s]);
+          tc_commit(&S.ring_empty[do_s]);
+          if (i + 1 < nq) {
+            q_a = q_n;
+            q_s = q_ns;
+            do_a = do_n;
+            do_s = do_ns;
           }
-          if (lane == 0) tc_commit(&S.s_full);
-          if (i == nq - 1) if (lane == 0) tc_commit(&S.kv_empty);
-          // dV += Pᵀ dO_i, dK += dSᵀ Q_i, one quarter of the query rows at a time
-#pragma unroll
-          for (int qr = 0; qr < 4; ++qr) {
-            if (!mbar_wait_warp(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
-            ++ds_waits[qr];
-            if (i == 0 && qr == 0 && dkdv_pending) {  // accumulators still hold the previous item
-              if (!mbar_wait_warp(&S.dkdv_free, free_waits & 1, abort_flag)) { ok = false; break; }
-              ++free_waits;
-              dkdv_pending = false;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-              const SmemDesc od = attn::mnmajor_base(do_addr);
-#pragma unroll
-              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-                tc_mma_ts_h(tmem + Cfg::DV_COL, tmem + Cfg::ST_COL + packed_col(kk), od.lo + attn::mnmajor_step(kk),
-                            od.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (qr == 3) {
-              if (lane == 0) tc_commit(&S.pt_free);
-              pt_pending = true;
-            }
-            if (lane == 0) {
-              const SmemDesc qd = attn::mnmajor_base(q_addr);
-#pragma unroll
-              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-                tc_mma_ts_h(tmem + Cfg::DK_COL, tmem + Cfg::DPT_COL + packed_col(kk), qd.lo + attn::mnmajor_step(kk),
-                            qd.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (qr == 3) {
-              if (lane == 0) tc_commit(&S.dst_free);
-              dst_pending = true;
-            }
-          }
-          if (!ok) break;
-          if (lane == 0) tc_commit(&S.ring_empty[q_stage]);
-          if (lane == 0) tc_commit(&S.ring_empty[do_stage]);
         }
         if (!ok) break;
-        if (nq == 0) if (lane == 0) tc_commit(&S.kv_empty);
-        if (lane == 0) tc_commit(&S.dkdv_full);
+        g += nq;
+        tc_commit(&S.dkdv_full);
+        tc_commit(&S.kv_empty);
         dkdv_pending = true;
       }
     }
-  } else if (warp < 2 + EPI_WARPS) {
-    // ---------------- Pᵀ / dSᵀ epilogue (thread = key row) ----------------
+  } else if (warp < 2 + DKV_EPI) {
+    // ---------------- Pᵀ / dS'ᵀ epilogue (thread = key row) ----------------
     const int ew = warp - 2;
-    const int g = ew >> 2;
+    const int qg = ew >> 2;  // group of 32 query columns
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const int kr = quarter * 32 + lane;  // key row inside the tile
     const float hc = 0.5f * p.scale;
-    uint32_t s_waits = 0;
+    const uint64_t hc2 = attn::f2(__float_as_uint(hc), __float_as_uint(hc));
+    // this thread's row of dS'ᵀ in the query box of this group; its 16-byte
+    // pieces 4 (qg & 1) .. +3 at their 128-byte-swizzle positions
+    uint8_t* ds_row = sDS + (qg >> 1) * 16384 + kr * 128;
+    const int jb = 4 * (qg & 1);
+    int g = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
       if (idx >= total) break;
       const DkvItem c = dkv_item(p, idx);
       const UserInfo& u = c.u;
       KeyMask km;
-      km.rj = c.kt * BT + quarter * 32 + lane;
+      km.rj = c.kt * BT + kr;
       km.cls = km.rj < u.eS ? 0 : (km.rj < u.eR ? 1 : (km.rj < u.n ? 2 : 3));
       km.ts_j = km.cls == 1 ? p.ts[u.start + km.rj] : 0;
       const bool warp_us = __all_sync(0xffffffffu, km.cls == 0);
@@ -767,112 +788,110 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t* ts_u = p.ts + u.start;
       const int nq = c.qs.count();
       for (int i = 0; i < nq && ok; ++i) {
-        const int q0 = c.qs.qt(i, c.kt) * BT;
+        const int gi = g + i;
+        const int q0 = c.qs.qt(i, c.kt) * BT + qg * 32;  // first query row of this warp's group
         // stamps of the query rows this lane broadcasts in the masked chunks,
         // loaded before the wait so that their latency is hidden
-        int64_t adj[4];
-#pragma unroll
-        for (int qr = 0; qr < 4; ++qr)
-          adj[qr] = any_rt ? query_adj(u, ts_u, q0 + 32 * qr + 16 * g + (lane & 15)) : INT64_MIN;
-        if (!mbar_wait(&S.s_full, s_waits & 1, abort_flag)) { ok = false; break; }
-        ++s_waits;
+        const int64_t adj0 = any_rt ? query_adj(u, ts_u, q0 + (lane & 15)) : INT64_MIN;
+        const int64_t adj1 = any_rt ? query_adj(u, ts_u, q0 + 16 + (lane & 15)) : INT64_MIN;
+        // phase 1: Pᵀ and M ⊙ silu' from Sᵀ
+        if (!mbar_wait(&S.s_full, gi & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // four quarters of 32 query columns; this warp takes 16 of each
-        // (pairs of quarters per loop trip keep the code small enough for the
-        // instruction cache; the buffer index stays static)
-        uint32_t sr[2][16], dr[2][16], pp[8], pd[8];
-        tmem_ld16(tmem + Cfg::ST_COL + 16 * g + lane_sel, sr[0]);
-        tmem_ld16(tmem + Cfg::DPT_COL + 16 * g + lane_sel, dr[0]);
+        const uint32_t t_s = tmem + Cfg::r_col(gi & 1) + qg * 32 + lane_sel;
+        const uint32_t t_d = tmem + Cfg::r_col((gi + 1) & 1) + qg * 32 + lane_sel;
+        uint32_t buf[2][16], pp[8], dsl[2][8];
+        tmem_ld16(t_s, buf[0]);
+        tmem_ld16(t_s + 16, buf[1]);
         tmem_wait_ld();
-#pragma unroll 1
-        for (int q2 = 0; q2 < 4; q2 += 2) {
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const int qr = q2 + b;
-            const int cb = 32 * qr + 16 * g;
-            if (qr < 3) {
-              tmem_ld16(tmem + Cfg::ST_COL + cb + 32 + lane_sel, sr[b ^ 1]);
-              tmem_ld16(tmem + Cfg::DPT_COL + cb + 32 + lane_sel, dr[b ^ 1]);
-            }
-            pds_chunk_k(sr[b], dr[b], q0 + cb, u, km, warp_us, q2 == 0 ? adj[b] : adj[2 + b], hc, pp, pd);
-            tmem_st8(tmem + Cfg::ST_COL + cb + lane_sel, pp);
-            tmem_st8(tmem + Cfg::DPT_COL + cb + lane_sel, pd);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.ds_full[qr]);
-            if (qr < 3) tmem_wait_ld();
-          }
+        for (int ch = 0; ch < 2; ++ch) {
+          p_chunk_k(buf[ch], q0 + 16 * ch, u, km, warp_us, ch ? adj1 : adj0, hc2, pp, dsl[ch]);
+          tmem_st8(t_s + 8 * ch, pp);  // Pᵀ over Sᵀ columns this warp has read
         }
+        // phase 2: dS'ᵀ = (M ⊙ silu') ⊙ dPᵀ, once dPᵀ is there and dK(gi - 1)
+        // has finished reading the shared dS'ᵀ tile
+        if (!mbar_wait(&S.dp_full, gi & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld16(t_d, buf[0]);
+        tmem_ld16(t_d + 16, buf[1]);
+        tmem_wait_ld();
+        if (gi >= 1 && !mbar_wait(&S.dk_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t pd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pd[e] = attn::ds_pair(dsl[ch][e], buf[ch][2 * e], buf[ch][2 * e + 1]);
+          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch) ^ (kr & 7)) * 16)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch + 1) ^ (kr & 7)) * 16)) =
+              make_uint4(pd[4], pd[5], pd[6], pd[7]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ds_ready);
       }
+      g += nq;
     }
   } else {
-    // ---------------- dK / dV output (thread = key row) ----------------
+    // ---------------- dV / dK output (thread = key row) ----------------
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
-    uint8_t* mr = sMr + (warp - 2 - EPI_WARPS) * (MRING * MSLOT);
     const bool has_m = p.m0 != nullptr && p.m1 != nullptr;
-    constexpr int NC = D / 32, NCH = 2 * NC;  // chunks: dV 0 .. NC-1, then dK
-    uint32_t full_waits = 0;
+    constexpr int NC = D / 32;
+    int n_items = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
       if (idx >= total) break;
       const DkvItem c = dkv_item(p, idx);
-      const int row0 = c.kt * BT + quarter * 32;
-      const int nvalid = c.u.n - row0;
+      const int rl = c.kt * BT + quarter * 32 + lane;  // this lane's key row, segment-relative
+      const bool row_ok = rl < c.u.n;
       const bool any = c.qs.count() > 0;
-      const int64_t rbase = (int64_t)c.u.start + row0;
+      const int64_t grow = (int64_t)c.u.start + rl;
       const float inv_n = 1.0f / (float)c.u.n;
-      const uint16_t* mvb = has_m ? p.m1 + rbase * p.ldm + c.h * D : nullptr;
-      const uint16_t* mkb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
-      if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
-#pragma unroll
-        for (int s = 0; s < MRING; ++s) {
-          mslot_fetch(mr + s * MSLOT, s < NC ? mvb + s * 32 : mkb + (s - NC) * 32, p.ldm, nvalid, lane);
-          cp_async_commit();
-        }
-        if (lane < nvalid) {
-          if (NC > MRING) prefetch_l2(mvb + lane * p.ldm + MRING * 32, (NC - MRING) * 64);
-          const int k0 = MRING > NC ? MRING - NC : 0;
-          prefetch_l2(mkb + lane * p.ldm + k0 * 32, (NC - k0) * 64);
-        }
+      if (has_m && row_ok) {
+        prefetch_l2(p.m1 + grow * p.ldm + c.h * D, D * 2);
+        prefetch_l2(p.m0 + grow * p.ldm + c.h * D, D * 2);
       }
-      if (!mbar_wait_sleepy(&S.dkdv_full, full_waits & 1, abort_flag)) { ok = false; break; }
-      ++full_waits;
+      if (!mbar_wait_sleepy(&S.dkdv_full, n_items & 1, abort_flag)) { ok = false; break; }
+      ++n_items;
       tc_fence_after();
-      int slot = 0;
 #pragma unroll 1
-      for (int ch = 0; ch < NCH; ++ch) {  // dV (P carries no 1/n_u), then dK
+      for (int ch = 0; ch < 2 * NC; ++ch) {  // dV chunks, then dK chunks
         const bool is_k = ch >= NC;
         const int cc = is_k ? ch - NC : ch;
         uint32_t rr[32];
         tmem_ld32(tmem + (is_k ? Cfg::DK_COL : Cfg::DV_COL) + cc * 32 + lane_sel, rr);
         tmem_wait_ld();
-        if (ch == NCH - 1) {
+        if (ch == 2 * NC - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.dkdv_free);
         }
-        const float sc = is_k ? p.scale * inv_n : inv_n;  // dK: the factor c / n_u left out of dSᵀ
+        if (!row_ok) continue;
+        // dV: Pᵀ carries no 1/n_u; dK: dS'ᵀ carries neither c nor 1/n_u
+        const float sc = is_k ? p.scale * inv_n : inv_n;
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
         if (has_m) {
-          cp_async_wait<MRING - 1>();
-          __syncwarp();
-          attn::mul_slot_32<TG>(x, mr + slot * MSLOT, lane);
-          __syncwarp();
-          const int nx = ch + MRING;
-          if (nx < NCH) mslot_fetch(mr + slot * MSLOT, nx < NC ? mvb + nx * 32 : mkb + (nx - NC) * 32, p.ldm, nvalid, lane);
-          cp_async_commit();
-          slot = slot == MRING - 1 ? 0 : slot + 1;
+          const uint16_t* mrow = (is_k ? p.m0 : p.m1) + grow * p.ldm + c.h * D + cc * 32;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 mm = *reinterpret_cast<const uint4*>(mrow + 8 * v);
+            const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              x[8 * v + 2 * t] *= lo16<TG>(w[t]);
+              x[8 * v + 2 * t + 1] *= hi16<TG>(w[t]);
+            }
+          }
         }
-        attn::store_rows16_32(x, stg, reinterpret_cast<TG*>((is_k ? p.g0 : p.g1) + rbase * p.ldg + c.h * D + cc * 32),
-                              p.ldg, nvalid, lane);
+        uint16_t* orow = (is_k ? p.g0 : p.g1) + grow * p.ldg + c.h * D + cc * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(orow + 8 * v) = pack8<TG>(x + 8 * v);
       }
     }
-    if (has_m) cp_async_wait<0>();
   }
 
   if (!ok) {
@@ -896,7 +915,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     auto kern = attn_bwd_dkdv_kernel<D, TG>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
+    kern<<<grid, DKV_THREADS, DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

@@ -71,6 +71,76 @@ __device__ __forceinline__ void silu_and_grad_half(float h, float& silu, float& 
   dsilu = fmaf(silu, 1.0f - sg, sg);
 }
 
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (f32x2 arithmetic, sm_100+): two scores per instruction
+// for everything but the transcendental, which stays one tanh.approx.f32 per
+// score (its f16x2 form evaluates no faster).  A tcgen05.ld leaves the scores
+// of consecutive columns in consecutive registers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_f16x2_2(uint64_t v) {
+  uint32_t lo, hi;
+  unf2(v, lo, hi);
+  return pack_f16x2(__uint_as_float(lo), __uint_as_float(hi));
+}
+// For raw scores s0, s1 and upstream products dp0, dp1 (fp32 bits) and the
+// pair (c/2, c/2): the packed f16 pairs silu(c s) and silu'(c s) dp, with
+// σ = (1 + tanh(c s / 2)) / 2, silu = c s σ, silu' = σ + silu (1 - σ).
+__device__ __forceinline__ void silu_dsilu_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1, uint64_t hc2,
+                                                uint32_t& p, uint32_t& ds) {
+  const uint64_t h = mul2(f2(s0, s1), hc2);
+  uint32_t h0, h1;
+  unf2(h, h0, h1);
+  const uint64_t t = f2(__float_as_uint(tanh_approx(__uint_as_float(h0))), __float_as_uint(tanh_approx(__uint_as_float(h1))));
+  const uint64_t half = f2(0x3F000000u, 0x3F000000u), mhalf = f2(0xBF000000u, 0xBF000000u);
+  const uint64_t sg = fma2(t, half, half);
+  const uint64_t sl = fma2(h, t, h);
+  const uint64_t omsg = fma2(t, mhalf, half);
+  const uint64_t dsl = fma2(sl, omsg, sg);
+  p = pack_f16x2_2(sl);
+  ds = pack_f16x2_2(mul2(dsl, f2(dp0, dp1)));
+}
+// The same in two steps, for an epilogue that has the scores before dP: from
+// the scores the packed f16 pairs silu(c s) and silu'(c s); later, with dp,
+// the packed f16 pair silu' dp.
+__device__ __forceinline__ void silu_pair_split(uint32_t s0, uint32_t s1, uint64_t hc2, uint32_t& p, uint32_t& dsl16) {
+  const uint64_t h = mul2(f2(s0, s1), hc2);
+  uint32_t h0, h1;
+  unf2(h, h0, h1);
+  const uint64_t t = f2(__float_as_uint(tanh_approx(__uint_as_float(h0))), __float_as_uint(tanh_approx(__uint_as_float(h1))));
+  const uint64_t half = f2(0x3F000000u, 0x3F000000u), mhalf = f2(0xBF000000u, 0xBF000000u);
+  const uint64_t sg = fma2(t, half, half);
+  const uint64_t sl = fma2(h, t, h);
+  const uint64_t omsg = fma2(t, mhalf, half);
+  p = pack_f16x2_2(sl);
+  dsl16 = pack_f16x2_2(fma2(sl, omsg, sg));
+}
+__device__ __forceinline__ uint32_t ds_pair(uint32_t dsl16, uint32_t dp0, uint32_t dp1) {
+  const uint64_t d = f2(__float_as_uint(f16_lo(dsl16)), __float_as_uint(f16_hi(dsl16)));
+  return pack_f16x2_2(mul2(d, f2(dp0, dp1)));
+}
+// 32-bit mask keeping element 0 (low half) and / or element 1 (high half) of a packed f16 pair
+__device__ __forceinline__ uint32_t keep_mask(bool v0, bool v1) {
+  return (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+}
+
 // A warp holds 32 consecutive rows (lane = row) x 32 values; write them as
 // the 16-bit type TG to rows row0 .. row0+31 of out (row stride ld elements),
 // skipping rows >= nvalid, through a 2 KB staging buffer so that each store
