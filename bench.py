@@ -40,10 +40,10 @@ METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/
 # traffic until it is captured again.
 TRAFFIC = {
     "attn_bwd": dict(file="hstu_attention_attn_b300/csrc/attn_bwd_sm103.cu",
-                     sha256="6b45b57320a07fe62324c5367b0972fd8a26ffe26c0b358dbffa838a2e6d21ff",
-                     bytes_per_pair=(568.65e6 + 148.29e6) / 24977261,
-                     note="ncu capture of the 40,960-token training batch (24,977,261 visible pairs), "
-                          "scaled by visible pairs"),
+                     sha256="3fb1f3e2b7de6152492e6ea6073eb3e346bd174edf0a9d1545801b0a32df597a",
+                     bytes_per_pair=(1828.66e6 + 518.46e6) / 82381761,
+                     note="ncu capture of the 131,297-token training batch (82,381,761 visible pairs, inputs "
+                          "larger than L2), scaled by visible pairs"),
 }
 
 
