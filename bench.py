@@ -369,6 +369,37 @@ def run_extras(dev, pk):
     out["inference_sweep"] = {"workload": "22-layer stack forward per request of 8 User + 1000 Seq + 64 RealTime "
                                           "tokens + K candidates (CUDA Graph replay), d_model 1024, 8 heads x 128",
                               "points": sweep}
+    # one request of K = 500 candidates scored in chunks of 100 against its history,
+    # encoded once (history pass + 5 chunk passes, one CUDA Graph), against one pass
+    from hstu_attention_attn_b300.layer import HstuLayer, HstuStack
+    K, chunk = 500, 100
+    batch = synth.make_batch(rng, synth.inference_users(K, 1))
+    n_hist = batch.T - K
+    x = torch.from_numpy(synth.normal(rng, (batch.T, sh.D))).to(dev).to(torch.bfloat16)
+    db = device_batch(batch, dev)
+    layers = [HstuLayer(sh.D, sh.H, sh.dh, *(torch.from_numpy(w) for w in ws), dtype=torch.bfloat16, device=dev)
+              for ws in weights]
+    stack = HstuStack(layers)
+    stack.score_chunked(x, db.gid, db.ts, n_hist, chunk)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        stack.score_chunked(x, db.gid, db.ts, n_hist, chunk)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        stack.score_chunked(x, db.gid, db.ts, n_hist, chunk)
+    chunked_ms = _event_ms(g.replay, 20)
+    whole_ms, _ = _stack_graph_ms(weights, torch.bfloat16, batch, x.float(), 20, dev)
+    # chunks without the cache: the whole stack on history + one chunk, once per chunk
+    b1 = synth.make_batch(rng, synth.inference_users(chunk, 1))
+    x1 = torch.from_numpy(synth.normal(rng, (b1.T, sh.D))).to(dev)
+    per_chunk_ms, _ = _stack_graph_ms(weights, torch.bfloat16, b1, x1, 20, dev)
+    out["chunked_scoring"] = {"workload": f"one request (8 User + 1000 Seq + 64 RealTime + {K} candidates), 22 layers, "
+                                          f"d_model 1024, bf16: history encoded once, candidates in chunks of {chunk}",
+                              "chunk": chunk, "chunked_ms": chunked_ms, "one_pass_ms": whole_ms,
+                              "chunks_recomputing_history_ms": per_chunk_ms * ((K + chunk - 1) // chunk),
+                              "candidates_per_s_chunked": K / (chunked_ms * 1e-3)}
     return out
 
 # ---------------------------------------------------------------------------

@@ -15,8 +15,12 @@
 namespace mtgr {
 
 // ---- launchers defined in the other translation units ----
-cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, UserInfo*, int32_t*, cudaStream_t);
-cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t, int32_t*, int32_t*, cudaStream_t);
+// n_norm: per-user n_u of the 1/n_u factor, q_begin: per-user first query row
+// the forward computes (device arrays; NULL = the segment length / 0)
+cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, UserInfo*, int32_t*, cudaStream_t,
+                             const int32_t* n_norm = nullptr, const int32_t* q_begin = nullptr);
+cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t, int32_t*, int32_t*, cudaStream_t,
+                        const int32_t* n_norm = nullptr, const int32_t* q_begin = nullptr);
 cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
                                   int64_t*, cudaStream_t);
 cudaError_t launch_expand_rows(const void*, const int32_t*, int64_t, void*, int64_t, int64_t, cudaStream_t);
@@ -289,15 +293,18 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
                                       const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d, float eps,
                                       void* y, __half* o, float* mean, float* rstd, uint8_t* ws,
                                       const AttnWs& w, cudaStream_t s, bool plan_ready = false,
-                                      bool y_f16 = false) {
+                                      bool y_f16 = false, const int32_t* n_norm = nullptr,
+                                      const int32_t* q_begin = nullptr, bool do_gate = true) {
   // plan_ready: an earlier call on the same batch left its status word and work
   // lists in this workspace (the layers of a stack share them)
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   if (!plan_ready) MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_fwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  if (!plan_ready) MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_fwd plan");
+  if (!plan_ready)
+    MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s, n_norm, q_begin), "attn_fwd plan");
   MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
+  if (!do_gate) return MTGR_OK;
   const int HD = H * d;
   cudaError_t e =
       y_f16   ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, static_cast<__half*>(y), mean, rstd, T, HD,
@@ -648,7 +655,8 @@ static mtgr_status check_layer(const mtgr_layer_weights* w, const int32_t* offse
 static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, void* x_out,
                                   const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
                                   const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
-                                  size_t workspace_bytes, mtgr_stream_t stream, bool plan_ready) {
+                                  size_t workspace_bytes, mtgr_stream_t stream, bool plan_ready,
+                                  const int32_t* n_norm = nullptr) {
   mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
   if (st != MTGR_OK) return st;
   REQUIRE(sv != nullptr, MTGR_ERR_INVALID_ARG, "saved is NULL");
@@ -711,7 +719,7 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
     const __half* a = static_cast<const __half*>(sv->uqkv);
     r = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, offsets, B, gid, ts, T, H, d, w->eps_ln,
                            sv->y, static_cast<__half*>(sv->o), sv->ln_mean, sv->ln_rstd, ws + L.attn_base, L.attn, s,
-                           plan_ready, /*y_f16=*/true);
+                           plan_ready, /*y_f16=*/true, n_norm);
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     r = mtgr_hstu_attn_fwd(a + HD, a + 2 * HD, a + 3 * HD, a, N4, offsets, B, gid, ts, T, H, d, w->eps_ln, sv->y,
@@ -912,6 +920,262 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   return mtgr_group_layernorm_bwd(dxn, x, sv->gln_mean, sv->gln_rstd, gid, w->gamma, dx_out, dx, gr->dgamma,
                                   gr->dbeta, T, D, dtype, ws + L.gln_part,
                                   mtgr_group_layernorm_bwd_workspace_size(T, D), stream);
+}
+
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Chunked candidate scoring of one request, the history encoded once
+// ---------------------------------------------------------------------------
+namespace mtgr {
+namespace {
+// meta[0..1] = offsets {0, T}, meta[2] = n_u, meta[3] = first query row; the
+// segment's group ids and stamps: history rows 0 .. n_hist-1, then candidates
+// c0 .. c0+c-1 of the request (rows n_hist + c0 .. of gid / ts).
+__global__ void chunk_meta_kernel(int32_t* meta, uint8_t* gid_out, int64_t* ts_out, const uint8_t* gid,
+                                  const int64_t* ts, int32_t n_hist, int32_t c0, int32_t c, int32_t n_total,
+                                  int32_t q0) {
+  const int T = n_hist + c;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i == 0) {
+    meta[0] = 0;
+    meta[1] = T;
+    meta[2] = n_total;
+    meta[3] = q0;
+  }
+  if (gid_out && i < T) {
+    const int src = i < n_hist ? i : n_hist + c0 + (i - n_hist);
+    gid_out[i] = gid[src];
+    ts_out[i] = ts[src];
+  }
+}
+
+struct ChunkWs {
+  size_t meta, gid, ts, layer, xn, dsilu, o, y, gstat, lstat, total;
+};
+// rows_a: rows of the attention segment; rows_c: rows of the projections
+static ChunkWs chunk_ws(int64_t rows_a, int64_t rows_c, int D, int H, int d, mtgr_dtype dt) {
+  ChunkWs w;
+  const int64_t HD = (int64_t)H * d;
+  size_t o = 0;
+  w.meta = o;
+  o += 256;
+  w.gid = o;
+  o += align256((size_t)rows_a);
+  w.ts = o;
+  o += align256((size_t)rows_a * 8);
+  w.layer = o;
+  o += layer_ws(1, rows_a, D, H, d, dt).total;
+  w.xn = o;
+  o += align256((size_t)rows_c * D * 2);
+  w.dsilu = o;
+  o += align256((size_t)rows_c * 4 * HD * 2);
+  w.o = o;
+  o += align256((size_t)rows_a * HD * 2);
+  w.y = o;
+  o += align256((size_t)rows_c * HD * 2);
+  w.gstat = o;
+  o += align256((size_t)rows_c * 8);
+  w.lstat = o;
+  o += align256((size_t)rows_a * 8);
+  w.total = o;
+  return w;
+}
+
+// Cache layout: every layer's [U|Q|K|V] rows (history, then one chunk), then
+// every layer's f16 copies of W_uqkv and W_o (used by the MTGR_BF16 path, made
+// once by the history call instead of once per chunk).
+static size_t cache_rows_bytes(int32_t n_layers, int32_t n_hist, int32_t chunk, int32_t H, int32_t d) {
+  return align256((size_t)n_layers * ((size_t)n_hist + chunk) * 4 * (size_t)H * d * 2);
+}
+static size_t cache_w16_bytes(int32_t D, int32_t H, int32_t d) {
+  const size_t N4 = 4 * (size_t)H * d;
+  return align256((size_t)D * N4 * 2) + align256((size_t)H * d * D * 2);
+}
+
+static mtgr_status check_chunked(const mtgr_layer_weights* w, int32_t n_layers, int32_t chunk, int32_t n_hist,
+                                 int32_t n_cand, mtgr_dtype dtype) {
+  REQUIRE(w != nullptr && n_layers >= 1, MTGR_ERR_INVALID_ARG, "weights is NULL or n_layers < 1");
+  REQUIRE(dtype == MTGR_BF16 || dtype == MTGR_F16, MTGR_ERR_UNSUPPORTED,
+          "chunked candidate scoring runs on the 16-bit tensor-core path (MTGR_BF16 or MTGR_F16)");
+  REQUIRE(n_hist >= 0 && n_cand >= 0 && chunk >= 1, MTGR_ERR_INVALID_ARG, "n_hist, n_cand >= 0 and chunk >= 1");
+  REQUIRE((int64_t)n_hist + chunk < (int64_t(1) << 30), MTGR_ERR_UNSUPPORTED, "request too long");
+  for (int32_t l = 1; l < n_layers; ++l)
+    REQUIRE(w[l].d_model == w[0].d_model && w[l].n_heads == w[0].n_heads && w[l].d_h == w[0].d_h,
+            MTGR_ERR_INVALID_ARG, "every layer must have the same d_model, n_heads and d_h");
+  return MTGR_OK;
+}
+}  // namespace
+}  // namespace mtgr
+
+extern "C" {
+
+size_t mtgr_stack_cache_size(int32_t n_layers, int32_t n_hist, int32_t chunk, int32_t d_model, int32_t n_heads,
+                             int32_t d_h) {
+  if (n_layers < 1 || n_hist < 0 || chunk < 1 || d_model <= 0 || n_heads <= 0 || d_h <= 0) return 0;
+  return cache_rows_bytes(n_layers, n_hist, chunk, n_heads, d_h) +
+         (size_t)n_layers * cache_w16_bytes(d_model, n_heads, d_h);
+}
+
+size_t mtgr_stack_chunk_workspace_size(int32_t n_hist, int32_t chunk, int32_t d_model, int32_t n_heads, int32_t d_h,
+                                       mtgr_dtype dtype) {
+  if (n_hist < 0 || chunk < 1 || d_model <= 0 || n_heads <= 0 || d_h <= 0) return 0;
+  const size_t a = chunk_ws(n_hist, n_hist, d_model, n_heads, d_h, dtype).total;
+  const size_t b = chunk_ws((int64_t)n_hist + chunk, chunk, d_model, n_heads, d_h, dtype).total;
+  return a > b ? a : b;
+}
+
+mtgr_status mtgr_hstu_stack_hist_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x_hist, void* act,
+                                     void* cache, int32_t chunk, const uint8_t* gid, const int64_t* ts, int32_t n_hist,
+                                     int32_t n_cand, mtgr_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     mtgr_stream_t stream) {
+  mtgr_status st = check_chunked(w, n_layers, chunk, n_hist, n_cand, dtype);
+  if (st != MTGR_OK) return st;
+  const int D = w->d_model, H = w->n_heads, d = w->d_h;
+  const int64_t HD = (int64_t)H * d, N4 = 4 * HD;
+  const ChunkWs C = chunk_ws(n_hist, n_hist, D, H, d, dtype);
+  REQUIRE(workspace && aligned16(workspace) &&
+              workspace_bytes >= mtgr_stack_chunk_workspace_size(n_hist, chunk, D, H, d, dtype),
+          MTGR_ERR_WORKSPACE, "workspace missing or smaller than mtgr_stack_chunk_workspace_size()");
+  REQUIRE(cache && aligned16(cache), MTGR_ERR_INVALID_ARG, "cache is NULL or not 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == MTGR_BF16) {  // the chunk calls use these f16 copies of the weights
+    uint8_t* wc = static_cast<uint8_t*>(cache) + cache_rows_bytes(n_layers, n_hist, chunk, H, d);
+    for (int32_t l = 0; l < n_layers; ++l) {
+      __half* cw = reinterpret_cast<__half*>(wc + (size_t)l * cache_w16_bytes(D, H, d));
+      MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w[l].w_uqkv), N4, cw, N4, D, (int)N4, s),
+                    "stack_hist W_uqkv f16");
+      MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w[l].w_o), D,
+                                       cw + align256((size_t)D * N4 * 2) / 2, D, HD, D, s),
+                    "stack_hist W_o f16");
+    }
+  }
+  if (n_hist == 0) return MTGR_OK;
+  REQUIRE(x_hist && act && gid && ts, MTGR_ERR_INVALID_ARG, "NULL pointer");
+  REQUIRE(aligned16(x_hist) && aligned16(act), MTGR_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + C.meta);
+  chunk_meta_kernel<<<1, 32, 0, s>>>(meta, nullptr, nullptr, gid, ts, n_hist, 0, 0, n_hist + n_cand, 0);
+  MTGR_CUDA_TRY(cudaGetLastError(), "stack_hist meta");
+  mtgr_layer_saved sv{};
+  sv.xn = ws + C.xn;
+  sv.dsilu = ws + C.dsilu;
+  sv.o = ws + C.o;
+  sv.y = ws + C.y;
+  sv.gln_mean = reinterpret_cast<float*>(ws + C.gstat);
+  sv.gln_rstd = sv.gln_mean + n_hist;
+  sv.ln_mean = reinterpret_cast<float*>(ws + C.lstat);
+  sv.ln_rstd = sv.ln_mean + n_hist;
+  const size_t act_half = align256((size_t)n_hist * D * 2);
+  const void* in = x_hist;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    void* out = static_cast<uint8_t*>(act) + (l & 1) * act_half;
+    sv.uqkv = static_cast<uint8_t*>(cache) + (size_t)l * ((size_t)n_hist + chunk) * N4 * 2;
+    // history rows see history rows only: their activations are those of the whole request, with its n_u
+    st = layer_fwd_impl(w + l, in, out, &sv, meta, 1, gid, ts, n_hist, dtype, ws + C.layer,
+                        layer_ws(1, n_hist, D, H, d, dtype).total, stream, l > 0, meta + 2);
+    if (st != MTGR_OK) return st;
+    in = out;
+  }
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_hstu_stack_cand_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x_cand, void* x_out,
+                                     void* act, void* cache, int32_t chunk, const uint8_t* gid, const int64_t* ts,
+                                     int32_t n_hist, int32_t n_cand, int32_t c0, int32_t c, mtgr_dtype dtype,
+                                     void* workspace, size_t workspace_bytes, mtgr_stream_t stream) {
+  mtgr_status st = check_chunked(w, n_layers, chunk, n_hist, n_cand, dtype);
+  if (st != MTGR_OK) return st;
+  REQUIRE(c >= 0 && c <= chunk && c0 >= 0 && (int64_t)c0 + c <= n_cand, MTGR_ERR_INVALID_ARG,
+          "the chunk must satisfy 0 <= c <= chunk and c0 + c <= n_cand");
+  const int D = w->d_model, H = w->n_heads, d = w->d_h;
+  const int64_t HD = (int64_t)H * d, N4 = 4 * HD;
+  const int64_t Tc = (int64_t)n_hist + c;
+  const ChunkWs C = chunk_ws(Tc, c, D, H, d, dtype);
+  REQUIRE(workspace && aligned16(workspace) &&
+              workspace_bytes >= mtgr_stack_chunk_workspace_size(n_hist, chunk, D, H, d, dtype),
+          MTGR_ERR_WORKSPACE, "workspace missing or smaller than mtgr_stack_chunk_workspace_size()");
+  if (c == 0) return MTGR_OK;
+  REQUIRE(x_cand && x_out && cache && gid && ts && (n_layers == 1 || act), MTGR_ERR_INVALID_ARG, "NULL pointer");
+  REQUIRE(x_cand != x_out && (n_layers == 1 || (act != x_cand && act != x_out)), MTGR_ERR_INVALID_ARG,
+          "x_cand, x_out and act must be distinct");
+  REQUIRE(aligned16(x_cand) && aligned16(x_out) && aligned16(act) && aligned16(cache), MTGR_ERR_INVALID_ARG,
+          "tensors must be 16-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + C.meta);
+  uint8_t* gid_c = ws + C.gid;
+  int64_t* ts_c = reinterpret_cast<int64_t*>(ws + C.ts);
+  chunk_meta_kernel<<<(unsigned)((Tc + 255) / 256), 256, 0, s>>>(meta, gid_c, ts_c, gid, ts, n_hist, c0, c,
+                                                                  n_hist + n_cand, n_hist);
+  MTGR_CUDA_TRY(cudaGetLastError(), "stack_cand meta");
+  const LayerWs L = layer_ws(1, Tc, D, H, d, dtype);
+  uint8_t* lws = ws + C.layer;
+  int32_t* status = reinterpret_cast<int32_t*>(lws + L.attn_base + L.attn.status);
+  __half* xn = reinterpret_cast<__half*>(ws + C.xn);
+  __half* o = reinterpret_cast<__half*>(ws + C.o);
+  __half* y = reinterpret_cast<__half*>(ws + C.y);
+  float* gmean = reinterpret_cast<float*>(ws + C.gstat);
+  float* lmean = reinterpret_cast<float*>(ws + C.lstat);
+  using bf = __nv_bfloat16;
+  const bool bf_io = dtype == MTGR_BF16;
+  const void* in = x_cand;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const mtgr_layer_weights& W = w[l];
+    void* out = ((n_layers - 1 - l) & 1) ? act : x_out;  // the last layer writes x_out
+    __half* a = reinterpret_cast<__half*>(static_cast<uint8_t*>(cache) + (size_t)l * ((size_t)n_hist + chunk) * N4 * 2);
+    const __half* wu16 = static_cast<const __half*>(W.w_uqkv);
+    const __half* wo16 = static_cast<const __half*>(W.w_o);
+    if (bf_io) {  // f16 copies made by the history call
+      const __half* cw = reinterpret_cast<const __half*>(static_cast<const uint8_t*>(cache) +
+                                                         cache_rows_bytes(n_layers, n_hist, chunk, H, d) +
+                                                         (size_t)l * cache_w16_bytes(D, H, d));
+      wu16 = cw;
+      wo16 = cw + align256((size_t)D * N4 * 2) / 2;
+    }
+    // 1. GLN of the candidate rows (group ids from the segment's candidate part)
+    cudaError_t e = bf_io ? launch_gln_fwd(static_cast<const bf*>(in), xn, gmean, gmean + c, gid_c + n_hist, W.gamma,
+                                           W.beta, c, D, W.eps_gln, s)
+                          : launch_gln_fwd(static_cast<const __half*>(in), xn, gmean, gmean + c, gid_c + n_hist,
+                                           W.gamma, W.beta, c, D, W.eps_gln, s);
+    if (e != cudaSuccess) return cuda_status(e, "cand gln");
+    // 2. [U|Q|K|V] of the candidates, appended to the cached history rows
+    {
+      GemmArgs g{};
+      g.M = c; g.N = N4; g.K = D;
+      g.A = reinterpret_cast<const bf*>(xn); g.lda = D; g.a_mn_major = false;
+      g.B = reinterpret_cast<const bf*>(wu16); g.ldb = N4; g.b_mn_major = true;
+      g.ab_f16 = true;
+      g.epi = EPI_SILU; g.C = a + (size_t)n_hist * N4; g.c_f16 = true; g.ldc = N4;
+      g.Z = reinterpret_cast<bf*>(ws + C.dsilu); g.ldz = N4; g.z_f16 = true;
+      g.splits = 1; g.status = status; g.name = "gemm_uqkv";
+      MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "cand uqkv gemm");
+    }
+    // 3. attention of the candidate query tiles over [history | chunk], n_u of the whole request
+    st = attn_fwd_bf16_core(a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, meta, 1, gid_c, ts_c, Tc, H, d, W.eps_ln,
+                            nullptr, o, nullptr, nullptr, lws + L.attn_base, L.attn, s, l > 0, true, meta + 2,
+                            meta + 3, /*do_gate=*/false);
+    if (st != MTGR_OK) return st;
+    // 4. LN(O) ⊙ U of the candidate rows
+    e = launch_ln_gate_fwd(o + (size_t)n_hist * HD, a + (size_t)n_hist * N4, N4, y, lmean, lmean + c, c, (int)HD,
+                           W.eps_ln, s);
+    if (e != cudaSuccess) return cuda_status(e, "cand gate");
+    // 5. x' = x + y·W_o
+    {
+      GemmArgs g{};
+      g.M = c; g.N = D; g.K = HD;
+      g.A = reinterpret_cast<const bf*>(y); g.lda = HD; g.a_mn_major = false;
+      g.B = reinterpret_cast<const bf*>(wo16); g.ldb = D; g.b_mn_major = true;
+      g.ab_f16 = true;
+      g.epi = EPI_RESIDUAL; g.C = out; g.c_f16 = !bf_io; g.ldc = D; g.R = static_cast<const bf*>(in); g.ldr = D;
+      g.r_f16 = !bf_io;
+      g.splits = 1; g.status = status; g.name = "gemm_out";
+      MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "cand out gemm");
+    }
+    in = out;
+  }
+  return MTGR_OK;
 }
 
 }  // extern "C"

@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row0 = c.qt * BT + quarter * 32;  // segment-relative first row of this warp
       const int nvalid = c.u.n - row0;
       const bool any = c.keys.count() > 0;
-      const float cn = p.scale / (float)c.u.n;  // the factor c / n_u left out of dS
+      const float cn = p.scale / (float)c.u.nu;  // the factor c / n_u left out of dS
       const int64_t rbase = (int64_t)c.u.start + row0;
       const uint16_t* mb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
       if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
       const bool row_ok = rl < c.u.n;
       const bool any = c.qs.count() > 0;
       const int64_t grow = (int64_t)c.u.start + rl;
-      const float inv_n = 1.0f / (float)c.u.n;
+      const float inv_n = 1.0f / (float)c.u.nu;
       if (has_m && row_ok) {
         prefetch_l2(p.m1 + grow * p.ldm + c.h * D, D * 2);
         prefetch_l2(p.m0 + grow * p.ldm + c.h * D, D * 2);

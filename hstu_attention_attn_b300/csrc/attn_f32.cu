@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(128) attn_f32_fwd_kernel(const float* __restri
       if (d < dh) acc[m] += p * v[j * ld + h * dh + d];
     }
   }
-  const float inv_n = 1.0f / (float)u.n;
+  const float inv_n = 1.0f / (float)u.nu;
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
     const int d = lane + 32 * m;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(128) attn_f32_bwd_dq_kernel(
   if (i < u.start || i >= u.start + u.n) return;
   const int ri = (int)(i - u.start);
   const float c = rsqrtf((float)dh);
-  const float inv_n = 1.0f / (float)u.n;
+  const float inv_n = 1.0f / (float)u.nu;
   float qv[NV], gv[NV], acc[NV];
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(128) attn_f32_bwd_dkdv_kernel(
   if (j < u.start || j >= u.start + u.n) return;
   const int rj = (int)(j - u.start);
   const float c = rsqrtf((float)dh);
-  const float inv_n = 1.0f / (float)u.n;
+  const float inv_n = 1.0f / (float)u.nu;
   float kv[NV], vv[NV], ak[NV], av[NV];
 #pragma unroll
   for (int m = 0; m < NV; ++m) {

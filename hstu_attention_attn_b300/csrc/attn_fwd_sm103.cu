@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
       if (!mbar_wait(&S.o_full[ob], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       if (grp * 32 < D) {
-        const float inv_n = 1.0f / (float)u.n;
+        const float inv_n = 1.0f / (float)u.nu;
         const int row0 = c.qt * BQ + quarter * 32;  // segment-relative first row of this warp
         uint32_t rr[32];
         tmem_ld32(tmem + Cfg::o_col(ob) + grp * 32 + lane_sel, rr);

@@ -9,7 +9,8 @@ namespace mtgr {
 // One warp per user: clamp the segment to [0, T], find the first RealTime and
 // first candidate token, and (optionally) check the metadata.
 __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B, const uint8_t* __restrict__ gid,
-                                 int64_t T, UserInfo* __restrict__ users, int32_t* __restrict__ status) {
+                                 int64_t T, UserInfo* __restrict__ users, int32_t* __restrict__ status,
+                                 const int32_t* __restrict__ n_norm, const int32_t* __restrict__ q_begin) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= B) return;
@@ -40,7 +41,9 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
   if (eR < eS) eR = eS;  // only with a bad group order; keeps eS <= eR <= n
   bits = __reduce_or_sync(0xffffffffu, bits);
   if (lane == 0) {
-    if (users) users[b] = UserInfo{(int32_t)s0, n, eS, eR};
+    const int nu = n_norm ? max(n_norm[b], 1) : n;
+    const int q0 = q_begin ? min(max(q_begin[b], 0), n) : 0;
+    if (users) users[b] = UserInfo{(int32_t)s0, n, eS, eR, nu, q0};
     if (status && bits) atomicOr(status, bits);
   }
 }
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     if (lane == 0) {
       atomicAdd(&hist[0][c], (singles ? nt : (nt + 1) / 2) * H);
       atomicAdd(&hist[1][c], nt * H);
-      atomicAdd(&hist[2][c], nt * H);
+      atomicAdd(&hist[2][c], (nt - u.q0 / kTile) * H);
     }
   }
   __syncthreads();
@@ -106,10 +109,11 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     const int np = singles ? nt : (nt + 1) / 2;  // forward items per head
     const int c = user_cost(u);
     int pf = 0, pb = 0, pq = 0;
+    const int t0 = u.q0 / kTile, nq = nt - t0;  // query tiles of the per-tile list
     if (lane == 0) {
       pf = atomicAdd(&hist[0][c], np * H);
       pb = atomicAdd(&hist[1][c], nt * H);
-      pq = atomicAdd(&hist[2][c], nt * H);
+      pq = atomicAdd(&hist[2][c], nq * H);
     }
     pf = __shfl_sync(0xffffffffu, pf, 0);
     pb = __shfl_sync(0xffffffffu, pb, 0);
@@ -121,8 +125,12 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     }
     for (int e = lane; e < nt * H; e += 32) {  // head e / nt, tile e % nt
       const int h = e / nt, t = e - h * nt;
-      const int64_t ob = (int64_t)pb + e, oq = (int64_t)pq + e;
+      const int64_t ob = (int64_t)pb + e;
       if (ob < max_items) bwd_items[ob] = WorkItem{b, t | (h << 16)};
+    }
+    for (int e = lane; e < nq * H; e += 32) {  // head e / nq, tile t0 + e % nq
+      const int h = e / nq, t = t0 + (e - h * nq);
+      const int64_t oq = (int64_t)pq + e;
       if (oq < max_items) dq_items[oq] = WorkItem{b, t | (h << 16)};
     }
   }
@@ -190,20 +198,20 @@ __global__ void visible_counts_kernel(const int32_t* __restrict__ offsets, const
 // Host wrappers (internal)
 // ---------------------------------------------------------------------------
 cudaError_t launch_user_info(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, UserInfo* users,
-                             int32_t* status, cudaStream_t s) {
+                             int32_t* status, cudaStream_t s, const int32_t* n_norm, const int32_t* q_begin) {
   if (B <= 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (int)(((int64_t)B * 32 + threads - 1) / threads);
   TraceScope tr("plan_users", s);
-  user_info_kernel<<<blocks, threads, 0, s>>>(offsets, B, gid, T, users, status);
+  user_info_kernel<<<blocks, threads, 0, s>>>(offsets, B, gid, T, users, status, n_norm, q_begin);
   return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, int32_t H, int32_t* ws,
-                        int32_t* status, cudaStream_t s) {
+                        int32_t* status, cudaStream_t s, const int32_t* n_norm, const int32_t* q_begin) {
   const PlanLayout L = plan_layout(B, T, H);
   UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
-  cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s);
+  cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s, n_norm, q_begin);
   if (e != cudaSuccess) return e;
   // single query tiles per forward item when even (T/128 + B) / 2 pairs per
   // head would not fill the SMs twice (short requests): twice the items

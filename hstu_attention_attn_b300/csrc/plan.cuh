@@ -21,9 +21,11 @@ constexpr int kTile = 128;
 
 struct UserInfo {
   int32_t start;  // first token (absolute)
-  int32_t n;      // tokens in the segment (n_u)
+  int32_t n;      // tokens in the segment
   int32_t eS;     // first RealTime token, segment-relative (== n if none after)
   int32_t eR;     // first candidate token, segment-relative
+  int32_t nu;     // n_u of the 1/n_u factor: n, unless the caller gives it
+  int32_t q0;     // first query row the forward computes (segment-relative; 0 unless given)
 };
 
 struct WorkItem {
@@ -137,7 +139,7 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T, int32_t 
   L.max_items = (T / kTile + (int64_t)B + 1) * (H > 0 ? H : 1);
   int64_t o = 0;
   L.users = o;
-  o += 4 * (int64_t)B;
+  o += 6 * (int64_t)B;
   L.counts = o;
   o += 4;
   L.fwd_items = o;

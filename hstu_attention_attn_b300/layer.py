@@ -181,6 +181,34 @@ class HstuStack:
             h = o
         return h
 
+    def score_chunked(self, x, gid, ts, n_hist, chunk):
+        """One ranking request scored in chunks of candidates with its history
+        encoded once: x [n_hist + n_cand, D] holds the request's rows (history
+        first), gid / ts its device metadata.  The history rows run through the
+        stack once (each layer's [U|Q|K|V] of the history kept in a cache); then
+        every chunk of `chunk` candidates runs through the stack against that
+        cache.  Returns the candidates' last-layer rows [n_cand, D], equal to
+        those of the whole request run at once."""
+        l0 = self.layers[0]
+        T, D = x.shape
+        n_cand = T - n_hist
+        H, dh = l0.H, l0.dh
+        dev = x.device
+        cache = torch.empty(max(mtgr.mtgr_stack_cache_size(len(self.layers), n_hist, chunk, D, H, dh), 256),
+                            dtype=torch.uint8, device=dev)
+        ws = workspace(mtgr.mtgr_stack_chunk_workspace_size(n_hist, chunk, D, H, dh, _dt(x.dtype)), dev)
+        half = (n_hist * D * x.element_size() + 255) // 256 * 256
+        act = torch.empty(2 * half // x.element_size() + 8, dtype=x.dtype, device=dev)
+        weights = [l.weights for l in self.layers]
+        mtgr.mtgr_hstu_stack_hist_fwd(weights, x[:n_hist], act, cache, chunk, gid, ts, n_hist, n_cand, ws)
+        out = torch.empty(n_cand, D, dtype=x.dtype, device=dev)
+        tmp = torch.empty(chunk, D, dtype=x.dtype, device=dev)
+        for c0 in range(0, n_cand, chunk):
+            c = min(chunk, n_cand - c0)
+            mtgr.mtgr_hstu_stack_cand_fwd(weights, x[n_hist + c0:n_hist + c0 + c], out[c0:c0 + c], tmp[:c], cache,
+                                          chunk, gid, ts, n_hist, n_cand, c0, ws)
+        return out
+
     def capture(self, x, db: DeviceBatch):
         """Capture the stack's forward on x (a static buffer the caller refills
         between replays) and db; returns the static output buffer."""

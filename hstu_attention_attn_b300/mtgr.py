@@ -81,6 +81,14 @@ EXPORTS = {
     "mtgr_hstu_stack_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                       C.POINTER(LayerSaved), C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
                                       C.c_int64, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "mtgr_stack_cache_size": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "mtgr_stack_chunk_workspace_size": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
+    "mtgr_hstu_stack_hist_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int,
+                                           C.c_void_p, C.c_size_t, C.c_void_p]),
+    "mtgr_hstu_stack_cand_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                           C.c_int32, C.c_int32, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
     "mtgr_hstu_layer_bwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.POINTER(LayerSaved), C.c_void_p,
                                       C.c_void_p, C.POINTER(LayerGrads), C.c_void_p, C.c_int32, C.c_void_p,
                                       C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -260,6 +268,34 @@ def mtgr_hstu_layer_fwd(weights: LayerWeights, x, x_out, saved: LayerSaved, offs
            lib().mtgr_hstu_layer_fwd(C.byref(weights), _p(x), _p(x_out), C.byref(saved), _p(offsets),
                                      offsets.numel() - 1, _p(gid), _p(ts), T, _dtype(x), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_stack_cache_size(n_layers, n_hist, chunk, d_model, n_heads, d_h) -> int:
+    return int(lib().mtgr_stack_cache_size(n_layers, n_hist, chunk, d_model, n_heads, d_h))
+
+
+def mtgr_stack_chunk_workspace_size(n_hist, chunk, d_model, n_heads, d_h, dtype) -> int:
+    return int(lib().mtgr_stack_chunk_workspace_size(n_hist, chunk, d_model, n_heads, d_h, dtype))
+
+
+def mtgr_hstu_stack_hist_fwd(weights, x_hist, act, cache, chunk, gid, ts, n_hist, n_cand, workspace, stream=None):
+    """History rows of one request through every layer (cache filled); weights: LayerWeights per layer."""
+    arr = (LayerWeights * len(weights))(*weights)
+    _check("mtgr_hstu_stack_hist_fwd",
+           lib().mtgr_hstu_stack_hist_fwd(arr, len(weights), _p(x_hist), _p(act), _p(cache), chunk, _p(gid), _p(ts),
+                                          n_hist, n_cand, _dtype(x_hist), _p(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mtgr_hstu_stack_cand_fwd(weights, x_cand, x_out, act, cache, chunk, gid, ts, n_hist, n_cand, c0, workspace,
+                             stream=None):
+    """One chunk of candidates (rows of x_cand) of the request through every layer against the cached history."""
+    arr = (LayerWeights * len(weights))(*weights)
+    _check("mtgr_hstu_stack_cand_fwd",
+           lib().mtgr_hstu_stack_cand_fwd(arr, len(weights), _p(x_cand), _p(x_out), _p(act), _p(cache), chunk,
+                                          _p(gid), _p(ts), n_hist, n_cand, c0, x_cand.shape[0], _dtype(x_cand),
+                                          _p(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
 
 
 def mtgr_hstu_stack_fwd(weights, x, x_out, act, saved: LayerSaved, offsets, gid, ts, T, workspace, stream=None):

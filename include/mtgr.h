@@ -289,6 +289,47 @@ MTGR_API mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_
                                 const uint8_t* gid, const int64_t* ts, int64_t T, mtgr_dtype dtype,
                                 void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
 
+/* Chunked candidate scoring of one ranking request, the history encoded once
+ * (paper-daily "MTGR：美团外卖生成式推荐Scaling Law落地实践", inference: the user
+ * profile and the thousand behaviour tokens are encoded once and every
+ * candidate shares that result; fun-rec chapter 7.3, §7.3.1).  A request is one
+ * user: n_hist history rows (User*, Seq*, RealTime*) followed by n_cand
+ * candidate rows; gid, ts: device [n_hist + n_cand] for the whole request.
+ * Under the dynamic mixed mask a history row sees history rows only and a
+ * candidate sees the history and itself, so the history's activations at every
+ * layer are those of the whole request, and a chunk of candidates scored
+ * against them gives exactly the rows it would get in the whole request.  n_u
+ * is the whole request's token count n_hist + n_cand in both calls.
+ * cache: device, mtgr_stack_cache_size() bytes, caller-owned: layer l's
+ * [U|Q|K|V] (f16, [n_hist + chunk][4*H*d_h]) at byte offset
+ * l * (n_hist + chunk) * 4*H*d_h * 2, history rows first, then room for one
+ * chunk; after all layers' rows, the f16 copies of every layer's weights that
+ * the MTGR_BF16 chunk calls use (made once by the history call).  The weights
+ * must not change between the history call and the chunk calls.
+ * Workspace: mtgr_stack_chunk_workspace_size().  MTGR_BF16 or MTGR_F16
+ * only (16-bit tensor-core path); same error rules as the layer calls.
+ *
+ * mtgr_hstu_stack_hist_fwd: the n_layers layers on the history rows; x_hist
+ *   [n_hist, D] (dtype); act: [2][n_hist, D] scratch (dtype, each half 256-byte
+ *   aligned in size).  Fills the history rows of every layer's cache.
+ * mtgr_hstu_stack_cand_fwd: the n_layers layers on candidates c0 .. c0+c-1
+ *   (c <= chunk): x_cand [c, D] -> x_out [c, D]; act: [c, D] scratch (dtype)
+ *   when n_layers > 1; x_cand, x_out, act distinct.  Overwrites the chunk rows
+ *   of the cache, so chunks run one after the other on one cache. */
+MTGR_API size_t mtgr_stack_cache_size(int32_t n_layers, int32_t n_hist, int32_t chunk, int32_t d_model,
+                                      int32_t n_heads, int32_t d_h);
+MTGR_API size_t mtgr_stack_chunk_workspace_size(int32_t n_hist, int32_t chunk, int32_t d_model, int32_t n_heads,
+                                                int32_t d_h, mtgr_dtype dtype);
+MTGR_API mtgr_status mtgr_hstu_stack_hist_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x_hist,
+                                              void* act, void* cache, int32_t chunk, const uint8_t* gid,
+                                              const int64_t* ts, int32_t n_hist, int32_t n_cand, mtgr_dtype dtype,
+                                              void* workspace, size_t workspace_bytes, mtgr_stream_t stream);
+MTGR_API mtgr_status mtgr_hstu_stack_cand_fwd(const mtgr_layer_weights* w, int32_t n_layers, const void* x_cand,
+                                              void* x_out, void* act, void* cache, int32_t chunk, const uint8_t* gid,
+                                              const int64_t* ts, int32_t n_hist, int32_t n_cand, int32_t c0,
+                                              int32_t c, mtgr_dtype dtype, void* workspace, size_t workspace_bytes,
+                                              mtgr_stream_t stream);
+
 /* dx_out: [T, D] upstream gradient; dx: [T, D] (dtype), includes the residual path.
  * MTGR_BF16: the layer runs its products on f16 operands (exact f16 copies of
  * the bf16 weights, f16 activations) and carries its gradients in f16 scaled

@@ -10,7 +10,7 @@
 int main() {
   int n, eS, eR;
   while (std::scanf("%d %d %d", &n, &eS, &eR) == 3) {
-    const mtgr::UserInfo u{0, n, eS, eR};
+    const mtgr::UserInfo u{0, n, eS, eR, n, 0};
     const int nt = mtgr::ceil_div(n, mtgr::kTile);
     std::printf("U %d %d %d %d\n", n, eS, eR, nt);
     for (int qt = 0; qt < nt; ++qt) {
