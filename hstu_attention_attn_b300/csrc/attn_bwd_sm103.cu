@@ -33,15 +33,8 @@ namespace mtgr {
 namespace {
 using attn::BT;
 using attn::item_at;
-using attn::packed_col;
 using attn::silu_and_grad_half;
-using attn::MRING;
-using attn::MSLOT;
-using attn::mslot_fetch;
 
-constexpr int NUM_THREADS = 448;  // 14 warps
-constexpr int EPI_WARPS = 8;
-constexpr int RING = 4;
 
 struct BwdParams {
   const UserInfo* users;
@@ -85,22 +78,30 @@ __device__ __forceinline__ RowMask row_mask(const UserInfo& u, const int64_t* ts
 // =============================================================================
 // dQ kernel
 // =============================================================================
+// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue (thread = query
+// row; 4 lane quarters x 4 groups of 32 key columns), 18..21 output (TMEM ->
+// 16-bit dQ, one warp per lane quarter).
+constexpr int DQ_THREADS = 704;
+constexpr int DQ_EPI = 16;
+constexpr int DQ_OUT = 4;
+
 template <int D>
 struct DqCfg {
   static constexpr int TILE = BT * D * 2;
-  static constexpr int Q_OFF = 0, DO_OFF = TILE, RING_OFF = 2 * TILE;
-  static constexpr int STG_OFF = RING_OFF + RING * TILE;  // 4 output warps x 2 KB
-  static constexpr int MR_OFF = STG_OFF + 4 * 2048;         // 4 output warps x multiplier ring
-  static constexpr int BAR_OFF = MR_OFF + 4 * MRING * MSLOT;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int RING = D == 128 ? 4 : 8;  // K / V tiles in flight
+  static constexpr int Q_OFF = 0, DO_OFF = TILE, DS_OFF = 2 * TILE;
+  static constexpr int RING_OFF = DS_OFF + BT * BT * 2;  // dS': [128 queries][128 keys] f16
+  static constexpr int BAR_OFF = RING_OFF + RING * TILE;
+  static constexpr int SMEM = BAR_OFF + 512 + 1024;
+  // S in columns [0, 128), dP in [128, 256), two dQ accumulators after them
   static constexpr uint32_t S_COL = 0, DP_COL = 128;
   __device__ static constexpr uint32_t dq_col(int b) { return 256u + (uint32_t)b * D; }
 };
 
 struct DqBars {
   uint64_t qdo_full, qdo_empty;
-  uint64_t ring_full[RING], ring_empty[RING];
-  uint64_t s_full, ds_full[4], dsr_free, dq_full[2], dq_free[2];
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t s_full, s_read, dp_full, ds_ready, dq_done, dq_full[2], dq_free[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -120,71 +121,65 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
   return c;
 }
 
-// 16 (s, dp) pairs of one query row, keys j0 .. j0+15 -> 8 packed f16 values
-// of dS' = M ⊙ silu'(s c) ⊙ dp (dS without its factor c / n_u, which the dQ
-// output applies once per element).
-__device__ __forceinline__ void ds_chunk_q(const uint32_t (&sr)[16], const uint32_t (&dr)[16], int j0,
-                                           const UserInfo& u, const RowMask& m, int64_t tk, float hc,
-                                           uint32_t (&pk)[8]) {
+// 16 scores of one query row, keys j0 .. j0+15 -> 8 packed f16 values of
+// M ⊙ silu'(s c) (the factor dS' = M ⊙ silu' ⊙ dP takes once dP is there; dS'
+// leaves out c / n_u, which the dQ output applies).  The chunk class depends
+// only on j0, so it is uniform across the warp.
+__device__ __forceinline__ void dsl_chunk_q(const uint32_t (&sr)[16], int j0, const UserInfo& u, const RowMask& m,
+                                            int64_t tk, float hc, uint64_t hc2, uint32_t (&dsl)[8]) {
   if (j0 + 16 <= u.eS) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float v[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        v[t] = __uint_as_float(dr[2 * e + t]) * ds;
-      }
-      pk[e] = pack_f16x2(v[0], v[1]);
-    }
+    for (int e = 0; e < 8; ++e) dsl[e] = attn::dsilu_pair(sr[2 * e], sr[2 * e + 1], hc2);
   } else if (j0 >= u.eR) {
+    // candidate keys (or keys past the segment): only the diagonal is visible
     const int ed = m.ri - j0;
     const bool diag = m.cand && m.row_ok && ed >= 0 && ed < 16;
-    float s_d = 0.f, dp_d = 0.f;
+    float s_d = 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      s_d = (e == ed) ? __uint_as_float(sr[e]) : s_d;
-      dp_d = (e == ed) ? __uint_as_float(dr[e]) : dp_d;
-    }
+    for (int e = 0; e < 16; ++e) s_d = (e == ed) ? __uint_as_float(sr[e]) : s_d;
     float sl, ds;
     silu_and_grad_half(s_d * hc, sl, ds);
-    const float vd = diag ? dp_d * ds : 0.f;
+    const float vd = diag ? ds : 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) pk[e] = pack_f16x2((2 * e == ed) ? vd : 0.f, (2 * e + 1 == ed) ? vd : 0.f);
+    for (int e = 0; e < 8; ++e) dsl[e] = pack_f16x2((2 * e == ed) ? vd : 0.f, (2 * e + 1 == ed) ? vd : 0.f);
   } else {
     // the chunk overlaps the RealTime keys: branch-free predicate; tk holds the
     // stamp of key j0 + (lane & 15) (attn::rt_key_stamp), broadcast
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float v[2];
+      bool vis[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int jj = j0 + 2 * e + t;
-        const bool vis = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
-        float sl, ds;
-        silu_and_grad_half(__uint_as_float(sr[2 * e + t]) * hc, sl, ds);
-        v[t] = vis ? __uint_as_float(dr[2 * e + t]) * ds : 0.f;
+        vis[t] = (jj < u.eS) | (attn::shfl_i64(tk, 2 * e + t) < m.thr) | (m.cand & (jj == m.ri));
       }
-      pk[e] = pack_f16x2(v[0], v[1]);
+      dsl[e] = attn::dsilu_pair(sr[2 * e], sr[2 * e + 1], hc2) & attn::keep_mask(vis[0], vis[1]);
     }
   }
 }
 
+// One item = (user, query tile, head): Q and dO stay in shared memory while
+// the key tiles the query tile sees stream through a ring (K_j, then V_j).
+// Per key tile j: S = Q K_jᵀ and dP = dO V_jᵀ (SS, fp32 in TMEM); the epilogue
+// turns S into M ⊙ silu' (kept in registers) and signals that S may be
+// overwritten, then, with dP, stores dS' = M ⊙ silu' ⊙ dP (f16) to shared
+// memory; dQ += dS' K_j (SS) accumulates in TMEM.  The issue order S(j+1) as
+// soon as S(j) has been read, dP(j+1) as soon as dP(j) has been read, then
+// dQ(j) keeps the epilogue, which the transcendental paces, busy.
 template <int D, typename TG>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdParams p) {
   using Cfg = DqCfg<D>;
+  constexpr int RING = Cfg::RING;
   const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + Cfg::Q_OFF;
   uint8_t* sdO = base + Cfg::DO_OFF;
+  uint8_t* sDS = base + Cfg::DS_OFF;
   uint8_t* sRing = base + Cfg::RING_OFF;
-  uint8_t* sStg = base + Cfg::STG_OFF;
-  uint8_t* sMr = base + Cfg::MR_OFF;
   DqBars& S = *reinterpret_cast<DqBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -196,11 +191,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&S.ring_empty[i], 1);
     }
     mbar_init(&S.s_full, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&S.ds_full[i], EPI_WARPS);
-    mbar_init(&S.dsr_free, 1);
+    mbar_init(&S.s_read, DQ_EPI);
+    mbar_init(&S.dp_full, 1);
+    mbar_init(&S.ds_ready, DQ_EPI);
+    mbar_init(&S.dq_done, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.dq_full[i], 1);
-      mbar_init(&S.dq_free[i], 4);
+      mbar_init(&S.dq_free[i], DQ_OUT);
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -223,8 +220,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   bool ok = true;
 
   if (warp == 0) {
-    {  // whole warp; lane 0 issues
-      // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      // ---------------- TMA producer: Q, dO per item; K_j, V_j per key tile ----------------
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
       for (int r = 0; ok; ++r) {
@@ -232,198 +229,207 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
         const int col_h = c.h * D;
-        if (!mbar_wait_warp_sleepy(&S.qdo_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_sleepy(&S.qdo_empty, (n_items & 1) ^ 1, abort_flag)) { ok = false; break; }
         ++n_items;
-        if (lane == 0) mbar_arrive_expect_tx(&S.qdo_full, 2 * Cfg::TILE);
+        mbar_arrive_expect_tx(&S.qdo_full, 2 * Cfg::TILE);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          if (lane == 0) tma_load_2d(sQ + cc * 16384, &tmQ, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
-          if (lane == 0) tma_load_2d(sdO + cc * 16384, &tmdO, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+          tma_load_2d(sQ + cc * 16384, &tmQ, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
+          tma_load_2d(sdO + cc * 16384, &tmdO, &S.qdo_full, col_h + 64 * cc, c.u.start + c.qt * BT);
         }
         const int nk = c.keys.count();
         for (int i = 0; i < nk && ok; ++i) {
           const int row = c.u.start + c.keys.kt(i, c.qt) * BT;
 #pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!mbar_wait_warp_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+          for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
+            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
             uint8_t* dst = sRing + stage * Cfg::TILE;
-            if (lane == 0) mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-              if (lane == 0) tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
+              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
             if (++stage == RING) { stage = 0; ph ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
-    {  // whole warp; lane 0 issues
+    if (lane == 0) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
       constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), ring_addr = smem_u32(sRing);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), ds_addr = smem_u32(sDS);
+      const uint32_t ring_addr = smem_u32(sRing);
       int stage = 0, n_items = 0;
-      uint32_t ph = 0, ds_waits[4] = {0, 0, 0, 0}, dsr_waits = 0, dqf_waits[2] = {0, 0};
-      bool dsr_pending = false, dq_pending[2] = {false, false};
+      uint32_t ph = 0;
+      int g = 0;  // global key-tile count of this CTA
+      bool dq_pending[2] = {false, false};
+      auto next_stage = [&](uint32_t& addr, int& st) -> bool {
+        if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
+        addr = ring_addr + stage * Cfg::TILE;
+        st = stage;
+        if (++stage == RING) { stage = 0; ph ^= 1; }
+        return true;
+      };
+      // S(gt) = Q K_gtᵀ once the epilogue has read S(gt - 1)
+      auto issue_s = [&](int gt, uint32_t k_a) -> bool {
+        if (gt >= 1 && !mbar_wait(&S.s_read, (gt - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(k_a);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss_h(tmem + Cfg::S_COL, qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk), kd.hi,
+                      idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&S.s_full);
+        return true;
+      };
+      // dP(gt) = dO V_gtᵀ once the epilogue has read dP(gt - 1) (it has, when dS'(gt - 1) is ready)
+      auto issue_dp = [&](int gt, uint32_t v_a, int v_s) -> bool {
+        if (gt >= 1 && !mbar_wait(&S.ds_ready, (gt - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(v_a);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss_h(tmem + Cfg::DP_COL, od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk), vd.hi,
+                      idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&S.dp_full);
+        tc_commit(&S.ring_empty[v_s]);  // V_gt has no other reader
+        return true;
+      };
       for (int r = 0; ok; ++r) {
         const int idx = item_at(r);
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
         const int qb = n_items & 1;
-        if (!mbar_wait_warp(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         const int nk = c.keys.count();
+        uint32_t k_a = 0, v_a = 0;
+        int k_s = 0, v_s = 0;
+        if (nk > 0) {
+          if (!next_stage(k_a, k_s) || !issue_s(g, k_a) || !next_stage(v_a, v_s) || !issue_dp(g, v_a, v_s)) {
+            ok = false;
+            break;
+          }
+        }
         for (int i = 0; i < nk && ok; ++i) {
-          // S = Q K_iᵀ (S columns are free: the epilogue read them before ds_full[1])
-          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
-          const int k_stage = stage;
-          const uint32_t k_addr = ring_addr + stage * Cfg::TILE;
-          if (++stage == RING) { stage = 0; ph ^= 1; }
-          tc_fence_after();
-          if (lane == 0) {
-            const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(k_addr);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss_h(tmem + Cfg::S_COL, qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk), kd.hi,
-                          idesc_s, kk > 0 ? 1u : 0u);
-          }
-          // dP = dO V_iᵀ overwrites the dS the previous dQ MMAs read
-          if (!mbar_wait_warp(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
-          const int v_stage = stage;
-          const uint32_t v_addr = ring_addr + stage * Cfg::TILE;
-          if (++stage == RING) { stage = 0; ph ^= 1; }
-          if (dsr_pending) {
-            if (!mbar_wait_warp(&S.dsr_free, dsr_waits & 1, abort_flag)) { ok = false; break; }
-            ++dsr_waits;
-            dsr_pending = false;
+          const int gi = g + i;
+          uint32_t k_n = 0, v_n = 0;
+          int k_ns = 0, v_ns = 0;
+          if (i + 1 < nk && (!next_stage(k_n, k_ns) || !issue_s(gi + 1, k_n))) { ok = false; break; }
+          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag)) { ok = false; break; }
+          if (i + 1 < nk && (!next_stage(v_n, v_ns) || !issue_dp(gi + 1, v_n, v_ns))) { ok = false; break; }
+          if (i == 0 && dq_pending[qb]) {  // this accumulator still holds an older item's dQ
+            // the drain of item n_items - 3 (the older item on this accumulator)
+            if (!mbar_wait(&S.dq_free[qb], ((n_items - 3) >> 1) & 1, abort_flag)) { ok = false; break; }
+            dq_pending[qb] = false;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(v_addr);
+          {  // dQ += dS' K_j
+            const SmemDesc sd = attn::kmajor_base(ds_addr), kd = attn::mnmajor_base(k_a);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss_h(tmem + Cfg::DP_COL, od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk),
-                          vd.hi, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < BT / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::dq_col(qb), sd.lo + attn::kmajor_step(kk), sd.hi, kd.lo + attn::mnmajor_step(kk),
+                          kd.hi, idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          if (lane == 0) tc_commit(&S.s_full);
-          if (lane == 0) tc_commit(&S.ring_empty[v_stage]);
-          if (i == nk - 1) if (lane == 0) tc_commit(&S.qdo_empty);
-          // dQ += dS K_i, one quarter of the keys at a time
-#pragma unroll
-          for (int qr = 0; qr < 4; ++qr) {
-            if (!mbar_wait_warp(&S.ds_full[qr], ds_waits[qr] & 1, abort_flag)) { ok = false; break; }
-            ++ds_waits[qr];
-            if (i == 0 && qr == 0 && dq_pending[qb]) {  // accumulator still holds an older item's dQ
-              if (!mbar_wait_warp(&S.dq_free[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
-              ++dqf_waits[qb];
-              dq_pending[qb] = false;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-              const SmemDesc kd = attn::mnmajor_base(k_addr);
-#pragma unroll
-              for (int kk = 2 * qr; kk < 2 * qr + 2; ++kk)
-                tc_mma_ts_h(tmem + Cfg::dq_col(qb), tmem + Cfg::DP_COL + packed_col(kk), kd.lo + attn::mnmajor_step(kk),
-                            kd.hi, idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          if (!ok) break;
-          if (lane == 0) tc_commit(&S.dsr_free);
-          dsr_pending = true;
-          if (lane == 0) tc_commit(&S.ring_empty[k_stage]);
+          tc_commit(&S.dq_done);
+          tc_commit(&S.ring_empty[k_s]);
+          k_a = k_n;
+          k_s = k_ns;
         }
         if (!ok) break;
-        if (nk == 0) if (lane == 0) tc_commit(&S.qdo_empty);
-        if (lane == 0) tc_commit(&S.dq_full[qb]);
+        g += nk;
+        tc_commit(&S.dq_full[qb]);
+        tc_commit(&S.qdo_empty);
         dq_pending[qb] = true;
       }
     }
-  } else if (warp < 2 + EPI_WARPS) {
-    // ---------------- dS epilogue (thread = query row) ----------------
+  } else if (warp < 2 + DQ_EPI) {
+    // ---------------- dS' epilogue (thread = query row) ----------------
     const int ew = warp - 2;
-    const int g = ew >> 2;  // 32-column block of each 64-column half
+    const int kg = ew >> 2;  // group of 32 key columns
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const int qr = quarter * 32 + lane;  // query row inside the tile
     const float hc = 0.5f * p.scale;
-    uint32_t s_waits = 0;
+    const uint64_t hc2 = attn::f2(__float_as_uint(hc), __float_as_uint(hc));
+    // this thread's row of dS' in the key box of this group; its 16-byte pieces
+    // 4 (kg & 1) .. +3 at their 128-byte-swizzle positions
+    uint8_t* ds_row = sDS + (kg >> 1) * 16384 + qr * 128;
+    const int jb = 4 * (kg & 1);
+    int g = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
       if (idx >= total) break;
       const DqItem c = dq_item(p, idx);
       const UserInfo& u = c.u;
-      const RowMask m = row_mask(u, p.ts, c.qt * BT + quarter * 32 + lane);
+      const RowMask m = row_mask(u, p.ts, c.qt * BT + qr);
       const int64_t* ts_u = p.ts + u.start;
       const int nk = c.keys.count();
       for (int i = 0; i < nk && ok; ++i) {
-        const int k0 = c.keys.kt(i, c.qt) * BT;
+        const int gi = g + i;
+        const int j0 = c.keys.kt(i, c.qt) * BT + kg * 32;  // first key of this warp's group
         // stamps of the keys this lane broadcasts, loaded before the wait
-        int64_t tk[4];
-#pragma unroll
-        for (int qr = 0; qr < 4; ++qr) tk[qr] = attn::rt_key_stamp(u, ts_u, k0 + 32 * qr + 16 * g, lane);
-        if (!mbar_wait(&S.s_full, s_waits & 1, abort_flag)) { ok = false; break; }
-        ++s_waits;
+        const int64_t tk0 = attn::rt_key_stamp(u, ts_u, j0, lane), tk1 = attn::rt_key_stamp(u, ts_u, j0 + 16, lane);
+        // phase 1: M ⊙ silu' from S
+        if (!mbar_wait(&S.s_full, gi & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // four quarters of 32 key columns; this warp takes 16 of each (block
-        // 2*qr + g); the next quarter's loads are in flight during the math
-        uint32_t sr[2][16], dr[2][16], pk[8];
-        tmem_ld16(tmem + Cfg::S_COL + 16 * g + lane_sel, sr[0]);
-        tmem_ld16(tmem + Cfg::DP_COL + 16 * g + lane_sel, dr[0]);
+        uint32_t buf[2][16], dsl[2][8];
+        tmem_ld16(tmem + Cfg::S_COL + kg * 32 + lane_sel, buf[0]);
+        tmem_ld16(tmem + Cfg::S_COL + kg * 32 + 16 + lane_sel, buf[1]);
         tmem_wait_ld();
-#pragma unroll 1
-        for (int q2 = 0; q2 < 4; q2 += 2) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_read);  // the tensor core may overwrite S
+        dsl_chunk_q(buf[0], j0, u, m, tk0, hc, hc2, dsl[0]);
+        dsl_chunk_q(buf[1], j0 + 16, u, m, tk1, hc, hc2, dsl[1]);
+        // phase 2: dS' = (M ⊙ silu') ⊙ dP to shared memory, once dQ(gi - 1) has read the previous dS'
+        if (!mbar_wait(&S.dp_full, gi & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld16(tmem + Cfg::DP_COL + kg * 32 + lane_sel, buf[0]);
+        tmem_ld16(tmem + Cfg::DP_COL + kg * 32 + 16 + lane_sel, buf[1]);
+        tmem_wait_ld();
+        if (gi >= 1 && !mbar_wait(&S.dq_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const int qr = q2 + b;
-            const int cb = 32 * qr + 16 * g;
-            if (qr < 3) {
-              tmem_ld16(tmem + Cfg::S_COL + cb + 32 + lane_sel, sr[b ^ 1]);
-              tmem_ld16(tmem + Cfg::DP_COL + cb + 32 + lane_sel, dr[b ^ 1]);
-            }
-            ds_chunk_q(sr[b], dr[b], k0 + cb, u, m, q2 == 0 ? tk[b] : tk[2 + b], hc, pk);
-            tmem_st8(tmem + Cfg::DP_COL + cb + lane_sel, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.ds_full[qr]);
-            if (qr < 3) tmem_wait_ld();
-          }
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t pd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pd[e] = attn::ds_pair(dsl[ch][e], buf[ch][2 * e], buf[ch][2 * e + 1]);
+          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch) ^ (qr & 7)) * 16)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch + 1) ^ (qr & 7)) * 16)) =
+              make_uint4(pd[4], pd[5], pd[6], pd[7]);
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ds_ready);
       }
+      g += nk;
     }
   } else {
     // ---------------- dQ output (thread = query row) ----------------
     const int quarter = warp & 3;
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    uint8_t* stg = sStg + (warp - 2 - EPI_WARPS) * 2048;
-    uint8_t* mr = sMr + (warp - 2 - EPI_WARPS) * (MRING * MSLOT);
     const bool has_m = p.m0 != nullptr;
     constexpr int NC = D / 32;
-    uint32_t dqf_waits[2] = {0, 0};
     int n_items = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
       if (idx >= total) break;
       const DqItem c = dq_item(p, idx);
       const int qb = n_items & 1;
+      const uint32_t par = (n_items >> 1) & 1;
       ++n_items;
-      const int row0 = c.qt * BT + quarter * 32;  // segment-relative first row of this warp
-      const int nvalid = c.u.n - row0;
+      const int rl = c.qt * BT + quarter * 32 + lane;  // this lane's query row, segment-relative
+      const bool row_ok = rl < c.u.n;
       const bool any = c.keys.count() > 0;
-      const float cn = p.scale / (float)c.u.nu;  // the factor c / n_u left out of dS
-      const int64_t rbase = (int64_t)c.u.start + row0;
-      const uint16_t* mb = has_m ? p.m0 + rbase * p.ldm + c.h * D : nullptr;
-      if (has_m) {  // chunks 0 .. MRING-1 into the ring, the rest of the rows into L2
-#pragma unroll
-        for (int s = 0; s < MRING; ++s) {
-          if (s < NC) mslot_fetch(mr + s * MSLOT, mb + s * 32, p.ldm, nvalid, lane);
-          cp_async_commit();
-        }
-        if (NC > MRING && lane < nvalid) prefetch_l2(mb + lane * p.ldm + MRING * 32, (NC - MRING) * 64);
-      }
-      if (!mbar_wait_sleepy(&S.dq_full[qb], dqf_waits[qb] & 1, abort_flag)) { ok = false; break; }
-      ++dqf_waits[qb];
+      const int64_t grow = (int64_t)c.u.start + rl;
+      const float cn = p.scale / (float)c.u.nu;  // the factor c / n_u left out of dS'
+      const uint16_t* mrow = has_m ? p.m0 + grow * p.ldm + c.h * D : nullptr;
+      if (has_m && row_ok) prefetch_l2(mrow, D * 2);
+      if (!mbar_wait_sleepy(&S.dq_full[qb], par, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      int slot = 0;
+      uint16_t* orow = p.g0 + grow * p.ldg + c.h * D;
 #pragma unroll 1
       for (int cc = 0; cc < NC; ++cc) {
         uint32_t rr[32];
@@ -434,23 +440,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.dq_free[qb]);
         }
+        if (!row_ok) continue;
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * cn : 0.f;
         if (has_m) {
-          cp_async_wait<MRING - 1>();
-          __syncwarp();
-          attn::mul_slot_32<TG>(x, mr + slot * MSLOT, lane);
-          __syncwarp();
-          if (cc + MRING < NC) mslot_fetch(mr + slot * MSLOT, mb + (cc + MRING) * 32, p.ldm, nvalid, lane);
-          cp_async_commit();
-          slot = slot == MRING - 1 ? 0 : slot + 1;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 mm = *reinterpret_cast<const uint4*>(mrow + cc * 32 + 8 * v);
+            const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              x[8 * v + 2 * t] *= lo16<TG>(w[t]);
+              x[8 * v + 2 * t + 1] *= hi16<TG>(w[t]);
+            }
+          }
         }
-        attn::store_rows16_32(x, stg, reinterpret_cast<TG*>(p.g0 + rbase * p.ldg + c.h * D + cc * 32), p.ldg, nvalid,
-                              lane);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(orow + cc * 32 + 8 * v) = pack8<TG>(x + 8 * v);
       }
     }
-    if (has_m) cp_async_wait<0>();
   }
 
   if (!ok) {
@@ -923,7 +932,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = attn_bwd_dq_kernel<D, TG>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NUM_THREADS, DqCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pq);
+  kern<<<grid, DQ_THREADS, DqCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pq);
   return cudaGetLastError();
 }
 

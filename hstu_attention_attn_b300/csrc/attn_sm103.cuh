@@ -1,7 +1,7 @@
 // attn_sm103.cuh -- device helpers shared by the tcgen05 attention kernels
 // (forward, dK/dV backward, dQ backward): shared-memory operand descriptors of
-// the 128-row tiles, the persistent item order, SiLU in tanh form and the
-// coalesced bf16 row store through a small per-warp staging buffer.
+// the 128-row tiles, the persistent item order, SiLU in tanh form and its
+// packed fp32-pair evaluation.
 #pragma once
 #include "common.cuh"
 #include "plan.cuh"
@@ -12,31 +12,18 @@ namespace attn {
 constexpr int BT = 128;  // rows of every query / key tile
 
 // Shared-memory descriptors of a [128 rows][D] 16-bit tile staged as D/64
-// TMA boxes of [128][64] with 128-byte swizzle (16 KB per box).
-// K-major use (the reduction runs along the D columns), k-step kk of 16:
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-}
-// MN-major use (the reduction runs along the 128 rows), k-step kk of 16 rows:
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + kk * 2048, 16384, 1024);
-}
-
-// The same descriptors as 32-bit halves, for issue loops that spend one add
-// per operand per MMA (the MMA warp shares its sub-partition with epilogue
-// warps, so every instruction of the issue loop competes for issue slots):
-// the base of a tile, plus the low-half step of k-step kk.
+// TMA boxes of [128][64] with 128-byte swizzle (16 KB per box), as 32-bit
+// halves: K-major use (the reduction runs along the D columns, k-step kk of 16
+// at byte offset (kk/4)*16384 + (kk%4)*32) and MN-major use (the reduction runs
+// along the 128 rows, k-step kk at kk*2048, 64-element MN blocks 16 KB apart).
+// An issue loop spends one add per operand per MMA (the MMA warp shares its
+// sub-partition with epilogue warps, so every instruction of the issue loop
+// competes for issue slots): the base of a tile, plus the low-half step of
+// k-step kk.
 __device__ __forceinline__ SmemDesc kmajor_base(uint32_t tile) { return smem_desc_sw128_h(tile, 16, 1024); }
 __device__ __forceinline__ SmemDesc mnmajor_base(uint32_t tile) { return smem_desc_sw128_h(tile, 16384, 1024); }
 __host__ __device__ constexpr uint32_t kmajor_step(int kk) { return (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2); }
 __host__ __device__ constexpr uint32_t mnmajor_step(int kk) { return (uint32_t)(kk * 128); }
-
-// TMEM column (relative to the 128-column region of a score tile) of the
-// packed f16 operand for reduction step kk (rows/keys 16kk .. 16kk+15), when
-// the epilogue writes the 8 packed words of every 16-column chunk into the
-// first 8 columns of that chunk (so that no warp overwrites columns another
-// warp has yet to read).
-__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(16 * kk); }
 
 // 64-bit warp broadcast from lane src.
 __device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
@@ -100,25 +87,9 @@ __device__ __forceinline__ uint32_t pack_f16x2_2(uint64_t v) {
   unf2(v, lo, hi);
   return pack_f16x2(__uint_as_float(lo), __uint_as_float(hi));
 }
-// For raw scores s0, s1 and upstream products dp0, dp1 (fp32 bits) and the
-// pair (c/2, c/2): the packed f16 pairs silu(c s) and silu'(c s) dp, with
-// σ = (1 + tanh(c s / 2)) / 2, silu = c s σ, silu' = σ + silu (1 - σ).
-__device__ __forceinline__ void silu_dsilu_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1, uint64_t hc2,
-                                                uint32_t& p, uint32_t& ds) {
-  const uint64_t h = mul2(f2(s0, s1), hc2);
-  uint32_t h0, h1;
-  unf2(h, h0, h1);
-  const uint64_t t = f2(__float_as_uint(tanh_approx(__uint_as_float(h0))), __float_as_uint(tanh_approx(__uint_as_float(h1))));
-  const uint64_t half = f2(0x3F000000u, 0x3F000000u), mhalf = f2(0xBF000000u, 0xBF000000u);
-  const uint64_t sg = fma2(t, half, half);
-  const uint64_t sl = fma2(h, t, h);
-  const uint64_t omsg = fma2(t, mhalf, half);
-  const uint64_t dsl = fma2(sl, omsg, sg);
-  p = pack_f16x2_2(sl);
-  ds = pack_f16x2_2(mul2(dsl, f2(dp0, dp1)));
-}
-// The same in two steps, for an epilogue that has the scores before dP: from
-// the scores the packed f16 pairs silu(c s) and silu'(c s); later, with dp,
+// In two steps, for an epilogue that has the scores before dP: from raw scores
+// s0, s1 (fp32 bits) and hc2 = (c/2, c/2) the packed f16 pairs silu(c s) and
+// silu'(c s) = σ + silu (1 - σ), σ = (1 + tanh(c s / 2)) / 2; later, with dp,
 // the packed f16 pair silu' dp.
 __device__ __forceinline__ void silu_pair_split(uint32_t s0, uint32_t s1, uint64_t hc2, uint32_t& p, uint32_t& dsl16) {
   const uint64_t h = mul2(f2(s0, s1), hc2);
@@ -132,6 +103,18 @@ __device__ __forceinline__ void silu_pair_split(uint32_t s0, uint32_t s1, uint64
   p = pack_f16x2_2(sl);
   dsl16 = pack_f16x2_2(fma2(sl, omsg, sg));
 }
+// silu'(c s) alone, as a packed f16 pair
+__device__ __forceinline__ uint32_t dsilu_pair(uint32_t s0, uint32_t s1, uint64_t hc2) {
+  const uint64_t h = mul2(f2(s0, s1), hc2);
+  uint32_t h0, h1;
+  unf2(h, h0, h1);
+  const uint64_t t = f2(__float_as_uint(tanh_approx(__uint_as_float(h0))), __float_as_uint(tanh_approx(__uint_as_float(h1))));
+  const uint64_t half = f2(0x3F000000u, 0x3F000000u), mhalf = f2(0xBF000000u, 0xBF000000u);
+  const uint64_t sg = fma2(t, half, half);
+  const uint64_t sl = fma2(h, t, h);
+  const uint64_t omsg = fma2(t, mhalf, half);
+  return pack_f16x2_2(fma2(sl, omsg, sg));
+}
 __device__ __forceinline__ uint32_t ds_pair(uint32_t dsl16, uint32_t dp0, uint32_t dp1) {
   const uint64_t d = f2(__float_as_uint(f16_lo(dsl16)), __float_as_uint(f16_hi(dsl16)));
   return pack_f16x2_2(mul2(d, f2(dp0, dp1)));
@@ -139,71 +122,6 @@ __device__ __forceinline__ uint32_t ds_pair(uint32_t dsl16, uint32_t dp0, uint32
 // 32-bit mask keeping element 0 (low half) and / or element 1 (high half) of a packed f16 pair
 __device__ __forceinline__ uint32_t keep_mask(bool v0, bool v1) {
   return (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
-}
-
-// A warp holds 32 consecutive rows (lane = row) x 32 values; write them as
-// the 16-bit type TG to rows row0 .. row0+31 of out (row stride ld elements),
-// skipping rows >= nvalid, through a 2 KB staging buffer so that each store
-// instruction writes 8 rows x 64 contiguous bytes.
-template <typename TG>
-__device__ __forceinline__ void store_rows16_32(const float (&x)[32], uint8_t* stg, TG* out, int64_t ld, int nvalid,
-                                                int lane) {
-  __syncwarp();
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    uint4 w;
-    w.x = pack2<TG>(x[8 * v + 0], x[8 * v + 1]);
-    w.y = pack2<TG>(x[8 * v + 2], x[8 * v + 3]);
-    w.z = pack2<TG>(x[8 * v + 4], x[8 * v + 5]);
-    w.w = pack2<TG>(x[8 * v + 6], x[8 * v + 7]);
-    *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
-  }
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
-    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16));
-    if (r < nvalid) *reinterpret_cast<uint4*>(out + (int64_t)r * ld + c4 * 8) = w;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Multiplier chunks of an output warp, fetched ahead of use.  The output warps
-// may multiply each [32 rows][32 columns] gradient chunk elementwise by the
-// same block of a 16-bit multiplier (the layer passes silu'(z) of its UQKV
-// projection); a plain per-chunk load would put one HBM round trip per chunk
-// on the path that frees the TMEM accumulators, so the chunks go through a
-// ring of MRING shared slots (2 KB each, rows of 64 bytes with the 16-byte
-// pieces XOR-swizzled by (row >> 1) & 3, conflict-free for both the coalesced
-// fill and the row-per-lane read) filled with cp.async.
-// ---------------------------------------------------------------------------
-constexpr int MRING = 3;
-constexpr int MSLOT = 2048;
-
-// Copy rows 0 .. nvalid-1 (at most 32) of a [32][32] 16-bit block (row stride
-// ld elements) into a ring slot; one commit group per call is left to the caller.
-__device__ __forceinline__ void mslot_fetch(uint8_t* slot, const uint16_t* src, int64_t ld, int nvalid, int lane) {
-  const uint32_t s = smem_u32(slot);
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int r = it * 8 + (lane >> 2), c4 = lane & 3;
-    if (r < nvalid) cp_async16(s + r * 64 + ((c4 ^ ((r >> 1) & 3)) * 16), src + (int64_t)r * ld + c4 * 8);
-  }
-}
-
-// x[0..31] *= the 32 multipliers (16-bit type TG) of row `lane` in a ring slot.
-template <typename TG>
-__device__ __forceinline__ void mul_slot_32(float (&x)[32], const uint8_t* slot, int lane) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 mm = *reinterpret_cast<const uint4*>(slot + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16));
-    const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      x[8 * v + 2 * t] *= lo16<TG>(w[t]);
-      x[8 * v + 2 * t + 1] *= hi16<TG>(w[t]);
-    }
-  }
 }
 
 }  // namespace attn
