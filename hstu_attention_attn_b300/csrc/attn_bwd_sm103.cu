@@ -11,22 +11,21 @@
 // Two persistent kernels, neither of which needs atomics:
 //  * dK/dV (key-tile major): one item = (user, key tile, head), looping over
 //    the query tiles that see the key tile (dynamic mixed mask, fun-rec
-//    chapter 7.3, §7.3.4).  Per query tile:  Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (TMEM);
-//    the epilogue writes Pᵀ (f16) over Sᵀ and dSᵀ (f16) over dPᵀ in TMEM; then
-//    dV += Pᵀ dO and dK += dSᵀ Q with the A operand read from TMEM.
+//    chapter 7.3, §7.3.4).  Per query tile: Sᵀ = K Qᵀ and dPᵀ = V dOᵀ in two
+//    alternating TMEM regions; the epilogue writes Pᵀ (f16) over Sᵀ and dSᵀ
+//    (f16) to shared memory; dV += Pᵀ dO reads Pᵀ from TMEM, dK += dSᵀ Q reads
+//    dSᵀ from shared memory.
 //  * dQ (query-tile major): one item = (user, query tile, head), looping over
-//    the key tiles the query tile sees.  Per key tile: S = Q Kᵀ, dP = dO Vᵀ;
-//    the epilogue writes dS (f16) over dP; dQ += dS K from TMEM.  dQ lives in
-//    one of two TMEM accumulators, so the store of one item overlaps the next.
-// Recomputing S and dP in the dQ kernel costs 3 extra MMAs per tile pair but
+//    the key tiles the query tile sees.  Per key tile: S = Q Kᵀ, dP = dO Vᵀ
+//    (two alternating dP buffers); the epilogue writes dS (f16) over dP and
+//    dQ += dS K reads it from TMEM.
+// Recomputing S and dP in the dQ kernel costs 2 extra MMAs per tile pair but
 // avoids accumulating dQ across CTAs through L2 reductions (64 KB of fp32
 // read-modify-write per tile pair).
 //
-// In both, the epilogue of a 128x128 tile is handed to the tensor core in
-// four quarters of 32 columns, so the MMAs of one quarter run while the next
-// is computed.  Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..9 epilogue (two
-// warpgroups, each taking 16 of the 32 columns of a quarter), 10..13 output
-// (TMEM -> bf16).
+// Warps in both: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue
+// (thread = TMEM lane = tile row; 4 lane quarters x 4 groups of 32 columns),
+// 18..21 output (TMEM -> 16-bit gradients).
 #include "attn_sm103.cuh"
 
 namespace mtgr {
@@ -88,20 +87,22 @@ constexpr int DQ_OUT = 4;
 template <int D>
 struct DqCfg {
   static constexpr int TILE = BT * D * 2;
-  static constexpr int RING = D == 128 ? 4 : 8;  // K / V tiles in flight
-  static constexpr int Q_OFF = 0, DO_OFF = TILE, DS_OFF = 2 * TILE;
-  static constexpr int RING_OFF = DS_OFF + BT * BT * 2;  // dS': [128 queries][128 keys] f16
+  static constexpr int RING = D == 128 ? 5 : 8;  // K / V tiles in flight
+  static constexpr int Q_OFF = 0, DO_OFF = TILE, RING_OFF = 2 * TILE;
   static constexpr int BAR_OFF = RING_OFF + RING * TILE;
   static constexpr int SMEM = BAR_OFF + 512 + 1024;
-  // S in columns [0, 128), dP in [128, 256), two dQ accumulators after them
-  static constexpr uint32_t S_COL = 0, DP_COL = 128;
-  __device__ static constexpr uint32_t dq_col(int b) { return 256u + (uint32_t)b * D; }
+  // S in columns [0, 128), two dP / dS' buffers in [128, 384), the dQ
+  // accumulators after them (one for d_h = 128, two for d_h = 64)
+  static constexpr int NQB = 384 + 2 * D <= 512 ? 2 : 1;
+  static constexpr uint32_t S_COL = 0;
+  __device__ static constexpr uint32_t dp_col(int b) { return 128u + 128u * (uint32_t)b; }
+  __device__ static constexpr uint32_t dq_col(int b) { return 384u + (uint32_t)b * D; }
 };
 
 struct DqBars {
   uint64_t qdo_full, qdo_empty;
   uint64_t ring_full[8], ring_empty[8];
-  uint64_t s_full, s_read, dp_full, ds_ready, dq_done, dq_full[2], dq_free[2];
+  uint64_t s_full, s_read, dp_full[2], ds_ready[2], dq_done[2], dq_full[2], dq_free[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -160,12 +161,14 @@ __device__ __forceinline__ void dsl_chunk_q(const uint32_t (&sr)[16], int j0, co
 
 // One item = (user, query tile, head): Q and dO stay in shared memory while
 // the key tiles the query tile sees stream through a ring (K_j, then V_j).
-// Per key tile j: S = Q K_jᵀ and dP = dO V_jᵀ (SS, fp32 in TMEM); the epilogue
+// Per key tile j: S = Q K_jᵀ (SS) and dP = dO V_jᵀ (SS) in TMEM; the epilogue
 // turns S into M ⊙ silu' (kept in registers) and signals that S may be
-// overwritten, then, with dP, stores dS' = M ⊙ silu' ⊙ dP (f16) to shared
-// memory; dQ += dS' K_j (SS) accumulates in TMEM.  The issue order S(j+1) as
-// soon as S(j) has been read, dP(j+1) as soon as dP(j) has been read, then
-// dQ(j) keeps the epilogue, which the transcendental paces, busy.
+// overwritten, then, with dP, writes dS' = M ⊙ silu' ⊙ dP (f16) over dP;
+// dQ += dS' K_j accumulates in TMEM with dS' read from TMEM (TS).  dP
+// alternates between two buffers, so dP(j+1) runs while the epilogue and
+// dQ(j) still use dP(j); the issue order S(j+1), dP(j+1), dQ(j) keeps the
+// epilogue, which the transcendental paces, busy.  Q and dO are released after
+// the last dP of an item, so the next item's load overlaps its last dQ.
 template <int D, typename TG>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -173,12 +176,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                        const BwdParams p) {
   using Cfg = DqCfg<D>;
   constexpr int RING = Cfg::RING;
+  constexpr int NQB = Cfg::NQB;
   const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + Cfg::Q_OFF;
   uint8_t* sdO = base + Cfg::DO_OFF;
-  uint8_t* sDS = base + Cfg::DS_OFF;
   uint8_t* sRing = base + Cfg::RING_OFF;
   DqBars& S = *reinterpret_cast<DqBars*>(base + Cfg::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,12 +195,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.s_read, DQ_EPI);
-    mbar_init(&S.dp_full, 1);
-    mbar_init(&S.ds_ready, DQ_EPI);
-    mbar_init(&S.dq_done, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.dp_full[i], 1);
+      mbar_init(&S.ds_ready[i], DQ_EPI);
       mbar_init(&S.dq_full[i], 1);
       mbar_init(&S.dq_free[i], DQ_OUT);
+      mbar_init(&S.dq_done[i], 1);
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -258,12 +261,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
       constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), ds_addr = smem_u32(sDS);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO);
       const uint32_t ring_addr = smem_u32(sRing);
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
       int g = 0;  // global key-tile count of this CTA
-      bool dq_pending[2] = {false, false};
       auto next_stage = [&](uint32_t& addr, int& st) -> bool {
         if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
         addr = ring_addr + stage * Cfg::TILE;
@@ -283,16 +285,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc_commit(&S.s_full);
         return true;
       };
-      // dP(gt) = dO V_gtᵀ once the epilogue has read dP(gt - 1) (it has, when dS'(gt - 1) is ready)
+      // dP(gt) = dO V_gtᵀ into buffer gt & 1 once dQ(gt - 2) has read dS'(gt - 2)
+      // there (the epilogue read dP(gt - 2) before it wrote dS'(gt - 2)).  One
+      // barrier per buffer: dQ(gt - 1) may have completed too (at an item's start).
       auto issue_dp = [&](int gt, uint32_t v_a, int v_s) -> bool {
-        if (gt >= 1 && !mbar_wait(&S.ds_ready, (gt - 1) & 1, abort_flag)) return false;
+        if (gt >= 2 && !mbar_wait(&S.dq_done[gt & 1], ((gt - 2) >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(v_a);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::DP_COL, od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk), vd.hi,
-                      idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.dp_full);
+          tc_mma_ss_h(tmem + Cfg::dp_col(gt & 1), od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk),
+                      vd.hi, idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&S.dp_full[gt & 1]);
         tc_commit(&S.ring_empty[v_s]);  // V_gt has no other reader
         return true;
       };
@@ -300,9 +304,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         const int idx = item_at(r);
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
-        const int qb = n_items & 1;
-        if (!mbar_wait(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
+        const int it = n_items, qb = it % NQB;
+        if (!mbar_wait(&S.qdo_full, it & 1, abort_flag)) { ok = false; break; }
         ++n_items;
+        // the accumulator still holds item it - NQB until the output warps have read it
+        bool acc_free = it < NQB;
+        auto wait_acc = [&]() -> bool {
+          if (acc_free) return true;
+          acc_free = true;
+          return mbar_wait(&S.dq_free[qb], ((it - NQB) / NQB) & 1, abort_flag);
+        };
         const int nk = c.keys.count();
         uint32_t k_a = 0, v_a = 0;
         int k_s = 0, v_s = 0;
@@ -312,36 +323,43 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             break;
           }
         }
+        if (nk <= 1) tc_commit(&S.qdo_empty);  // the item's last S and dP are issued
         for (int i = 0; i < nk && ok; ++i) {
           const int gi = g + i;
-          uint32_t k_n = 0, v_n = 0;
-          int k_ns = 0, v_ns = 0;
-          if (i + 1 < nk && (!next_stage(k_n, k_ns) || !issue_s(gi + 1, k_n))) { ok = false; break; }
-          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag)) { ok = false; break; }
-          if (i + 1 < nk && (!next_stage(v_n, v_ns) || !issue_dp(gi + 1, v_n, v_ns))) { ok = false; break; }
-          if (i == 0 && dq_pending[qb]) {  // this accumulator still holds an older item's dQ
-            // the drain of item n_items - 3 (the older item on this accumulator)
-            if (!mbar_wait(&S.dq_free[qb], ((n_items - 3) >> 1) & 1, abort_flag)) { ok = false; break; }
-            dq_pending[qb] = false;
+          uint32_t k_n = 0;
+          int k_ns = 0;
+          if (i + 1 < nk) {
+            uint32_t v_n = 0;
+            int v_ns = 0;
+            if (!next_stage(k_n, k_ns) || !issue_s(gi + 1, k_n) || !next_stage(v_n, v_ns) ||
+                !issue_dp(gi + 1, v_n, v_ns)) {
+              ok = false;
+              break;
+            }
+            if (i + 2 == nk) tc_commit(&S.qdo_empty);
           }
+          if (!mbar_wait(&S.ds_ready[gi & 1], (gi >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (i == 0 && !wait_acc()) { ok = false; break; }
           tc_fence_after();
-          {  // dQ += dS' K_j
-            const SmemDesc sd = attn::kmajor_base(ds_addr), kd = attn::mnmajor_base(k_a);
+          {  // dQ += dS' K_j; keys 16kk..16kk+15: column group kk/2, packed half kk&1
+            const SmemDesc kd = attn::mnmajor_base(k_a);
+            const uint32_t a_t = tmem + Cfg::dp_col(gi & 1);
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-              tc_mma_ss_h(tmem + Cfg::dq_col(qb), sd.lo + attn::kmajor_step(kk), sd.hi, kd.lo + attn::mnmajor_step(kk),
+              tc_mma_ts_h(tmem + Cfg::dq_col(qb), a_t + 32 * (kk >> 1) + 8 * (kk & 1), kd.lo + attn::mnmajor_step(kk),
                           kd.hi, idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&S.dq_done);
+          tc_commit(&S.dq_done[gi & 1]);
           tc_commit(&S.ring_empty[k_s]);
           k_a = k_n;
           k_s = k_ns;
         }
-        if (!ok) break;
+        if (!ok || !wait_acc()) {  // (an item without keys has not waited yet)
+          ok = false;
+          break;
+        }
         g += nk;
         tc_commit(&S.dq_full[qb]);
-        tc_commit(&S.qdo_empty);
-        dq_pending[qb] = true;
       }
     }
   } else if (warp < 2 + DQ_EPI) {
@@ -353,10 +371,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const int qr = quarter * 32 + lane;  // query row inside the tile
     const float hc = 0.5f * p.scale;
     const uint64_t hc2 = attn::f2(__float_as_uint(hc), __float_as_uint(hc));
-    // this thread's row of dS' in the key box of this group; its 16-byte pieces
-    // 4 (kg & 1) .. +3 at their 128-byte-swizzle positions
-    uint8_t* ds_row = sDS + (kg >> 1) * 16384 + qr * 128;
-    const int jb = 4 * (kg & 1);
     int g = 0;
     for (int r = 0; ok; ++r) {
       const int idx = item_at(r);
@@ -367,7 +381,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int64_t* ts_u = p.ts + u.start;
       const int nk = c.keys.count();
       for (int i = 0; i < nk && ok; ++i) {
-        const int gi = g + i;
+        const int gi = g + i, b = gi & 1;
         const int j0 = c.keys.kt(i, c.qt) * BT + kg * 32;  // first key of this warp's group
         // stamps of the keys this lane broadcasts, loaded before the wait
         const int64_t tk0 = attn::rt_key_stamp(u, ts_u, j0, lane), tk1 = attn::rt_key_stamp(u, ts_u, j0 + 16, lane);
@@ -383,26 +397,25 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (lane == 0) mbar_arrive(&S.s_read);  // the tensor core may overwrite S
         dsl_chunk_q(buf[0], j0, u, m, tk0, hc, hc2, dsl[0]);
         dsl_chunk_q(buf[1], j0 + 16, u, m, tk1, hc, hc2, dsl[1]);
-        // phase 2: dS' = (M ⊙ silu') ⊙ dP to shared memory, once dQ(gi - 1) has read the previous dS'
-        if (!mbar_wait(&S.dp_full, gi & 1, abort_flag)) { ok = false; break; }
+        // phase 2: dS' = (M ⊙ silu') ⊙ dP, packed f16 over the first 16 columns
+        // of this warp's 32 (which only this warp reads)
+        if (!mbar_wait(&S.dp_full[b], (gi >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        tmem_ld16(tmem + Cfg::DP_COL + kg * 32 + lane_sel, buf[0]);
-        tmem_ld16(tmem + Cfg::DP_COL + kg * 32 + 16 + lane_sel, buf[1]);
+        const uint32_t t_dp = tmem + Cfg::dp_col(b) + kg * 32 + lane_sel;
+        tmem_ld16(t_dp, buf[0]);
+        tmem_ld16(t_dp + 16, buf[1]);
         tmem_wait_ld();
-        if (gi >= 1 && !mbar_wait(&S.dq_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t pd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) pd[e] = attn::ds_pair(dsl[ch][e], buf[ch][2 * e], buf[ch][2 * e + 1]);
-          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch) ^ (qr & 7)) * 16)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
-          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch + 1) ^ (qr & 7)) * 16)) =
-              make_uint4(pd[4], pd[5], pd[6], pd[7]);
+          tmem_st8(t_dp + 8 * ch, pd);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.ds_ready);
+        if (lane == 0) mbar_arrive(&S.ds_ready[b]);
       }
       g += nk;
     }
@@ -417,8 +430,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int idx = item_at(r);
       if (idx >= total) break;
       const DqItem c = dq_item(p, idx);
-      const int qb = n_items & 1;
-      const uint32_t par = (n_items >> 1) & 1;
+      const int qb = n_items % NQB;
+      const uint32_t par = (n_items / NQB) & 1;
       ++n_items;
       const int rl = c.qt * BT + quarter * 32 + lane;  // this lane's query row, segment-relative
       const bool row_ok = rl < c.u.n;

@@ -55,6 +55,11 @@ class HstuAttention:
             self._ws = workspace(n, self.device)
         return self._ws
 
+    def device_status(self):
+        """MTGR_STATUS_* bits the last forward or backward left in its status
+        word (0: every bounded wait completed).  Waits for the device."""
+        return 0 if self._ws is None else int(self._ws[:4].view(torch.int32).item())
+
     def forward(self, q, k, v, u, db: DeviceBatch, ld=None):
         T, HD = db.T, self.H * self.dh
         ld = ld if ld is not None else q.stride(0)

@@ -105,6 +105,27 @@ def test_attention_bwd_bf16_ragged(orc, dh, ts_hi):
     dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
     dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
     torch.cuda.synchronize()
+    assert op.device_status() == 0
+    ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
+    for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
+        assert_close_bf16(to_np(got), r, TOL_BF16, name)
+
+
+@pytest.mark.parametrize("dh", [128, 64])
+def test_attention_bwd_bf16_many_items_per_cta(orc, dh):
+    """About 41k ragged tokens: several query-tile and key-tile items per CTA,
+    so the TMEM accumulators, the score buffers and the Q/dO stage are reused
+    across items (one dQ accumulator per CTA for d_h = 128, two for d_h = 64)."""
+    need_gpu()
+    rng = np.random.default_rng(71 + dh)
+    batch = synth.make_batch(rng, ragged_users() * 24, ts_hi=3000)
+    H = 2
+    assert sum((int(n) + 127) // 128 for n in np.diff(batch.offsets)) * H > 2 * 148
+    op, db, (q, k, v, u), host, ld, y, saved = _run_fwd(batch, H, dh, rng)
+    dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
+    dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
+    torch.cuda.synchronize()
+    assert op.device_status() == 0
     ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
         assert_close_bf16(to_np(got), r, TOL_BF16, name)
@@ -123,6 +144,7 @@ def test_attention_bwd_bf16_small_workload_sampled(orc):
     dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
     dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db)
     torch.cuda.synchronize()
+    assert op.device_status() == 0
     lens = np.diff(batch.offsets)
     pick = sorted(set([int(np.argmin(lens)), int(np.argsort(lens)[len(lens) // 2])] +
                       [int(i) for i in np.where(lens <= 1000)[0][:4]]))
@@ -150,6 +172,7 @@ def test_attention_bf16_longest_user(orc):
     dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
     dq, dk, dv, du = op.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
     torch.cuda.synchronize()
+    assert op.device_status() == 0
     ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
         assert_close_bf16(to_np(got), r, TOL_BF16, name)
