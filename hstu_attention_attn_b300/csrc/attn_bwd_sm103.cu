@@ -447,6 +447,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       for (int cc = 0; cc < NC; ++cc) {
         uint32_t rr[32];
         tmem_ld32(tmem + Cfg::dq_col(qb) + cc * 32 + lane_sel, rr);
+        uint4 mm[4];  // the multipliers of this chunk load while the TMEM read completes
+        if (has_m && row_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) mm[v] = *reinterpret_cast<const uint4*>(mrow + cc * 32 + 8 * v);
+        }
         tmem_wait_ld();
         if (cc == NC - 1) {
           tc_fence_before();
@@ -460,8 +465,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (has_m) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 mm = *reinterpret_cast<const uint4*>(mrow + cc * 32 + 8 * v);
-            const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
+            const uint32_t w[4] = {mm[v].x, mm[v].y, mm[v].z, mm[v].w};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               x[8 * v + 2 * t] *= lo16<TG>(w[t]);
@@ -514,7 +518,7 @@ struct DkvCfg {
 struct DkvBars {
   uint64_t kv_full, kv_empty;
   uint64_t ring_full[8], ring_empty[8];
-  uint64_t s_full, dp_full, ds_ready, pv_done, dk_done, dkdv_full, dkdv_free;
+  uint64_t s_full, dp_full, p_ready, dp_read, ds_ready, pv_done, dk_done, dkdv_full, dv_free, dk_free;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -590,9 +594,12 @@ __device__ __forceinline__ void p_chunk_k(const uint32_t (&sr)[16], int q0, cons
 // (keeping M ⊙ silu' in registers), then, once dPᵀ is there, dS'ᵀ = M ⊙ silu'
 // ⊙ dPᵀ (f16) to shared memory; the tensor core adds
 //   dV += Pᵀ dO_g  (A from TMEM),  dK += dS'ᵀ Q_g  (A from shared memory).
-// Issue order per tile: S(g+1) into the region dPᵀ(g) has just left, dV(g),
-// dP(g+1) into the region Pᵀ(g) leaves once dV(g) has read it, then dK(g), so
-// the SiLU of tile g+1 runs while the tensor core works on tile g.
+// The epilogue signals three points of tile g: Pᵀ(g) written (dV(g) may
+// start), dPᵀ(g) read into registers (Sᵀ(g+1) may take its region) and dS'ᵀ(g)
+// stored (dK(g) may start).  Issue order per tile: Sᵀ(g+1), dV(g), dPᵀ(g+1)
+// into the region Pᵀ(g) leaves once dV(g) has read it, then dK(g), so the
+// tensor core works on tile g and the scores of g+1 while the epilogue
+// computes dS'ᵀ(g) and then the SiLU of tile g+1.
 template <int D, typename TG>
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -619,11 +626,14 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.dp_full, 1);
+    mbar_init(&S.p_ready, DKV_EPI);
+    mbar_init(&S.dp_read, DKV_EPI);
     mbar_init(&S.ds_ready, DKV_EPI);
     mbar_init(&S.pv_done, 1);
     mbar_init(&S.dk_done, 1);
     mbar_init(&S.dkdv_full, 1);
-    mbar_init(&S.dkdv_free, DKV_OUT);
+    mbar_init(&S.dv_free, DKV_OUT);
+    mbar_init(&S.dk_free, DKV_OUT);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -688,7 +698,6 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
       int g = 0;  // global query-tile count of this CTA
-      bool dkdv_pending = false;
       // next ring stage (address, index), waiting until it is full
       auto next_stage = [&](uint32_t& addr, int& st) -> bool {
         if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
@@ -723,8 +732,16 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         const int idx = item_at(r);
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
-        if (!mbar_wait(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
+        const int it = n_items;
+        if (!mbar_wait(&S.kv_full, it & 1, abort_flag)) { ok = false; break; }
         ++n_items;
+        // dV and dK of item it - 1 stay in TMEM until the output warps have read them
+        bool dv_ok = it == 0, dk_ok = it == 0;
+        auto wait_free = [&](bool& flag, uint64_t* bar) -> bool {
+          if (flag) return true;
+          flag = true;
+          return mbar_wait(bar, (it - 1) & 1, abort_flag);
+        };
         const int nq = c.qs.count();
         uint32_t q_a = 0, do_a = 0;
         int q_s = 0, do_s = 0;
@@ -733,19 +750,22 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           issue_s(g, q_a);
           if (!next_stage(do_a, do_s) || !issue_dp(g, do_a)) { ok = false; break; }
         }
+        if (nq <= 1) tc_commit(&S.kv_empty);  // the item's last Sᵀ and dPᵀ are issued
         for (int i = 0; i < nq && ok; ++i) {
           const int gi = g + i;
-          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag)) { ok = false; break; }
+          // Pᵀ(gi) is in TMEM and dPᵀ(gi) has been read (so Sᵀ(gi + 1) may
+          // take its region); both come early in the epilogue of tile gi
+          if (!mbar_wait(&S.p_ready, gi & 1, abort_flag) || !mbar_wait(&S.dp_read, gi & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           uint32_t q_n = 0, do_n = 0;
           int q_ns = 0, do_ns = 0;
-          if (i + 1 < nq) {  // the next tile's scores while the epilogue starts on them
+          if (i + 1 < nq) {  // the next tile's scores while the epilogue works on dS'ᵀ(gi)
             if (!next_stage(q_n, q_ns)) { ok = false; break; }
             issue_s(gi + 1, q_n);
           }
-          if (i == 0 && dkdv_pending) {  // the accumulators still hold the previous item
-            if (!mbar_wait(&S.dkdv_free, (n_items - 2) & 1, abort_flag)) { ok = false; break; }
-            dkdv_pending = false;
-          }
+          if (!wait_free(dv_ok, &S.dv_free)) { ok = false; break; }
           tc_fence_after();
           {  // dV += Pᵀ dO_g: Pᵀ packed in region g & 1 (query rows 16kk..: column 32(kk/2) + 8(kk%2))
             const SmemDesc od = attn::mnmajor_base(do_a);
@@ -757,7 +777,12 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           tc_commit(&S.pv_done);
           // dP of the next tile goes into the region Pᵀ(g) leaves, as soon as dV(g)
           // has read it, before dK(g), so that the epilogue gets it early
-          if (i + 1 < nq && (!next_stage(do_n, do_ns) || !issue_dp(gi + 1, do_n))) { ok = false; break; }
+          if (i + 1 < nq) {
+            if (!next_stage(do_n, do_ns) || !issue_dp(gi + 1, do_n)) { ok = false; break; }
+            if (i + 2 == nq) tc_commit(&S.kv_empty);
+          }
+          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag) || !wait_free(dk_ok, &S.dk_free)) { ok = false; break; }
+          tc_fence_after();
           {  // dK += dS'ᵀ Q_g
             const SmemDesc sd = attn::kmajor_base(ds_addr), qd = attn::mnmajor_base(q_a);
 #pragma unroll
@@ -775,11 +800,13 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
             do_s = do_ns;
           }
         }
-        if (!ok) break;
+        // (an item without query tiles has not waited for the accumulators yet)
+        if (!ok || !wait_free(dv_ok, &S.dv_free) || !wait_free(dk_ok, &S.dk_free)) {
+          ok = false;
+          break;
+        }
         g += nq;
         tc_commit(&S.dkdv_full);
-        tc_commit(&S.kv_empty);
-        dkdv_pending = true;
       }
     }
   } else if (warp < 2 + DKV_EPI) {
@@ -830,6 +857,10 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           p_chunk_k(buf[ch], q0 + 16 * ch, u, km, warp_us, ch ? adj1 : adj0, hc2, pp, dsl[ch]);
           tmem_st8(t_s + 8 * ch, pp);  // Pᵀ over Sᵀ columns this warp has read
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_ready);  // dV(gi) may read Pᵀ
         // phase 2: dS'ᵀ = (M ⊙ silu') ⊙ dPᵀ, once dPᵀ is there and dK(gi - 1)
         // has finished reading the shared dS'ᵀ tile
         if (!mbar_wait(&S.dp_full, gi & 1, abort_flag)) { ok = false; break; }
@@ -837,6 +868,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         tmem_ld16(t_d, buf[0]);
         tmem_ld16(t_d + 16, buf[1]);
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.dp_read);  // Sᵀ(gi + 1) may overwrite dPᵀ
         if (gi >= 1 && !mbar_wait(&S.dk_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
@@ -847,7 +881,6 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch + 1) ^ (kr & 7)) * 16)) =
               make_uint4(pd[4], pd[5], pd[6], pd[7]);
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -884,11 +917,18 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         const int cc = is_k ? ch - NC : ch;
         uint32_t rr[32];
         tmem_ld32(tmem + (is_k ? Cfg::DK_COL : Cfg::DV_COL) + cc * 32 + lane_sel, rr);
+        // the multipliers of this chunk load while the TMEM read completes
+        uint4 mm[4];
+        if (has_m && row_ok) {
+          const uint16_t* mrow = (is_k ? p.m0 : p.m1) + grow * p.ldm + c.h * D + cc * 32;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) mm[v] = *reinterpret_cast<const uint4*>(mrow + 8 * v);
+        }
         tmem_wait_ld();
-        if (ch == 2 * NC - 1) {
+        if (ch == NC - 1 || ch == 2 * NC - 1) {  // dV (then dK) may be overwritten by the next item
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&S.dkdv_free);
+          if (lane == 0) mbar_arrive(is_k ? &S.dk_free : &S.dv_free);
         }
         if (!row_ok) continue;
         // dV: Pᵀ carries no 1/n_u; dK: dS'ᵀ carries neither c nor 1/n_u
@@ -897,11 +937,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * sc : 0.f;
         if (has_m) {
-          const uint16_t* mrow = (is_k ? p.m0 : p.m1) + grow * p.ldm + c.h * D + cc * 32;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 mm = *reinterpret_cast<const uint4*>(mrow + 8 * v);
-            const uint32_t w[4] = {mm.x, mm.y, mm.z, mm.w};
+            const uint32_t w[4] = {mm[v].x, mm[v].y, mm[v].z, mm[v].w};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               x[8 * v + 2 * t] *= lo16<TG>(w[t]);
