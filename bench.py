@@ -253,7 +253,9 @@ def workload_config(args, batch, H, dh, D=None):
                 "l2": (f"inputs larger than L2 (x and dx_out are {batch.T * 2048 / 2**20:.0f} MiB each)"
                        if batch.T * 2048 > 126 * 2**20 else
                        f"working set larger than L2 (uqkv and silu'(z) are {batch.T * 2 * 4096 * 2 / 2**20:.0f} MiB)"),
-                "parallelism": "replicas only"}
+                "parallelism": "replicas only",
+                "e2e_upstream_gradient": "only the candidate rows of dx' are copied in (the loss is on the "
+                                         "candidates; dx' is zero elsewhere and is expanded on the device)"}
     return {"workload": f"MTGR-small-like attention fwd+bwd: {batch.B} users, {batch.T} tokens, {H} heads x d_h {dh}",
             "tokens": int(batch.T), "users": int(batch.B), "n_heads": H, "d_h": dh,
             "l2": "inputs larger than L2", "parallelism": "replicas only"}
