@@ -216,6 +216,7 @@ struct LayerWs {
   AttnWs attn;
   size_t attn_base, dY, dZ, dxn, gln_part, wpart, w16, dxo16, gscale, total;
   int splits_uqkv, splits_o;
+  int splits_out;  // forward output projection: split over K when its tiles leave most SMs idle
 };
 // Split-K count for a weight-gradient GEMM (M x N output, K = tokens): the
 // persistent kernel runs tiles x splits work units over the SMs, and each
@@ -253,9 +254,16 @@ static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, m
   o += align256((size_t)gln_bwd_blocks(T) * 8 * D * sizeof(float));
   w.splits_uqkv = dt == MTGR_BF16 ? choose_splits(D, 4 * HD, T) : 1;  // weight gradients: bf16 path only
   w.splits_o = dt == MTGR_BF16 ? choose_splits(HD, D, T) : 1;
+  // x' = x + y·W_o has ceil(T/128)·ceil(D/256) output tiles: a short batch
+  // (one ranking request) leaves most SMs without one, so it runs split over
+  // K = H·d_h into fp32 slices that one pass adds to the residual
+  const int64_t out_tiles = ((T + 127) / 128) * ((D + 255) / 256);
+  w.splits_out = (dt != MTGR_F32 && T > 0 && 2 * out_tiles <= num_sms()) ? choose_splits(T, D, HD) : 1;
   const size_t p1 = (size_t)w.splits_uqkv * D * 4 * HD, p2 = (size_t)w.splits_o * HD * D;
+  const size_t p3 = w.splits_out > 1 ? (size_t)w.splits_out * T * D : 0;
+  const size_t pm = p1 > p2 ? (p1 > p3 ? p1 : p3) : (p2 > p3 ? p2 : p3);
   w.wpart = o;
-  o += align256((p1 > p2 ? p1 : p2) * sizeof(float));
+  o += align256(pm * sizeof(float));
   w.w16 = o;
   if (dt == MTGR_BF16) o += align256((size_t)D * 4 * HD * 2) + align256((size_t)HD * D * 2);
   w.dxo16 = o;
@@ -647,9 +655,32 @@ static mtgr_status check_layer(const mtgr_layer_weights* w, const int32_t* offse
   REQUIRE(w->w_uqkv && w->w_o && w->gamma && w->beta, MTGR_ERR_INVALID_ARG, "NULL weight");
   REQUIRE(aligned16(w->w_uqkv) && aligned16(w->w_o) && aligned16(w->gamma) && aligned16(w->beta),
           MTGR_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+  REQUIRE((w->w_uqkv_f16 == nullptr) == (w->w_o_f16 == nullptr), MTGR_ERR_INVALID_ARG,
+          "set both f16 weight copies or neither");
+  REQUIRE(aligned16(w->w_uqkv_f16) && aligned16(w->w_o_f16), MTGR_ERR_INVALID_ARG,
+          "f16 weight copies must be 16-byte aligned");
   REQUIRE(ws && aligned16(ws) && ws_bytes >= layer_ws(B, T, D, H, d, dtype).total, MTGR_ERR_WORKSPACE,
           "workspace missing or smaller than mtgr_layer_workspace_size()");
   return MTGR_OK;
+}
+
+// f16 operands of a MTGR_BF16 layer's two weight matrices: the caller's copies
+// when given, else conversions into the workspace at c.
+static cudaError_t layer_weights_f16(const mtgr_layer_weights* w, __half* c, const __half** wu16,
+                                     const __half** wo16, cudaStream_t s) {
+  const int D = w->d_model;
+  const int64_t HD = (int64_t)w->n_heads * w->d_h, N4 = 4 * HD;
+  if (w->w_uqkv_f16) {
+    *wu16 = static_cast<const __half*>(w->w_uqkv_f16);
+    *wo16 = static_cast<const __half*>(w->w_o_f16);
+    return cudaSuccess;
+  }
+  __half* co = c + align256((size_t)D * N4 * 2) / 2;
+  cudaError_t e = launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_uqkv), N4, c, N4, D, (int)N4, s);
+  if (e == cudaSuccess) e = launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_o), D, co, D, HD, D, s);
+  *wu16 = c;
+  *wo16 = co;
+  return e;
 }
 
 static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, void* x_out,
@@ -680,14 +711,7 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
   const __half* wu16 = static_cast<const __half*>(w->w_uqkv);
   const __half* wo16 = static_cast<const __half*>(w->w_o);
   if (bf_io) {
-    __half* c = reinterpret_cast<__half*>(ws + L.w16);
-    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_uqkv), N4, c, N4, D, (int)N4, s),
-                  "layer_fwd W_uqkv f16");
-    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_o), D, c + align256((size_t)D * N4 * 2) / 2,
-                                     D, HD, D, s),
-                  "layer_fwd W_o f16");
-    wu16 = c;
-    wo16 = c + align256((size_t)D * N4 * 2) / 2;
+    MTGR_CUDA_TRY(layer_weights_f16(w, reinterpret_cast<__half*>(ws + L.w16), &wu16, &wo16, s), "layer_fwd W f16");
     // xn = GLN(x) in f16
     cudaError_t e = launch_gln_fwd(static_cast<const __nv_bfloat16*>(x), static_cast<__half*>(sv->xn), sv->gln_mean,
                                    sv->gln_rstd, gid, w->gamma, w->beta, T, D, w->eps_gln, s);
@@ -733,17 +757,46 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
     g.A = static_cast<const bf*>(sv->y); g.lda = HD; g.a_mn_major = false;
     g.B = reinterpret_cast<const bf*>(wo16); g.ldb = D; g.b_mn_major = true;
     g.ab_f16 = true;
-    // x' = x + y·W_o in the layer's dtype
-    g.epi = EPI_RESIDUAL; g.C = x_out; g.c_f16 = !bf_io; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
-    g.r_f16 = !bf_io;
-    g.splits = 1; g.status = status; g.name = "gemm_out";
-    MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
+    g.status = status; g.name = "gemm_out";
+    if (L.splits_out > 1) {
+      // x' = x + Σ_k slices of y·W_o, the slices in fp32
+      float* parts = reinterpret_cast<float*>(ws + L.wpart);
+      g.epi = EPI_F32; g.C = parts; g.ldc = D; g.splits = L.splits_out;
+      MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
+      MTGR_CUDA_TRY(launch_split_reduce_residual(parts, gemm_splits(HD, L.splits_out), T * D, T * D, x, x_out, !bf_io,
+                                                 s),
+                    "layer_fwd out reduce");
+    } else {
+      // x' = x + y·W_o in the layer's dtype
+      g.epi = EPI_RESIDUAL; g.C = x_out; g.c_f16 = !bf_io; g.ldc = D; g.R = static_cast<const bf*>(x); g.ldr = D;
+      g.r_f16 = !bf_io;
+      g.splits = 1;
+      MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd out gemm");
+    }
   } else {
     MTGR_CUDA_TRY(launch_gemm_f32(EPI_RESIDUAL, T, D, HD, static_cast<const float*>(sv->y), HD, 1,
                                   static_cast<const float*>(w->w_o), D, 1, static_cast<float*>(x_out), D,
                                   static_cast<const float*>(x), D, nullptr, 0, s),
                   "layer_fwd out gemm");
   }
+  return MTGR_OK;
+}
+
+mtgr_status mtgr_layer_weights_to_f16(const mtgr_layer_weights* w, void* w_uqkv_f16, void* w_o_f16,
+                                      mtgr_stream_t stream) {
+  REQUIRE(w != nullptr && w->w_uqkv && w->w_o && w_uqkv_f16 && w_o_f16, MTGR_ERR_INVALID_ARG, "NULL pointer");
+  const int D = w->d_model;
+  const int64_t HD = (int64_t)w->n_heads * w->d_h, N4 = 4 * HD;
+  REQUIRE(D > 0 && HD > 0 && D % 8 == 0 && HD % 8 == 0, MTGR_ERR_INVALID_ARG, "bad layer dims");
+  REQUIRE(aligned16(w->w_uqkv) && aligned16(w->w_o) && aligned16(w_uqkv_f16) && aligned16(w_o_f16),
+          MTGR_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_uqkv), N4, static_cast<__half*>(w_uqkv_f16),
+                                   N4, D, (int)N4, s),
+                "weights_to_f16 W_uqkv");
+  MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const __nv_bfloat16*>(w->w_o), D, static_cast<__half*>(w_o_f16), D, HD,
+                                   D, s),
+                "weights_to_f16 W_o");
   return MTGR_OK;
 }
 
@@ -817,14 +870,7 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
   const __half* dxo16 = nullptr;
   const float* inv_scale = nullptr;
   if (dtype == MTGR_BF16) {
-    __half* c = reinterpret_cast<__half*>(ws + L.w16);
-    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(w->w_uqkv), N4, c, N4, D, (int)N4, s),
-                  "layer_bwd W_uqkv f16");
-    MTGR_CUDA_TRY(launch_bf16_to_f16(static_cast<const bf*>(w->w_o), D, c + align256((size_t)D * N4 * 2) / 2, D, HD,
-                                     D, s),
-                  "layer_bwd W_o f16");
-    wu16 = c;
-    wo16 = c + align256((size_t)D * N4 * 2) / 2;
+    MTGR_CUDA_TRY(layer_weights_f16(w, reinterpret_cast<__half*>(ws + L.w16), &wu16, &wo16, s), "layer_bwd W f16");
     float* gs = reinterpret_cast<float*>(ws + L.gscale + 16);
     MTGR_CUDA_TRY(launch_grad_to_f16(static_cast<const bf*>(dx_out), reinterpret_cast<__half*>(ws + L.dxo16), T * D,
                                      reinterpret_cast<unsigned*>(ws + L.gscale), gs, s),

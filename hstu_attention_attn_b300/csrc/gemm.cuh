@@ -59,6 +59,10 @@ inline int gemm_splits(int64_t K, int splits) {
   s = nk > 0 ? (nk + per - 1) / per : 1;
   return (int)s;
 }
+// 16-bit out[i] = R[i] + sum_s parts[s*stride + i] for i < n (n and stride
+// multiples of 8, 16-byte aligned; f16 or bf16 R and out)
+cudaError_t launch_split_reduce_residual(const float* parts, int splits, int64_t stride, int64_t n, const void* R,
+                                         void* out, bool f16, cudaStream_t s);
 // fp32 out[i] = sum_s parts[s*stride + i] for i < n
 cudaError_t launch_split_reduce(const float* parts, int splits, int64_t stride, int64_t n, float* out,
                                 cudaStream_t s);

@@ -371,7 +371,48 @@ __global__ void split_reduce_kernel(const float* __restrict__ parts, int splits,
   out[i] = s;
 }
 
+// out = R + sum over the split-K slices, 8 elements (16 bytes of 16-bit
+// output) per thread: the residual epilogue of an output projection that ran
+// split over K because its output tiles alone would leave most SMs idle.
+template <typename T>
+__global__ void split_reduce_residual_kernel(const float* __restrict__ parts, int splits, int64_t stride, int64_t n8,
+                                             const T* __restrict__ R, T* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 r = *reinterpret_cast<const uint4*>(R + 8 * i);
+  const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+  float x[8];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    x[2 * t] = lo16<T>(rw[t]);
+    x[2 * t + 1] = hi16<T>(rw[t]);
+  }
+  for (int k = 0; k < splits; ++k) {
+    const float4* pk = reinterpret_cast<const float4*>(parts + k * stride + 8 * i);
+    const float4 a = pk[0], b = pk[1];
+    x[0] += a.x; x[1] += a.y; x[2] += a.z; x[3] += a.w;
+    x[4] += b.x; x[5] += b.y; x[6] += b.z; x[7] += b.w;
+  }
+  *reinterpret_cast<uint4*>(out + 8 * i) = pack8<T>(x);
+}
+
 }  // namespace
+
+cudaError_t launch_split_reduce_residual(const float* parts, int splits, int64_t stride, int64_t n, const void* R,
+                                         void* out, bool f16, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if (n % 8 != 0 || stride % 8 != 0) return cudaErrorInvalidValue;
+  TraceScope tr("split_reduce_out", s);
+  const int64_t n8 = n / 8;
+  const unsigned blocks = (unsigned)((n8 + 255) / 256);
+  if (f16)
+    split_reduce_residual_kernel<__half><<<blocks, 256, 0, s>>>(parts, splits, stride, n8,
+                                                                static_cast<const __half*>(R), static_cast<__half*>(out));
+  else
+    split_reduce_residual_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        parts, splits, stride, n8, static_cast<const __nv_bfloat16*>(R), static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_split_reduce(const float* parts, int splits, int64_t stride, int64_t n, float* out,
                                 cudaStream_t s) {

@@ -101,6 +101,26 @@ class HstuLayer:
         self.weights = mtgr.make_weights(d_model, n_heads, d_h, self.w_uqkv, self.w_o, self.gamma, self.beta,
                                          eps_gln, eps_ln)
         self._ws = None
+        self._w16 = None
+
+    def keep_f16_weights(self):
+        """bf16 layer with fixed weights (inference): make f16 copies of W_uqkv
+        and W_o once, which every later call reads instead of converting them
+        again.  Call again after changing the weights (the copies are
+        rewritten in place, so a captured CUDA Graph reads the new ones);
+        drop_f16_weights() returns to converting on every call."""
+        if self.dtype != torch.bfloat16:
+            return
+        if self._w16 is None:  # refreshed in place afterwards, so captured graphs stay valid
+            self._w16 = (torch.empty_like(self.w_uqkv, dtype=torch.float16),
+                         torch.empty_like(self.w_o, dtype=torch.float16))
+        self.weights.w_uqkv_f16 = self.weights.w_o_f16 = None
+        mtgr.mtgr_layer_weights_to_f16(self.weights, *self._w16)
+        self.weights.w_uqkv_f16, self.weights.w_o_f16 = (t.data_ptr() for t in self._w16)
+
+    def drop_f16_weights(self):
+        self.weights.w_uqkv_f16 = self.weights.w_o_f16 = None
+        self._w16 = None
 
     def _workspace(self, db):
         n = mtgr.mtgr_layer_workspace_size(db.B, db.T, self.D, self.H, self.dh, _dt(self.dtype))
@@ -148,10 +168,15 @@ class HstuStack:
     layers) and one workspace, so after the first run nothing is allocated and
     the whole stack can be captured."""
 
-    def __init__(self, layers):
+    def __init__(self, layers, keep_f16_weights=True):
+        """keep_f16_weights: bf16 layers keep f16 copies of their weights
+        (HstuLayer.keep_f16_weights), so a forward pass converts nothing."""
         self.layers = list(layers)
         self._key = None
         self._graph = None
+        if keep_f16_weights:
+            for layer in self.layers:
+                layer.keep_f16_weights()
 
     def _prepare(self, x, db):
         key = (db.B, db.T, x.dtype, x.device)

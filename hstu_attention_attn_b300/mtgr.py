@@ -33,7 +33,7 @@ class MtgrError(RuntimeError):
 class LayerWeights(C.Structure):
     _fields_ = [("d_model", C.c_int32), ("n_heads", C.c_int32), ("d_h", C.c_int32),
                 ("w_uqkv", C.c_void_p), ("w_o", C.c_void_p), ("gamma", C.c_void_p), ("beta", C.c_void_p),
-                ("eps_gln", C.c_float), ("eps_ln", C.c_float)]
+                ("eps_gln", C.c_float), ("eps_ln", C.c_float), ("w_uqkv_f16", C.c_void_p), ("w_o_f16", C.c_void_p)]
 
 
 class LayerSaved(C.Structure):
@@ -75,6 +75,7 @@ EXPORTS = {
                            + [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t,
                                                  C.c_void_p]),
     "mtgr_layer_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
+    "mtgr_layer_weights_to_f16": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.c_void_p, C.c_void_p]),
     "mtgr_hstu_layer_fwd": (C.c_int, [C.POINTER(LayerWeights), C.c_void_p, C.c_void_p, C.POINTER(LayerSaved),
                                       C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int,
                                       C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -260,6 +261,11 @@ def make_saved(d) -> LayerSaved:
 
 def make_grads(d) -> LayerGrads:
     return LayerGrads(*[_p(d[n]) for n, _ in LayerGrads._fields_])
+
+
+def mtgr_layer_weights_to_f16(weights: LayerWeights, w_uqkv_f16, w_o_f16, stream=None):
+    _check("mtgr_layer_weights_to_f16",
+           lib().mtgr_layer_weights_to_f16(C.byref(weights), _p(w_uqkv_f16), _p(w_o_f16), _stream(stream)))
 
 
 def mtgr_hstu_layer_fwd(weights: LayerWeights, x, x_out, saved: LayerSaved, offsets, gid, ts, T, workspace,

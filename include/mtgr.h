@@ -242,7 +242,24 @@ typedef struct {
   const float* beta;    /* [4, D] fp32 */
   float eps_gln;        /* 1e-5 */
   float eps_ln;         /* 1e-5 */
+  /* Optional, MTGR_BF16 only: f16 copies of w_uqkv and w_o (same shapes,
+   * 16-byte aligned, caller-owned), as written by mtgr_layer_weights_to_f16.
+   * When both are set the layer's tensor-core operands are read from them;
+   * when both are NULL (zero-initialised struct) every forward and backward
+   * call converts the weights into its workspace first (two kernels).  The
+   * caller keeps them equal to the bf16 weights: refresh them after every
+   * weight update (inference with fixed weights converts once).  Setting
+   * only one is MTGR_ERR_INVALID_ARG; the other dtypes ignore them. */
+  const void* w_uqkv_f16;
+  const void* w_o_f16;
 } mtgr_layer_weights;
+
+/* f16 copies of a MTGR_BF16 layer's w_uqkv and w_o into caller-owned device
+ * buffers of D*4*H*d_h and H*d_h*D f16 elements (16-byte aligned).  Each
+ * value is the bf16 weight rounded to f16 (exact in f16's normal range).
+ * Reads only d_model, n_heads, d_h, w_uqkv and w_o of *w. */
+MTGR_API mtgr_status mtgr_layer_weights_to_f16(const mtgr_layer_weights* w, void* w_uqkv_f16, void* w_o_f16,
+                                      mtgr_stream_t stream);
 
 typedef struct {        /* written by the forward, read by the backward: f16 in the MTGR_BF16 and
                            MTGR_F16 paths (11 significand bits between the steps), fp32 in MTGR_F32 */

@@ -45,9 +45,14 @@ def test_chunked_candidates_equal_whole_request_and_oracle(orc, dtype, user, chu
     chunked = stack.score_chunked(xd, db.gid, db.ts, n_hist, chunk)
     torch.cuda.synchronize()
     got = to_np(chunked)
-    # the same rows as the whole request through the same kernels (summation order
-    # differs only in the candidate's own key, which sits in another tile position)
-    assert_close(got, to_np(whole)[n_hist:], 1e-3, "chunked vs whole request")
+    # the same rows as the whole request through the same kernels, up to the
+    # order of fp32 sums: the candidate's own key sits in another tile position,
+    # and the whole request (more rows) runs its output projection split over K
+    # where a chunk does not, so x' is rounded to 16 bits from another fp32 sum;
+    # held to 5e-3 beyond one rounding of the stored type, 4x inside the bound
+    # against the oracle below
+    check_close = assert_close_bf16 if dtype == torch.bfloat16 else assert_close_f16
+    check_close(got, to_np(whole)[n_hist:], 5e-3, "chunked vs whole request")
     # the oracle's layers chained over the whole request on the same 16-bit inputs
     rnd = bf16_round if dtype == torch.bfloat16 else (lambda a: np.asarray(f16_round(a), np.float64))
     h = rnd(x)

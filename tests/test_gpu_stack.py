@@ -58,3 +58,39 @@ def test_stack_graph_replay_equals_eager(orc):
         got = to_np(outs[l])
         assert_close_bf16(got, ref["x_out"], TOL_BF16, f"layer {l}")
         inp = got
+
+
+def test_kept_f16_weights_give_identical_results():
+    """A bf16 layer reading f16 copies of its weights made once
+    (mtgr_layer_weights_to_f16) returns what it returns when every call
+    converts them (bit for bit, except the order of the dγ/dβ atomics);
+    setting only one copy is refused."""
+    need_gpu()
+    from hstu_attention_attn_b300 import mtgr
+    D, H, dh = 256, 2, 128
+    base, ws, stack = _stack(D, H, dh, 1, USERS, 81)
+    layer = stack.layers[0]
+    db = device_batch(base.batch)
+    x = dev(base.x, BF)
+    dxo = dev(np.random.default_rng(3).standard_normal(base.x.shape).astype(np.float32), BF)
+    layer.drop_f16_weights()
+    y0, sv0 = layer.forward(x, db)
+    y0 = y0.clone()
+    dx0, g0 = layer.backward(x, sv0, dxo, db)
+    dx0, g0 = dx0.clone(), {k: v.clone() for k, v in g0.items()}
+    layer.keep_f16_weights()
+    y1, sv1 = layer.forward(x, db)
+    dx1, g1 = layer.backward(x, sv1, dxo, db)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(dx0, dx1)
+    for k in ("dw_uqkv", "dw_o"):
+        assert torch.equal(g0[k], g1[k]), k
+    # dγ and dβ are summed through shared-memory atomics, whose order varies
+    for k in ("dgamma", "dbeta"):
+        assert torch.allclose(g0[k], g1[k], rtol=1e-5, atol=1e-5), k
+    w16 = layer._w16
+    assert torch.equal(w16[0], layer.w_uqkv.to(torch.float16)) and torch.equal(w16[1], layer.w_o.to(torch.float16))
+    layer.weights.w_o_f16 = None
+    with pytest.raises(mtgr.MtgrError, match="both f16 weight copies"):
+        layer.forward(x, db)
+    layer.drop_f16_weights()
