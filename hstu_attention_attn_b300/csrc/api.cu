@@ -46,7 +46,10 @@ cudaError_t launch_attn_f32_bwd(const float*, const float*, const float*, int64_
                                 int, const int64_t*, int64_t, int, int, float*, float*, float*, int64_t,
                                 const float*, const float*, const float*, cudaStream_t);
 cudaError_t launch_attn_fwd_f16(const __half*, const __half*, const __half*, int64_t, int64_t, int, int,
-                                const int32_t*, int32_t, const int64_t*, __half*, int32_t*, cudaStream_t);
+                                const int32_t*, int32_t, const int64_t*, __half*, int32_t*, cudaStream_t, float*);
+template <typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd_parts(const float*, int64_t, __half*, const TU*, int64_t, TY*, float*, float*, int64_t,
+                                     int, float, cudaStream_t);
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts, void* dq,
                                 void* dk, void* dv, int64_t ldg, const void* mq, const void* mk, const void* mv,
@@ -190,8 +193,15 @@ static size_t esize(mtgr_dtype dt) { return dt == MTGR_F32 ? 4 : 2; }
 // tensor-core operands are f16: q, k, v are converted once (exactly) into f16
 // copies, and dO, P, dS are produced in f16 (11 significand bits instead of 8).
 struct AttnWs {
-  size_t status, plan, dO, qkv16, total;
+  size_t status, plan, dO, qkv16, opart, total;
+  bool key_split;
 };
+// Key split of the forward: when even twice the per-query-tile items of the
+// batch (at most (T/128 + B)·H) fit in one wave, each item's key tiles are
+// shared by two CTAs (a ranking request of one user: 72 items for 148 SMs).
+static bool attn_key_split(int32_t B, int64_t T, int32_t H) {
+  return 2 * ((T / 128 + B) * (int64_t)H) <= num_sms();
+}
 static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt, bool convert_qkv = true) {
   AttnWs w;
   const size_t THD = (size_t)T * H * d;
@@ -204,6 +214,9 @@ static AttnWs attn_ws(int32_t B, int64_t T, int32_t H, int32_t d, mtgr_dtype dt,
   o += align256(THD * esize(dt));
   w.qkv16 = o;
   if (dt == MTGR_BF16 && convert_qkv) o += 3 * align256(THD * 2);
+  w.key_split = dt != MTGR_F32 && T > 0 && attn_key_split(B, T, H);
+  w.opart = o;
+  if (w.key_split) o += align256(2 * THD * sizeof(float));  // two [T, H*d] fp32 halves, T*H*d apart
   w.total = o;
   return w;
 }
@@ -311,10 +324,22 @@ static mtgr_status attn_fwd_bf16_core(const __half* q16, const __half* k16, cons
   if (T == 0 || B == 0) return MTGR_OK;
   if (!plan_ready)
     MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s, n_norm, q_begin), "attn_fwd plan");
-  MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s), "attn_fwd tcgen05");
+  // the key split needs the gate (which adds the halves) and every query row
+  const bool split = w.key_split && do_gate && q_begin == nullptr;
+  float* opart = split ? reinterpret_cast<float*>(ws + w.opart) : nullptr;
+  MTGR_CUDA_TRY(launch_attn_fwd_f16(q16, k16, v16, ld16, T, H, d, plan, B, ts, o, status, s, opart),
+                "attn_fwd tcgen05");
   if (!do_gate) return MTGR_OK;
   const int HD = H * d;
+  const int64_t ps = T * HD;  // the halves' distance (the forward kernel's pstride)
   cudaError_t e =
+      split ? (y_f16   ? launch_ln_gate_fwd_parts(opart, ps, o, static_cast<const __half*>(u), ldu,
+                                                  static_cast<__half*>(y), mean, rstd, T, HD, eps, s)
+               : u_f16 ? launch_ln_gate_fwd_parts(opart, ps, o, static_cast<const __half*>(u), ldu,
+                                                  static_cast<__nv_bfloat16*>(y), mean, rstd, T, HD, eps, s)
+                       : launch_ln_gate_fwd_parts(opart, ps, o, static_cast<const __nv_bfloat16*>(u), ldu,
+                                                  static_cast<__nv_bfloat16*>(y), mean, rstd, T, HD, eps, s))
+      :
       y_f16   ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, static_cast<__half*>(y), mean, rstd, T, HD,
                                    eps, s)
       : u_f16 ? launch_ln_gate_fwd(o, static_cast<const __half*>(u), ldu, static_cast<__nv_bfloat16*>(y), mean, rstd,

@@ -68,6 +68,13 @@ struct FwdParams {
   const int64_t* ts;
   __half* O;  // [T, H*D] f16
   int64_t ldo;
+  // key split (2 when the items alone would leave most SMs idle, else 1):
+  // item v of the kernel is part v % split of list item v / split, taking its
+  // share of the key tiles; each part then writes its O (already / n_u) in
+  // fp32 to Opart + part * pstride ([T, H*D]) instead of O, and the gate adds them
+  int split;
+  float* Opart;
+  int64_t pstride;
   int H;
   float scale;  // 1/sqrt(d_h)
   int32_t* status;
@@ -77,14 +84,21 @@ struct ItemCtx {
   UserInfo u;
   QTileKeys keys;
   int qt, h;
+  int part, k0, n;  // key split part; its key tiles are keys.kt(k0 .. k0 + n - 1)
+  __device__ __forceinline__ int kt(int j) const { return keys.kt(k0 + j, qt); }
 };
-__device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int idx) {
+__device__ __forceinline__ ItemCtx item_ctx(const FwdParams& p, int v) {
   ItemCtx c;
+  const int idx = p.split == 2 ? v >> 1 : v;
+  c.part = v - idx * p.split;
   const WorkItem wi = p.items[idx];
   c.h = wi.h();
   c.u = p.users[wi.b];
   c.qt = wi.t();
   c.keys = qtile_keys(c.u, c.qt);
+  const int nk = c.keys.count(), h0 = p.split == 2 ? (nk + 1) >> 1 : nk;
+  c.k0 = c.part ? h0 : 0;
+  c.n = c.part ? nk - h0 : h0;
   return c;
 }
 
@@ -132,9 +146,10 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers each
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ CUtensorMap tmP,
                     const FwdParams p) {
   using Cfg = FwdCfg<D>;
-  const int total = p.counts[0];
+  const int total = p.counts[0] * p.split;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -170,6 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
+    if (p.split > 1) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
   __syncthreads();
@@ -205,12 +221,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
           tma_load_2d(sQ + qb * Cfg::TILE + cc * 16384, &tmQ, &S.q_full[qb], col_h + 64 * cc, c.u.start + c.qt * BQ);
-        const int n = c.keys.count();
+        const int n = c.n;
         const int row0 = c.u.start;
-        for (int t = 0; t < 2 && t < n && ok; ++t) ok = load_kv(&tmK, row0 + c.keys.kt(t, c.qt) * BKV, col_h);
+        for (int t = 0; t < 2 && t < n && ok; ++t) ok = load_kv(&tmK, row0 + c.kt(t) * BKV, col_h);
         for (int j = 0; j < n && ok; ++j) {
-          ok = load_kv(&tmV, row0 + c.keys.kt(j, c.qt) * BKV, col_h);
-          if (ok && j + 2 < n) ok = load_kv(&tmK, row0 + c.keys.kt(j + 2, c.qt) * BKV, col_h);
+          ok = load_kv(&tmV, row0 + c.kt(j) * BKV, col_h);
+          if (ok && j + 2 < n) ok = load_kv(&tmK, row0 + c.kt(j + 2) * BKV, col_h);
         }
       }
     }
@@ -248,7 +264,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
         const int qb = it & 1, ob = it & 1;
         const uint32_t q_addr = smem_u32(sQ + qb * Cfg::TILE);
         if (!mbar_wait(&S.q_full[qb], (it >> 1) & 1, abort_flag)) { ok = false; break; }
-        const int n = c.keys.count();
+        const int n = c.n;
+        // a part without keys writes zeros; its accumulator must still be free
+        if (n == 0 && it >= 2 && !mbar_wait(&S.o_free[ob], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
         for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(g + t, q_addr);
         for (int j = 0; j < n && ok; ++j) {
           const int gj = g + j, sb = gj & 1;
@@ -294,10 +312,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
       int64_t thr = INT64_MIN;
       if (row_ok && ri >= u.eS) thr = p.ts[u.start + ri] + (cand ? 0 : 1);
       const int64_t* ts_u = p.ts + u.start;
-      const int n = c.keys.count();
+      const int n = c.n;
       for (int j = 0; j < n && ok; ++j) {
         const int gj = g + j, sb = gj & 1;
-        const int jg = c.keys.kt(j, c.qt) * BKV + grp * 32;  // first key of this warp's column group
+        const int jg = c.kt(j) * BKV + grp * 32;  // first key of this warp's column group
         // stamps of the keys this lane broadcasts in masked chunks, loaded before the wait
         const int64_t tk0 = attn::rt_key_stamp(u, ts_u, jg, lane), tk1 = attn::rt_key_stamp(u, ts_u, jg + 16, lane);
         if (!mbar_wait(&S.s_full[sb], (gj >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -328,6 +346,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
         uint32_t rr[32];
         tmem_ld32(tmem + Cfg::o_col(ob) + grp * 32 + lane_sel, rr);
         tmem_wait_ld();
+        if (p.split > 1) {
+          // key-split part: fp32 partial O (zeros for a part without keys, whose
+          // accumulator holds stale values: select, not scale), in two [32][16]
+          // fp32 boxes through the same 64-byte-swizzled staging as the f16 box
+          const bool any = c.n > 0;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (lane == 0) tma_store_wait_read_n<0>();
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float4 w;
+              w.x = any ? __uint_as_float(rr[16 * hh + 4 * v + 0]) * inv_n : 0.f;
+              w.y = any ? __uint_as_float(rr[16 * hh + 4 * v + 1]) * inv_n : 0.f;
+              w.z = any ? __uint_as_float(rr[16 * hh + 4 * v + 2]) * inv_n : 0.f;
+              w.w = any ? __uint_as_float(rr[16 * hh + 4 * v + 3]) * inv_n : 0.f;
+              *reinterpret_cast<float4*>(box_buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = w;
+            }
+            if (row0 + 32 <= u.n) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmP, box_buf, c.h * D + grp * 32 + 16 * hh, u.start + row0, c.part);
+                tma_store_commit();
+              }
+            } else {
+              __syncwarp();
+              float* pbase = p.Opart + c.part * p.pstride + (int64_t)(u.start + row0) * p.ldo + c.h * D + grp * 32 +
+                             16 * hh;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int rw = k * 8 + (lane >> 2), c4 = lane & 3;
+                const uint4 val = *reinterpret_cast<const uint4*>(box_buf + rw * 64 + ((c4 ^ ((rw >> 1) & 3)) * 16));
+                if (row0 + rw < u.n) *reinterpret_cast<uint4*>(pbase + (int64_t)rw * p.ldo + c4 * 4) = val;
+              }
+            }
+          }
+        } else {
         // row r_in's 32 values as f16 -> box_buf[lane][64 bytes], 16-byte pieces
         // XOR-swizzled by row (the 64-byte swizzle of a [32][32] f16 TMA box);
         // the previous box store must have finished reading the buffer
@@ -363,6 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
             if (row0 + rw < u.n) *reinterpret_cast<uint4*>(obase + (int64_t)rw * p.ldo + c4 * 8) = val;
           }
         }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -387,20 +444,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
 }  // namespace
 
 // q, k, v: [T, *] f16 with row stride ld; O: [T, H*d] f16 (scaled by 1/n_u).
+// opart: nullptr, or [2][T, H*d] fp32 for a key-split launch (each query tile's
+// keys in two halves on two CTAs; O is then not written, the gate adds the halves).
 cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, int64_t T, int H,
                                 int d, const int32_t* plan, int32_t B, const int64_t* ts, __half* O, int32_t* status,
-                                cudaStream_t s) {
+                                cudaStream_t s, float* opart) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv, to, tp;
   if (!make_tmap_f16_2d(&tq, q, T, HD, ld, 64, BQ) || !make_tmap_f16_2d(&tk, k, T, HD, ld, 64, BKV) ||
       !make_tmap_f16_2d(&tv, v, T, HD, ld, 64, BKV) || !make_tmap_out(&to, OUT_F16, O, T, HD, HD, 0, 32, 32))
     return cudaErrorInvalidValue;
+  // the two key halves' fp32 partial O: [2][T][H*d], [32 rows][16 fp32] boxes
+  tp = to;  // unused without the split
+  if (opart && !make_tmap_out(&tp, OUT_F32, opart, T, HD, HD, 2, 16, 32)) return cudaErrorInvalidValue;
   FwdParams p;
   p.users = reinterpret_cast<const UserInfo*>(plan + L.users);
   p.items = reinterpret_cast<const WorkItem*>(plan + L.dq_items);  // one item per (user, query tile, head)
   p.counts = plan + L.counts + 2;
+  p.split = opart ? 2 : 1;
+  p.Opart = opart;
+  p.pstride = T * HD;
   p.ts = ts;
   p.O = O;
   p.ldo = HD;
@@ -409,18 +474,19 @@ cudaError_t launch_attn_fwd_f16(const __half* q, const __half* k, const __half* 
   p.status = status;
   // persistent: one CTA per SM (the item count lives on the device; CTAs without an item exit at once)
   const int64_t max_items = L.max_items;
-  const int grid = (int)(max_items < num_sms() ? max_items : num_sms());
+  const int64_t units = max_items * p.split;
+  const int grid = (int)(units < num_sms() ? units : num_sms());
   TraceScope tr("attn_fwd", s);
   if (d == 128) {
     auto kern = attn_fwd_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<128>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, to, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<128>::SMEM, s>>>(tq, tk, tv, to, tp, p);
   } else if (d == 64) {
     auto kern = attn_fwd_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<64>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, to, p);
+    kern<<<grid, NUM_THREADS, FwdCfg<64>::SMEM, s>>>(tq, tk, tv, to, tp, p);
   } else {
     return cudaErrorInvalidValue;
   }

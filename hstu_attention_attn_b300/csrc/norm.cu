@@ -323,14 +323,29 @@ template <typename TOi, typename TU, typename TY, int NCH>
 __global__ void __launch_bounds__(256) ln_gate_fwd_kernel(const TOi* __restrict__ O, const TU* __restrict__ U,
                                                           int64_t ldu, TY* __restrict__ Y,
                                                           float* __restrict__ mean, float* __restrict__ rstd,
-                                                          int64_t rows, int n, float eps) {
+                                                          int64_t rows, int n, float eps,
+                                                          const float* __restrict__ opart, int64_t pstride,
+                                                          TOi* __restrict__ o_out) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
     float v[NCH][8];
     float s = 0.f;
     ROW_CHUNKS_FOR(m, c, lane, n) {
-      load8(O + r * n + 8 * c, v[m]);
+      if (opart) {
+        // O = the two key halves' fp32 partial sums, rounded to O's stored type
+        // (and stored) before the statistics, as an unsplit forward stores it
+        const float4* pa = reinterpret_cast<const float4*>(opart + r * n + 8 * c);
+        const float4* pb = reinterpret_cast<const float4*>(opart + pstride + r * n + 8 * c);
+        const float4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
+        const float t[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
+                            a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[m][i] = to_f32<TOi>(from_f32<TOi>(t[i]));
+        store8(o_out + r * n + 8 * c, v[m]);
+      } else {
+        load8(O + r * n + 8 * c, v[m]);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) s += v[m][i];
     }
@@ -478,8 +493,21 @@ cudaError_t launch_ln_gate_fwd(const TOi* O, const TU* U, int64_t ldu, TY* Y, fl
                                int64_t rows, int n, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   TraceScope tr("gate_fwd", s);
-  NCH_DISPATCH(n, (ln_gate_fwd_kernel<TOi, TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(O, U, ldu, Y, mean, rstd,
-                                                                                     rows, n, eps)));
+  NCH_DISPATCH(n, (ln_gate_fwd_kernel<TOi, TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(
+                      O, U, ldu, Y, mean, rstd, rows, n, eps, nullptr, 0, nullptr)));
+  return cudaGetLastError();
+}
+
+// The gate of a key-split forward: O = opart[0] + opart[1] ([rows, n] fp32 each,
+// pstride apart), written to O in f16, then the gate as above.
+template <typename TU, typename TY>
+cudaError_t launch_ln_gate_fwd_parts(const float* opart, int64_t pstride, __half* O, const TU* U, int64_t ldu, TY* Y,
+                                     float* mean, float* rstd, int64_t rows, int n, float eps, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  if (n % 8 != 0 || pstride % 8 != 0) return cudaErrorInvalidValue;
+  TraceScope tr("gate_fwd", s);
+  NCH_DISPATCH(n, (ln_gate_fwd_kernel<__half, TU, TY, NCHV><<<row_blocks(rows), 256, 0, s>>>(
+                      O, U, ldu, Y, mean, rstd, rows, n, eps, opart, pstride, O)));
   return cudaGetLastError();
 }
 
@@ -539,6 +567,15 @@ template cudaError_t launch_ln_gate_fwd<__half, __half, bf16_t>(const __half*, c
                                                                 float*, float*, int64_t, int, float, cudaStream_t);
 template cudaError_t launch_ln_gate_fwd<__half, __half, __half>(const __half*, const __half*, int64_t, __half*,
                                                                float*, float*, int64_t, int, float, cudaStream_t);
+template cudaError_t launch_ln_gate_fwd_parts<bf16_t, bf16_t>(const float*, int64_t, __half*, const bf16_t*, int64_t,
+                                                             bf16_t*, float*, float*, int64_t, int, float,
+                                                             cudaStream_t);
+template cudaError_t launch_ln_gate_fwd_parts<__half, bf16_t>(const float*, int64_t, __half*, const __half*, int64_t,
+                                                             bf16_t*, float*, float*, int64_t, int, float,
+                                                             cudaStream_t);
+template cudaError_t launch_ln_gate_fwd_parts<__half, __half>(const float*, int64_t, __half*, const __half*, int64_t,
+                                                             __half*, float*, float*, int64_t, int, float,
+                                                             cudaStream_t);
 template cudaError_t launch_ln_gate_bwd<float, float, float, float, float>(const float*, const float*,
                                                                            const float*, int64_t, const float*,
                                                                            const float*, float*, float*, int64_t,
