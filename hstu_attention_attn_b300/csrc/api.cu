@@ -712,11 +712,12 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
                                   const mtgr_layer_saved* sv, const int32_t* offsets, int32_t B, const uint8_t* gid,
                                   const int64_t* ts, int64_t T, mtgr_dtype dtype, void* workspace,
                                   size_t workspace_bytes, mtgr_stream_t stream, bool plan_ready,
-                                  const int32_t* n_norm = nullptr) {
+                                  const int32_t* n_norm = nullptr, bool keep_dsilu = true) {
+  // keep_dsilu = false: a forward for inference, which writes no silu'(z)
   mtgr_status st = check_layer(w, offsets, B, gid, T, dtype, workspace, workspace_bytes);
   if (st != MTGR_OK) return st;
   REQUIRE(sv != nullptr, MTGR_ERR_INVALID_ARG, "saved is NULL");
-  REQUIRE(T == 0 || (x && x_out && sv->xn && sv->dsilu && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
+  REQUIRE(T == 0 || (x && x_out && sv->xn && (sv->dsilu || !keep_dsilu) && sv->uqkv && sv->o && sv->y && sv->gln_mean &&
                      sv->gln_rstd && sv->ln_mean && sv->ln_rstd && ts),
           MTGR_ERR_INVALID_ARG, "NULL tensor");
   REQUIRE(aligned16(x) && aligned16(x_out) && aligned16(sv->xn) && aligned16(sv->dsilu) && aligned16(sv->uqkv) &&
@@ -754,7 +755,8 @@ static mtgr_status layer_fwd_impl(const mtgr_layer_weights* w, const void* x, vo
     g.B = reinterpret_cast<const bf*>(wu16); g.ldb = N4; g.b_mn_major = true;
     g.ab_f16 = true;
     // [U|Q|K|V] = silu(z) and silu'(z), both f16
-    g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4; g.Z = static_cast<bf*>(sv->dsilu); g.ldz = N4;
+    g.epi = EPI_SILU; g.C = sv->uqkv; g.c_f16 = true; g.ldc = N4;
+    g.Z = keep_dsilu ? static_cast<bf*>(sv->dsilu) : nullptr; g.ldz = N4;
     g.z_f16 = true;
     g.splits = 1; g.status = status; g.name = "gemm_uqkv";
     MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "layer_fwd uqkv gemm");
@@ -848,7 +850,7 @@ mtgr_status mtgr_hstu_stack_fwd(const mtgr_layer_weights* w, int32_t n_layers, c
     void* out = ((n_layers - 1 - l) & 1) ? act : x_out;  // the last layer writes x_out
     // one work-list build serves every layer: they share the batch and the workspace
     const mtgr_status r = layer_fwd_impl(w + l, in, out, sv, offsets, B, gid, ts, T, dtype, workspace,
-                                         workspace_bytes, stream, l > 0);
+                                         workspace_bytes, stream, l > 0, nullptr, /*keep_dsilu=*/false);
     if (r != MTGR_OK) return r;
     in = out;
   }
@@ -1145,7 +1147,7 @@ mtgr_status mtgr_hstu_stack_hist_fwd(const mtgr_layer_weights* w, int32_t n_laye
     sv.uqkv = static_cast<uint8_t*>(cache) + (size_t)l * ((size_t)n_hist + chunk) * N4 * 2;
     // history rows see history rows only: their activations are those of the whole request, with its n_u
     st = layer_fwd_impl(w + l, in, out, &sv, meta, 1, gid, ts, n_hist, dtype, ws + C.layer,
-                        layer_ws(1, n_hist, D, H, d, dtype).total, stream, l > 0, meta + 2);
+                        layer_ws(1, n_hist, D, H, d, dtype).total, stream, l > 0, meta + 2, /*keep_dsilu=*/false);
     if (st != MTGR_OK) return st;
     in = out;
   }
@@ -1219,7 +1221,7 @@ mtgr_status mtgr_hstu_stack_cand_fwd(const mtgr_layer_weights* w, int32_t n_laye
       g.B = reinterpret_cast<const bf*>(wu16); g.ldb = N4; g.b_mn_major = true;
       g.ab_f16 = true;
       g.epi = EPI_SILU; g.C = a + (size_t)n_hist * N4; g.c_f16 = true; g.ldc = N4;
-      g.Z = reinterpret_cast<bf*>(ws + C.dsilu); g.ldz = N4; g.z_f16 = true;
+      g.Z = nullptr; g.ldz = N4; g.z_f16 = true;  // inference: no silu'(z)
       g.splits = 1; g.status = status; g.name = "gemm_uqkv";
       MTGR_CUDA_TRY(launch_gemm_bf16(g, s), "cand uqkv gemm");
     }

@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         }
         if (p.epi == EPI_SILU) {
           // C = silu(z); Z = silu'(z) = σ(z)(1 + z(1 - σ(z))), the factor that
-          // the backward applies to the gradient of silu(z)
+          // the backward applies to the gradient of silu(z) (not written when
+          // Z is null: a forward that keeps nothing for a backward)
           float dz[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -318,10 +319,12 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
             dz[i] = sg * fmaf(x[i], 1.0f - sg, 1.0f);
             x[i] *= sg;
           }
-          if (p.z_f16)
+          if (p.Z == nullptr) {
+          } else if (p.z_f16) {
             stage_store16<__half>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
-          else
+          } else {
             stage_store16<__nv_bfloat16>(dz, out_slot(), &tmZ, (int)col0, (int)row0, lane);
+          }
         } else if (p.epi == EPI_RESIDUAL) {
           cp_async_wait<1>();
           __syncwarp();
@@ -446,8 +449,9 @@ cudaError_t launch_gemm_bf16(const GemmArgs& a, cudaStream_t s) {
                        ? make_tmap_out(&tmC, OUT_F32, a.C, a.M, a.N, a.ldc, splits, 32, 32)
                        : make_tmap_out(&tmC, a.c_f16 ? OUT_F16 : OUT_BF16, a.C, a.M, a.N, a.ldc, 0, 32, 32);
   const bool okZ =
-      a.epi == EPI_SILU ? make_tmap_out(&tmZ, a.z_f16 ? OUT_F16 : OUT_BF16, a.Z, a.M, a.N, a.ldz, 0, 32, 32) : true;
-  if (a.epi != EPI_SILU) tmZ = tmC;
+      a.epi == EPI_SILU && a.Z ? make_tmap_out(&tmZ, a.z_f16 ? OUT_F16 : OUT_BF16, a.Z, a.M, a.N, a.ldz, 0, 32, 32)
+                               : true;
+  if (a.epi != EPI_SILU || !a.Z) tmZ = tmC;
   if (!okC || !okZ) return cudaErrorInvalidValue;
   p.a_mn = a.a_mn_major;
   p.b_mn = a.b_mn_major;

@@ -296,7 +296,9 @@ MTGR_API mtgr_status mtgr_hstu_layer_fwd(const mtgr_layer_weights* w, const void
  * output; the last layer writes x_out.  w: host array of n_layers weight sets,
  * all with the same d_model, n_heads, d_h.  act: [T, D] scratch (dtype,
  * distinct from x and x_out) when n_layers > 1.  saved: one set of buffers
- * that every layer overwrites (inference keeps nothing between layers).  The
+ * that every layer overwrites (inference keeps nothing between layers); its
+ * dsilu is neither written nor required (may be NULL), since nothing runs a
+ * backward on it, which saves the UQKV projection a second output.  The
  * attention work lists are built once for all layers (they depend only on the
  * batch).  Workspace: mtgr_layer_workspace_size of one layer.  The call
  * allocates nothing and never synchronises, so it can be captured in a CUDA
