@@ -269,9 +269,12 @@ static LayerWs layer_ws(int32_t B, int64_t T, int32_t D, int32_t H, int32_t d, m
   w.splits_o = dt == MTGR_BF16 ? choose_splits(HD, D, T) : 1;
   // x' = x + y·W_o has ceil(T/128)·ceil(D/256) output tiles: a short batch
   // (one ranking request) leaves most SMs without one, so it runs split over
-  // K = H·d_h into fp32 slices that one pass adds to the residual
+  // K = H·d_h into fp32 slices that one pass adds to the residual.  Every
+  // slice costs T·D fp32 written and read again, so take as many as fit in one
+  // wave, at most 4.
   const int64_t out_tiles = ((T + 127) / 128) * ((D + 255) / 256);
-  w.splits_out = (dt != MTGR_F32 && T > 0 && 2 * out_tiles <= num_sms()) ? choose_splits(T, D, HD) : 1;
+  const int64_t fit = out_tiles > 0 ? num_sms() / out_tiles : 1;
+  w.splits_out = (dt != MTGR_F32 && T > 0 && fit >= 2) ? gemm_splits(HD, (int)(fit < 4 ? fit : 4)) : 1;
   const size_t p1 = (size_t)w.splits_uqkv * D * 4 * HD, p2 = (size_t)w.splits_o * HD * D;
   const size_t p3 = w.splits_out > 1 ? (size_t)w.splits_out * T * D : 0;
   const size_t pm = p1 > p2 ? (p1 > p3 ? p1 : p3) : (p2 > p3 ? p2 : p3);
