@@ -37,7 +37,7 @@ using attn::item_at;
 using attn::silu_half;
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NUM_THREADS = 576;  // 18 warps
+constexpr int NUM_THREADS = 608;  // 19 warps
 constexpr int EPI_WARPS = 16;
 constexpr int RING = 4;
 constexpr int STG_BYTES = 2048;  // per-warp O staging: one [32][32] f16 box
@@ -143,7 +143,7 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[N], int j0, const Us
 }
 
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers each
+__global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const __grid_constant__ CUtensorMap tmP,
@@ -197,16 +197,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      // order per item: Q; K_0, K_1; then V_j, K_{j+2} for j = 0 .. n-1
-      int stage = 0;
-      uint32_t ph = 0;
-      auto load_kv = [&](const CUtensorMap* m, int row, int col_h) -> bool {
-        if (!mbar_wait(&S.ring_empty[stage], ph ^ 1, abort_flag)) return false;
-        uint8_t* dst = sRing + stage * Cfg::TILE;
-        mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+      // K tiles through a 2-stage ring (read by the S issuer), V tiles through
+      // another (read by the PV issuer); order per item: Q; K_0, K_1; then
+      // V_j, K_{j+2} for j = 0 .. n-1
+      int st[2] = {0, 0};
+      uint32_t ph[2] = {0, 0};
+      auto load_kv = [&](int which, int row, int col_h) -> bool {  // which: 0 K, 1 V
+        const int slot = 2 * which + st[which];
+        if (!mbar_wait(&S.ring_empty[slot], ph[which] ^ 1, abort_flag)) return false;
+        uint8_t* dst = sRing + slot * Cfg::TILE;
+        mbar_arrive_expect_tx(&S.ring_full[slot], Cfg::TILE);
+        const CUtensorMap* m = which ? &tmV : &tmK;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tma_load_2d(dst + cc * 16384, m, &S.ring_full[stage], col_h + 64 * cc, row);
-        if (++stage == RING) { stage = 0; ph ^= 1; }
+        for (int cc = 0; cc < D / 64; ++cc) tma_load_2d(dst + cc * 16384, m, &S.ring_full[slot], col_h + 64 * cc, row);
+        if (++st[which] == 2) { st[which] = 0; ph[which] ^= 1; }
         return true;
       };
       int it = 0;
@@ -223,76 +227,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 18 warps: 96 registers eac
           tma_load_2d(sQ + qb * Cfg::TILE + cc * 16384, &tmQ, &S.q_full[qb], col_h + 64 * cc, c.u.start + c.qt * BQ);
         const int n = c.n;
         const int row0 = c.u.start;
-        for (int t = 0; t < 2 && t < n && ok; ++t) ok = load_kv(&tmK, row0 + c.kt(t) * BKV, col_h);
+        for (int t = 0; t < 2 && t < n && ok; ++t) ok = load_kv(0, row0 + c.kt(t) * BKV, col_h);
         for (int j = 0; j < n && ok; ++j) {
-          ok = load_kv(&tmV, row0 + c.kt(j) * BKV, col_h);
-          if (ok && j + 2 < n) ok = load_kv(&tmK, row0 + c.kt(j + 2) * BKV, col_h);
+          ok = load_kv(1, row0 + c.kt(j) * BKV, col_h);
+          if (ok && j + 2 < n) ok = load_kv(0, row0 + c.kt(j + 2) * BKV, col_h);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- S issuer: S(gs) = Q · K_gsᵀ into buffer gs & 1, once
+      // PV(gs - 2) has finished reading the P that buffer held ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BQ, BKV, false, false);
-      constexpr uint32_t idesc_o = idesc_f16_f32(BQ, D, false, true);
       const uint32_t ring_addr = smem_u32(sRing);
-      int stage = 0;
-      uint32_t ph = 0;
-      int g = 0;  // global key-tile count of this CTA (S/P buffer g & 1)
-      // S(gs) = Q · K_gsᵀ into buffer gs & 1, once PV(gs - 2) has finished
-      // reading the P that buffer held
-      auto issue_s = [&](int gs, uint32_t q_addr) -> bool {
-        const int sb = gs & 1;
-        if (gs >= 2 && !mbar_wait(&S.pv_done[sb], ((gs - 2) >> 1) & 1, abort_flag)) return false;
-        if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
-        tc_fence_after();
-        const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(ring_addr + stage * Cfg::TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::s_col(sb), qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk),
-                      kd.hi, idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.s_full[sb]);
-        tc_commit(&S.ring_empty[stage]);
-        if (++stage == RING) { stage = 0; ph ^= 1; }
-        return true;
-      };
-      int it = 0;
+      int ks = 0;
+      uint32_t kph = 0;
+      int g = 0, it = 0;
       for (int r = 0; ok; ++r, ++it) {
         const int idx = item_at(r);
         if (idx >= total) break;
         const ItemCtx c = item_ctx(p, idx);
-        const int qb = it & 1, ob = it & 1;
+        const int qb = it & 1;
         const uint32_t q_addr = smem_u32(sQ + qb * Cfg::TILE);
         if (!mbar_wait(&S.q_full[qb], (it >> 1) & 1, abort_flag)) { ok = false; break; }
         const int n = c.n;
-        // a part without keys writes zeros; its accumulator must still be free
-        if (n == 0 && it >= 2 && !mbar_wait(&S.o_free[ob], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        for (int t = 0; t < 2 && t < n && ok; ++t) ok = issue_s(g + t, q_addr);
-        for (int j = 0; j < n && ok; ++j) {
+        for (int t = 0; t < n; ++t) {
+          const int gs = g + t, sb = gs & 1;
+          if (gs >= 2 && !mbar_wait(&S.pv_done[sb], ((gs - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.ring_full[ks], kph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(ring_addr + ks * Cfg::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss_h(tmem + Cfg::s_col(sb), qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk),
+                        kd.hi, idesc_s, kk > 0 ? 1u : 0u);
+          tc_commit(&S.s_full[sb]);
+          tc_commit(&S.ring_empty[ks]);
+          if (++ks == 2) { ks = 0; kph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&S.q_empty[qb]);  // once the item's products of Q complete
+        g += n;
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---------------- PV issuer: O += P(j) V_j once the epilogue has written P(j) ----------------
+      constexpr uint32_t idesc_o = idesc_f16_f32(BQ, D, false, true);
+      const uint32_t ring_addr = smem_u32(sRing);
+      int vs = 0;
+      uint32_t vph = 0;
+      int g = 0, it = 0;
+      for (int r = 0; ok; ++r, ++it) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const ItemCtx c = item_ctx(p, idx);
+        const int ob = it & 1;
+        const int n = c.n;
+        // the accumulator still holds item it - 2 until the epilogue has read it
+        // (waited also by a part without keys, which writes zeros)
+        if (it >= 2 && !mbar_wait(&S.o_free[ob], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        for (int j = 0; j < n; ++j) {
           const int gj = g + j, sb = gj & 1;
           if (!mbar_wait(&S.p_full[sb], (gj >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (j == 0 && it >= 2 && !mbar_wait(&S.o_free[ob], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.ring_full[2 + vs], vph, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const SmemDesc vd = attn::mnmajor_base(ring_addr + stage * Cfg::TILE);
+          const SmemDesc vd = attn::mnmajor_base(ring_addr + (2 + vs) * Cfg::TILE);
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)  // keys 16kk..16kk+15: column group kk/2, packed half kk&1
             tc_mma_ts_h(tmem + Cfg::o_col(ob), tmem + Cfg::s_col(sb) + 32 * (kk >> 1) + 8 * (kk & 1),
                         vd.lo + attn::mnmajor_step(kk), vd.hi, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&S.pv_done[sb]);
-          tc_commit(&S.ring_empty[stage]);
-          if (++stage == RING) { stage = 0; ph ^= 1; }
-          if (j + 2 < n) ok = issue_s(gj + 2, q_addr);
+          tc_commit(&S.ring_empty[2 + vs]);
+          if (++vs == 2) { vs = 0; vph ^= 1; }
         }
         if (!ok) break;
         tc_commit(&S.o_full[ob]);
-        tc_commit(&S.q_empty[qb]);
         g += n;
       }
     }
   } else {
     // ---------------- epilogue warps ----------------
-    const int ew = warp - 2;             // 0..15
+    const int ew = warp - 3;             // 0..15
     const int grp = ew >> 2;             // group of 32 key columns of S (and of O)
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
