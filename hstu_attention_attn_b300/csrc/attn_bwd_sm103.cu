@@ -77,10 +77,11 @@ __device__ __forceinline__ RowMask row_mask(const UserInfo& u, const int64_t* ts
 // =============================================================================
 // dQ kernel
 // =============================================================================
-// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue (thread = query
-// row; 4 lane quarters x 4 groups of 32 key columns), 18..21 output (TMEM ->
-// 16-bit dQ, one warp per lane quarter).
-constexpr int DQ_THREADS = 704;
+// Warps: 0 TMA, 1 first MMA issuer (S, dP) + TMEM owner, 2..17 score epilogue
+// (thread = query row; 4 lane quarters x 4 groups of 32 key columns), 18..21
+// output (TMEM -> 16-bit dQ, one warp per lane quarter), 22 second MMA issuer
+// (dQ), so that each issuer waits only for its own operands.
+constexpr int DQ_THREADS = 736;  // + the second MMA issuer (warp 22)
 constexpr int DQ_EPI = 16;
 constexpr int DQ_OUT = 4;
 
@@ -88,6 +89,7 @@ template <int D>
 struct DqCfg {
   static constexpr int TILE = BT * D * 2;
   static constexpr int RING = D == 128 ? 5 : 8;  // K / V tiles in flight
+  static constexpr int KR = D == 128 ? 3 : 4, VR = RING - KR;  // K stages (held until dQ), V stages
   static constexpr int Q_OFF = 0, DO_OFF = TILE, RING_OFF = 2 * TILE;
   static constexpr int BAR_OFF = RING_OFF + RING * TILE;
   static constexpr int SMEM = BAR_OFF + 512 + 1024;
@@ -191,7 +193,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     mbar_init(&S.qdo_empty, 1);
     for (int i = 0; i < RING; ++i) {
       mbar_init(&S.ring_full[i], 1);
-      mbar_init(&S.ring_empty[i], 1);
+      // a K stage is read by S (first issuer) and dQ (second issuer), a V stage by dP
+      mbar_init(&S.ring_empty[i], i < Cfg::KR ? 2 : 1);
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.s_read, DQ_EPI);
@@ -225,8 +228,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer: Q, dO per item; K_j, V_j per key tile ----------------
-      int stage = 0, n_items = 0;
-      uint32_t ph = 0;
+      // K tiles through a ring of KR stages, V tiles through one of VR stages
+      int st[2] = {0, 0};
+      uint32_t ph[2] = {0, 0};
+      int n_items = 0;
       for (int r = 0; ok; ++r) {
         const int idx = item_at(r);
         if (idx >= total) break;
@@ -245,104 +250,94 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           const int row = c.u.start + c.keys.kt(i, c.qt) * BT;
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
-            if (!mbar_wait_sleepy(&S.ring_empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
-            uint8_t* dst = sRing + stage * Cfg::TILE;
-            mbar_arrive_expect_tx(&S.ring_full[stage], Cfg::TILE);
+            const int slot = (kv ? Cfg::KR : 0) + st[kv];
+            if (!mbar_wait_sleepy(&S.ring_empty[slot], ph[kv] ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* dst = sRing + slot * Cfg::TILE;
+            mbar_arrive_expect_tx(&S.ring_full[slot], Cfg::TILE);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[stage], col_h + 64 * cc, row);
-            if (++stage == RING) { stage = 0; ph ^= 1; }
+              tma_load_2d(dst + cc * 16384, kv == 0 ? &tmK : &tmV, &S.ring_full[slot], col_h + 64 * cc, row);
+            if (++st[kv] == (kv ? Cfg::VR : Cfg::KR)) { st[kv] = 0; ph[kv] ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- first issuer: S(j) = Q K_jᵀ and dP(j) = dO V_jᵀ ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
-      constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO);
       const uint32_t ring_addr = smem_u32(sRing);
-      int stage = 0, n_items = 0;
-      uint32_t ph = 0;
+      int ks = 0, vs = 0, n_items = 0;
+      uint32_t kph = 0, vph = 0;
       int g = 0;  // global key-tile count of this CTA
-      auto next_stage = [&](uint32_t& addr, int& st) -> bool {
-        if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
-        addr = ring_addr + stage * Cfg::TILE;
-        st = stage;
-        if (++stage == RING) { stage = 0; ph ^= 1; }
-        return true;
-      };
-      // S(gt) = Q K_gtᵀ once the epilogue has read S(gt - 1)
-      auto issue_s = [&](int gt, uint32_t k_a) -> bool {
-        if (gt >= 1 && !mbar_wait(&S.s_read, (gt - 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(k_a);
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DqItem c = dq_item(p, idx);
+        if (!mbar_wait(&S.qdo_full, n_items & 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        const int nk = c.keys.count();
+        for (int i = 0; i < nk; ++i) {
+          const int gt = g + i;
+          // S(gt) once the epilogue has read S(gt - 1) (one S buffer)
+          if (gt >= 1 && !mbar_wait(&S.s_read, (gt - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.ring_full[ks], kph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const SmemDesc qd = attn::kmajor_base(q_addr), kd = attn::kmajor_base(ring_addr + ks * Cfg::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::S_COL, qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk), kd.hi,
-                      idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.s_full);
-        return true;
-      };
-      // dP(gt) = dO V_gtᵀ into buffer gt & 1 once dQ(gt - 2) has read dS'(gt - 2)
-      // there (the epilogue read dP(gt - 2) before it wrote dS'(gt - 2)).  One
-      // barrier per buffer: dQ(gt - 1) may have completed too (at an item's start).
-      auto issue_dp = [&](int gt, uint32_t v_a, int v_s) -> bool {
-        if (gt >= 2 && !mbar_wait(&S.dq_done[gt & 1], ((gt - 2) >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(v_a);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::S_COL, qd.lo + attn::kmajor_step(kk), qd.hi, kd.lo + attn::kmajor_step(kk),
+                          kd.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&S.s_full);
+          tc_commit(&S.ring_empty[ks]);  // first of the K stage's two readers
+          if (++ks == Cfg::KR) { ks = 0; kph ^= 1; }
+          // dP(gt) into buffer gt & 1 once dQ(gt - 2) has read dS'(gt - 2) there
+          if (gt >= 2 && !mbar_wait(&S.dq_done[gt & 1], ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+          const int vslot = Cfg::KR + vs;
+          if (!mbar_wait(&S.ring_full[vslot], vph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const SmemDesc od = attn::kmajor_base(do_addr), vd = attn::kmajor_base(ring_addr + vslot * Cfg::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::dp_col(gt & 1), od.lo + attn::kmajor_step(kk), od.hi, vd.lo + attn::kmajor_step(kk),
-                      vd.hi, idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.dp_full[gt & 1]);
-        tc_commit(&S.ring_empty[v_s]);  // V_gt has no other reader
-        return true;
-      };
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::dp_col(gt & 1), od.lo + attn::kmajor_step(kk), od.hi,
+                          vd.lo + attn::kmajor_step(kk), vd.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&S.dp_full[gt & 1]);
+          tc_commit(&S.ring_empty[vslot]);
+          if (++vs == Cfg::VR) { vs = 0; vph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&S.qdo_empty);  // Q and dO are free once the item's S and dP complete
+        g += nk;
+      }
+    }
+  } else if (warp == 2 + DQ_EPI + DQ_OUT) {
+    if (lane == 0) {
+      // ---------------- second issuer: dQ += dS'(j) K_j (dS' read from TMEM) ----------------
+      constexpr uint32_t idesc_dq = idesc_f16_f32(BT, D, false, true);
+      const uint32_t ring_addr = smem_u32(sRing);
+      int ks = 0, n_items = 0;
+      int g = 0;
       for (int r = 0; ok; ++r) {
         const int idx = item_at(r);
         if (idx >= total) break;
         const DqItem c = dq_item(p, idx);
         const int it = n_items, qb = it % NQB;
-        if (!mbar_wait(&S.qdo_full, it & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         // the accumulator still holds item it - NQB until the output warps have read it
-        bool acc_free = it < NQB;
-        auto wait_acc = [&]() -> bool {
-          if (acc_free) return true;
-          acc_free = true;
-          return mbar_wait(&S.dq_free[qb], ((it - NQB) / NQB) & 1, abort_flag);
-        };
+        if (it >= NQB && !mbar_wait(&S.dq_free[qb], ((it - NQB) / NQB) & 1, abort_flag)) { ok = false; break; }
         const int nk = c.keys.count();
-        uint32_t k_a = 0, v_a = 0;
-        int k_s = 0, v_s = 0;
-        if (nk > 0) {
-          if (!next_stage(k_a, k_s) || !issue_s(g, k_a) || !next_stage(v_a, v_s) || !issue_dp(g, v_a, v_s)) {
-            ok = false;
-            break;
-          }
-        }
-        if (nk <= 1) tc_commit(&S.qdo_empty);  // the item's last S and dP are issued
-        for (int i = 0; i < nk && ok; ++i) {
+        for (int i = 0; i < nk; ++i) {
           const int gi = g + i;
-          uint32_t k_n = 0;
-          int k_ns = 0;
-          if (i + 1 < nk) {
-            uint32_t v_n = 0;
-            int v_ns = 0;
-            if (!next_stage(k_n, k_ns) || !issue_s(gi + 1, k_n) || !next_stage(v_n, v_ns) ||
-                !issue_dp(gi + 1, v_n, v_ns)) {
-              ok = false;
-              break;
-            }
-            if (i + 2 == nk) tc_commit(&S.qdo_empty);
-          }
+          // dS'(gi) is in TMEM (and S(gi), hence K_gi's load, completed before it)
           if (!mbar_wait(&S.ds_ready[gi & 1], (gi >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (i == 0 && !wait_acc()) { ok = false; break; }
           tc_fence_after();
-          {  // dQ += dS' K_j; keys 16kk..16kk+15: column group kk/2, packed half kk&1
-            const SmemDesc kd = attn::mnmajor_base(k_a);
+          {  // keys 16kk..16kk+15: column group kk/2, packed half kk&1
+            const SmemDesc kd = attn::mnmajor_base(ring_addr + ks * Cfg::TILE);
             const uint32_t a_t = tmem + Cfg::dp_col(gi & 1);
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
@@ -350,16 +345,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                           kd.hi, idesc_dq, (i > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&S.dq_done[gi & 1]);
-          tc_commit(&S.ring_empty[k_s]);
-          k_a = k_n;
-          k_s = k_ns;
+          tc_commit(&S.ring_empty[ks]);  // second reader of the K stage
+          if (++ks == Cfg::KR) ks = 0;
         }
-        if (!ok || !wait_acc()) {  // (an item without keys has not waited yet)
-          ok = false;
-          break;
-        }
-        g += nk;
+        if (!ok) break;
         tc_commit(&S.dq_full[qb]);
+        g += nk;
       }
     }
   } else if (warp < 2 + DQ_EPI) {
