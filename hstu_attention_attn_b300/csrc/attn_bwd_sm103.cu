@@ -23,9 +23,10 @@
 // avoids accumulating dQ across CTAs through L2 reductions (64 KB of fp32
 // read-modify-write per tile pair).
 //
-// Warps in both: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue
-// (thread = TMEM lane = tile row; 4 lane quarters x 4 groups of 32 columns),
-// 18..21 output (TMEM -> 16-bit gradients).
+// Warps in both: 0 TMA, 1 the first MMA issuer (the score products) + TMEM
+// owner, 2..17 score epilogue (thread = TMEM lane = tile row; 4 lane quarters
+// x 4 groups of 32 columns), 18..21 output (TMEM -> 16-bit gradients), 22 the
+// second MMA issuer (the gradient products).
 #include "attn_sm103.cuh"
 
 namespace mtgr {
@@ -485,10 +486,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 // =============================================================================
 // dK/dV kernel
 // =============================================================================
-// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..17 score epilogue (thread = key
-// row; 4 lane quarters x 4 groups of 32 query columns), 18..21 output (TMEM ->
-// 16-bit dV then dK, one warp per lane quarter).
-constexpr int DKV_THREADS = 704;
+// Warps: 0 TMA, 1 first MMA issuer (Sᵀ, dPᵀ) + TMEM owner, 2..17 score
+// epilogue (thread = key row; 4 lane quarters x 4 groups of 32 query columns),
+// 18..21 output (TMEM -> 16-bit dV then dK, one warp per lane quarter), 22
+// second MMA issuer (dV, dK).
+constexpr int DKV_THREADS = 736;  // + the second MMA issuer (warp 22)
 constexpr int DKV_EPI = 16;
 constexpr int DKV_OUT = 4;
 
@@ -509,7 +511,7 @@ struct DkvCfg {
 struct DkvBars {
   uint64_t kv_full, kv_empty;
   uint64_t ring_full[8], ring_empty[8];
-  uint64_t s_full, dp_full, p_ready, dp_read, ds_ready, pv_done, dk_done, dkdv_full, dv_free, dk_free;
+  uint64_t s_full, dp_full, p_ready[2], dp_read, ds_ready, pv_done[2], dk_done, dkdv_full, dv_free, dk_free;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -587,10 +589,10 @@ __device__ __forceinline__ void p_chunk_k(const uint32_t (&sr)[16], int q0, cons
 //   dV += Pᵀ dO_g  (A from TMEM),  dK += dS'ᵀ Q_g  (A from shared memory).
 // The epilogue signals three points of tile g: Pᵀ(g) written (dV(g) may
 // start), dPᵀ(g) read into registers (Sᵀ(g+1) may take its region) and dS'ᵀ(g)
-// stored (dK(g) may start).  Issue order per tile: Sᵀ(g+1), dV(g), dPᵀ(g+1)
-// into the region Pᵀ(g) leaves once dV(g) has read it, then dK(g), so the
-// tensor core works on tile g and the scores of g+1 while the epilogue
-// computes dS'ᵀ(g) and then the SiLU of tile g+1.
+// stored (dK(g) may start).  Two warps issue the products, each waiting only
+// for its own operands: the first Sᵀ(g+1) then dPᵀ(g+1) (into the region Pᵀ(g)
+// leaves once dV(g) has read it), the second dV(g) then dK(g); a Q or dO stage
+// of the ring is free once both have read it.
 template <int D, typename TG>
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -613,14 +615,16 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     mbar_init(&S.kv_empty, 1);
     for (int i = 0; i < RING; ++i) {
       mbar_init(&S.ring_full[i], 1);
-      mbar_init(&S.ring_empty[i], 1);
+      mbar_init(&S.ring_empty[i], 2);  // read by both issuers (Q: Sᵀ and dK; dO: dPᵀ and dV)
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.dp_full, 1);
-    mbar_init(&S.p_ready, DKV_EPI);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.p_ready[i], DKV_EPI);
+      mbar_init(&S.pv_done[i], 1);
+    }
     mbar_init(&S.dp_read, DKV_EPI);
     mbar_init(&S.ds_ready, DKV_EPI);
-    mbar_init(&S.pv_done, 1);
     mbar_init(&S.dk_done, 1);
     mbar_init(&S.dkdv_full, 1);
     mbar_init(&S.dv_free, DKV_OUT);
@@ -681,50 +685,75 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- first issuer: Sᵀ(g) = K Q_gᵀ and dPᵀ(g) = V dO_gᵀ ----------------
       constexpr uint32_t idesc_s = idesc_f16_f32(BT, BT, false, false);
-      constexpr uint32_t idesc_g = idesc_f16_f32(BT, D, false, true);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       const uint32_t ring_addr = smem_u32(sRing);
       int stage = 0, n_items = 0;
       uint32_t ph = 0;
       int g = 0;  // global query-tile count of this CTA
-      // next ring stage (address, index), waiting until it is full
-      auto next_stage = [&](uint32_t& addr, int& st) -> bool {
+      auto next_stage = [&](int& st) -> bool {
         if (!mbar_wait(&S.ring_full[stage], ph, abort_flag)) return false;
-        addr = ring_addr + stage * Cfg::TILE;
         st = stage;
         if (++stage == RING) { stage = 0; ph ^= 1; }
-        return true;
-      };
-      // Sᵀ(gt) = K Qᵀ into region gt & 1 (which held dPᵀ(gt - 1), already read)
-      auto issue_s = [&](int gt, uint32_t q_a) {
-        tc_fence_after();
-        const SmemDesc kd = attn::kmajor_base(k_addr), qd = attn::kmajor_base(q_a);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::r_col(gt & 1), kd.lo + attn::kmajor_step(kk), kd.hi, qd.lo + attn::kmajor_step(kk),
-                      qd.hi, idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.s_full);
-      };
-      // dPᵀ(gt) = V dOᵀ into region (gt + 1) & 1, once dV(gt - 1) has read Pᵀ(gt - 1) there
-      auto issue_dp = [&](int gt, uint32_t do_a) -> bool {
-        if (gt >= 1 && !mbar_wait(&S.pv_done, (gt - 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const SmemDesc vd = attn::kmajor_base(v_addr), od = attn::kmajor_base(do_a);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_h(tmem + Cfg::r_col((gt + 1) & 1), vd.lo + attn::kmajor_step(kk), vd.hi,
-                      od.lo + attn::kmajor_step(kk), od.hi, idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&S.dp_full);
         return true;
       };
       for (int r = 0; ok; ++r) {
         const int idx = item_at(r);
         if (idx >= total) break;
         const DkvItem c = dkv_item(p, idx);
+        if (!mbar_wait(&S.kv_full, n_items & 1, abort_flag)) { ok = false; break; }
+        ++n_items;
+        const int nq = c.qs.count();
+        for (int i = 0; i < nq; ++i) {
+          const int gt = g + i;
+          int q_s = 0, do_s = 0;
+          // Sᵀ(gt) into region gt & 1 once the epilogue has read dPᵀ(gt - 1) there
+          if (gt >= 1 && !mbar_wait(&S.dp_read, (gt - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!next_stage(q_s)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const SmemDesc kd = attn::kmajor_base(k_addr), qd = attn::kmajor_base(ring_addr + q_s * Cfg::TILE);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::r_col(gt & 1), kd.lo + attn::kmajor_step(kk), kd.hi, qd.lo + attn::kmajor_step(kk),
+                          qd.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&S.s_full);
+          tc_commit(&S.ring_empty[q_s]);
+          // dPᵀ(gt) into region (gt + 1) & 1 once dV(gt - 1) has read Pᵀ(gt - 1) there
+          if (gt >= 1 && !mbar_wait(&S.pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!next_stage(do_s)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const SmemDesc vd = attn::kmajor_base(v_addr), od = attn::kmajor_base(ring_addr + do_s * Cfg::TILE);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss_h(tmem + Cfg::r_col((gt + 1) & 1), vd.lo + attn::kmajor_step(kk), vd.hi,
+                          od.lo + attn::kmajor_step(kk), od.hi, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&S.dp_full);
+          tc_commit(&S.ring_empty[do_s]);
+        }
+        if (!ok) break;
+        tc_commit(&S.kv_empty);  // K and V are free once the item's Sᵀ and dPᵀ complete
+        g += nq;
+      }
+    }
+  } else if (warp == 2 + DKV_EPI + DKV_OUT) {
+    if (lane == 0) {
+      // ---------------- second issuer: dV += Pᵀ dO_g (Pᵀ from TMEM), dK += dS'ᵀ Q_g ----------------
+      constexpr uint32_t idesc_g = idesc_f16_f32(BT, D, false, true);
+      const uint32_t ds_addr = smem_u32(sDS);
+      const uint32_t ring_addr = smem_u32(sRing);
+      int stage = 0, n_items = 0;
+      uint32_t ph = 0;
+      int g = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DkvItem c = dkv_item(p, idx);
         const int it = n_items;
-        if (!mbar_wait(&S.kv_full, it & 1, abort_flag)) { ok = false; break; }
         ++n_items;
         // dV and dK of item it - 1 stay in TMEM until the output warps have read them
         bool dv_ok = it == 0, dk_ok = it == 0;
@@ -734,48 +763,34 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           return mbar_wait(bar, (it - 1) & 1, abort_flag);
         };
         const int nq = c.qs.count();
-        uint32_t q_a = 0, do_a = 0;
-        int q_s = 0, do_s = 0;
-        if (nq > 0) {
-          if (!next_stage(q_a, q_s)) { ok = false; break; }
-          issue_s(g, q_a);
-          if (!next_stage(do_a, do_s) || !issue_dp(g, do_a)) { ok = false; break; }
-        }
-        if (nq <= 1) tc_commit(&S.kv_empty);  // the item's last Sᵀ and dPᵀ are issued
-        for (int i = 0; i < nq && ok; ++i) {
+        for (int i = 0; i < nq; ++i) {
           const int gi = g + i;
-          // Pᵀ(gi) is in TMEM and dPᵀ(gi) has been read (so Sᵀ(gi + 1) may
-          // take its region); both come early in the epilogue of tile gi
-          if (!mbar_wait(&S.p_ready, gi & 1, abort_flag) || !mbar_wait(&S.dp_read, gi & 1, abort_flag)) {
+          const int q_s = stage, do_s = (stage + 1) % RING;  // the ring holds Q_g, then dO_g
+          const uint32_t ph_q = ph, ph_do = (stage + 1 == RING) ? ph ^ 1 : ph;
+          if ((stage += 2) >= RING) { stage -= RING; ph ^= 1; }
+          if (!mbar_wait(&S.p_ready[gi & 1], (gi >> 1) & 1, abort_flag) || !wait_free(dv_ok, &S.dv_free) ||
+              !mbar_wait(&S.ring_full[do_s], ph_do, abort_flag)) {
             ok = false;
             break;
           }
-          uint32_t q_n = 0, do_n = 0;
-          int q_ns = 0, do_ns = 0;
-          if (i + 1 < nq) {  // the next tile's scores while the epilogue works on dS'ᵀ(gi)
-            if (!next_stage(q_n, q_ns)) { ok = false; break; }
-            issue_s(gi + 1, q_n);
-          }
-          if (!wait_free(dv_ok, &S.dv_free)) { ok = false; break; }
           tc_fence_after();
           {  // dV += Pᵀ dO_g: Pᵀ packed in region g & 1 (query rows 16kk..: column 32(kk/2) + 8(kk%2))
-            const SmemDesc od = attn::mnmajor_base(do_a);
+            const SmemDesc od = attn::mnmajor_base(ring_addr + do_s * Cfg::TILE);
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
               tc_mma_ts_h(tmem + Cfg::DV_COL, tmem + Cfg::r_col(gi & 1) + 32 * (kk >> 1) + 8 * (kk & 1),
                           od.lo + attn::mnmajor_step(kk), od.hi, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&S.pv_done);
-          // dP of the next tile goes into the region Pᵀ(g) leaves, as soon as dV(g)
-          // has read it, before dK(g), so that the epilogue gets it early
-          if (i + 1 < nq) {
-            if (!next_stage(do_n, do_ns) || !issue_dp(gi + 1, do_n)) { ok = false; break; }
-            if (i + 2 == nq) tc_commit(&S.kv_empty);
+          tc_commit(&S.pv_done[gi & 1]);
+          tc_commit(&S.ring_empty[do_s]);
+          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag) || !wait_free(dk_ok, &S.dk_free) ||
+              !mbar_wait(&S.ring_full[q_s], ph_q, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag) || !wait_free(dk_ok, &S.dk_free)) { ok = false; break; }
           tc_fence_after();
           {  // dK += dS'ᵀ Q_g
-            const SmemDesc sd = attn::kmajor_base(ds_addr), qd = attn::mnmajor_base(q_a);
+            const SmemDesc sd = attn::kmajor_base(ds_addr), qd = attn::mnmajor_base(ring_addr + q_s * Cfg::TILE);
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
               tc_mma_ss_h(tmem + Cfg::DK_COL, sd.lo + attn::kmajor_step(kk), sd.hi, qd.lo + attn::mnmajor_step(kk),
@@ -783,13 +798,6 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
           }
           tc_commit(&S.dk_done);
           tc_commit(&S.ring_empty[q_s]);
-          tc_commit(&S.ring_empty[do_s]);
-          if (i + 1 < nq) {
-            q_a = q_n;
-            q_s = q_ns;
-            do_a = do_n;
-            do_s = do_ns;
-          }
         }
         // (an item without query tiles has not waited for the accumulators yet)
         if (!ok || !wait_free(dv_ok, &S.dv_free) || !wait_free(dk_ok, &S.dk_free)) {
@@ -851,7 +859,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.p_ready);  // dV(gi) may read Pᵀ
+        if (lane == 0) mbar_arrive(&S.p_ready[gi & 1]);  // dV(gi) may read Pᵀ
         // phase 2: dS'ᵀ = (M ⊙ silu') ⊙ dPᵀ, once dPᵀ is there and dK(gi - 1)
         // has finished reading the shared dS'ᵀ tile
         if (!mbar_wait(&S.dp_full, gi & 1, abort_flag)) { ok = false; break; }
