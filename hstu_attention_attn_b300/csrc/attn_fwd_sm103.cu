@@ -16,15 +16,19 @@
 // Persistent kernel, one CTA per SM; a work item is one query tile of one
 // (user, head).  The score tiles are double-buffered in TMEM, so the tensor
 // core computes S of key tile j+1 while the epilogue turns S_j into P_j:
-//   warp 0       TMA: Q per item (two buffers), then K and V tiles through a
-//                4-stage ring in the order the MMAs consume them
-//   warp 1       MMA issuer (one thread) + TMEM owner
-//   warps 2..17  epilogue: 4 lane quarters x 4 groups of 32 key columns
+//   warp 0       TMA: Q per item (one buffer, released once the item's last S
+//                completes), then K tiles through a 3-stage ring and V tiles
+//                through a 2-stage ring
+//   warp 1       S issuer (one thread) + TMEM owner
+//   warp 2       PV issuer (one thread)
+//   warps 3..18  epilogue: 4 lane quarters x 4 groups of 32 key columns
 //                (thread = query row = TMEM lane), then the O store
-// Per key tile j (global count g over the CTA's items, buffer g & 1) the
-// issuer runs PV(j), then S(j+2) into the buffer PV(j) has just read, after
-// PV(j) has completed; S(j+1) was issued before PV(j), so the epilogue of
-// tile j+1 overlaps PV(j).
+// Key tiles are counted over the CTA's items (g); tile g uses score buffer
+// g & 1.  The S issuer writes S(g) once PV(g - 2) has read the P that buffer
+// held, so S(g + 1) is computed while the epilogue turns S(g) into P(g) and
+// PV(g) runs.  Each issuer waits only on its own operands: a thread that
+// issues blocks while the tensor core drains its queue, and two issuers keep
+// one product queued behind the other.
 // TMEM (512 columns): S/P buffers [0,128) and [128,256); two O accumulators
 // of d_h columns from 256 (items alternate, so one item's O store overlaps the
 // next item's products).  P overwrites S as packed f16: the 32 keys of column
@@ -39,13 +43,14 @@ using attn::silu_half;
 constexpr int BQ = 128, BKV = 128;
 constexpr int NUM_THREADS = 608;  // 19 warps
 constexpr int EPI_WARPS = 16;
-constexpr int RING = 4;
+// shared memory: QB buffers of Q, then the K ring (KR stages) and the V ring (VR)
+constexpr int QB = 1, KR = 3, VR = 2, RING = KR + VR;
 constexpr int STG_BYTES = 2048;  // per-warp O staging: one [32][32] f16 box
 
 template <int D>
 struct FwdCfg {
   static constexpr int TILE = BQ * D * 2;  // one Q / K / V tile (f16)
-  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int RING_OFF = QB * TILE;
   static constexpr int STG_OFF = RING_OFF + RING * TILE;  // O staging, one buffer per epilogue warp
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
@@ -54,7 +59,7 @@ struct FwdCfg {
 };
 
 struct FwdBars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[QB], q_empty[QB];
   uint64_t ring_full[RING], ring_empty[RING];
   uint64_t s_full[2], p_full[2], pv_done[2], o_full[2], o_free[2];
   uint32_t tmem_base;
@@ -161,8 +166,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.q_full[i], 1);
-      mbar_init(&S.q_empty[i], 1);
+      if (i < QB) {
+        mbar_init(&S.q_full[i], 1);
+        mbar_init(&S.q_empty[i], 1);
+      }
       mbar_init(&S.s_full[i], 1);
       mbar_init(&S.p_full[i], EPI_WARPS);
       mbar_init(&S.pv_done[i], 1);
@@ -203,14 +210,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
       int st[2] = {0, 0};
       uint32_t ph[2] = {0, 0};
       auto load_kv = [&](int which, int row, int col_h) -> bool {  // which: 0 K, 1 V
-        const int slot = 2 * which + st[which];
+        const int slot = (which ? KR : 0) + st[which];
         if (!mbar_wait(&S.ring_empty[slot], ph[which] ^ 1, abort_flag)) return false;
         uint8_t* dst = sRing + slot * Cfg::TILE;
         mbar_arrive_expect_tx(&S.ring_full[slot], Cfg::TILE);
         const CUtensorMap* m = which ? &tmV : &tmK;
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) tma_load_2d(dst + cc * 16384, m, &S.ring_full[slot], col_h + 64 * cc, row);
-        if (++st[which] == 2) { st[which] = 0; ph[which] ^= 1; }
+        if (++st[which] == (which ? VR : KR)) { st[which] = 0; ph[which] ^= 1; }
         return true;
       };
       int it = 0;
@@ -219,8 +226,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
         if (idx >= total) break;
         const ItemCtx c = item_ctx(p, idx);
         const int col_h = c.h * D;
-        const int qb = it & 1;
-        if (!mbar_wait(&S.q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        const int qb = it % QB;
+        if (!mbar_wait(&S.q_empty[qb], ((it / QB) & 1) ^ 1, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(&S.q_full[qb], Cfg::TILE);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
@@ -247,9 +254,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
         const int idx = item_at(r);
         if (idx >= total) break;
         const ItemCtx c = item_ctx(p, idx);
-        const int qb = it & 1;
+        const int qb = it % QB;
         const uint32_t q_addr = smem_u32(sQ + qb * Cfg::TILE);
-        if (!mbar_wait(&S.q_full[qb], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&S.q_full[qb], (it / QB) & 1, abort_flag)) { ok = false; break; }
         const int n = c.n;
         for (int t = 0; t < n; ++t) {
           const int gs = g + t, sb = gs & 1;
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
                         kd.hi, idesc_s, kk > 0 ? 1u : 0u);
           tc_commit(&S.s_full[sb]);
           tc_commit(&S.ring_empty[ks]);
-          if (++ks == 2) { ks = 0; kph ^= 1; }
+          if (++ks == KR) { ks = 0; kph ^= 1; }
         }
         if (!ok) break;
         tc_commit(&S.q_empty[qb]);  // once the item's products of Q complete
@@ -290,16 +297,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)  // 19 warps
         for (int j = 0; j < n; ++j) {
           const int gj = g + j, sb = gj & 1;
           if (!mbar_wait(&S.p_full[sb], (gj >> 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&S.ring_full[2 + vs], vph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&S.ring_full[KR + vs], vph, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const SmemDesc vd = attn::mnmajor_base(ring_addr + (2 + vs) * Cfg::TILE);
+          const SmemDesc vd = attn::mnmajor_base(ring_addr + (KR + vs) * Cfg::TILE);
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)  // keys 16kk..16kk+15: column group kk/2, packed half kk&1
             tc_mma_ts_h(tmem + Cfg::o_col(ob), tmem + Cfg::s_col(sb) + 32 * (kk >> 1) + 8 * (kk & 1),
                         vd.lo + attn::mnmajor_step(kk), vd.hi, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&S.pv_done[sb]);
-          tc_commit(&S.ring_empty[2 + vs]);
-          if (++vs == 2) { vs = 0; vph ^= 1; }
+          tc_commit(&S.ring_empty[KR + vs]);
+          if (++vs == VR) { vs = 0; vph ^= 1; }
         }
         if (!ok) break;
         tc_commit(&S.o_full[ob]);
