@@ -555,7 +555,8 @@ def run_mine(args):
         def unpack(blk):
             o = starts
             db_ = DeviceBatch(blk[o[0]:o[0] + 4 * (batch.B + 1)].view(torch.int32), blk[o[1]:o[1] + T],
-                              blk[o[2]:o[2] + 8 * T].view(torch.int64), batch.B, T)
+                              blk[o[2]:o[2] + 8 * T].view(torch.int64), batch.B, T,
+                              np.ascontiguousarray(batch.offsets, dtype=np.int32))
             rows_ = blk[o[3]:o[3] + 4 * n_rows].view(torch.int32)
             dxc_ = blk[o[4]:o[4] + 2 * n_rows * D].view(torch.bfloat16).view(n_rows, D)
             return db_, rows_, dxc_

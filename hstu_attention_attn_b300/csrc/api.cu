@@ -20,7 +20,7 @@ namespace mtgr {
 cudaError_t launch_user_info(const int32_t*, int32_t, const uint8_t*, int64_t, UserInfo*, int32_t*, cudaStream_t,
                              const int32_t* n_norm = nullptr, const int32_t* q_begin = nullptr);
 cudaError_t launch_plan(const int32_t*, int32_t, const uint8_t*, int64_t, int32_t, int32_t*, int32_t*, cudaStream_t,
-                        const int32_t* n_norm = nullptr, const int32_t* q_begin = nullptr);
+                        const int32_t* n_norm = nullptr, const int32_t* q_begin = nullptr, int64_t ds_cap = 0);
 cudaError_t launch_visible_counts(const int32_t*, int32_t, const uint8_t*, const int64_t*, int64_t, int32_t*,
                                   int64_t*, cudaStream_t);
 cudaError_t launch_expand_rows(const void*, const int32_t*, int64_t, void*, int64_t, int64_t, cudaStream_t);
@@ -53,7 +53,7 @@ cudaError_t launch_ln_gate_fwd_parts(const float*, int64_t, __half*, const TU*, 
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts, void* dq,
                                 void* dk, void* dv, int64_t ldg, const void* mq, const void* mk, const void* mv,
-                                bool g_f16, int32_t* status, cudaStream_t s);
+                                bool g_f16, int32_t* status, cudaStream_t s, uint8_t* ds_store, int64_t ds_cap);
 
 // ---- kernel tracing ----
 namespace {
@@ -308,6 +308,24 @@ static mtgr_status check_meta(const int32_t* offsets, int32_t B, const uint8_t* 
   return MTGR_OK;
 }
 
+// The backward's dS tile store: the bytes of the caller's workspace beyond
+// the `used` bytes the call needs, from the next 1024-byte boundary, as whole
+// dS tiles (plan.cuh); no slots when nothing is left over.
+struct DsStore {
+  uint8_t* base = nullptr;
+  int64_t slots = 0;
+};
+static DsStore ds_store_region(uint8_t* ws, size_t ws_bytes, size_t used) {
+  DsStore r;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ws), end = a + ws_bytes;
+  const uintptr_t start = (a + used + 1023) & ~uintptr_t(1023);
+  if (ws_bytes > used && end > start && (end - start) >= (uintptr_t)kDsTileBytes) {
+    r.base = reinterpret_cast<uint8_t*>(start);
+    r.slots = (int64_t)((end - start) / kDsTileBytes);
+  }
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // bf16-path attention on f16 tensor-core operands (shared by the attention
 // entry points and the layer).  u is bf16 or f16 (u_f16); y, dq/dk/dv/du bf16.
@@ -360,12 +378,12 @@ static mtgr_status attn_bwd_bf16_core(const void* dy, const __half* q16, const _
                                       const __half* o, const float* mean, const float* rstd, const int32_t* offsets,
                                       int32_t B, const uint8_t* gid, const int64_t* ts, int64_t T, int H, int d,
                                       void* dq, void* dk, void* dv, void* du, int64_t ldg, const void* dsilu,
-                                      uint8_t* ws, const AttnWs& w, cudaStream_t s) {
+                                      uint8_t* ws, const AttnWs& w, cudaStream_t s, const DsStore& ds) {
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
   MTGR_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "attn_bwd status");
   if (T == 0 || B == 0) return MTGR_OK;
-  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s), "attn_bwd plan");
+  MTGR_CUDA_TRY(launch_plan(offsets, B, gid, T, H, plan, status, s, nullptr, nullptr, ds.slots), "attn_bwd plan");
   const int64_t HD = (int64_t)H * d;
   __half* dO = reinterpret_cast<__half*>(ws + w.dO);
   cudaError_t e =
@@ -378,7 +396,7 @@ static mtgr_status attn_bwd_bf16_core(const void* dy, const __half* q16, const _
   const uint16_t* m16 = static_cast<const uint16_t*>(dsilu);
   MTGR_CUDA_TRY(launch_attn_bwd_f16(q16, k16, v16, ld16, dO, T, H, d, plan, B, ts, dq, dk, dv, ldg,
                                     m16 ? m16 + HD : nullptr, m16 ? m16 + 2 * HD : nullptr,
-                                    m16 ? m16 + 3 * HD : nullptr, layer16, status, s),
+                                    m16 ? m16 + 3 * HD : nullptr, layer16, status, s, ds.base, ds.slots),
                 "attn_bwd tcgen05");
   return MTGR_OK;
 }
@@ -458,6 +476,18 @@ mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const u
   return MTGR_OK;
 }
 
+mtgr_status mtgr_debug_plan_counts(const void* workspace, int32_t B, int32_t* counts_host, mtgr_stream_t stream) {
+  REQUIRE(workspace != nullptr && counts_host != nullptr && B >= 0, MTGR_ERR_INVALID_ARG,
+          "NULL workspace / counts_host or B < 0");
+  // the attention workspace (first in a layer workspace): status word, then the plan
+  const int32_t* plan = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(workspace) + 256);
+  const int32_t* counts = plan + plan_layout(B, 0, 1).counts;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MTGR_CUDA_TRY(cudaMemcpyAsync(counts_host, counts, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, s), "plan counts");
+  MTGR_CUDA_TRY(cudaStreamSynchronize(s), "plan counts");
+  return MTGR_OK;
+}
+
 mtgr_status mtgr_debug_wait_timeout(int32_t* status_word, mtgr_stream_t stream) {
   REQUIRE(status_word != nullptr, MTGR_ERR_INVALID_ARG, "status_word is NULL");
   MTGR_CUDA_TRY(launch_wait_timeout(status_word, reinterpret_cast<cudaStream_t>(stream)), "wait_timeout");
@@ -533,6 +563,21 @@ mtgr_status mtgr_group_layernorm_bwd(const void* dy, const void* x, const float*
 size_t mtgr_attn_workspace_size(int32_t B, int64_t T, int32_t n_heads, int32_t d_h, mtgr_dtype dtype) {
   if (B < 0 || T < 0 || n_heads <= 0 || d_h <= 0) return 0;
   return attn_ws(B, T, n_heads, d_h, dtype).total;
+}
+
+size_t mtgr_attn_ds_store_size(const int32_t* offsets_host, int32_t B, int32_t n_heads, int32_t d_h,
+                               mtgr_dtype dtype) {
+  if (offsets_host == nullptr || B <= 0 || n_heads <= 0) return 0;
+  if (dtype != MTGR_BF16 || (d_h != 64 && d_h != 128)) return 0;
+  int64_t tiles = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t n = (int64_t)offsets_host[b + 1] - offsets_host[b];
+    if (n < 0) return 0;
+    const int64_t nt = (n + kTile - 1) / kTile;
+    tiles += nt * nt;
+  }
+  if (tiles == 0) return 0;
+  return (size_t)tiles * n_heads * kDsTileBytes + 1024;  // + the 1024-byte alignment of the store
 }
 
 static mtgr_status check_attn(const void* q, const void* k, const void* v, const void* u, int64_t ld_in,
@@ -635,7 +680,8 @@ mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, con
     return attn_bwd_bf16_core(static_cast<const bf*>(dy), q16, k16, v16, HD, u, false, ld_in,
                               static_cast<const __half*>(o_saved), ln_mean, ln_rstd, offsets, B, gid, ts, T, n_heads,
                               d_h, static_cast<bf*>(dq), static_cast<bf*>(dk), static_cast<bf*>(dv),
-                              static_cast<bf*>(du), ld_grad, static_cast<const bf*>(dsilu_uqkv), ws, w, s);
+                              static_cast<bf*>(du), ld_grad, static_cast<const bf*>(dsilu_uqkv), ws, w, s,
+                              ds_store_region(ws, workspace_bytes, w.total));
   }
   int32_t* status = reinterpret_cast<int32_t*>(ws + w.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + w.plan);
@@ -947,7 +993,8 @@ mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, cons
     __half* dz = static_cast<__half*>(dZ);
     r = attn_bwd_bf16_core(dY, a + HD, a + 2 * HD, a + 3 * HD, N4, a, true, N4, static_cast<const __half*>(sv->o),
                            sv->ln_mean, sv->ln_rstd, offsets, B, gid, ts, T, H, d, dz + HD, dz + 2 * HD, dz + 3 * HD,
-                           dz, N4, sv->dsilu, ws + L.attn_base, L.attn, s);
+                           dz, N4, sv->dsilu, ws + L.attn_base, L.attn, s,
+                           ds_store_region(ws, workspace_bytes, L.total));
   } else {
     const float* a = static_cast<const float*>(sv->uqkv);
     float* dz = static_cast<float*>(dZ);

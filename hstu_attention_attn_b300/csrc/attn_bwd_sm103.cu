@@ -21,12 +21,17 @@
 //    dQ += dS K reads it from TMEM.
 // Recomputing S and dP in the dQ kernel costs 2 extra MMAs per tile pair but
 // avoids accumulating dQ across CTAs through L2 reductions (64 KB of fp32
-// read-modify-write per tile pair).
+// read-modify-write per tile pair).  When the caller lends a store for them,
+// the dK/dV kernel also copies each dSᵀ tile (32 KB) to HBM and a third
+// kernel forms dQ = dS K from the stored tiles: one product per tile pair and
+// 64 KB of HBM traffic (written once, read once) instead of two recomputed
+// products; the plan decides on the device which dQ kernel runs.
 //
 // Warps in both: 0 TMA, 1 the first MMA issuer (the score products) + TMEM
 // owner, 2..17 score epilogue (thread = TMEM lane = tile row; 4 lane quarters
 // x 4 groups of 32 columns), 18..21 output (TMEM -> 16-bit gradients), 22 the
-// second MMA issuer (the gradient products).
+// second MMA issuer (the gradient products); 23 in the dK/dV kernel copies
+// the dSᵀ tiles to the store.
 #include "attn_sm103.cuh"
 
 namespace mtgr {
@@ -50,6 +55,11 @@ struct BwdParams {
   int H;
   float scale;  // 1/sqrt(d_h)
   int32_t* status;
+  // stored dS tiles (plan.cuh): the dK/dV kernel writes each dS'ᵀ tile to its
+  // slot and the dQ pass reads them back, when *ds_on (set by the plan) is 1
+  uint8_t* ds_store;
+  const int64_t* ds_base;
+  const int32_t* ds_on;
 };
 
 // ---------------------------------------------------------------------------
@@ -113,11 +123,12 @@ struct DqBars {
 struct DqItem {
   UserInfo u;
   QTileKeys keys;
-  int qt, h;
+  int qt, h, b;
 };
 __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int idx) {
   DqItem c;
   const WorkItem wi = p.items[idx];
+  c.b = wi.b;
   c.h = wi.h();
   c.u = p.users[wi.b];
   c.qt = wi.t();
@@ -180,6 +191,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   using Cfg = DqCfg<D>;
   constexpr int RING = Cfg::RING;
   constexpr int NQB = Cfg::NQB;
+  if (p.ds_on != nullptr && *p.ds_on != 0) return;  // dQ comes from the stored dS tiles instead
   const int total = p.count[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -484,13 +496,209 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 }
 
 // =============================================================================
+// dQ from the stored dS tiles
+// =============================================================================
+// When the dK/dV kernel has kept its dS'ᵀ tiles, dQ needs one product per
+// tile pair instead of three: dQ += dS' K_j, with dS' read straight from the
+// stored [128 keys][128 queries] tile (the MN-major form of the A operand) and
+// K_j MN-major as in the recomputing kernel.  The kernel streams 32 KB of dS'
+// per tile pair from HBM, so memory, not the tensor core, sets its pace.
+// Warps: 0 loads (bulk copy of the dS'ᵀ tile, TMA of K_j), 1 MMA issuer +
+// TMEM owner, 2..9 output (TMEM -> 16-bit dQ; 4 lane quarters x 2 column
+// halves).  Two dQ accumulators of d_h columns alternate between items.
+constexpr int DQS_THREADS = 320;
+constexpr int DQS_OUT = 8;
+
+template <int D>
+struct DqsCfg {
+  static constexpr int KTILE = BT * D * 2;
+  static constexpr int STAGE = kDsTileBytes + KTILE;  // [dS'ᵀ tile][K_j], both 1024-byte aligned
+  static constexpr int STAGES = D == 128 ? 3 : 4;
+  static constexpr int BAR_OFF = STAGES * STAGE;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int TMEM_COLS = 2 * D;  // 256 or 128
+};
+
+struct DqsBars {
+  uint64_t full[4], empty[4], acc_full[2], acc_free[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, typename TG>
+__global__ void __launch_bounds__(DQS_THREADS, 1)
+    attn_bwd_dq_ds_kernel(const __grid_constant__ CUtensorMap tmK, const BwdParams p) {
+  using Cfg = DqsCfg<D>;
+  constexpr int ST = Cfg::STAGES;
+  if (p.ds_on == nullptr || *p.ds_on == 0) return;  // the tiles were not kept: the recomputing kernel runs
+  const int total = p.count[0];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqsBars& S = *reinterpret_cast<DqsBars*>(base + Cfg::BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_free[i], DQS_OUT);
+    }
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmK);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- loads: per key tile j, the stored dS'ᵀ(qt, j) and K_j ----------------
+      int st = 0;
+      uint32_t ph = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DqItem c = dq_item(p, idx);
+        const int nt = ceil_div(c.u.n, BT);
+        const int64_t b0 = p.ds_base[c.b];
+        const int nk = c.keys.count();
+        for (int j = 0; j < nk; ++j) {
+          const int kt = c.keys.kt(j, c.qt);
+          if (!mbar_wait_sleepy(&S.empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+          uint8_t* dst = base + st * Cfg::STAGE;
+          mbar_arrive_expect_tx(&S.full[st], Cfg::STAGE);
+          bulk_load(dst, p.ds_store + ds_slot(b0, nt, c.h, kt, c.qt) * kDsTileBytes, kDsTileBytes, &S.full[st]);
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_load_2d(dst + kDsTileBytes + cc * 16384, &tmK, &S.full[st], c.h * D + 64 * cc, c.u.start + kt * BT);
+          if (++st == ST) { st = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: dQ(item) += dS'(j) K_j into accumulator it & 1 ----------------
+      constexpr uint32_t idesc = idesc_f16_f32(BT, D, true, true);
+      const uint32_t sbase = smem_u32(base);
+      int st = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      for (int r = 0; ok; ++r, ++it) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DqItem c = dq_item(p, idx);
+        const int ab = it & 1;
+        // the accumulator holds item it - 2 until the output warps have read it
+        if (it >= 2 && !mbar_wait(&S.acc_free[ab], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const int nk = c.keys.count();
+        for (int j = 0; j < nk; ++j) {
+          if (!mbar_wait(&S.full[st], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = sbase + st * Cfg::STAGE;
+          const SmemDesc ad = attn::mnmajor_base(sa), bd = attn::mnmajor_base(sa + kDsTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)  // keys 16kk .. 16kk+15
+            tc_mma_ss_h(tmem + ab * D, ad.lo + attn::mnmajor_step(kk), ad.hi, bd.lo + attn::mnmajor_step(kk), bd.hi,
+                        idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&S.empty[st]);
+          if (++st == ST) { st = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&S.acc_full[ab]);
+      }
+    }
+  } else {
+    // ---------------- dQ output (thread = query row; this warp's half of the columns) ----------------
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const bool has_m = p.m0 != nullptr;
+    constexpr int NC = D / 64;  // 32-column chunks per half
+    int it = 0;
+    for (int r = 0; ok; ++r, ++it) {
+      const int idx = item_at(r);
+      if (idx >= total) break;
+      const DqItem c = dq_item(p, idx);
+      const int ab = it & 1;
+      const int rl = c.qt * BT + quarter * 32 + lane;  // this lane's query row, segment-relative
+      const bool row_ok = rl < c.u.n;
+      const bool any = c.keys.count() > 0;
+      const int64_t grow = (int64_t)c.u.start + rl;
+      const float cn = p.scale / (float)c.u.nu;  // the factor c / n_u left out of dS'
+      const int col0 = half * (D / 2);
+      const uint16_t* mrow = has_m ? p.m0 + grow * p.ldm + c.h * D + col0 : nullptr;
+      if (has_m && row_ok) prefetch_l2(mrow, D);
+      if (!mbar_wait_sleepy(&S.acc_full[ab], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint16_t* orow = p.g0 + grow * p.ldg + c.h * D + col0;
+#pragma unroll 1
+      for (int cc = 0; cc < NC; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + ab * D + col0 + cc * 32 + lane_sel, rr);
+        uint4 mm[4];  // the multipliers of this chunk load while the TMEM read completes
+        if (has_m && row_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) mm[v] = *reinterpret_cast<const uint4*>(mrow + cc * 32 + 8 * v);
+        }
+        tmem_wait_ld();
+        if (cc == NC - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.acc_free[ab]);
+        }
+        if (!row_ok) continue;
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = any ? __uint_as_float(rr[e]) * cn : 0.f;
+        if (has_m) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t w[4] = {mm[v].x, mm[v].y, mm[v].z, mm[v].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              x[8 * v + 2 * t] *= lo16<TG>(w[t]);
+              x[8 * v + 2 * t + 1] *= hi16<TG>(w[t]);
+            }
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(orow + cc * 32 + 8 * v) = pack8<TG>(x + 8 * v);
+      }
+    }
+  }
+
+  if (!ok) {
+    *abort_flag = 1;
+    if (p.status) atomicOr(p.status, DEV_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+// =============================================================================
 // dK/dV kernel
 // =============================================================================
 // Warps: 0 TMA, 1 first MMA issuer (Sᵀ, dPᵀ) + TMEM owner, 2..17 score
 // epilogue (thread = key row; 4 lane quarters x 4 groups of 32 query columns),
 // 18..21 output (TMEM -> 16-bit dV then dK, one warp per lane quarter), 22
-// second MMA issuer (dV, dK).
-constexpr int DKV_THREADS = 736;  // + the second MMA issuer (warp 22)
+// second MMA issuer (dV, dK), 23 the dS'ᵀ tile store (when the caller keeps
+// the tiles for the dQ pass).
+constexpr int DKV_THREADS = 768;
 constexpr int DKV_EPI = 16;
 constexpr int DKV_OUT = 4;
 
@@ -512,6 +720,7 @@ struct DkvBars {
   uint64_t kv_full, kv_empty;
   uint64_t ring_full[8], ring_empty[8];
   uint64_t s_full, dp_full, p_ready[2], dp_read, ds_ready, pv_done[2], dk_done, dkdv_full, dv_free, dk_free;
+  uint64_t ds_copied;  // the store has read dS'ᵀ(g) out of shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -519,11 +728,12 @@ struct DkvBars {
 struct DkvItem {
   UserInfo u;
   KTileQueries qs;
-  int kt, h;
+  int kt, h, b;
 };
 __device__ __forceinline__ DkvItem dkv_item(const BwdParams& p, int idx) {
   DkvItem c;
   const WorkItem wi = p.items[idx];
+  c.b = wi.b;
   c.h = wi.h();
   c.u = p.users[wi.b];
   c.kt = wi.t();
@@ -629,6 +839,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     mbar_init(&S.dkdv_full, 1);
     mbar_init(&S.dv_free, DKV_OUT);
     mbar_init(&S.dk_free, DKV_OUT);
+    mbar_init(&S.ds_copied, 1);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -648,6 +859,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
   bool ok = true;
+  const bool store_on = p.ds_on != nullptr && *p.ds_on != 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -808,6 +1020,33 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         tc_commit(&S.dkdv_full);
       }
     }
+  } else if (warp == 3 + DKV_EPI + DKV_OUT) {
+    // ---------------- dS'ᵀ store: each tile the epilogue leaves in shared memory
+    // also goes, by one bulk copy, to its slot of the caller's store ----------------
+    if (store_on && lane == 0) {
+      const uint64_t pol = l2_evict_first();  // written once, read once by the dQ pass
+      int g = 0;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_at(r);
+        if (idx >= total) break;
+        const DkvItem c = dkv_item(p, idx);
+        const int nt = ceil_div(c.u.n, BT);
+        const int64_t b0 = p.ds_base[c.b];
+        const int nq = c.qs.count();
+        for (int i = 0; i < nq; ++i) {
+          const int gi = g + i;
+          if (!mbar_wait(&S.ds_ready, gi & 1, abort_flag)) { ok = false; break; }
+          const int64_t slot = ds_slot(b0, nt, c.h, c.kt, c.qs.qt(i, c.kt));
+          bulk_store(p.ds_store + slot * kDsTileBytes, sDS, kDsTileBytes, pol);
+          tma_store_commit();
+          tma_store_wait_read_n<0>();  // the epilogue may write dS'ᵀ(gi + 1) once the copy has read the tile
+          mbar_arrive(&S.ds_copied);
+        }
+        if (!ok) break;
+        g += nq;
+      }
+      tma_store_wait_all();
+    }
   } else if (warp < 2 + DKV_EPI) {
     // ---------------- Pᵀ / dS'ᵀ epilogue (thread = key row) ----------------
     const int ew = warp - 2;
@@ -870,16 +1109,20 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.dp_read);  // Sᵀ(gi + 1) may overwrite dPᵀ
-        if (gi >= 1 && !mbar_wait(&S.dk_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+        uint4 pd[4];  // the row's 32 values of dS'ᵀ as four 16-byte pieces
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          uint32_t pd[8];
+          uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pd[e] = attn::ds_pair(dsl[ch][e], buf[ch][2 * e], buf[ch][2 * e + 1]);
-          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch) ^ (kr & 7)) * 16)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
-          *reinterpret_cast<uint4*>(ds_row + (((jb + 2 * ch + 1) ^ (kr & 7)) * 16)) =
-              make_uint4(pd[4], pd[5], pd[6], pd[7]);
+          for (int e = 0; e < 8; ++e) w[e] = attn::ds_pair(dsl[ch][e], buf[ch][2 * e], buf[ch][2 * e + 1]);
+          pd[2 * ch] = make_uint4(w[0], w[1], w[2], w[3]);
+          pd[2 * ch + 1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
+        // the shared tile is free once dK(gi - 1) and (with the store) its copy have read it
+        if (gi >= 1 && !mbar_wait(&S.dk_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+        if (store_on && gi >= 1 && !mbar_wait(&S.ds_copied, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(ds_row + (((jb + v) ^ (kr & 7)) * 16)) = pd[v];
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -978,6 +1221,17 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
+  if (pq.ds_on != nullptr) {
+    // dQ from the kept dS tiles; the recomputing kernel below then returns at once
+    // (which of the two works is decided on the device, by the plan)
+    TraceScope tr("attn_bwd_dq", s);
+    auto kern = attn_bwd_dq_ds_kernel<D, TG>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqsCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, DQS_THREADS, DqsCfg<D>::SMEM, s>>>(tk, pq);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   TraceScope tr("attn_bwd_dq", s);
   auto kern = attn_bwd_dq_kernel<D, TG>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM);
@@ -992,11 +1246,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 // (g_f16) or bf16 with row stride ldg, each multiplied elementwise by the
 // multiplier block mq / mk / mv of the same type when given (row stride
 // 4*H*d; the layer passes silu'(z) of its UQKV projection).  Every row of
-// every segment is written.
+// every segment is written.  ds_store, ds_cap: the caller's store of dS tiles
+// (1024-byte aligned, ds_cap tiles; the plan was built with the same ds_cap),
+// or nullptr / 0 for the dQ pass that recomputes S and dP.
 cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* v, int64_t ld, const __half* dO,
                                 int64_t T, int H, int d, const int32_t* plan, int32_t B, const int64_t* ts, void* dq,
                                 void* dk, void* dv, int64_t ldg, const void* mq, const void* mk, const void* mv,
-                                bool g_f16, int32_t* status, cudaStream_t s) {
+                                bool g_f16, int32_t* status, cudaStream_t s, uint8_t* ds_store, int64_t ds_cap) {
   if (T == 0 || B == 0) return cudaSuccess;
   const PlanLayout L = plan_layout(B, T, H);
   const int HD = H * d;
@@ -1012,6 +1268,11 @@ cudaError_t launch_attn_bwd_f16(const __half* q, const __half* k, const __half* 
   pa.H = H;
   pa.scale = 1.0f / sqrtf((float)d);
   pa.status = status;
+  if (ds_store != nullptr && ds_cap > 0) {
+    pa.ds_store = ds_store;
+    pa.ds_base = reinterpret_cast<const int64_t*>(plan + L.ds_base);
+    pa.ds_on = plan + L.counts + 3;
+  }
   BwdParams pq = pa;
   pa.items = reinterpret_cast<const WorkItem*>(plan + L.bwd_items);
   pa.count = plan + L.counts + 1;

@@ -60,9 +60,12 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
                                                           WorkItem* __restrict__ fwd_items,
                                                           WorkItem* __restrict__ bwd_items,
                                                           WorkItem* __restrict__ dq_items, int64_t max_items,
+                                                          int64_t* __restrict__ ds_base, int64_t ds_cap,
                                                           int32_t* __restrict__ status) {
   __shared__ int32_t hist[3][kBuckets];  // items of each list per cost bucket, then cursors
   __shared__ int32_t tot[3];
+  __shared__ long long wsum[32];
+  __shared__ long long ds_run;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
   for (int i = tid; i < 3 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
@@ -134,11 +137,47 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
       if (oq < max_items) dq_items[oq] = WorkItem{b, t | (h << 16)};
     }
   }
+  // dS tile slots (plan.cuh): exclusive prefix over the users, in user order,
+  // of H * nt^2; the backward keeps its dS tiles only when all of them fit
+  if (tid == 0) ds_run = 0;
   __syncthreads();
+  if (ds_base != nullptr) {
+    for (int c0 = 0; c0 < B; c0 += (int)blockDim.x) {
+      const int b = c0 + tid;
+      long long v = 0;
+      if (b < B) {
+        const long long nt = ceil_div(users[b].n, kTile);
+        v = (long long)H * nt * nt;
+      }
+      long long x = v;  // inclusive scan in the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      if (warp == 0) {  // inclusive scan of the warp sums
+        long long w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) w += y;
+        }
+        wsum[lane] = w;
+      }
+      __syncthreads();
+      if (b < B) ds_base[b] = ds_run + (warp > 0 ? wsum[warp - 1] : 0) + x - v;
+      __syncthreads();
+      if (tid == 0) ds_run += wsum[31];
+      __syncthreads();
+    }
+  }
   if (tid == 0) {
     counts[0] = tot[0];
     counts[1] = tot[1];
     counts[2] = tot[2];
+    counts[3] = (ds_base != nullptr && ds_cap > 0 && ds_run <= ds_cap) ? 1 : 0;
     if ((tot[0] > max_items || tot[1] > max_items || tot[2] > max_items) && status) atomicOr(status, DEV_ERR_PLAN);
   }
 }
@@ -207,8 +246,11 @@ cudaError_t launch_user_info(const int32_t* offsets, int32_t B, const uint8_t* g
   return cudaGetLastError();
 }
 
+// ds_cap: dS tile slots the caller's store holds (0: the backward recomputes S
+// and dP for dQ; the plan then skips the slot prefix)
 cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, int64_t T, int32_t H, int32_t* ws,
-                        int32_t* status, cudaStream_t s, const int32_t* n_norm, const int32_t* q_begin) {
+                        int32_t* status, cudaStream_t s, const int32_t* n_norm, const int32_t* q_begin,
+                        int64_t ds_cap) {
   const PlanLayout L = plan_layout(B, T, H);
   UserInfo* users = reinterpret_cast<UserInfo*>(ws + L.users);
   cudaError_t e = launch_user_info(offsets, B, gid, T, users, status, s, n_norm, q_begin);
@@ -219,7 +261,9 @@ cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, i
   TraceScope tr("plan_items", s);
   plan_items_kernel<<<1, 1024, 0, s>>>(users, B, H, singles, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.bwd_items),
-                                       reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items, status);
+                                       reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items,
+                                       ds_cap > 0 ? reinterpret_cast<int64_t*>(ws + L.ds_base) : nullptr, ds_cap,
+                                       status);
   return cudaGetLastError();
 }
 

@@ -125,7 +125,9 @@ __host__ __device__ __forceinline__ KTileQueries ktile_queries(const UserInfo& u
 // running CTAs share the user's streamed operands through L2.
 struct PlanLayout {
   int64_t users;      // UserInfo[B]
-  int64_t counts;     // [4]: items of the fwd / bwd key-tile / bwd query-tile lists, (reserved)
+  int64_t counts;     // [4]: items of the fwd / bwd key-tile / bwd query-tile lists; 1 when the
+                      // backward keeps its dS tiles (the batch's tiles fit the caller's store), else 0
+  int64_t ds_base;    // int64[B] (8-byte aligned): first dS tile slot of each user
   int64_t fwd_items;  // WorkItem[max_items]: (user, first query tile of a pair, head)
   int64_t bwd_items;  // WorkItem[max_items]: (user, key tile, head)
   int64_t dq_items;   // WorkItem[max_items]: (user, query tile, head)
@@ -133,6 +135,16 @@ struct PlanLayout {
   int64_t max_items;
 };
 constexpr int kBuckets = 1024;
+
+// The backward's stored dS tiles: one [128 key rows][128 query columns] f16
+// tile, in the 128-byte-swizzled layout of two [128][64] boxes, per (user,
+// head, key tile, query tile) of the user's full tile grid, at slot
+//   ds_base[b] + (h * nt + kt) * nt + qt,   nt = ceil(n_b / 128),
+// with ds_base[b] = H * sum over users b' < b of nt_b'^2.
+constexpr int kDsTileBytes = kTile * kTile * 2;
+__host__ __device__ __forceinline__ int64_t ds_slot(int64_t base, int nt, int h, int kt, int qt) {
+  return base + ((int64_t)h * nt + kt) * nt + qt;
+}
 
 __host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T, int32_t H) {
   PlanLayout L;
@@ -142,6 +154,9 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t B, int64_t T, int32_t 
   o += 6 * (int64_t)B;
   L.counts = o;
   o += 4;
+  o = (o + 1) & ~int64_t(1);  // 8-byte alignment (the plan itself starts 256-byte aligned)
+  L.ds_base = o;
+  o += 2 * (int64_t)B;
   L.fwd_items = o;
   o += 2 * L.max_items;
   L.bwd_items = o;

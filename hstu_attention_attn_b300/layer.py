@@ -21,6 +21,7 @@ class DeviceBatch:
     ts: torch.Tensor        # int64 [T]
     B: int
     T: int
+    offsets_host: np.ndarray | None = None  # the same offsets in host memory (sizes the dS tile store)
 
 
 def device_batch(batch, device="cuda", pin=False) -> DeviceBatch:
@@ -31,7 +32,16 @@ def device_batch(batch, device="cuda", pin=False) -> DeviceBatch:
             t = t.pin_memory()
         return t.to(device, non_blocking=pin)
     return DeviceBatch(mk(batch.offsets, torch.int32), mk(batch.gid, torch.uint8), mk(batch.ts, torch.int64),
-                       len(batch.offsets) - 1, int(batch.offsets[-1]))
+                       len(batch.offsets) - 1, int(batch.offsets[-1]),
+                       np.ascontiguousarray(batch.offsets, dtype=np.int32))
+
+
+def ds_store_bytes(db: DeviceBatch, n_heads, d_h, dtype) -> int:
+    """Workspace bytes beyond the required size with which the bf16 backward
+    keeps its dS tiles and forms dQ from them (0 without host offsets)."""
+    if db.offsets_host is None or dtype != torch.bfloat16:
+        return 0
+    return mtgr.mtgr_attn_ds_store_size(db.offsets_host, n_heads, d_h, mtgr.MTGR_BF16)
 
 
 def _dt(dtype):
@@ -45,12 +55,15 @@ def workspace(nbytes, device="cuda"):
 class HstuAttention:
     """Y = LayerNorm(A·V) ⊙ U with A = M ⊙ silu(QKᵀ/sqrt(d_h)) / n_u (jagged, per head)."""
 
-    def __init__(self, n_heads, d_h, dtype=torch.bfloat16, eps=1e-5, device="cuda"):
+    def __init__(self, n_heads, d_h, dtype=torch.bfloat16, eps=1e-5, device="cuda", ds_store=True):
         self.H, self.dh, self.dtype, self.eps, self.device = n_heads, d_h, dtype, eps, device
+        self.ds_store = ds_store  # lend the backward a store for its dS tiles
         self._ws = None
 
     def _workspace(self, db):
         n = mtgr.mtgr_attn_workspace_size(db.B, db.T, self.H, self.dh, _dt(self.dtype))
+        if self.ds_store:
+            n += ds_store_bytes(db, self.H, self.dh, self.dtype)
         if self._ws is None or self._ws.numel() < n:
             self._ws = workspace(n, self.device)
         return self._ws
@@ -91,8 +104,9 @@ class HstuLayer:
     """One HSTU layer: x' = x + (LN(attn(silu(GLN(x) W_uqkv))) ⊙ U) W_o, forward and backward."""
 
     def __init__(self, d_model, n_heads, d_h, w_uqkv, w_o, gamma, beta, dtype=torch.bfloat16, eps_gln=1e-5,
-                 eps_ln=1e-5, device="cuda"):
+                 eps_ln=1e-5, device="cuda", ds_store=True):
         self.D, self.H, self.dh, self.dtype, self.device = d_model, n_heads, d_h, dtype, device
+        self.ds_store = ds_store  # lend the backward a store for its dS tiles
         to = dict(device=device)
         self.w_uqkv = torch.as_tensor(w_uqkv).to(dtype=dtype, **to).contiguous()
         self.w_o = torch.as_tensor(w_o).to(dtype=dtype, **to).contiguous()
@@ -122,8 +136,10 @@ class HstuLayer:
         self.weights.w_uqkv_f16 = self.weights.w_o_f16 = None
         self._w16 = None
 
-    def _workspace(self, db):
+    def _workspace(self, db, bwd=True):
         n = mtgr.mtgr_layer_workspace_size(db.B, db.T, self.D, self.H, self.dh, _dt(self.dtype))
+        if bwd and self.ds_store:
+            n += ds_store_bytes(db, self.H, self.dh, self.dtype)
         if self._ws is None or self._ws.numel() < n:
             self._ws = workspace(n, self.device)
         return self._ws
@@ -185,7 +201,7 @@ class HstuStack:
         l0 = self.layers[0]
         self._act = [torch.empty_like(x), torch.empty_like(x)]
         self._saved = l0.alloc_saved(db.T)
-        ws = l0._workspace(db)
+        ws = l0._workspace(db, bwd=False)
         for layer in self.layers:
             layer._ws = ws
         self._key, self._graph = key, None

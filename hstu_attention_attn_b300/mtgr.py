@@ -62,11 +62,13 @@ EXPORTS = {
                                                                 C.c_size_t, C.c_void_p]),
     "mtgr_group_layernorm_bwd_noalloc": (C.c_int, [C.c_void_p] * 10 + [C.c_int64, C.c_int32, C.c_int, C.c_void_p]),
     "mtgr_debug_wait_timeout": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "mtgr_debug_plan_counts": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "mtgr_expand_rows": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64, C.c_int32, C.c_int,
                                    C.c_void_p]),
     "mtgr_stochastic_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32] + [C.c_void_p] * 4),
     "mtgr_token_balanced_split": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32] + [C.c_void_p] * 3),
     "mtgr_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int]),
+    "mtgr_attn_ds_store_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
     "mtgr_hstu_attn_fwd": (C.c_int, [C.c_void_p] * 4 + [C.c_int64, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
                                                          C.c_int64, C.c_int32, C.c_int32, C.c_float]
                            + [C.c_void_p] * 4 + [C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -226,6 +228,21 @@ def mtgr_group_layernorm_bwd_noalloc(dy, x, mean, rstd, gid, gamma, dx_residual,
 
 def mtgr_attn_workspace_size(B, T, n_heads, d_h, dtype) -> int:
     return lib().mtgr_attn_workspace_size(B, T, n_heads, d_h, dtype)
+
+
+def mtgr_debug_plan_counts(workspace, B, stream=None):
+    """[forward items, dK/dV items, dQ items, 1 if the backward kept its dS tiles]
+    of the last attention or layer call on `workspace` (synchronises)."""
+    out = np.zeros(4, dtype=np.int32)
+    _check("mtgr_debug_plan_counts", lib().mtgr_debug_plan_counts(_p(workspace), B, out.ctypes.data, _stream(stream)))
+    return [int(v) for v in out]
+
+
+def mtgr_attn_ds_store_size(offsets_host, n_heads, d_h, dtype) -> int:
+    """Extra workspace bytes with which the backward keeps its dS tiles;
+    offsets_host: the batch's B+1 offsets in host memory (array-like)."""
+    o = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    return lib().mtgr_attn_ds_store_size(o.ctypes.data, len(o) - 1, n_heads, d_h, dtype)
 
 
 def mtgr_hstu_attn_fwd(q, k, v, u, ld_in, offsets, gid, ts, T, n_heads, d_h, eps, y, o_saved, ln_mean, ln_rstd,

@@ -124,6 +124,15 @@ MTGR_API mtgr_status mtgr_validate_batch(const int32_t* offsets, int32_t B, cons
  * User/Seq keys are seen by every row; a RealTime key j is seen by RealTime
  * rows i with ts_j <= ts_i and by candidate rows i with ts_j < ts_i; a
  * candidate key is seen only by itself. */
+/* Copies to counts_host[0..3] (host memory) the plan counts that the last
+ * attention or layer call on `workspace` (device memory; a layer workspace
+ * holds its attention workspace first) left there for a batch of B users:
+ * the work items of the forward, of the dK/dV pass and of the dQ pass, and 1
+ * when that backward kept its dS tiles (mtgr_attn_ds_store_size), else 0.
+ * Synchronises `stream`.  For inspection and tests. */
+MTGR_API mtgr_status mtgr_debug_plan_counts(const void* workspace, int32_t B, int32_t* counts_host,
+                                            mtgr_stream_t stream);
+
 MTGR_API mtgr_status mtgr_debug_visible_counts(const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
                                       int64_t T, int32_t* cnt, int64_t* total_pairs, mtgr_stream_t stream);
 
@@ -194,6 +203,22 @@ MTGR_API mtgr_status mtgr_group_layernorm_bwd_noalloc(const void* dy, const void
  * dQ accumulator).  Its first 4 bytes are the call's device status word
  * (MTGR_STATUS_* bits; cleared by each call, set if a bounded wait gave up). */
 MTGR_API size_t mtgr_attn_workspace_size(int32_t B, int64_t T, int32_t n_heads, int32_t d_h, mtgr_dtype dtype);
+
+/* Extra workspace with which the MTGR_BF16 backward (mtgr_hstu_attn_bwd,
+ * mtgr_hstu_layer_bwd) keeps its dS tiles: one 128 x 128 f16 tile (32 KB) per
+ * head and per (query tile, key tile) of each user's tile grid,
+ * n_heads * sum_b ceil(n_b/128)^2 tiles plus 1024 bytes of alignment, where
+ * n_b = offsets_host[b+1] - offsets_host[b] (offsets_host: the batch's B+1
+ * offsets in HOST memory).  0 for other dtypes or d_h, or for bad offsets.
+ * A backward whose workspace holds at least this many bytes beyond its
+ * required size copies each dS tile of the dK/dV pass to HBM and forms dQ =
+ * dS K from the stored tiles (one product per tile pair) instead of
+ * recomputing S and dP (three); the gradients are the same up to f32
+ * summation order.  The device decides from the metadata it was given: when
+ * the tiles of the batch do not fit the extra bytes, the recomputing pass
+ * runs.  Derivation of the backward: marovi.ai "Métodos" block formula. */
+MTGR_API size_t mtgr_attn_ds_store_size(const int32_t* offsets_host, int32_t B, int32_t n_heads, int32_t d_h,
+                                        mtgr_dtype dtype);
 
 /* q, k, v, u: [T, *] with row stride ld_in elements (e.g. views into one
  * [T, 4*H*d_h] buffer).  In the MTGR_BF16 path the tensor-core operands are

@@ -109,3 +109,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         mtgr.mtgr_version()
     with pytest.raises(RuntimeError, match="missing"):
         mtgr.mtgr_token_balanced_split([3, 4, 5], 2)
+
+
+def test_ds_store_size_query(lib):
+    """Bytes of the backward's dS tile store: one 128 x 128 f16 tile per head
+    and per cell of each user's (query tile, key tile) grid, plus 1024 bytes
+    of alignment; 0 where the store is not used.  Host memory only."""
+    import numpy as np
+    from hstu_attention_attn_b300 import mtgr
+    rng = np.random.default_rng(5)
+    lens = np.concatenate([[0, 1, 127, 128, 129, 256, 1092], rng.integers(0, 3000, 50)])
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    grid = sum(((int(n) + 127) // 128) ** 2 for n in lens)
+    for H, dh in ((8, 128), (2, 64)):
+        assert mtgr.mtgr_attn_ds_store_size(offs, H, dh, mtgr.MTGR_BF16) == H * grid * 32768 + 1024
+    assert mtgr.mtgr_attn_ds_store_size(offs, 8, 128, mtgr.MTGR_F32) == 0
+    assert mtgr.mtgr_attn_ds_store_size(offs, 8, 32, mtgr.MTGR_BF16) == 0
+    assert mtgr.mtgr_attn_ds_store_size(offs, 0, 128, mtgr.MTGR_BF16) == 0
+    assert mtgr.mtgr_attn_ds_store_size(np.array([0, 0, 0], np.int32), 8, 128, mtgr.MTGR_BF16) == 0
+    assert mtgr.mtgr_attn_ds_store_size(np.array([0, 300, 200], np.int32), 8, 128, mtgr.MTGR_BF16) == 0

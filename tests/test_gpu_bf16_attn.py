@@ -4,8 +4,8 @@ import numpy as np
 import pytest
 import torch
 
-from hstu_attention_attn_b300 import synth
-from hstu_attention_attn_b300.layer import HstuAttention, device_batch
+from hstu_attention_attn_b300 import mtgr, synth
+from hstu_attention_attn_b300.layer import HstuAttention, device_batch, workspace
 from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users, sub_batch
 from tests.util import TOL_BF16, assert_close_bf16, assert_close_f16, to_np
 
@@ -176,3 +176,38 @@ def test_attention_bf16_longest_user(orc):
     ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
     for name, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
         assert_close_bf16(to_np(got), r, TOL_BF16, name)
+
+
+@pytest.mark.parametrize("dh", [128, 64])
+def test_attention_bwd_bf16_ds_store_and_recompute(orc, dh):
+    """The two dQ passes of the backward: with a store for the dS tiles (the
+    dK/dV pass keeps them and dQ = dS K reads them back), without one, and
+    with a store too small for the batch (the plan falls back to recomputing
+    S and dP on the device).  Each against the oracle; the plan's flag says
+    which pass ran."""
+    need_gpu()
+    rng = np.random.default_rng(81 + dh)
+    batch = synth.make_batch(rng, ragged_users() * 6, ts_hi=3000)
+    H = 2
+    op, db, (q, k, v, u), host, ld, y, saved = _run_fwd(batch, H, dh, rng)
+    dY = rng.standard_normal(tuple(y.shape)).astype(np.float32)
+    ref = orc.attn_bwd(batch, H, dh, *host, bf16_round(dY))
+    need = mtgr.mtgr_attn_ds_store_size(batch.offsets, H, dh, mtgr.MTGR_BF16)
+    tiles = sum(((int(n) + 127) // 128) ** 2 for n in np.diff(batch.offsets))
+    assert need == H * tiles * 128 * 128 * 2 + 1024
+    base = mtgr.mtgr_attn_workspace_size(batch.B, batch.T, H, dh, mtgr.MTGR_BF16)
+    runs = {}
+    for name, extra, kept in (("store", need, 1), ("none", 0, 0), ("short", need // 2, 0)):
+        run = HstuAttention(H, dh, BF, ds_store=False)
+        run._ws = workspace(base + extra)
+        dq, dk, dv, du = run.backward(dev(dY, BF), q, k, v, u, saved, db, ld=ld)
+        torch.cuda.synchronize()
+        assert run.device_status() == 0
+        assert mtgr.mtgr_debug_plan_counts(run._ws, batch.B)[3] == kept, name
+        for gname, got, r in zip(("dq", "dk", "dv", "du"), (dq, dk, dv, du), ref):
+            assert_close_bf16(to_np(got), r, TOL_BF16, f"{gname} ({name})")
+        runs[name] = [to_np(t) for t in (dq, dk, dv, du)]
+    for i, gname in enumerate(("dq", "dk", "dv", "du")):  # recorded: both passes already meet the oracle bound
+        a, b = runs["store"][i].astype(np.float64), runs["none"][i].astype(np.float64)
+        print(f"{gname}: stored vs recomputed dS, max |diff| / RMS = "
+              f"{np.abs(a - b).max() / (np.sqrt(np.mean(b ** 2)) + 1e-30):.2e}")

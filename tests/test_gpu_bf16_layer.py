@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from hstu_attention_attn_b300 import synth
+from hstu_attention_attn_b300 import mtgr, synth
 from hstu_attention_attn_b300.layer import HstuLayer, device_batch
 from tests.gpu_common import bf16_round, dev, need_gpu, ragged_users
 from tests.util import TOL_BF16, assert_close, assert_close_bf16, assert_close_f16, to_np
@@ -83,6 +83,8 @@ def test_layer_bwd_bf16_steps(orc, D, H, dh):
     _, sv = layer.forward(x, db)
     dx, g = layer.backward(x, sv, dev(L.dx_out, BF), db)
     torch.cuda.synchronize()
+    # the layer lends its backward a store for the dS tiles: dQ came from them
+    assert mtgr.mtgr_debug_plan_counts(layer._ws, b.B)[3] == 1
     HD = H * dh
     xb, dxo = bf16_round(L.x), bf16_round(L.dx_out)
     wu, wo = bf16_round(L.w_uqkv), bf16_round(L.w_o)
