@@ -40,10 +40,11 @@ METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/
 # traffic until it is captured again.
 TRAFFIC = {
     "attn_bwd": dict(file="hstu_attention_attn_b300/csrc/attn_bwd_sm103.cu",
-                     sha256="e10d134a0840be045810ec499d51abab4705f14abb277f18770de3e00f1b0f35",
-                     bytes_per_pair=(1833.89e6 + 514.64e6) / 82381761,
+                     sha256="7782ce32b9b49991d3a5194e08529220284212a7135b77bc20ea88541d72ddb2",
+                     bytes_per_pair=(1942.95e6 + 2135.91e6) / 82381761,
                      note="ncu capture of the 131,297-token training batch (82,381,761 visible pairs, inputs "
-                          "larger than L2), scaled by visible pairs"),
+                          "larger than L2), scaled by visible pairs; the kernel also writes the dS tiles "
+                          "(32 KB per tile pair) that the dQ kernel reads"),
 }
 
 
@@ -96,6 +97,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other workloads (MTGR-small attention, 22-layer stacks, inference sweep)")
+    ap.add_argument("--no-ds-store", dest="ds_store", action="store_false",
+                    help="lend the attention backward no store for its dS tiles (dQ recomputes S and dP)")
     return ap.parse_args()
 
 
@@ -254,6 +257,8 @@ def workload_config(args, batch, H, dh, D=None):
                        if batch.T * 2048 > 126 * 2**20 else
                        f"working set larger than L2 (uqkv and silu'(z) are {batch.T * 2 * 4096 * 2 / 2**20:.0f} MiB)"),
                 "parallelism": "replicas only",
+                "attn_bwd_dq": ("dQ = dS K from the dS tiles the dK/dV kernel stores" if args.ds_store
+                                else "dQ kernel recomputes S and dP"),
                 "e2e_upstream_gradient": "only the candidate rows of dx' are copied in (the loss is on the "
                                          "candidates; dx' is zero elsewhere and is expanded on the device)"}
     return {"workload": f"MTGR-small-like attention fwd+bwd: {batch.B} users, {batch.T} tokens, {H} heads x d_h {dh}",
@@ -440,7 +445,7 @@ def run_mine(args):
     bf = torch.bfloat16
     if args.workload == "large_train":
         layer = HstuLayer(D, H, dh, torch.from_numpy(L.w_uqkv), torch.from_numpy(L.w_o), torch.from_numpy(L.gamma),
-                          torch.from_numpy(L.beta), dtype=bf, device=dev)
+                          torch.from_numpy(L.beta), dtype=bf, device=dev, ds_store=args.ds_store)
         x_h = torch.from_numpy(L.x).to(bf).pin_memory()
         dxo_h = torch.from_numpy(L.dx_out).to(bf).pin_memory()
         x = x_h.to(dev)
@@ -455,7 +460,7 @@ def run_mine(args):
             layer.forward(x, db, saved, x_out)
             layer.backward(x, saved, dxo, db, dx, grads)
     else:
-        op = HstuAttention(H, dh, bf, device=dev)
+        op = HstuAttention(H, dh, bf, device=dev, ds_store=args.ds_store)
         q, k, v, u = (torch.from_numpy(m).to(dev).to(bf) for m in (A.q, A.k, A.v, A.u))
         dy = torch.randn(T, H * dh, device=dev, dtype=bf, generator=torch.Generator(dev).manual_seed(5))
 

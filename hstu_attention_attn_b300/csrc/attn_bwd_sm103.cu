@@ -696,9 +696,11 @@ __global__ void __launch_bounds__(DQS_THREADS, 1)
 // Warps: 0 TMA, 1 first MMA issuer (Sᵀ, dPᵀ) + TMEM owner, 2..17 score
 // epilogue (thread = key row; 4 lane quarters x 4 groups of 32 query columns),
 // 18..21 output (TMEM -> 16-bit dV then dK, one warp per lane quarter), 22
-// second MMA issuer (dV, dK), 23 the dS'ᵀ tile store (when the caller keeps
-// the tiles for the dQ pass).
-constexpr int DKV_THREADS = 768;
+// second MMA issuer (dV, dK), and in the STORE instantiation 23, the dS'ᵀ tile
+// store (launched when the caller lends a store for the dQ pass).  Both
+// instantiations are compiled for 24 warps (80 registers a thread): with the
+// budget of 23 warps the compiler spills more in the epilogue.
+constexpr int dkv_threads(bool store) { return store ? 768 : 736; }
 constexpr int DKV_EPI = 16;
 constexpr int DKV_OUT = 4;
 
@@ -803,8 +805,8 @@ __device__ __forceinline__ void p_chunk_k(const uint32_t (&sr)[16], int q0, cons
 // for its own operands: the first Sᵀ(g+1) then dPᵀ(g+1) (into the region Pᵀ(g)
 // leaves once dV(g) has read it), the second dV(g) then dK(g); a Q or dO stage
 // of the ring is free once both have read it.
-template <int D, typename TG>
-__global__ void __launch_bounds__(DKV_THREADS, 1)
+template <int D, typename TG, bool STORE>
+__global__ void __launch_bounds__(768, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const BwdParams p) {
@@ -859,7 +861,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
   bool ok = true;
-  const bool store_on = p.ds_on != nullptr && *p.ds_on != 0;
+  const bool store_on = STORE && p.ds_on != nullptr && *p.ds_on != 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1020,7 +1022,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         tc_commit(&S.dkdv_full);
       }
     }
-  } else if (warp == 3 + DKV_EPI + DKV_OUT) {
+  } else if (STORE && warp == 3 + DKV_EPI + DKV_OUT) {
     // ---------------- dS'ᵀ store: each tile the epilogue leaves in shared memory
     // also goes, by one bulk copy, to its slot of the caller's store ----------------
     if (store_on && lane == 0) {
@@ -1214,10 +1216,11 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e;
   {
     TraceScope tr("attn_bwd", s);
-    auto kern = attn_bwd_dkdv_kernel<D, TG>;
+    const bool store = pa.ds_on != nullptr;
+    auto kern = store ? attn_bwd_dkdv_kernel<D, TG, true> : attn_bwd_dkdv_kernel<D, TG, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, DKV_THREADS, DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
+    kern<<<grid, dkv_threads(store), DkvCfg<D>::SMEM, s>>>(tq, tk, tv, tdo, pa);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

@@ -57,7 +57,9 @@ class HstuAttention:
 
     def __init__(self, n_heads, d_h, dtype=torch.bfloat16, eps=1e-5, device="cuda", ds_store=True):
         self.H, self.dh, self.dtype, self.eps, self.device = n_heads, d_h, dtype, eps, device
-        self.ds_store = ds_store  # lend the backward a store for its dS tiles
+        # lend the backward a store for its dS tiles (ds_store_bytes more workspace):
+        # dQ then needs one product per tile pair instead of three
+        self.ds_store = ds_store
         self._ws = None
 
     def _workspace(self, db):
@@ -106,7 +108,7 @@ class HstuLayer:
     def __init__(self, d_model, n_heads, d_h, w_uqkv, w_o, gamma, beta, dtype=torch.bfloat16, eps_gln=1e-5,
                  eps_ln=1e-5, device="cuda", ds_store=True):
         self.D, self.H, self.dh, self.dtype, self.device = d_model, n_heads, d_h, dtype, device
-        self.ds_store = ds_store  # lend the backward a store for its dS tiles
+        self.ds_store = ds_store  # as HstuAttention.ds_store
         to = dict(device=device)
         self.w_uqkv = torch.as_tensor(w_uqkv).to(dtype=dtype, **to).contiguous()
         self.w_o = torch.as_tensor(w_o).to(dtype=dtype, **to).contiguous()

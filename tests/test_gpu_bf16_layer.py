@@ -83,7 +83,7 @@ def test_layer_bwd_bf16_steps(orc, D, H, dh):
     _, sv = layer.forward(x, db)
     dx, g = layer.backward(x, sv, dev(L.dx_out, BF), db)
     torch.cuda.synchronize()
-    # the layer lends its backward a store for the dS tiles: dQ came from them
+    # the layer lends its backward a store for the dS tiles (by default): dQ came from them
     assert mtgr.mtgr_debug_plan_counts(layer._ws, b.B)[3] == 1
     HD = H * dh
     xb, dxo = bf16_round(L.x), bf16_round(L.dx_out)
