@@ -243,7 +243,9 @@ MTGR_API mtgr_status mtgr_hstu_attn_fwd(const void* q, const void* k, const void
  * then be 4*H*d_h; column blocks U, Q, K, V, each head-major) and every
  * gradient is also multiplied elementwise by its block.  The layer passes
  * silu'(z) of its UQKV pre-activation z, which fuses the SiLU backward of the
- * projection into this call. */
+ * projection into this call.  Workspace: mtgr_attn_workspace_size; with
+ * mtgr_attn_ds_store_size more bytes the MTGR_BF16 backward keeps its dS
+ * tiles and forms dQ from them. */
 MTGR_API mtgr_status mtgr_hstu_attn_bwd(const void* dy, const void* q, const void* k, const void* v, const void* u,
                                int64_t ld_in, const void* o_saved, const float* ln_mean, const float* ln_rstd,
                                const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,
@@ -379,7 +381,9 @@ MTGR_API mtgr_status mtgr_hstu_stack_cand_fwd(const mtgr_layer_weights* w, int32
  * the bf16 weights, f16 activations) and carries its gradients in f16 scaled
  * by a power of two s chosen from max|dx_out| (so that f16's range holds them
  * whatever the loss scale; an all-zero or non-finite dx_out uses s = 1); dx,
- * dw_*, dgamma and dbeta leave scaled back.  The scaling is exact. */
+ * dw_*, dgamma and dbeta leave scaled back.  The scaling is exact.
+ * Workspace: mtgr_layer_workspace_size; with mtgr_attn_ds_store_size more
+ * bytes the attention backward keeps its dS tiles (see there). */
 MTGR_API mtgr_status mtgr_hstu_layer_bwd(const mtgr_layer_weights* w, const void* x, const mtgr_layer_saved* saved,
                                 const void* dx_out, void* dx, const mtgr_layer_grads* grads,
                                 const int32_t* offsets, int32_t B, const uint8_t* gid, const int64_t* ts,

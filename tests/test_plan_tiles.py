@@ -40,6 +40,8 @@ def plan_lists(tmp_path_factory):
             f = line.split()
             if f[0] == "U":
                 res.append({"nt": int(f[4]), "Q": {}, "K": {}, "P": []})
+            elif f[0] in ("SR", "SW"):
+                res[-1][f[0]] = [int(v) for v in f[1:]]
             elif f[0] == "Q":
                 res[-1]["Q"][int(f[1])] = [int(v) for v in f[2:]]
             elif f[0] == "K":
@@ -100,3 +102,18 @@ def test_tile_lists_equal_the_visible_tiles(plan_lists):
                 assert [kt for kt, _, b in mem if b] == want_b
                 assert all(a or b for _, a, b in mem)
     assert visited > 1000
+
+
+def test_ds_tile_slots_written_and_read_agree(plan_lists):
+    """The backward's stored dS tiles: the dK/dV pass writes tile (head, key
+    tile, query tile) to the slot the dQ pass reads it from, every visited
+    pair of every head has a slot of its own, and all slots lie in the user's
+    H * nt^2 range (plan.cuh's ds_slot, compiled as host code)."""
+    users = _users()
+    lists = plan_lists([(nU + nS + nR + K, nU + nS, nU + nS + nR) for nU, nS, nR, K in users])
+    for (nU, nS, nR, K), L in zip(users, lists):
+        nt, rd, wr = L["nt"], L["SR"], L["SW"]
+        assert len(rd) == len(set(rd)) and len(wr) == len(set(wr)), (nU, nS, nR, K)
+        assert sorted(rd) == sorted(wr), (nU, nS, nR, K)
+        assert all(0 <= v < 3 * nt * nt for v in rd), (nU, nS, nR, K)
+        assert len(rd) == 3 * sum(len(v) for v in L["Q"].values())
