@@ -48,6 +48,12 @@ __global__ void user_info_kernel(const int32_t* __restrict__ offsets, int32_t B,
   }
 }
 
+// Users whose records (and tile costs) the plan kernel stages in shared memory
+// first, so that its warps, which walk the users one after another, do not
+// wait on a global load per user; larger batches read them from global memory.
+constexpr int kPlanSmemUsers = 4096;
+static size_t plan_smem_bytes(int32_t B) { return B <= kPlanSmemUsers ? (size_t)B * (sizeof(UserInfo) + 4) : 0; }
+
 // One block: order users by their work (tile products), largest first, then
 // write each list user by user, head by head, tile by tile.  A user's items
 // for one head are consecutive, so the persistent kernels (which deal items
@@ -66,9 +72,16 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
   __shared__ int32_t tot[3];
   __shared__ long long wsum[32];
   __shared__ long long ds_run;
+  extern __shared__ __align__(16) uint8_t plan_dyn[];  // plan_smem_bytes(B): user records, then tile costs
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
+  const bool staged = B <= kPlanSmemUsers;
+  UserInfo* s_users = reinterpret_cast<UserInfo*>(plan_dyn);
+  int32_t* s_cost = reinterpret_cast<int32_t*>(plan_dyn + (size_t)(staged ? B : 0) * sizeof(UserInfo));
+  if (staged)
+    for (int i = tid; i < B; i += blockDim.x) s_users[i] = users[i];
   for (int i = tid; i < 3 * kBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
+  auto user_at = [&](int b) { return staged ? s_users[b] : users[b]; };
   auto user_cost = [&](const UserInfo& u) {  // whole warp; the same value on every lane
     const int nt = ceil_div(u.n, kTile);
     int c = 0;
@@ -77,10 +90,11 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
     return min(c, kBuckets - 1);
   };
   for (int b = warp; b < B; b += nw) {
-    const UserInfo u = users[b];
+    const UserInfo u = user_at(b);
     const int nt = ceil_div(u.n, kTile);
     const int c = user_cost(u);
     if (lane == 0) {
+      if (staged) s_cost[b] = c;
       atomicAdd(&hist[0][c], (singles ? nt : (nt + 1) / 2) * H);
       atomicAdd(&hist[1][c], nt * H);
       atomicAdd(&hist[2][c], (nt - u.q0 / kTile) * H);
@@ -107,10 +121,10 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
   }
   __syncthreads();
   for (int b = warp; b < B; b += nw) {
-    const UserInfo u = users[b];
+    const UserInfo u = user_at(b);
     const int nt = ceil_div(u.n, kTile);
     const int np = singles ? nt : (nt + 1) / 2;  // forward items per head
-    const int c = user_cost(u);
+    const int c = staged ? s_cost[b] : user_cost(u);
     int pf = 0, pb = 0, pq = 0;
     const int t0 = u.q0 / kTile, nq = nt - t0;  // query tiles of the per-tile list
     if (lane == 0) {
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(1024) plan_items_kernel(const UserInfo* __rest
       const int b = c0 + tid;
       long long v = 0;
       if (b < B) {
-        const long long nt = ceil_div(users[b].n, kTile);
+        const long long nt = ceil_div(user_at(b).n, kTile);
         v = (long long)H * nt * nt;
       }
       long long x = v;  // inclusive scan in the warp
@@ -259,7 +273,12 @@ cudaError_t launch_plan(const int32_t* offsets, int32_t B, const uint8_t* gid, i
   // head would not fill the SMs twice (short requests): twice the items
   const int singles = (T / kTile + B) * (int64_t)H <= 4 * (int64_t)num_sms() ? 1 : 0;
   TraceScope tr("plan_items", s);
-  plan_items_kernel<<<1, 1024, 0, s>>>(users, B, H, singles, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
+  const size_t dyn = plan_smem_bytes(B);
+  if (dyn > 48 * 1024) {
+    cudaError_t e2 = cudaFuncSetAttribute(plan_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e2 != cudaSuccess) return e2;
+  }
+  plan_items_kernel<<<1, 1024, dyn, s>>>(users, B, H, singles, ws + L.counts, reinterpret_cast<WorkItem*>(ws + L.fwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.bwd_items),
                                        reinterpret_cast<WorkItem*>(ws + L.dq_items), L.max_items,
                                        ds_cap > 0 ? reinterpret_cast<int64_t*>(ws + L.ds_base) : nullptr, ds_cap,
