@@ -40,7 +40,7 @@ METRIC = "masked HSTU attn fwd+bwd useful TFLOP/s, % BF16 tensor peak; tokens/s/
 # traffic until it is captured again.
 TRAFFIC = {
     "attn_bwd": dict(file="hstu_attention_attn_b300/csrc/attn_bwd_sm103.cu",
-                     sha256="7782ce32b9b49991d3a5194e08529220284212a7135b77bc20ea88541d72ddb2",
+                     sha256="88dc13bd18d7a5d17d0769befba18209b7c9a7b1f327718687990206bd21ce33",
                      bytes_per_pair=(1942.95e6 + 2135.91e6) / 82381761,
                      note="ncu capture of the 131,297-token training batch (82,381,761 visible pairs, inputs "
                           "larger than L2), scaled by visible pairs; the kernel also writes the dS tiles "

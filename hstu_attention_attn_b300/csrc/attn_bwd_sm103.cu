@@ -8,7 +8,7 @@
 //   dQ = dS K,   dK = dSᵀ Q,   silu'(s) = σ(s)(1 + s(1 - σ(s))).
 // There is no softmax, so no row statistics are needed: S is recomputed.
 //
-// Two persistent kernels, neither of which needs atomics:
+// Persistent kernels, none of which needs atomics:
 //  * dK/dV (key-tile major): one item = (user, key tile, head), looping over
 //    the query tiles that see the key tile (dynamic mixed mask, fun-rec
 //    chapter 7.3, §7.3.4).  Per query tile: Sᵀ = K Qᵀ and dPᵀ = V dOᵀ in two
@@ -27,11 +27,13 @@
 // 64 KB of HBM traffic (written once, read once) instead of two recomputed
 // products; the plan decides on the device which dQ kernel runs.
 //
-// Warps in both: 0 TMA, 1 the first MMA issuer (the score products) + TMEM
-// owner, 2..17 score epilogue (thread = TMEM lane = tile row; 4 lane quarters
-// x 4 groups of 32 columns), 18..21 output (TMEM -> 16-bit gradients), 22 the
-// second MMA issuer (the gradient products); 23 in the dK/dV kernel copies
-// the dSᵀ tiles to the store.
+// Warps of the dK/dV and recomputing dQ kernels: 0 TMA, 1 the first MMA
+// issuer (the score products) + TMEM owner, 2..17 score epilogue (thread =
+// TMEM lane = tile row; 4 lane quarters x 4 groups of 32 columns), 18..21
+// output (TMEM -> 16-bit gradients), 22 the second MMA issuer (the gradient
+// products); 23 in the dK/dV kernel's store instantiation copies the dSᵀ
+// tiles to the store.  The dQ kernel that reads the stored tiles has its own
+// warp layout (below).
 #include "attn_sm103.cuh"
 
 namespace mtgr {
