@@ -80,6 +80,15 @@ def test_expand_rows_rejects_bad_arguments_on_the_host(lib):
     assert lib.mtgr_expand_rows(p, p, -1, p, 4, 8, mtgr.MTGR_BF16, None) == mtgr.MTGR_ERR_INVALID_ARG
 
 
+def test_plan_counts_rejects_bad_arguments_on_the_host(lib):
+    import ctypes as C
+    from hstu_attention_attn_b300 import mtgr
+    out = (C.c_int32 * 4)()
+    assert lib.mtgr_debug_plan_counts(None, 4, out, None) == mtgr.MTGR_ERR_INVALID_ARG
+    assert lib.mtgr_debug_plan_counts(C.addressof(out), 4, None, None) == mtgr.MTGR_ERR_INVALID_ARG
+    assert lib.mtgr_debug_plan_counts(C.addressof(out), -1, out, None) == mtgr.MTGR_ERR_INVALID_ARG
+
+
 def test_wait_timeout_check_rejects_null_status(lib):
     from hstu_attention_attn_b300 import mtgr
     assert lib.mtgr_debug_wait_timeout(None, None) == mtgr.MTGR_ERR_INVALID_ARG
